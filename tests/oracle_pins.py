@@ -1,0 +1,416 @@
+"""Pins for the CPU oracle: checks against facts fixed by the method's
+definition and by mathematics, never by re-typing the oracle's own formula.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle is wrong.  ``test_oracle_pins.py`` runs them on the real oracle and
+``test_oracle_mutants.py`` runs them on copies of the oracle with a planted
+mistake, to show that each plausible mistake fails at least one pin.
+
+Kinds of pin used (sources: the AT-10 pattern page, sec. 3 "RMSNorm
+variants", sec. 4 "Linear modes", sec. 5 "MLAProlog"; the SK-03 skeleton
+page, "quantised variant (AT-11)"; the SK-14 skeleton page,
+"QuantMatMulReduceSum"):
+  * closed forms: constant rows, one-hot rows, constructed exact ties;
+  * invariants: scale invariance, identity / permutation weights, the
+    composition of the two-stage chain, the skinny-form fold;
+  * brute force: exact rationals (fractions + 60-digit decimal) on tiny
+    inputs, Python integers for the int8 matmul, a table search for bf16;
+  * library cross-checks: torch.nn.functional.rms_norm and matmul in float64.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+
+import exact
+from oracle import bf16_bits_to_f64
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_bits_of_f32(v):
+    """Standard float32 -> bf16 bit trick (independent of the oracle's codec)."""
+    a = np.asarray(v, dtype=np.float32)
+    b = np.ascontiguousarray(a.reshape(-1)).view(np.uint32)
+    r = ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+    return r.reshape(a.shape) if a.ndim else r[0]
+
+
+def _rand_bf16(rng, shape, sigma=1.0):
+    return _bf16_bits_of_f32((rng.standard_normal(shape) * sigma).astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# bf16 codec
+# ---------------------------------------------------------------------------
+
+def pin_bf16_codec(orc):
+    cases = {
+        1.0: 0x3F80, -2.0: 0xC000, 0.0: 0x0000,
+        1.0 + 2.0**-8: 0x3F80,            # tie -> even (down)
+        1.0 + 3 * 2.0**-8: 0x3F82,        # tie -> even (up)
+        1.0 + 2.0**-8 + 2.0**-30: 0x3F81,  # just above the tie
+        2.0**-133: 0x0001,                # smallest subnormal
+        2.0**-134: 0x0000,                # half of it: tie -> even (zero)
+        3 * 2.0**-134: 0x0002,            # 1.5 quanta: tie -> even (2)
+        (2 - 2.0**-7) * 2.0**127: 0x7F7F,  # largest finite
+        (2 - 2.0**-8) * 2.0**127: 0x7F80,  # max + half ulp overflows (tie, odd max)
+        float("inf"): 0x7F80, -float("inf"): 0xFF80,
+    }
+    for v, want in cases.items():
+        got = int(orc.bf16_rne(v)[0])
+        assert got == want, (v, hex(got), hex(want))
+    assert int(orc.bf16_rne(-0.0)[0]) == 0x8000
+    assert (int(orc.bf16_rne(float("nan"))[0]) & 0x7FFF) > 0x7F80
+    # round trip of every finite pattern
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        vals = (bits << np.uint32(16)).view(np.float32).astype(np.float64)
+    fin = np.isfinite(vals)
+    back = orc.bf16_rne(vals[fin])
+    assert np.array_equal(back, bits[fin].astype(np.uint16))
+    # binary32 inputs: the well-known bit trick on the float's bits
+    rng = _rng(1)
+    f = (rng.standard_normal(20000) * np.exp(rng.uniform(-30, 30, 20000))).astype(np.float32)
+    assert np.array_equal(orc.bf16_rne(f.astype(np.float64)), _bf16_bits_of_f32(f))
+    # binary64 inputs: brute force against the table of neighbours
+    d = rng.standard_normal(400) * np.exp(rng.uniform(-80, 80, 400))
+    got = orc.bf16_rne(d)
+    for v, g in zip(d, got):
+        want, _ = exact.bf16_round_exact(float(v))
+        assert int(g) == want, (v, hex(int(g)), hex(want))
+
+
+# ---------------------------------------------------------------------------
+# AT-03 RMSNorm
+# ---------------------------------------------------------------------------
+
+def pin_rmsnorm_variants_agree(orc):
+    rng = _rng(2)
+    for K in (7, 256, 1000, 4096):
+        x = _rand_bf16(rng, (6, K), 3.0)
+        g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+        ya, ra = orc.rmsnorm_f64(x, g, 1e-6, 0)
+        yb, rb = orc.rmsnorm_f64(x, g, 1e-6, 1)
+        assert np.allclose(ra, rb, rtol=4e-16 * 8, atol=0), (K, np.max(np.abs(ra / rb - 1)))
+        assert np.allclose(ya, yb, rtol=4e-15, atol=0)
+
+
+def pin_rmsnorm_closed_forms(orc):
+    K = 64
+    g = _bf16_bits_of_f32(np.linspace(0.5, 1.5, K).astype(np.float32))
+    gv = bf16_bits_to_f64(g)
+    for variant in (0, 1):
+        for c in (0.75, -3.0, 1e-3):
+            x = np.full((1, K), _bf16_bits_of_f32(np.float32(c)), np.uint16)
+            cv = bf16_bits_to_f64(x[0, 0])
+            eps = 1e-6
+            y, r = orc.rmsnorm_f64(x, g, eps, variant)
+            want_r = exact.dec_sqrt_recip(Fraction(cv) ** 2 + Fraction(eps))
+            assert exact.rel_close(r[0], want_r, 4e-16 * 4), (variant, c)
+            want_y = np.array([float(Fraction(cv) * want_r * Fraction(gk)) for gk in gv])
+            assert np.allclose(y[0], want_y, rtol=1e-15, atol=0)
+            # eps = 0: a constant row normalises to +-gamma exactly up to rounding
+            y0, _ = orc.rmsnorm_f64(x, g, 0.0, variant)
+            assert np.allclose(y0[0], np.sign(cv) * gv, rtol=2e-16 * 4, atol=0)
+        # one-hot row: y_j = sign(c) * sqrt(K) * gamma_j, zero elsewhere (eps = 0)
+        for j, c in ((0, 2.0), (17, -0.5), (K - 1, 9.0)):
+            x = np.zeros((1, K), np.uint16)
+            x[0, j] = _bf16_bits_of_f32(np.float32(c))
+            y, _ = orc.rmsnorm_f64(x, g, 0.0, variant)
+            want = np.zeros(K)
+            want[j] = np.sign(c) * np.sqrt(K) * gv[j]
+            assert np.allclose(y[0], want, rtol=4e-16 * 4, atol=0), (variant, j)
+
+
+def pin_rmsnorm_scale_invariance(orc):
+    rng = _rng(3)
+    x = _rand_bf16(rng, (4, 300))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, 300).astype(np.float32))
+    xv = bf16_bits_to_f64(x)
+    for variant in (0, 1):
+        y1, _ = orc.rmsnorm_f64(x, g, 0.0, variant)
+        for j in (-3, 1, 5):
+            xs = orc.bf16_rne(xv * 2.0**j).reshape(x.shape)  # exact power-of-two scaling
+            assert np.array_equal(bf16_bits_to_f64(xs), xv * 2.0**j)
+            y2, _ = orc.rmsnorm_f64(xs, g, 0.0, variant)
+            assert np.allclose(y1, y2, rtol=4e-16 * 4, atol=0), (variant, j)
+
+
+def pin_rmsnorm_exact_small(orc):
+    """Brute force: rstd and y from exact rationals (60-digit square root)."""
+    rng = _rng(4)
+    for variant in (0, 1):
+        for K in (1, 3, 8):
+            x = _rand_bf16(rng, (3, K))
+            g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+            eps = 1e-6
+            y, r = orc.rmsnorm_f64(x, g, eps, variant)
+            for t in range(3):
+                xs = [Fraction(exact.bf16_value(b)) for b in x[t]]
+                ms = sum(v * v for v in xs) / K
+                rr = exact.dec_sqrt_recip(ms + Fraction(eps))
+                assert exact.rel_close(r[t], rr, 1e-15), (variant, K, t)
+                for k in range(K):
+                    want = xs[k] * rr * Fraction(exact.bf16_value(g[k]))
+                    assert exact.rel_close(y[t, k], want, 1e-15) or abs(float(want)) < 1e-300
+
+
+def pin_rmsnorm_torch(orc):
+    import torch
+    rng = _rng(5)
+    x = _rand_bf16(rng, (16, 512), 2.0)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, 512).astype(np.float32))
+    xt = torch.from_numpy(bf16_bits_to_f64(x))
+    gt = torch.from_numpy(bf16_bits_to_f64(g))
+    want = torch.nn.functional.rms_norm(xt, (512,), weight=gt, eps=1e-6).numpy()
+    for variant in (0, 1):
+        y, _ = orc.rmsnorm_f64(x, g, 1e-6, variant)
+        assert np.allclose(y, want, rtol=1e-14, atol=1e-300)
+
+
+# ---------------------------------------------------------------------------
+# AT-10 RMSNorm + Linear (form 0) and the FP32 mhc_pre form (form 1)
+# ---------------------------------------------------------------------------
+
+def pin_linear_identity_and_permutation(orc):
+    rng = _rng(6)
+    K = 48
+    x = _rand_bf16(rng, (5, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    one = _bf16_bits_of_f32(np.float32(1.0))
+    y, _ = orc.rmsnorm_f64(x, g, 1e-6, 0)
+    a_bits = orc.bf16_rne(y.ravel()).reshape(y.shape)
+    # W = I: the projection returns the bf16-cast normed activations unchanged
+    W = np.zeros((K, K), np.uint16)
+    W[np.arange(K), np.arange(K)] = one
+    _, out = orc.rmsnorm_linear(x, g, W, 1e-6, 0, 0)
+    assert np.array_equal(out, a_bits)
+    # W[n, k] = 1 iff k == perm[n]: out[:, n] = a[:, perm[n]] (catches a transposed W)
+    perm = rng.permutation(K)
+    Wp = np.zeros((K, K), np.uint16)
+    Wp[np.arange(K), perm] = one
+    _, outp = orc.rmsnorm_linear(x, g, Wp, 1e-6, 0, 0)
+    assert np.array_equal(outp, a_bits[:, perm])
+    # N != K, rectangular: rows of W pick single features, with a scale of 2
+    two = _bf16_bits_of_f32(np.float32(2.0))
+    Wr = np.zeros((7, K), np.uint16)
+    cols = rng.choice(K, 7, replace=False)
+    Wr[np.arange(7), cols] = two
+    _, outr = orc.rmsnorm_linear(x, g, Wr, 1e-6, 0, 0)
+    assert np.array_equal(bf16_bits_to_f64(outr), 2.0 * bf16_bits_to_f64(a_bits[:, cols]))
+
+
+def pin_linear_exact_small(orc):
+    """Brute force of the whole AT-10 row on tiny shapes in exact rationals."""
+    rng = _rng(7)
+    for (T, K, N) in ((2, 3, 2), (3, 8, 5), (1, 5, 8)):
+        x = _rand_bf16(rng, (T, K))
+        g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+        W = _rand_bf16(rng, (N, K), 0.5)
+        eps = 1e-6
+        ref, out = orc.rmsnorm_linear(x, g, W, eps, 0, 0)
+        for t in range(T):
+            xs = [Fraction(exact.bf16_value(b)) for b in x[t]]
+            rr = exact.dec_sqrt_recip(sum(v * v for v in xs) / K + Fraction(eps))
+            a = []
+            for k in range(K):
+                bits, near = exact.bf16_round_exact(xs[k] * rr * Fraction(exact.bf16_value(g[k])))
+                assert not near  # the generator never hits a bf16 tie here
+                a.append(Fraction(exact.bf16_value(bits)))
+            for n in range(N):
+                s = sum(a[k] * Fraction(exact.bf16_value(W[n, k])) for k in range(K))
+                assert exact.rel_close(ref[t, n], s, 1e-15) or abs(float(s)) < 1e-300
+                bits, near = exact.bf16_round_exact(s)
+                assert near or int(out[t, n]) == bits, (T, K, N, t, n)
+
+
+def pin_linear_torch(orc):
+    import torch
+    rng = _rng(8)
+    T, K, N = 12, 320, 40
+    x = _rand_bf16(rng, (T, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    W = _rand_bf16(rng, (N, K), 0.02)
+    ref, out = orc.rmsnorm_linear(x, g, W, 1e-6, 0, 0)
+    xt = torch.from_numpy(bf16_bits_to_f64(x))
+    y = torch.nn.functional.rms_norm(xt, (K,), weight=torch.from_numpy(bf16_bits_to_f64(g)), eps=1e-6)
+    a = y.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    want = a @ torch.from_numpy(bf16_bits_to_f64(W)).T
+    scale = (a.abs() @ torch.from_numpy(np.abs(bf16_bits_to_f64(W))).T).numpy()
+    # a may differ in rare elements by one bf16 step (double rounding in torch)
+    assert np.all(np.abs(ref - want.numpy()) <= 2.0**-7 * scale * 0.05 + 1e-12 * scale)
+    # form 1 without gamma equals rstd * (x @ W^T): the skinny-form fold
+    ref1, out1 = orc.rmsnorm_linear(x, None, W, 1e-6, 0, 1)
+    xv, wv = bf16_bits_to_f64(x), bf16_bits_to_f64(W)
+    rstd = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + 1e-6)
+    fold = rstd[:, None] * (xv @ wv.T)
+    assert np.allclose(ref1, fold, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(out1, ref1.astype(np.float32))
+
+
+def pin_linear_form1_gamma(orc):
+    """Form 1 keeps the normed values unrounded: with W = I it returns them."""
+    rng = _rng(9)
+    K = 32
+    x = _rand_bf16(rng, (3, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    W = np.zeros((K, K), np.uint16)
+    W[np.arange(K), np.arange(K)] = _bf16_bits_of_f32(np.float32(1.0))
+    y, _ = orc.rmsnorm_f64(x, g, 1e-6, 0)
+    ref, out = orc.rmsnorm_linear(x, g, W, 1e-6, 0, 1)
+    assert np.array_equal(ref, y)
+    assert np.array_equal(out, y.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# MLA two-stage chain
+# ---------------------------------------------------------------------------
+
+def pin_mla_composition(orc):
+    rng = _rng(10)
+    T, K, N1, N2 = 4, 96, 40, 24
+    x = _rand_bf16(rng, (T, K))
+    Wa = _rand_bf16(rng, (N1, K), 0.1)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, N1).astype(np.float32))
+    Wb = _rand_bf16(rng, (N2, N1), 0.1)
+    qa, ref, out = orc.mla_q_chain(x, Wa, g, Wb, 1e-6, 1)
+    # stage 1 equals the bf16 rounding of an independent float64 matmul
+    s1 = bf16_bits_to_f64(x) @ bf16_bits_to_f64(Wa).T
+    for t in range(T):
+        for j in range(N1):
+            bits, near = exact.bf16_round_exact(float(s1[t, j]))
+            assert near or int(qa[t, j]) == bits
+    # stage 2 equals the single-stage AT-10 oracle applied to the stage-1 output
+    ref2, out2 = orc.rmsnorm_linear(qa, g, Wb, 1e-6, 1, 0)
+    assert np.array_equal(ref, ref2) and np.array_equal(out, out2)
+    # and the gamma really is applied: gamma = 1 gives a different result
+    ones = np.full(N1, _bf16_bits_of_f32(np.float32(1.0)), np.uint16)
+    _, _, out_1 = orc.mla_q_chain(x, Wa, ones, Wb, 1e-6, 1)
+    assert not np.array_equal(out, out_1)
+
+
+# ---------------------------------------------------------------------------
+# W8A8: per-token symmetric INT8 quant, exact INT32 matmul, dequant
+# ---------------------------------------------------------------------------
+
+def pin_quant_constructed_ties(orc):
+    # x chosen so that sum x^2 / 8 + eps = 4096 exactly: rstd = 1/64, amax = 127/64,
+    # qs = 64, and y * qs returns x exactly -> the codes are rint_half_even(x).
+    x = np.array([[127, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, 0.0]], np.float32)
+    ms = float(np.sum(x.astype(np.float64) ** 2)) / 8
+    eps = 4096.0 - ms
+    xb = _bf16_bits_of_f32(x)
+    for variant in (0, 1):
+        q, xs, rstd, v = orc.quant_rows_f32(xb, None, eps, variant)
+        assert rstd[0] == np.float32(1 / 64)
+        assert np.array_equal(v[0], x[0])
+        assert q[0].tolist() == [127, 2, 4, -2, 0, 2, 0, 0]
+        assert xs[0] == np.float32(127 / 64 / 127)
+
+
+def pin_quant_properties(orc):
+    rng = _rng(11)
+    T, K = 24, 512
+    x = _rand_bf16(rng, (T, K))
+    x[3] = 0  # an all-zero row
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    for variant in (0, 1):
+        q, xs, rstd, v = orc.quant_rows_f32(x, g, 1e-6, variant)
+        assert q.min() >= -127 and q.max() <= 127
+        y64, r64 = orc.rmsnorm_f64(x, g, 1e-6, variant)
+        for t in range(T):
+            if t == 3:
+                assert not q[t].any() and xs[t] == 0.0
+                continue
+            assert np.abs(q[t]).max() == 127
+            amax = np.abs(y64[t]).max()
+            assert abs(float(xs[t]) - amax / 127) <= 1e-6 * amax / 127
+            assert abs(float(rstd[t]) - r64[t]) <= 1e-6 * r64[t]
+            # reconstruction error of the symmetric code: at most half a step
+            err = np.abs(q[t].astype(np.float64) * float(xs[t]) - y64[t])
+            assert np.all(err <= 0.5 * float(xs[t]) * (1 + 1e-4))
+            # the code is the nearest integer to v (ties to even)
+            assert np.all(np.abs(q[t] - v[t].astype(np.float64)) <= 0.5)
+            assert np.array_equal(q[t], np.clip(np.rint(v[t]), -127, 127).astype(np.int8))
+
+
+def pin_gemm_s8_bruteforce(orc):
+    rng = _rng(12)
+    for (M, N, K) in ((1, 1, 1), (3, 4, 5), (5, 7, 33)):
+        A = rng.integers(-127, 128, (M, K)).astype(np.int8)
+        B = rng.integers(-127, 128, (N, K)).astype(np.int8)
+        C, ovf = orc.gemm_s8(A, B)
+        assert not ovf
+        for m in range(M):
+            for n in range(N):
+                assert int(C[m, n]) == sum(int(A[m, k]) * int(B[n, k]) for k in range(K))
+    A = rng.integers(-127, 128, (17, 300)).astype(np.int8)
+    B = rng.integers(-127, 128, (9, 300)).astype(np.int8)
+    C, _ = orc.gemm_s8(A, B)
+    assert np.array_equal(C, A.astype(np.int64) @ B.astype(np.int64).T)
+    # worst case fits int32 up to K = 133144 (127*127*K <= 2^31 - 1)
+    for K, want_ovf in ((1024, False), (133144, False), (133145, True)):
+        A = np.full((1, K), 127, np.int8)
+        B = np.full((2, K), 127, np.int8)
+        B[1] = -127
+        C, ovf = orc.gemm_s8(A, B)
+        assert ovf == want_ovf
+        if not want_ovf:
+            assert int(C[0, 0]) == 127 * 127 * K and int(C[0, 1]) == -127 * 127 * K
+
+
+def pin_dequant_exact(orc):
+    rng = _rng(13)
+    acc = rng.integers(-2**31, 2**31, (3, 5)).astype(np.int32)
+    xs = rng.uniform(1e-3, 1.0, 3).astype(np.float32)
+    ws = rng.uniform(1e-3, 1e-2, 5).astype(np.float32)
+    ref, out = orc.dequant_bf16(acc, xs, ws)
+    for m in range(3):
+        for n in range(5):
+            want = Fraction(int(acc[m, n])) * Fraction(float(xs[m])) * Fraction(float(ws[n]))
+            assert exact.rel_close(ref[m, n], want, 2.3e-16)
+            bits, near = exact.bf16_round_exact(want)
+            assert near or int(out[m, n]) == bits
+
+
+def pin_w8a8_composition(orc):
+    rng = _rng(14)
+    T, K, N = 6, 128, 20
+    x = _rand_bf16(rng, (T, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    Wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    ws = rng.uniform(1e-3, 1e-2, N).astype(np.float32)
+    r = orc.rmsnorm_linear_w8a8(x, g, Wq, ws, 1e-6, 0)
+    q, xs, _, _ = orc.quant_rows_f32(x, g, 1e-6, 0)
+    assert np.array_equal(r["q"], q) and np.array_equal(r["x_scale"], xs)
+    assert np.array_equal(r["acc"], q.astype(np.int64) @ Wq.astype(np.int64).T)
+    ref, out = orc.dequant_bf16(r["acc"], xs, ws)
+    assert np.array_equal(r["out"], out)
+    # and the quantised path approximates the unquantised FP32 form closely
+    yv, _ = orc.rmsnorm_f64(x, g, 1e-6, 0)
+    full = (yv @ Wq.astype(np.float64).T) * ws[None, :]
+    assert np.allclose(r["ref"], full, rtol=0, atol=0.02 * np.abs(full).max())
+
+
+ALL_PINS = [
+    pin_bf16_codec,
+    pin_rmsnorm_variants_agree,
+    pin_rmsnorm_closed_forms,
+    pin_rmsnorm_scale_invariance,
+    pin_rmsnorm_exact_small,
+    pin_rmsnorm_torch,
+    pin_linear_identity_and_permutation,
+    pin_linear_exact_small,
+    pin_linear_torch,
+    pin_linear_form1_gamma,
+    pin_mla_composition,
+    pin_quant_constructed_ties,
+    pin_quant_properties,
+    pin_gemm_s8_bruteforce,
+    pin_dequant_exact,
+    pin_w8a8_composition,
+]

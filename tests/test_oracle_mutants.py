@@ -1,0 +1,74 @@
+"""Planted mistakes: each test copies oracle.c, plants one plausible mistake
+(a dropped term, a wrong sign, index or rounding rule, a transposed operand),
+compiles the copy on the CPU into a temporary directory and runs every pin on
+it in a child process.  At least one pin must fail (or the child must crash),
+which shows that the pins would catch that mistake in the real oracle.
+"""
+import json
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, text in oracle.c, replacement).  Each text must occur exactly once.
+MUTANTS = [
+    ("drop_eps_rsqrt_form", "return 1.0 / sqrt(ms + eps);", "return 1.0 / sqrt(ms);"),
+    ("drop_inv_d_sqrt_div_form", "s += (v * v) * inv_d;", "s += (v * v);"),
+    ("mean_over_k_minus_1", "double inv_d = 1.0 / (double)K;", "double inv_d = 1.0 / (double)(K - 1);"),
+    ("drop_gamma_at10", "                if (gamma)\n                    v = v * orc_bf16_value(gamma[k]);\n                a[k]",
+     "                a[k]"),
+    ("drop_bf16_cast_of_normed", "a[k] = (form == 0) ? orc_bf16_value(orc_bf16_rne(v)) : v;", "a[k] = v;"),
+    ("transposed_weight", "const double *wr = wd + n * K;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[k];",
+     "const double *wr = wd + n;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[(k % N) * K + (k / N) % K];"),
+    ("wrong_sign_accumulate", "acc += a[k] * wr[k];", "acc -= a[k] * wr[k];"),
+    ("mla_drop_gamma", "v = v * orc_bf16_value(gamma_cq[j]);", "v = v * 1.0;"),
+    ("mla_stage2_unrounded_input", "z[j] = orc_bf16_value(orc_bf16_rne(v));", "z[j] = v;"),
+    ("quant_round_half_away", "float r = rintf(v);", "float r = roundf(v);"),
+    ("quant_scale_128", "float qs = 127.0f / amax;", "float qs = 128.0f / amax;"),
+    ("quant_dequant_scale_inverted", "x_scale[t] = amax / 127.0f;", "x_scale[t] = 127.0f / amax;"),
+    ("quant_drop_gamma", "            if (gamma)\n                y = y * bf16_as_float(gamma[k]);\n            float v = y * qs;",
+     "            float v = y * qs;"),
+    ("gemm_s8_off_by_one", "for (int64_t k = 0; k < K; ++k)\n                acc += (int64_t)A[m * K + k]",
+     "for (int64_t k = 1; k < K; ++k)\n                acc += (int64_t)A[m * K + k]"),
+    ("dequant_wrong_scale", "double scale = (double)x_scale[m] * (double)w_scale[n];",
+     "double scale = (double)x_scale[m] * (double)w_scale[m % N];"),
+    ("bf16_ties_away", "double r = nearbyint(m * 256.0);", "double r = round(m * 256.0);"),
+    ("bf16_truncate", "double r = nearbyint(m * 256.0);", "double r = floor(m * 256.0);"),
+]
+
+CHILD = textwrap.dedent("""
+    import json, sys
+    sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+    import oracle, oracle_pins
+    o = oracle.Oracle(oracle.load({so!r}))
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except Exception as e:  # AssertionError or a numpy error from garbage
+            failed.append(pin.__name__)
+    print(json.dumps(failed))
+""")
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutant = tmp_path / "oracle_mutant.c"
+    mutant.write_text(src.replace(old, new))
+    so = str(tmp_path / "liboracle_mutant.so")
+    import oracle
+    subprocess.run(["gcc", *oracle.CFLAGS, str(mutant), "-o", so, "-lm"], check=True)
+    code = CHILD.format(root=ROOT, tests=os.path.join(ROOT, "tests"), so=so)
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300, env=env)
+    if r.returncode != 0:
+        return  # the mutant crashed the child: caught
+    failed = json.loads(r.stdout.strip().splitlines()[-1])
+    assert failed, f"planted mistake {name} passed every pin"
