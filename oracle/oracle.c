@@ -326,12 +326,19 @@ int orc_mla_q_chain(const uint16_t *x, const uint16_t *W_qa, const uint16_t *gam
 /* (AT-05: amax = max|y|, multiplier 127/amax, rounding + saturating casts), */
 /* [SK03] AT-11 section (common.py quant: dequant scale = max|x| / 127).     */
 /*                                                                           */
-/*   x32 = float(x); s = sum of x32*x32 (variant A) or of x32*x32*(1/D) (B); */
+/*   x32 = float(x); terms x32*x32 (variant A) or (x32*x32)*(1/D) (B), each */
+/*   a binary32 product; s = the binary32 value of their sum (see below);    */
 /*   A: ms = s*(1/D); rstd = 1/sqrt(ms+eps)     B: rstd = 1/sqrt(s+eps)      */
 /*   y = (x32*rstd)*float(gamma); amax = max|y|; qs = 127/amax;              */
 /*   q = clamp(rint_half_even(y*qs), -127, 127); x_scale = amax/127.         */
 /* An all-zero row (amax == 0) gives q = 0 and x_scale = 0 (the pages are    */
 /* silent; no division by zero is performed).                                */
+/* The pages fix FP32 but not the order of the K-term sum.  Reading: s is    */
+/* the binary32 rounding of the exact sum of the binary32 terms.  The terms  */
+/* are summed in binary64, exact for bf16 data (squares carry 16 bits) of    */
+/* any realistic range, then rounded once; every later step is a single      */
+/* correctly rounded binary32 operation, so the integer codes are a         */
+/* function of the input alone, not of a summation order.                   */
 /* ------------------------------------------------------------------------ */
 
 int orc_quant_rows_f32(const uint16_t *x, const uint16_t *gamma, int64_t T, int64_t K,
@@ -344,14 +351,15 @@ int orc_quant_rows_f32(const uint16_t *x, const uint16_t *gamma, int64_t T, int6
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t *xr = x + t * K;
-        float s = 0.0f;
+        double s64 = 0.0;
         float rstd;
         if (variant == 0) {
             for (int64_t k = 0; k < K; ++k) {
                 float v = bf16_as_float(xr[k]);
                 float sq = v * v;
-                s = s + sq;
+                s64 += (double)sq;
             }
+            float s = (float)s64;
             float ms = s * inv_d;
             float var = ms + eps;
             rstd = 1.0f / sqrtf(var);
@@ -360,8 +368,9 @@ int orc_quant_rows_f32(const uint16_t *x, const uint16_t *gamma, int64_t T, int6
                 float v = bf16_as_float(xr[k]);
                 float sq = v * v;
                 float sc = sq * inv_d;
-                s = s + sc;
+                s64 += (double)sc;
             }
+            float s = (float)s64;
             float var = s + eps;
             float sd = sqrtf(var);
             rstd = 1.0f / sd;
