@@ -1,0 +1,456 @@
+"""Benchmark of the fused RMSNorm -> Linear projection on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qkv|tiny|mla|w8a8|skinny]
+                    [--impl ours|reference]
+
+Prints ONE JSON line.  The default workload is the pre-attention fused QKV
+projection x[4096,4096] -> W[6144,4096] (RMSNorm with gamma, rsqrt form,
+bf16 out); the metric is TFLOP/s of the projection (2*T*N*K per step), or
+GB/s for the HBM-bound workloads (skinny, tiny), TOPS for W8A8.
+
+A step is one call of the library's C entry point on inputs already resident
+in HBM.  Each step is timed with CUDA events on the launch stream; the L2
+(129 MB) is flushed between steps by writing a 256 MB buffer outside the
+timed events.  The dominant kernel's own duration comes from the library's
+event trace (events recorded around each launch on the same stream).
+
+--impl reference times the CPU oracle (oracle/) on the host cores on a
+bounded sample of rows of the same workload; it is a deliberately slow
+baseline, not a competitor.
+
+Multi-GPU: each rank runs an independent replica of the workload on its own
+GPU (the path needs no exchange); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth_inputs as si  # noqa: E402
+
+WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny")
+DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600}
+METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------- workloads
+class Work:
+    """Inputs (host numpy + device tensors) and the call of one workload."""
+
+    def __init__(self, name: str, device, T=None):
+        import torch
+        self.name = name
+        self.cfg = c = si.scaled(si.CONFIGS[name], T=T) if T else si.CONFIGS[name]
+        self.device = device
+        self.torch = torch
+        if name in ("qkv", "tiny", "skinny"):
+            self.h = si.make_projection(c)
+            T, K, N = c["T"], c["K"], c["N"]
+            self.flops = 2.0 * T * N * K
+            out_b = 2 if c["out_dtype"] == "bf16" else 4
+            self.bytes = 2.0 * T * K + 2.0 * N * K + (2.0 * K if c.get("has_gamma") else 0) + out_b * T * N
+        elif name == "mla":
+            self.h = si.make_mla(c)
+            T, K, N1, N2 = c["T"], c["K"], c["N1"], c["N2"]
+            self.flops = 2.0 * T * (N1 * K + N2 * N1)
+            self.bytes = 2.0 * (T * K + N1 * K + N1 + N2 * N1 + T * N2)
+        else:
+            self.h = si.make_w8a8(c)
+            T, K, N = c["T"], c["K"], c["N"]
+            self.flops = 2.0 * T * N * K
+            self.bytes = 2.0 * T * K + 1.0 * N * K + 2.0 * K + 4.0 * N + 2.0 * T * N
+        self.d = {k: self._to_dev(v) for k, v in self.h.items()}
+        self.out = self._alloc_out()
+        self.ws = None
+
+    def _to_dev(self, a):
+        torch = self.torch
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
+        if a.dtype == np.uint16:
+            t = t.view(torch.bfloat16)
+        return t.to(self.device)
+
+    def _alloc_out(self):
+        torch, c = self.torch, self.cfg
+        if self.name == "mla":
+            return torch.empty((c["T"], c["N2"]), dtype=torch.bfloat16, device=self.device)
+        dt = torch.float32 if c.get("out_dtype") == "fp32" else torch.bfloat16
+        return torch.empty((c["T"], c["N"]), dtype=dt, device=self.device)
+
+    def unit(self):
+        if self.name in ("skinny", "tiny"):
+            return "GB/s", self.bytes / 1e9
+        if self.name == "w8a8":
+            return "TOPS", self.flops / 1e12
+        return "TFLOP/s", self.flops / 1e12
+
+    def call(self, d=None, out=None, stream=None):
+        import rmsnorm_linear_projection_gb300 as rnl
+        d = d or self.d
+        out = self.out if out is None else out
+        c = self.cfg
+        if self.name in ("qkv", "tiny", "skinny"):
+            odt = rnl.OUT_FP32 if c["out_dtype"] == "fp32" else rnl.OUT_BF16
+            if self.ws is None:
+                self.ws = self.torch.empty(max(1, rnl.workspace_size(rnl.OP_BF16, c["T"], c["K"], c["N"], odt)),
+                                           dtype=self.torch.uint8, device=self.device)
+            return rnl.rmsnorm_linear_bf16(d["x"], d["gamma"], d["W"], eps=c["eps"], norm_mode=c["norm_mode"],
+                                           out=out, out_dtype=odt, workspace=self.ws, stream=stream)
+        if self.name == "mla":
+            if self.ws is None:
+                self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_MLA, c["T"], c["K"], c["N1"], c["N2"]),
+                                           dtype=self.torch.uint8, device=self.device)
+            return rnl.mla_q_chain(d["x"], d["W_qa"], d["gamma_cq"], d["W_qb"], eps=c["eps"],
+                                   norm_mode=c["norm_mode"], out=out, workspace=self.ws, stream=stream)
+        if self.ws is None:
+            self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_W8A8, c["T"], c["K"], c["N"]),
+                                       dtype=self.torch.uint8, device=self.device)
+        return rnl.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], eps=c["eps"],
+                                       norm_mode=c["norm_mode"], out=out, workspace=self.ws, stream=stream)
+
+    def dominant(self):
+        """(kernel name, algorithmic amount per launch, bound) of the roofline kernel."""
+        c = self.cfg
+        if self.name == "skinny":
+            return "skinny_stream", 2.0 * c["T"] * c["K"] + 2.0 * c["N"] * c["K"], "hbm"
+        if self.name == "tiny":
+            return "gemm_bf16", 2.0 * c["T"] * c["N"] * c["K"], "tensor"
+        if self.name == "mla":
+            return "gemm_bf16", None, "tensor"  # two launches with different shapes
+        if self.name == "w8a8":
+            return "gemm_int_dequant", 2.0 * c["T"] * c["N"] * c["K"], "tensor"
+        return "gemm_bf16", 2.0 * c["T"] * c["N"] * c["K"], "tensor"
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, ln in self.lines:
+            p = [s.strip() for s in ln.split(",")]
+            if len(p) < 9:
+                continue
+            rows.append((ts, p))
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows[-3:]
+        if not inside:
+            return None
+        sm = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in inside if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for _, p in inside:
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# --------------------------------------------------------------- CPU baseline
+def oracle_sample(work_name: str, target_s: float = 12.0):
+    """Time the CPU oracle on a bounded row sample; returns (value, unit, cores, sample, outputs)."""
+    import oracle
+    o = oracle.Oracle()
+    c = si.CONFIGS[work_name]
+    T = c["T"]
+    probe_rows = np.arange(min(4, T))
+
+    def run(rows):
+        if work_name in ("qkv", "tiny", "skinny"):
+            d = si.make_projection(c, rows=rows)
+            form = 1 if c["out_dtype"] == "fp32" else 0
+            t = time.perf_counter()
+            _, out = o.rmsnorm_linear(d["x"], d["gamma"], d["W"], c["eps"], c["norm_mode"], form)
+            return time.perf_counter() - t, out
+        if work_name == "mla":
+            d = si.make_mla(c, rows=rows)
+            t = time.perf_counter()
+            _, _, out = o.mla_q_chain(d["x"], d["W_qa"], d["gamma_cq"], d["W_qb"], c["eps"], c["norm_mode"])
+            return time.perf_counter() - t, out
+        d = si.make_w8a8(c, rows=rows)
+        t = time.perf_counter()
+        r = o.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], c["eps"], c["norm_mode"])
+        return time.perf_counter() - t, r["out"]
+
+    dt, _ = run(probe_rows)
+    per_row = max(dt / probe_rows.size, 1e-6)
+    n = int(min(T, max(probe_rows.size, target_s / per_row)))
+    rows = np.linspace(0, T - 1, n).round().astype(np.int64)
+    rows = np.unique(rows)
+    dt, out = run(rows)
+    frac = rows.size / T
+    if work_name in ("qkv", "tiny", "skinny"):
+        K, N = c["K"], c["N"]
+        flops, byt = 2.0 * T * N * K, 2.0 * T * K + 2.0 * N * K + 4.0 * T * N
+    elif work_name == "mla":
+        flops = 2.0 * T * (c["N1"] * c["K"] + c["N2"] * c["N1"])
+        byt = 0.0
+    else:
+        flops, byt = 2.0 * T * c["N"] * c["K"], 0.0
+    if work_name in ("skinny", "tiny"):
+        value, unit = byt * frac / dt / 1e9, "GB/s"
+    elif work_name == "w8a8":
+        value, unit = flops * frac / dt / 1e12, "TOPS"
+    else:
+        value, unit = flops * frac / dt / 1e12, "TFLOP/s"
+    sample = f"{rows.size} of {T} rows of the {work_name} workload (whole rows, all N outputs), {dt:.2f} s"
+    return value, unit, o.threads(), sample, rows, out, dt
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, timed on the host cores on a bounded row
+    sample of the same workload (rank 0 only; other ranks exit at once)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    c = si.CONFIGS[args.workload]
+    times, values = [], []
+    unit = cores = sample = None
+    for i in range(args.warmup + args.steps):
+        v, unit, cores, sample, _, _, dt = oracle_sample(args.workload, target_s=args.ref_seconds)
+        if i >= args.warmup:
+            times.append(dt)
+            values.append(v)
+    value = statistics.mean(values)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": args.workload, **{k: v for k, v in c.items() if k != "seed"}},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import rmsnorm_linear_projection_gb300 as rnl
+    from rmsnorm_linear_projection_gb300 import build as rnl_build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        rnl_build.build()
+    if dist is not None:
+        dist.barrier()
+    rnl.load()
+
+    w = Work(args.workload, device, T=args.T)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)  # 256 MB > L2
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        w.call()
+    torch.cuda.synchronize()
+    rnl.rnl_check_device_error()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    rnl.rnl_trace_read()
+    rnl.rnl_trace_enable(True)
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        w.call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    rnl.rnl_trace_enable(False)
+    trace = rnl.rnl_trace_read()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    rnl.rnl_check_device_error()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = sum(step_ms) / 1e3
+    if dist is not None:
+        tt = torch.tensor([total_s], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+
+    unit, amount = w.unit()
+    value = world * args.steps * amount / total_s
+
+    # roofline of the dominant kernel, from the library's per-launch events
+    peaks = _peaks()
+    per_kernel = {}
+    for name, ms in trace:
+        per_kernel.setdefault(name, []).append(ms)
+    dom_name, dom_amount, bound = w.dominant()
+    roofline = None
+    if dom_name in per_kernel:
+        durs = per_kernel[dom_name]
+        if w.name == "mla":
+            c = w.cfg
+            f1 = 2.0 * c["T"] * c["N1"] * c["K"]
+            f2 = 2.0 * c["T"] * c["N2"] * c["N1"]
+            dom_amount = (f1 + f2) / 2.0  # mean per launch over the two stages
+        avg_s = statistics.mean(durs) / 1e3
+        if bound == "hbm":
+            achieved, peak, punit = dom_amount / avg_s / 1e9, peaks["hbm"], "GB/s"
+        else:
+            achieved, peak, punit = dom_amount / avg_s / 1e12, peaks["bf16"], "TFLOP/s"
+        roofline = {"bound": bound, "kernel": dom_name, "achieved": achieved, "peak": peak,
+                    "peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
+                    "unit": punit, "frac": achieved / peak, "traffic": None,
+                    "avg_launch_ms": statistics.mean(durs)}
+    kernels = {k: {"launches": len(v), "total_ms": sum(v), "avg_ms": statistics.mean(v)}
+               for k, v in per_kernel.items()}
+    gpu_launches = len(trace)
+
+    # end to end: pinned host inputs -> device -> C call -> result back to host
+    e2e = None
+    if not args.no_e2e:
+        host_in = {}
+        for k, v in w.d.items():
+            if v is not None:
+                host_in[k] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                host_in[k].copy_(v)
+        host_out = torch.empty(w.out.shape, dtype=w.out.dtype, pin_memory=True)
+        dev_in = {k: (torch.empty_like(v) if v is not None else None) for k, v in w.d.items()}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+        n_e2e = max(3, min(args.steps, 50))
+        for i in range(n_e2e + 2):
+            if i == 2:
+                torch.cuda.synchronize()
+                te0 = time.perf_counter()
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            w.call(d=dev_in)
+            host_out.copy_(w.out, non_blocking=True)
+            torch.cuda.current_stream(device).synchronize()
+        te = (time.perf_counter() - te0) / n_e2e
+        e2e = {"value": world * amount / te, "unit": unit, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": te * 1e3}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu and not args.T:
+        v, u, cores, sample, rows, ref_out, _ = oracle_sample(args.workload, target_s=args.cpu_seconds)
+        got = w.out.cpu()
+        got = got.view(torch.int16).numpy().view(np.uint16) if got.dtype == torch.bfloat16 else got.numpy()
+        import oracle as orc_mod
+        if got.dtype == np.uint16:
+            g, o = orc_mod.bf16_bits_to_f64(got[rows]), orc_mod.bf16_bits_to_f64(ref_out)
+            parity = bool(np.all(np.abs(g - o) <= 1e-2 * np.maximum(1.0, np.abs(o))))
+        else:
+            g, o = got[rows].astype(np.float64), ref_out.astype(np.float64)
+            parity = bool(np.all(np.abs(g - o) <= 1e-3 * np.maximum(1.0, np.abs(o))))
+        cpu = {"value": v, "unit": u, "cores": cores, "kind": "oracle", "sample": sample,
+               "parity_on_sample": parity, "max_abs_diff": float(np.abs(g - o).max())}
+
+    if rank == 0:
+        c = w.cfg
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "u8/i32" if w.name == "w8a8" else "bf16",
+            "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": w.name, **{k: v for k, v in c.items() if k != "seed"},
+                       "l2": "flushed between timed steps (256 MB write outside the step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+            "clocks": clocks, "kernels": kernels,
+            "wall_s_timed_region": t1 - t0,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", choices=WORKLOADS, default="qkv")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--T", type=int, default=None,
+                    help="override the number of token rows (profiling captures of a smaller case)")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload] if args.impl == "ours" else 5
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,181 @@
+/*
+ * rnl.h -- C ABI of librnl: the fused RMSNorm -> Linear projection on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (sources are the web pages this method is described on):
+ *
+ *   AT-03 RMSNorm, per token row x[t, 0..K):
+ *       "PyPTO-Gym operator design pattern AT-10: RMSNorm + Linear fusion"
+ *       page, sec. 3 "V stage: the two RMSNorm variants".  FP32 throughout:
+ *       ms = mean of x^2; rsqrt form:  rstd = rsqrt(ms + eps);
+ *                         sqrt+div form: rstd = 1 / sqrt(ms + eps)
+ *       (the 1/K factor applied to each square before the sum);
+ *       y = (x * rstd) * gamma   (gamma optional).
+ *   AT-10 RMSNorm + Linear (same page, sec. 2 "standard compute flow" and
+ *       sec. 4 "C stage", BF16 mode): a = bf16(y);
+ *       out[t, n] = bf16(sum_k a[t, k] * W[n, k]), W stored [N, K]
+ *       (b_trans = True), fp32 accumulation.
+ *   mhc_pre skinny form (same page, sec. 8; "SK-03 Linear Projection
+ *       (Norm->MatMul)" page, "shape variant: huge reduction x tiny output
+ *       width"): no gamma, FP32 compute, FP32 output:
+ *       out[t, n] = fp32(sum_k y[t, k] * W[n, k]).
+ *   AT-11 RMSNorm + Linear + Quant (AT-10 page sec. 4, INT8 W8A8 mode; SK-03
+ *       page, "quantised variant (AT-11)"): per-token symmetric INT8 codes
+ *       q = sat(rint_half_even(y * 127 / amax)), amax = max_k |y[t, k]|,
+ *       x_scale = amax / 127; exact int32 acc = sum_k q[t, k] * Wq[n, k];
+ *       out = bf16(float(acc) * (x_scale[t] * w_scale[n])) (dequant order of
+ *       the "SK-14 general multi-MatMul skeleton" page, QuantMatMulReduceSum).
+ *   MLA q chain (AT-10 page, sec. 5 "MLAProlog" and sec. 9 golden chain):
+ *       qa = bf16(x @ W_qa^T); z = bf16(RMSNorm(qa) * gamma_cq);
+ *       out = bf16(z @ W_qb^T).
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer of the current CUDA device,
+ *     contiguous and row-major, owned by the caller.  The library allocates
+ *     no device memory: scratch space comes from the caller's `workspace`,
+ *     sized by rnl_workspace_size().
+ *   - bf16 data are passed as `const void*` (IEEE bfloat16 bit patterns).
+ *   - Base pointers (tensors and workspace) must be 16-byte aligned; K must
+ *     be a multiple of 8 (bf16 rows) -- the TMA copy engine moves rows whose
+ *     pitch is a multiple of 16 bytes.  T and N are arbitrary (tails are
+ *     handled).  T == 0 is a no-op.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  Argument errors are returned before anything is enqueued.
+ *     RNL_ERR_LAUNCH reports a CUDA launch error.  A kernel that gives up on
+ *     a wait (a bug, never expected) records it in a device error word that
+ *     rnl_check_device_error() reads.
+ *   - Calls on the same stream are ordered; calls that share a workspace
+ *     must not overlap on the GPU.
+ */
+#ifndef RNL_H
+#define RNL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream).  NULL = default stream. */
+typedef struct CUstream_st *rnl_stream_t;
+
+typedef enum rnl_status {
+  RNL_OK = 0,
+  RNL_ERR_NULL = 1,        /* a required pointer is NULL */
+  RNL_ERR_SHAPE = 2,       /* a size is negative, zero where not allowed, or too large */
+  RNL_ERR_ALIGN = 3,       /* a pointer or K violates the 16-byte rule */
+  RNL_ERR_ARG = 4,         /* bad mode / dtype value, or eps not finite or negative */
+  RNL_ERR_WORKSPACE = 5,   /* workspace smaller than rnl_workspace_size() */
+  RNL_ERR_LAUNCH = 6,      /* CUDA returned an error when launching */
+  RNL_ERR_TIMEOUT = 7,     /* a kernel gave up waiting (device error word set) */
+  RNL_ERR_UNSUPPORTED = 8, /* argument combination the library does not provide */
+  RNL_ERR_DEVICE = 9       /* no sm_103 device current, or a driver entry point missing */
+} rnl_status;
+
+/* AT-03 rsqrt_mode */
+enum { RNL_NORM_RSQRT = 0, RNL_NORM_SQRT_DIV = 1 };
+/* AT-09 out_dtype */
+enum { RNL_OUT_BF16 = 0, RNL_OUT_FP32 = 1 };
+/* operation ids for rnl_workspace_size */
+enum { RNL_OP_BF16 = 0, RNL_OP_W8A8 = 1, RNL_OP_MLA = 2, RNL_OP_GEMM_S8 = 3 };
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int rnl_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *rnl_status_string(rnl_status s);
+
+/*
+ * Bytes of workspace an operation needs for the given sizes (0 is possible).
+ *   RNL_OP_BF16:    T, K, N; N2 = out_dtype (RNL_OUT_BF16 / RNL_OUT_FP32)
+ *   RNL_OP_W8A8:    T, K, N; N2 ignored
+ *   RNL_OP_MLA:     T, K, N = N1, N2
+ *   RNL_OP_GEMM_S8: T = M, K, N; N2 ignored
+ * Returns (size_t)-1 for invalid sizes.  Host-only; needs no GPU.
+ */
+size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
+
+/*
+ * AT-10 RMSNorm + Linear, or (out_dtype = RNL_OUT_FP32) the mhc_pre FP32 form.
+ *   x      bf16 [T, K]          activations
+ *   gamma  bf16 [K] or NULL     has_gamma = (gamma != NULL); must be NULL
+ *                               with RNL_OUT_FP32 (the mhc_pre form has no
+ *                               gamma), else RNL_ERR_UNSUPPORTED
+ *   W      bf16 [N, K]          weight, K contiguous (b_trans = True)
+ *   eps    >= 0, finite
+ *   norm_mode  RNL_NORM_RSQRT or RNL_NORM_SQRT_DIV
+ *   out    bf16 [T, N] (RNL_OUT_BF16) or fp32 [T, N] (RNL_OUT_FP32)
+ * Kernels: bf16 out -> row-norm/cast pass then the tcgen05 GEMM;
+ * fp32 out with N <= 64 -> the split-K streaming kernel (one read of x);
+ * fp32 out with N > 64 -> row rstd pass then the GEMM with a row-scale
+ * epilogue.
+ */
+rnl_status rmsnorm_linear_bf16(const void *x, const void *gamma, const void *W, int64_t T,
+                               int64_t K, int64_t N, float eps, int norm_mode, void *out,
+                               int out_dtype, void *workspace, size_t workspace_bytes,
+                               rnl_stream_t stream);
+
+/*
+ * AT-11 RMSNorm + per-token INT8 quant + exact INT8 x INT8 -> INT32 matmul +
+ * FP32 dequant, BF16 out.
+ *   x        bf16 [T, K];  gamma bf16 [K] or NULL
+ *   Wq       int8 [N, K] with values in [-127, 127];  K % 16 == 0
+ *   w_scale  fp32 [N]     per-output-channel weight scale
+ *   out      bf16 [T, N]
+ *   q_out        optional int8 [T, K]: the activation codes (NULL = not written)
+ *   x_scale_out  optional fp32 [T]: amax / 127 per row (NULL = not written)
+ * The integer accumulation is exact for every input (chunks of at most 1024
+ * products are summed exactly on the tensor pipe, then added in int32);
+ * a sum outside the int32 range wraps as two's complement (impossible for
+ * K <= 133144).
+ */
+rnl_status rmsnorm_linear_w8a8(const void *x, const void *gamma, const int8_t *Wq,
+                               const float *w_scale, int64_t T, int64_t K, int64_t N, float eps,
+                               int norm_mode, void *out, int8_t *q_out, float *x_scale_out,
+                               void *workspace, size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * MLA two-stage q chain.
+ *   x bf16 [T, K];  W_qa bf16 [N1, K];  gamma_cq bf16 [N1];  W_qb bf16 [N2, N1]
+ *   out bf16 [T, N2];  qa_out optional bf16 [T, N1] (the stage-1 output)
+ *   N1 % 8 == 0.  norm_mode as above (the pages' MLAProlog uses sqrt+div).
+ */
+rnl_status mla_q_chain(const void *x, const void *W_qa, const void *gamma_cq, const void *W_qb,
+                       int64_t T, int64_t K, int64_t N1, int64_t N2, float eps, int norm_mode,
+                       void *out, void *qa_out, void *workspace, size_t workspace_bytes,
+                       rnl_stream_t stream);
+
+/*
+ * The exact integer matmul of the W8A8 path on its own (AT-09 INT8 mode):
+ * C[m, n] = sum_k A[m, k] * B[n, k], int8 inputs in [-127, 127], int32 out
+ * [M, N].  K % 16 == 0.  Used to check bit-exactness against a reference.
+ */
+rnl_status rnl_gemm_s8s8s32(const int8_t *A, const int8_t *B, int32_t *C, int64_t M, int64_t N,
+                            int64_t K, void *workspace, size_t workspace_bytes,
+                            rnl_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error words of
+ * every kernel module.  RNL_OK if no kernel gave up on a wait,
+ * RNL_ERR_TIMEOUT otherwise (*site, if not NULL, receives the first
+ * recorded wait site), RNL_ERR_LAUNCH if the synchronisation itself failed.
+ */
+rnl_status rnl_check_device_error(rnl_stream_t stream, int *site);
+
+/*
+ * Kernel timing trace.  While enabled, every kernel launch made by the
+ * library is bracketed by two CUDA events recorded on the launch stream
+ * (up to 16384 launches between reads).  rnl_trace_read() waits for the recorded
+ * events, copies up to `max` records (name, milliseconds) in launch order
+ * and clears the ring; it returns the number copied.  names receives
+ * 32-byte NUL-terminated strings.  Host bookkeeping only; not thread-safe.
+ */
+rnl_status rnl_trace_enable(int on);
+int rnl_trace_read(char (*names)[32], float *ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RNL_H */

@@ -1,0 +1,32 @@
+"""Fused RMSNorm -> Linear projection for one GB300 (sm_103a).
+
+Python binding of the C library ``librnl.so`` (header ``include/rnl.h``).
+The functions carry the names of the C entry points and only marshal
+arguments; the computation runs in the library's CUDA kernels.
+
+    rmsnorm_linear_bf16   AT-10 RMSNorm + Linear (bf16 out) / mhc_pre FP32 form
+    rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
+    mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
+    rnl_gemm_s8s8s32      the exact INT8 matmul on its own
+"""
+from ._native import (  # noqa: F401
+    EXPORTS,
+    NORM_RSQRT,
+    NORM_SQRT_DIV,
+    OP_BF16,
+    OP_GEMM_S8,
+    OP_MLA,
+    OP_W8A8,
+    OUT_BF16,
+    OUT_FP32,
+    RnlError,
+    load,
+    mla_q_chain,
+    rmsnorm_linear_bf16,
+    rmsnorm_linear_w8a8,
+    rnl_check_device_error,
+    rnl_gemm_s8s8s32,
+    rnl_trace_enable,
+    rnl_trace_read,
+    workspace_size,
+)

@@ -1,0 +1,230 @@
+"""ctypes binding of librnl.so (include/rnl.h).
+
+Argument marshalling only: tensors are checked for device, dtype and
+layout, outputs and workspace are allocated with torch when the caller
+passes none, and the raw pointers plus the current CUDA stream are handed to
+the C entry point of the same name.  Every step of the computation runs in
+the library's CUDA kernels; there is no other code path.  If the library
+has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "librnl.so")
+
+NORM_RSQRT, NORM_SQRT_DIV = 0, 1
+OUT_BF16, OUT_FP32 = 0, 1
+OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8 = 0, 1, 2, 3
+
+STATUS = {
+    0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
+    5: "RNL_ERR_WORKSPACE", 6: "RNL_ERR_LAUNCH", 7: "RNL_ERR_TIMEOUT", 8: "RNL_ERR_UNSUPPORTED",
+    9: "RNL_ERR_DEVICE",
+}
+
+EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
+           "rmsnorm_linear_w8a8", "mla_q_chain", "rnl_gemm_s8s8s32", "rnl_check_device_error",
+           "rnl_trace_enable", "rnl_trace_read")
+
+
+class RnlError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    P, I64, F, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "rnl_version": (I, []),
+        "rnl_status_string": (ctypes.c_char_p, [I]),
+        "rnl_workspace_size": (SZ, [I, I64, I64, I64, I64]),
+        "rmsnorm_linear_bf16": (I, [P, P, P, I64, I64, I64, F, I, P, I, P, SZ, P]),
+        "rmsnorm_linear_w8a8": (I, [P, P, P, P, I64, I64, I64, F, I, P, P, P, P, SZ, P]),
+        "mla_q_chain": (I, [P, P, P, P, I64, I64, I64, I64, F, I, P, P, P, SZ, P]),
+        "rnl_gemm_s8s8s32": (I, [P, P, P, I64, I64, I64, P, SZ, P]),
+        "rnl_check_device_error": (I, [P, ctypes.POINTER(I)]),
+        "rnl_trace_enable": (I, [I]),
+        "rnl_trace_read": (I, [P, ctypes.POINTER(F), I]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def load(path: str | None = None):
+    """Load librnl.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with "
+                                   "`python -m rmsnorm_linear_projection_gb300.build`")
+            lib = _declare(ctypes.CDLL(p))
+            if path is not None:
+                return lib
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        raise RnlError(status, what)
+
+
+def _need(t, name, dtype, shape, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def workspace_size(op: int, T: int, K: int, N: int, N2: int = 0) -> int:
+    v = load().rnl_workspace_size(op, T, K, N, N2)
+    if v == ctypes.c_size_t(-1).value:
+        raise RnlError(2, "rnl_workspace_size")
+    return int(v)
+
+
+def _workspace(nbytes, device, given):
+    if given is not None:
+        return given
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def rmsnorm_linear_bf16(x, gamma, W, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
+                        out_dtype=OUT_BF16, workspace=None, stream=None):
+    """AT-10 RMSNorm + Linear (bf16 out), or the mhc_pre FP32 form (fp32 out)."""
+    T, K = x.shape
+    N = W.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W, "W", torch.bfloat16, (N, K), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (K,), dev)
+    odt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+    if out is None:
+        out = torch.empty((T, N), dtype=odt, device=dev)
+    _need(out, "out", odt, (T, N), dev)
+    ws = _workspace(workspace_size(OP_BF16, T, K, N, out_dtype), dev, workspace)
+    _check(load().rmsnorm_linear_bf16(_ptr(x), _ptr(gamma), _ptr(W), T, K, N, float(eps),
+                                      int(norm_mode), _ptr(out), int(out_dtype), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "rmsnorm_linear_bf16")
+    return out
+
+
+def rmsnorm_linear_w8a8(x, gamma, Wq, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
+                        q_out=None, x_scale_out=None, workspace=None, stream=None):
+    """AT-11 RMSNorm + per-token INT8 quant + exact INT8 matmul + dequant (bf16 out)."""
+    T, K = x.shape
+    N = Wq.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(Wq, "Wq", torch.int8, (N, K), dev)
+    _need(w_scale, "w_scale", torch.float32, (N,), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (K,), dev)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, N), dev)
+    if q_out is not None:
+        _need(q_out, "q_out", torch.int8, (T, K), dev)
+    if x_scale_out is not None:
+        _need(x_scale_out, "x_scale_out", torch.float32, (T,), dev)
+    ws = _workspace(workspace_size(OP_W8A8, T, K, N), dev, workspace)
+    _check(load().rmsnorm_linear_w8a8(_ptr(x), _ptr(gamma), _ptr(Wq), _ptr(w_scale), T, K, N,
+                                      float(eps), int(norm_mode), _ptr(out), _ptr(q_out),
+                                      _ptr(x_scale_out), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(dev, stream)),
+           "rmsnorm_linear_w8a8")
+    return out
+
+
+def mla_q_chain(x, W_qa, gamma_cq, W_qb, eps=1e-6, norm_mode=NORM_SQRT_DIV, out=None,
+                qa_out=None, workspace=None, stream=None):
+    """MLA two-stage q chain: q_a projection -> RMSNorm * gamma_cq -> q_b projection."""
+    T, K = x.shape
+    N1, N2 = W_qa.shape[0], W_qb.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W_qa, "W_qa", torch.bfloat16, (N1, K), dev)
+    _need(gamma_cq, "gamma_cq", torch.bfloat16, (N1,), dev)
+    _need(W_qb, "W_qb", torch.bfloat16, (N2, N1), dev)
+    if out is None:
+        out = torch.empty((T, N2), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, N2), dev)
+    if qa_out is not None:
+        _need(qa_out, "qa_out", torch.bfloat16, (T, N1), dev)
+    ws = _workspace(workspace_size(OP_MLA, T, K, N1, N2), dev, workspace)
+    _check(load().mla_q_chain(_ptr(x), _ptr(W_qa), _ptr(gamma_cq), _ptr(W_qb), T, K, N1, N2,
+                              float(eps), int(norm_mode), _ptr(out), _ptr(qa_out), _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "mla_q_chain")
+    return out
+
+
+def rnl_gemm_s8s8s32(A, B, out=None, workspace=None, stream=None):
+    """Exact int8 x int8 -> int32 matmul C = A @ B^T (the W8A8 matmul on its own)."""
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    _need(A, "A", torch.int8, (M, K), dev)
+    _need(B, "B", torch.int8, (N, K), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    _need(out, "C", torch.int32, (M, N), dev)
+    ws = _workspace(workspace_size(OP_GEMM_S8, M, K, N), dev, workspace)
+    _check(load().rnl_gemm_s8s8s32(_ptr(A), _ptr(B), _ptr(out), M, N, K, _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "rnl_gemm_s8s8s32")
+    return out
+
+
+def rnl_check_device_error(stream=None, device=None):
+    """Synchronise and read the device error words; raises RnlError on a timeout."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    site = ctypes.c_int(0)
+    st = load().rnl_check_device_error(_stream(dev, stream), ctypes.byref(site))
+    if st != 0:
+        raise RnlError(st, f"device error (wait site {site.value})")
+
+
+def rnl_trace_enable(on: bool = True):
+    _check(load().rnl_trace_enable(1 if on else 0), "rnl_trace_enable")
+
+
+def rnl_trace_read(max_records: int = 16384):
+    """[(kernel name, milliseconds)] of the launches traced since the last read."""
+    names = (ctypes.c_char * 32 * max_records)()
+    ms = (ctypes.c_float * max_records)()
+    n = load().rnl_trace_read(ctypes.cast(names, ctypes.c_void_p), ms, max_records)
+    return [(bytes(names[i]).split(b"\0", 1)[0].decode(), float(ms[i])) for i in range(n)]

@@ -1,0 +1,450 @@
+// api.cu -- the C ABI declared in include/rnl.h: argument validation,
+// workspace layout, kernel selection by shape, TMA descriptor encoding,
+// device error words and the kernel timing trace.  Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace rnl {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+
+// ------------------------------------------------------------ device info
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// ------------------------------------------------------------ TMA encoding
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// ------------------------------------------------------------ trace ring
+constexpr int kTraceCap = 16384;
+struct TraceRec {
+  cudaEvent_t a = nullptr, b = nullptr;
+  char name[32] = {0};
+};
+bool g_trace_on = false;
+TraceRec g_trace[kTraceCap];
+int g_trace_n = 0;
+bool g_trace_pending = false;
+
+// ------------------------------------------------------------ validation
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool bad_eps(float eps) { return !std::isfinite(eps) || eps < 0.f; }
+inline bool bad_mode(int m) { return m != RNL_NORM_RSQRT && m != RNL_NORM_SQRT_DIV; }
+// sizes must stay inside int32 tile / TMA coordinate arithmetic
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+inline bool bad_dim(int64_t v) { return v < 0 || v > kMaxDim; }
+
+struct Carve {
+  char* p;
+  size_t used = 0;
+  explicit Carve(void* base) : p(static_cast<char*>(base)) {}
+  void* take(size_t bytes) {
+    void* r = p ? p + used : nullptr;
+    used += round_up(bytes);
+    return r;
+  }
+};
+
+// Workspace layouts (a null base just measures).
+struct BF16Layout {
+  void* A = nullptr;      // bf16 [T, K] normed activations (bf16 out)
+  float* rstd = nullptr;  // [T] (fp32 out, N > 64)
+  void* part = nullptr;   // skinny partials (fp32 out, N <= 64)
+  size_t bytes = 0;
+};
+BF16Layout bf16_layout(void* ws, int64_t T, int64_t K, int64_t N, int out_dtype) {
+  BF16Layout l;
+  Carve c(ws);
+  if (out_dtype == RNL_OUT_BF16) {
+    l.A = c.take(static_cast<size_t>(T) * K * 2);
+  } else if (N <= 64) {
+    l.part = c.take(skinny_workspace_bytes(T, K, N, 0));
+  } else {
+    l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  }
+  l.bytes = c.used;
+  return l;
+}
+
+struct W8A8Layout {
+  void* A = nullptr;        // bf16 [T, K] integer codes
+  void* Wb = nullptr;       // bf16 [N, K] widened weight
+  float* xs = nullptr;      // [T] x_scale when the caller passes none
+  size_t bytes = 0;
+};
+W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
+  W8A8Layout l;
+  Carve c(ws);
+  l.A = c.take(static_cast<size_t>(T) * K * 2);
+  l.Wb = c.take(static_cast<size_t>(N) * K * 2);
+  l.xs = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.bytes = c.used;
+  return l;
+}
+
+struct MLALayout {
+  void* qa = nullptr;  // bf16 [T, N1] stage-1 output when the caller passes none
+  void* z = nullptr;   // bf16 [T, N1] normed * gamma_cq
+  size_t bytes = 0;
+};
+MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
+  MLALayout l;
+  Carve c(ws);
+  l.qa = c.take(static_cast<size_t>(T) * N1 * 2);
+  l.z = c.take(static_cast<size_t>(T) * N1 * 2);
+  l.bytes = c.used;
+  return l;
+}
+
+struct S8Layout {
+  void* A = nullptr;
+  void* B = nullptr;
+  size_t bytes = 0;
+};
+S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
+  S8Layout l;
+  Carve c(ws);
+  l.A = c.take(static_cast<size_t>(M) * K * 2);
+  l.B = c.take(static_cast<size_t>(N) * K * 2);
+  l.bytes = c.used;
+  return l;
+}
+
+inline cudaStream_t cs(rnl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+// ------------------------------------------------------------ shared helpers
+rnl_status current_device(DeviceInfo* info) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return RNL_ERR_DEVICE;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.device < 0) {
+    DeviceInfo n;
+    n.device = dev;
+    if (cudaDeviceGetAttribute(&n.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return RNL_ERR_DEVICE;
+    }
+    if (n.major != 10 || n.minor != 3) return RNL_ERR_DEVICE;  // built for sm_103a only
+    d = n;
+  }
+  *info = d;
+  return RNL_OK;
+}
+
+rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                       uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return RNL_ERR_DEVICE;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RNL_OK : RNL_ERR_ARG;
+}
+
+void trace_before(cudaStream_t s) {
+  if (!g_trace_on || g_trace_n >= kTraceCap) return;
+  TraceRec& t = g_trace[g_trace_n];
+  if (t.a == nullptr) {
+    cudaEventCreate(&t.a);
+    cudaEventCreate(&t.b);
+  }
+  cudaEventRecord(t.a, s);
+  g_trace_pending = true;
+}
+
+void trace_after(cudaStream_t s, const char* name) {
+  if (!g_trace_on || !g_trace_pending || g_trace_n >= kTraceCap) return;
+  TraceRec& t = g_trace[g_trace_n];
+  cudaEventRecord(t.b, s);
+  std::snprintf(t.name, sizeof t.name, "%s", name);
+  ++g_trace_n;
+  g_trace_pending = false;
+}
+
+}  // namespace rnl
+
+using namespace rnl;
+
+extern "C" {
+
+int rnl_version(void) { return 100; }
+
+const char* rnl_status_string(rnl_status s) {
+  switch (s) {
+    case RNL_OK: return "ok";
+    case RNL_ERR_NULL: return "null pointer";
+    case RNL_ERR_SHAPE: return "bad shape";
+    case RNL_ERR_ALIGN: return "misaligned pointer or K";
+    case RNL_ERR_ARG: return "bad argument";
+    case RNL_ERR_WORKSPACE: return "workspace too small";
+    case RNL_ERR_LAUNCH: return "CUDA launch error";
+    case RNL_ERR_TIMEOUT: return "device wait timed out";
+    case RNL_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case RNL_ERR_DEVICE: return "no sm_103 device or driver entry point";
+  }
+  return "unknown status";
+}
+
+size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || bad_dim(N2)) return static_cast<size_t>(-1);
+  switch (op) {
+    case RNL_OP_BF16:
+      if (N2 != RNL_OUT_BF16 && N2 != RNL_OUT_FP32) return static_cast<size_t>(-1);
+      return bf16_layout(nullptr, T, K, N, static_cast<int>(N2)).bytes;
+    case RNL_OP_W8A8: return w8a8_layout(nullptr, T, K, N).bytes;
+    case RNL_OP_MLA: return mla_layout(nullptr, T, N).bytes;
+    case RNL_OP_GEMM_S8: return s8_layout(nullptr, T, K, N).bytes;
+  }
+  return static_cast<size_t>(-1);
+}
+
+rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, int64_t T,
+                               int64_t K, int64_t N, float eps, int norm_mode, void* out,
+                               int out_dtype, void* workspace, size_t workspace_bytes,
+                               rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps) ||
+      (out_dtype != RNL_OUT_BF16 && out_dtype != RNL_OUT_FP32))
+    return RNL_ERR_ARG;
+  if (out_dtype == RNL_OUT_FP32 && gamma != nullptr) return RNL_ERR_UNSUPPORTED;
+  if (T == 0) return RNL_OK;
+  if (!x || !W || !out) return RNL_ERR_NULL;
+  if (K % 8 != 0 || !aligned16(x) || !aligned16(W) || !aligned16(out) ||
+      (gamma && !aligned16(gamma)) || (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const BF16Layout need = bf16_layout(nullptr, T, K, N, out_dtype);
+  if (need.bytes > 0 && (!workspace || workspace_bytes < need.bytes)) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const BF16Layout l = bf16_layout(workspace, T, K, N, out_dtype);
+  cudaStream_t s = cs(stream);
+
+  if (out_dtype == RNL_OUT_BF16) {
+    st = launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
+    if (st != RNL_OK) return st;
+    GemmArgs g;
+    g.A = l.A;
+    g.B = W;
+    g.M = T;
+    g.N = N;
+    g.K = K;
+    g.out = out;
+    g.epi = Epi::kBf16;
+    return launch_gemm(g, s);
+  }
+  if (N <= 64)
+    return launch_skinny(x, W, T, K, N, eps, norm_mode, static_cast<float*>(out), l.part,
+                         workspace_bytes, dev.sm_count, s);
+  st = launch_row_rstd(x, T, K, eps, norm_mode, l.rstd, s);
+  if (st != RNL_OK) return st;
+  GemmArgs g;
+  g.A = x;
+  g.B = W;
+  g.M = T;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.row_scale = l.rstd;
+  g.epi = Epi::kRowScaleF32;
+  return launch_gemm(g, s);
+}
+
+rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* Wq,
+                               const float* w_scale, int64_t T, int64_t K, int64_t N, float eps,
+                               int norm_mode, void* out, int8_t* q_out, float* x_scale_out,
+                               void* workspace, size_t workspace_bytes, rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps)) return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!x || !Wq || !w_scale || !out) return RNL_ERR_NULL;
+  if (K % 16 != 0 || !aligned16(x) || !aligned16(Wq) || !aligned16(out) ||
+      (gamma && !aligned16(gamma)) || (q_out && !aligned16(q_out)) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const W8A8Layout need = w8a8_layout(nullptr, T, K, N);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const W8A8Layout l = w8a8_layout(workspace, T, K, N);
+  cudaStream_t s = cs(stream);
+  float* xs = x_scale_out ? x_scale_out : l.xs;
+  st = launch_norm_quant(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
+  if (st != RNL_OK) return st;
+  st = launch_s8_to_bf16(Wq, N * K, l.Wb, s);
+  if (st != RNL_OK) return st;
+  GemmArgs g;
+  g.A = l.A;
+  g.B = l.Wb;
+  g.M = T;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.row_scale = xs;
+  g.col_scale = w_scale;
+  g.epi = Epi::kDequantBf16;
+  return launch_gemm(g, s);
+}
+
+rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, const void* W_qb,
+                       int64_t T, int64_t K, int64_t N1, int64_t N2, float eps, int norm_mode,
+                       void* out, void* qa_out, void* workspace, size_t workspace_bytes,
+                       rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N1) || bad_dim(N2) || K == 0 || N1 == 0 || N2 == 0)
+    return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps)) return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!x || !W_qa || !gamma_cq || !W_qb || !out) return RNL_ERR_NULL;
+  if (K % 8 != 0 || N1 % 8 != 0 || !aligned16(x) || !aligned16(W_qa) || !aligned16(gamma_cq) ||
+      !aligned16(W_qb) || !aligned16(out) || (qa_out && !aligned16(qa_out)) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const MLALayout need = mla_layout(nullptr, T, N1);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const MLALayout l = mla_layout(workspace, T, N1);
+  cudaStream_t s = cs(stream);
+  void* qa = qa_out ? qa_out : l.qa;
+  GemmArgs g1;
+  g1.A = x;
+  g1.B = W_qa;
+  g1.M = T;
+  g1.N = N1;
+  g1.K = K;
+  g1.out = qa;
+  g1.epi = Epi::kBf16;
+  st = launch_gemm(g1, s);
+  if (st != RNL_OK) return st;
+  st = launch_norm_cast(qa, gamma_cq, T, N1, eps, norm_mode, l.z, nullptr, s);
+  if (st != RNL_OK) return st;
+  GemmArgs g2;
+  g2.A = l.z;
+  g2.B = W_qb;
+  g2.M = T;
+  g2.N = N2;
+  g2.K = N1;
+  g2.out = out;
+  g2.epi = Epi::kBf16;
+  return launch_gemm(g2, s);
+}
+
+rnl_status rnl_gemm_s8s8s32(const int8_t* A, const int8_t* B, int32_t* C, int64_t M, int64_t N,
+                            int64_t K, void* workspace, size_t workspace_bytes,
+                            rnl_stream_t stream) {
+  if (bad_dim(M) || bad_dim(N) || bad_dim(K) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (M == 0) return RNL_OK;
+  if (!A || !B || !C) return RNL_ERR_NULL;
+  if (K % 16 != 0 || !aligned16(A) || !aligned16(B) || !aligned16(C) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const S8Layout need = s8_layout(nullptr, M, K, N);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const S8Layout l = s8_layout(workspace, M, K, N);
+  cudaStream_t s = cs(stream);
+  st = launch_s8_to_bf16(A, M * K, l.A, s);
+  if (st != RNL_OK) return st;
+  st = launch_s8_to_bf16(B, N * K, l.B, s);
+  if (st != RNL_OK) return st;
+  GemmArgs g;
+  g.A = l.A;
+  g.B = l.B;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = C;
+  g.epi = Epi::kInt32;
+  return launch_gemm(g, s);
+}
+
+rnl_status rnl_check_device_error(rnl_stream_t stream, int* site) {
+  if (cudaStreamSynchronize(cs(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return RNL_ERR_LAUNCH;
+  }
+  unsigned int words[3] = {0, 0, 0};
+  if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
+      read_clear_error_skinny(&words[2]) != RNL_OK)
+    return RNL_ERR_LAUNCH;
+  for (unsigned int w : words) {
+    if (w != 0) {
+      if (site) *site = static_cast<int>((w >> 8) & 0xFFu);
+      return RNL_ERR_TIMEOUT;
+    }
+  }
+  if (site) *site = 0;
+  return RNL_OK;
+}
+
+rnl_status rnl_trace_enable(int on) {
+  g_trace_on = on != 0;
+  if (!g_trace_on) g_trace_pending = false;
+  return RNL_OK;
+}
+
+int rnl_trace_read(char (*names)[32], float* ms, int max) {
+  int n = g_trace_n < max ? g_trace_n : max;
+  for (int i = 0; i < n; ++i) {
+    TraceRec& t = g_trace[i];
+    float v = -1.f;
+    if (cudaEventSynchronize(t.b) == cudaSuccess && cudaEventElapsedTime(&v, t.a, t.b) == cudaSuccess) {
+      ms[i] = v;
+    } else {
+      cudaGetLastError();
+      ms[i] = -1.f;
+    }
+    if (names) std::memcpy(names[i], t.name, 32);
+  }
+  g_trace_n = 0;
+  g_trace_pending = false;
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,390 @@
+// gemm_tc.cu -- the C stage: out = epilogue(A[M,K] @ B[N,K]^T) on the
+// 5th-generation tensor cores (tcgen05), AT-09 "Linear" of the AT-10 pattern
+// page (sec. 4: matmul(x, w, dtype, b_trans=True), W stored [N, K]).
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer: 128x64 A tile and 256x64 B tile per stage
+//               (128-byte swizzle), 4-stage ring of 48 KB stages.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and one thread issues tcgen05.mma (M=128, N=256, K=16).
+//   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp one 32-lane
+//               quarter x 128 columns), convert, store to global memory.
+// Both operands are K-major, the layout the MMA reads directly, so the
+// weight needs no transpose (the pages pre-transpose it on the host for the
+// same reason).  The two accumulators let the epilogue of tile i overlap the
+// main loop of tile i+1.
+//
+// Exact integer mode (W8A8): A and B hold integers in [-127, 127] as bf16
+// (exact).  Every product is an integer of magnitude <= 16129 and the MMA
+// accumulates in fp32, which is exact while every partial sum stays below
+// 2^24; a chunk of 1024 products keeps |sum| <= 16,516,096 < 2^24.  So the
+// K loop is cut into chunks of 16 k-blocks (1024 products); each chunk goes
+// to its own accumulator and the epilogue converts it exactly to int32 and
+// adds it in registers.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace rnl {
+namespace {
+
+__device__ unsigned int g_err_gemm;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kChunkKBlocks = 16;  // 1024 products per exact chunk
+constexpr int kColsPerEpiWarp = BN / 2;
+constexpr int kGroups = kColsPerEpiWarp / 32;
+
+struct __align__(8) Ctrl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctrl);
+
+// Tile order: groups of 8 M-tiles, N fastest within a group column, so the
+// CTAs running at the same time share A panels and B panels in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
+  constexpr int G = 8;
+  const int group_tiles = G * num_n;
+  const int group = tile / group_tiles;
+  const int first_m = group * G;
+  const int gm = min(num_m - first_m, G);
+  const int r = tile - group * group_tiles;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, abort, &g_err_gemm, site);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                int M, int N, int K, void* __restrict__ out, const float* __restrict__ row_scale,
+                const float* __restrict__ col_scale) {
+  constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
+                         EPI == static_cast<int>(Epi::kInt32));
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + kStages * kStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (K + BK - 1) / BK;
+  const int kb_per_unit = kInt ? kChunkKBlocks : num_kb;
+  const int units_per_tile = (num_kb + kb_per_unit - 1) / kb_per_unit;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      mbar_init(smem_u32(&ctrl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);
+      mbar_init(smem_u32(&ctrl->tmem_empty[b]), kEpiWarps);
+    }
+    ctrl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctrl->tmem_base;
+  volatile int* abort = &ctrl->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      uint32_t stage = 0, phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_gemm, 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + stage * kStageBytes;
+          const uint32_t bar = smem_u32(&ctrl->full[stage]);
+          mbar_arrive_expect_tx(bar, kStageBytes);
+          tma_load_2d(sa, &map_a, bar, kb * BK, mb * BM);
+          tma_load_2d(sa + kABytes, &map_b, bar, kb * BK, nb * BN);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      uint32_t stage = 0, phase = 0, unit = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int u = 0; u < units_per_tile && ok; ++u, ++unit) {
+          const uint32_t buf = unit & 1u;
+          const uint32_t use = unit >> 1;
+          if (!mbar_wait(smem_u32(&ctrl->tmem_empty[buf]), (use & 1u) ^ 1u, abort, &g_err_gemm, 2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * BN;
+          const int kb0 = u * kb_per_unit;
+          const int kb1 = min(num_kb, kb0 + kb_per_unit);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort, &g_err_gemm, 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = base + stage * kStageBytes;
+            const uint64_t adesc = desc_kmajor_sw128(sa);
+            const uint64_t bdesc = desc_kmajor_sw128(sa + kABytes);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              // +32 bytes per 16-element K step inside the 128-byte row
+              umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                        (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(smem_u32(&ctrl->empty[stage]));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&ctrl->tmem_full[buf]));
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = ew >> 2;      // which 128 columns of the 256
+    const int row_local = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t unit = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      const int m = mb * BM + row_local;
+      const int n_base = nb * BN + half * kColsPerEpiWarp;
+      const bool row_ok = m < M;
+      float rs = 0.f;
+      if ((EPI == static_cast<int>(Epi::kRowScaleF32) || EPI == static_cast<int>(Epi::kDequantBf16)) && row_ok)
+        rs = __ldg(row_scale + m);
+      int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
+      if (kInt) {
+#pragma unroll
+        for (int c = 0; c < (kInt ? kGroups : 1); ++c)
+#pragma unroll
+          for (int j = 0; j < (kInt ? 32 : 1); ++j) iacc[c][j] = 0;
+      }
+      for (int u = 0; u < units_per_tile; ++u, ++unit) {
+        const uint32_t buf = unit & 1u;
+        const uint32_t use = unit >> 1;
+        if (!warp_wait(smem_u32(&ctrl->tmem_full[buf]), use & 1u, abort, 4)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kGroups; ++c) {
+          uint32_t r[32];
+          tmem_ld_32cols(tmem_base + lane_addr + buf * BN + half * kColsPerEpiWarp + c * 32, r);
+          tmem_ld_wait();
+          const int n0 = n_base + c * 32;
+          if constexpr (kInt) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) iacc[c][j] += __float2int_rn(__uint_as_float(r[j]));
+          } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
+            if (row_ok) {
+              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(m) * N;
+              if (n0 + 32 <= N && (N & 7) == 0) {
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]),
+                                                           __uint_as_float(r[2 * j + 1]));
+                  p[j] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(orow + n0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+              }
+            }
+          } else {  // kRowScaleF32
+            if (row_ok) {
+              float* orow = static_cast<float*>(out) + static_cast<int64_t>(m) * N;
+              if (n0 + 32 <= N && (N & 3) == 0) {
+                float4* dst = reinterpret_cast<float4*>(orow + n0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  dst[j] = make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                                       __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n0 + j < N) orow[n0 + j] = __uint_as_float(r[j]) * rs;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
+      }
+      if (!ok) break;
+      if constexpr (kInt) {
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < kGroups; ++c) {
+            const int n0 = n_base + c * 32;
+            if constexpr (EPI == static_cast<int>(Epi::kInt32)) {
+              int* orow = static_cast<int*>(out) + static_cast<int64_t>(m) * N;
+              if (n0 + 32 <= N && (N & 3) == 0) {
+                int4* dst = reinterpret_cast<int4*>(orow + n0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  dst[j] = make_int4(iacc[c][4 * j], iacc[c][4 * j + 1], iacc[c][4 * j + 2], iacc[c][4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n0 + j < N) orow[n0 + j] = iacc[c][j];
+              }
+            } else {
+              // AT-06 dequant, SK-14 skeleton page (QuantMatMulReduceSum):
+              // float(acc) * (x_scale * w_scale), then bf16.
+              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(m) * N;
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int n = n0 + j;
+                const float ws = n < N ? __ldg(col_scale + n) : 0.f;
+                v[j] = static_cast<float>(iacc[c][j]) * (rs * ws);
+              }
+              if (n0 + 32 <= N && (N & 7) == 0) {
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+                  p[j] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(orow + n0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(v[j]);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int EPI>
+rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
+  static bool attr_set[64] = {};
+  auto kern = gemm_kernel<EPI>;
+  if (dev.device < 0 || dev.device >= 64) return RNL_ERR_DEVICE;
+  if (!attr_set[dev.device]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return RNL_ERR_LAUNCH;
+    attr_set[dev.device] = true;
+  }
+  CUtensorMap ma, mb;
+  rnl_status st = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, g.K * 2, BK, BM);
+  if (st != RNL_OK) return st;
+  st = make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.B, g.K, g.N, g.K * 2, BK, BN);
+  if (st != RNL_OK) return st;
+  const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const unsigned grid = static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count);
+  trace_before(s);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, static_cast<int>(g.M), static_cast<int>(g.N),
+                                          static_cast<int>(g.K), g.out, g.row_scale, g.col_scale);
+  trace_after(s, name);
+  return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+}
+
+}  // namespace
+
+rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
+  if (g.M == 0) return RNL_OK;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  switch (g.epi) {
+    case Epi::kBf16: return launch_epi<0>(g, dev, s, "gemm_bf16");
+    case Epi::kRowScaleF32: return launch_epi<1>(g, dev, s, "gemm_rowscale_f32");
+    case Epi::kDequantBf16: return launch_epi<2>(g, dev, s, "gemm_int_dequant");
+    case Epi::kInt32: return launch_epi<3>(g, dev, s, "gemm_int_s32");
+  }
+  return RNL_ERR_ARG;
+}
+
+rnl_status read_clear_error_gemm(unsigned int* word) {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_gemm, sizeof v) != cudaSuccess) return RNL_ERR_LAUNCH;
+  if (v != 0 && cudaMemcpyToSymbol(g_err_gemm, &zero, sizeof zero) != cudaSuccess)
+    return RNL_ERR_LAUNCH;
+  *word = v;
+  return RNL_OK;
+}
+
+}  // namespace rnl

@@ -1,0 +1,81 @@
+// internal.h -- host-side interfaces between the C ABI (api.cu) and the
+// kernel modules (rowwise.cu, gemm_tc.cu, skinny.cu).  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "rnl.h"
+
+namespace rnl {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  int max_smem_optin = 0;
+};
+
+// Current device's properties (cached per device).  RNL_ERR_DEVICE if the
+// device is not a compute-capability 10.3 part.
+rnl_status current_device(DeviceInfo* info);
+
+// 2-D tensor map over a row-major matrix [outer, inner] of `elem_bytes`
+// elements with row pitch `row_bytes`; box = box_inner x box_outer elements;
+// 128-byte swizzle; out-of-range elements read as zero.
+rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                       uint32_t box_outer);
+
+// ---- kernel trace (api.cu) ----
+void trace_before(cudaStream_t s);
+void trace_after(cudaStream_t s, const char* name);
+
+// ---- row-wise kernels (rowwise.cu) ----
+// y = (x * rstd) * gamma cast to bf16 into A [T, K]; rstd_out optional.
+rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                            int mode, void* A, float* rstd_out, cudaStream_t s);
+// rstd only.
+rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int mode, float* rstd,
+                           cudaStream_t s);
+// norm + per-token symmetric int8 codes: A gets the codes as bf16 values,
+// q_out (optional) as int8, x_scale = amax / 127.
+rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                             int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
+// int8 -> bf16 (exact), n elements, n % 16 == 0.
+rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
+
+// ---- tcgen05 GEMM (gemm_tc.cu) ----
+enum class Epi : int {
+  kBf16 = 0,         // out bf16 = acc
+  kRowScaleF32 = 1,  // out fp32 = acc * row_scale[m]
+  kDequantBf16 = 2,  // out bf16 = float(exact int acc) * (row_scale[m] * col_scale[n])
+  kInt32 = 3,        // out int32 = exact int acc
+};
+
+struct GemmArgs {
+  const void* A = nullptr;  // bf16 [M, K]
+  const void* B = nullptr;  // bf16 [N, K]
+  int64_t M = 0, N = 0, K = 0;
+  void* out = nullptr;
+  const float* row_scale = nullptr;
+  const float* col_scale = nullptr;
+  Epi epi = Epi::kBf16;
+};
+rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s);
+
+// ---- skinny split-K streaming kernel (skinny.cu) ----
+size_t skinny_workspace_bytes(int64_t T, int64_t K, int64_t N, int sm_count);
+rnl_status launch_skinny(const void* x, const void* W, int64_t T, int64_t K, int64_t N, float eps,
+                         int mode, float* out, void* workspace, size_t ws_bytes, int sm_count,
+                         cudaStream_t s);
+
+// ---- device error words (one per kernel module) ----
+rnl_status read_clear_error_rowwise(unsigned int* word);
+rnl_status read_clear_error_gemm(unsigned int* word);
+rnl_status read_clear_error_skinny(unsigned int* word);
+
+}  // namespace rnl

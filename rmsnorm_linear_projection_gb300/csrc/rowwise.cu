@@ -1,0 +1,336 @@
+// rowwise.cu -- the per-token (V stage) kernels: RMSNorm statistics, the
+// normalise-and-cast pass that produces the GEMM's bf16 A operand, the
+// normalise-and-quantise pass of the W8A8 form, and the int8 -> bf16 widening
+// of operands for the exact integer GEMM.
+//
+// One warp per token row; every access to x is a 128-bit load (8 bf16), so a
+// row of K elements is read with K/8 vector loads spread over the 32 lanes.
+// Arithmetic is FP32 throughout (AT-10 pattern page, sec. 2: the RMSNorm runs
+// in FP32, then the result is cast to BF16 for the matmul).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace rnl {
+namespace {
+
+constexpr int kWarps = 8;  // rows per block
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// 8 bf16 (one 16-byte vector) -> 8 floats; element 2i is the low half of word i.
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 ldg16(const uint4* p) { return __ldg(p); }
+
+// AT-03 statistics of one row, FP32 (AT-10 pattern page, sec. 3):
+//   MODE 0, rsqrt form:    ms = (sum x^2) * (1/K);  rstd = rsqrt(ms + eps)
+//   MODE 1, sqrt+div form: ms = sum (x^2 * (1/K)); rstd = 1 / sqrt(ms + eps)
+template <int MODE>
+__device__ __forceinline__ float row_rstd(const uint4* xr, int nvec, float inv_d, float eps) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(ldg16(xr + v), f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (MODE == 0)
+        s = fmaf(f[j], f[j], s);
+      else
+        s = fmaf(f[j] * f[j], inv_d, s);
+    }
+  }
+  s = warp_sum(s);
+  if (MODE == 0) return rsqrtf(s * inv_d + eps);
+  return 1.0f / sqrtf(s + eps);
+}
+
+template <int MODE, bool GAMMA>
+__global__ void __launch_bounds__(kWarps * 32)
+    norm_cast_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                     int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                     float* __restrict__ rstd_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const uint4* xr = x + row * nvec;
+  const float rstd = row_rstd<MODE>(xr, nvec, inv_d, eps);
+  if (rstd_out != nullptr && lane == 0) rstd_out[row] = rstd;
+  uint4* ar = A + row * nvec;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(ldg16(xr + v), f);
+    if (GAMMA) {
+      float g[8];
+      unpack8(ldg16(gamma + v), g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = (f[j] * rstd) * g[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = f[j] * rstd;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(f[0], f[1]);
+    o.y = pack_bf16x2(f[2], f[3]);
+    o.z = pack_bf16x2(f[4], f[5]);
+    o.w = pack_bf16x2(f[6], f[7]);
+    ar[v] = o;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kWarps * 32)
+    row_rstd_kernel(const uint4* __restrict__ x, int64_t T, int nvec, float inv_d, float eps,
+                    float* __restrict__ rstd_out) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const float rstd = row_rstd<MODE>(x + row * nvec, nvec, inv_d, eps);
+  if ((threadIdx.x & 31) == 0) rstd_out[row] = rstd;
+}
+
+// Error-free transformation of a sum (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// rstd for the W8A8 front end, where the FP32 values decide integer codes.
+// Each term (x*x, or (x*x)*(1/K) for the sqrt+div form) is one binary32
+// product; the terms are added in float-float (hi + lo, TwoSum per term and
+// per lane merge), so the row's sum is known to about 2^-44 relative and is
+// rounded once to binary32 -- the FP32 value of the exact sum, independent of
+// the summation order.  Every later step is one correctly rounded binary32
+// operation (no fused multiply-add, no approximate reciprocal square root).
+template <int MODE>
+__device__ __forceinline__ float row_rstd_exactsum(const uint4* xr, int nvec, float inv_d,
+                                                   float eps) {
+  const int lane = threadIdx.x & 31;
+  float hi = 0.f, lo = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(ldg16(xr + v), f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float t = __fmul_rn(f[j], f[j]);
+      if (MODE == 1) t = __fmul_rn(t, inv_d);
+      float s, e;
+      two_sum(hi, t, s, e);
+      hi = s;
+      lo = __fadd_rn(lo, e);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    float s, e;
+    two_sum(hi, h2, s, e);
+    lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    hi = s;
+  }
+  const float ss = __fadd_rn(hi, lo);
+  if (MODE == 0) return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_d), eps)));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ss, eps)));
+}
+
+// AT-11 front end: RMSNorm, then AT-05 per-token symmetric INT8 codes
+// (SK-03 skeleton page, "quantised variant (AT-11)"; AT-10 page sec. 4):
+//   amax = max |y|; qs = 127 / amax; q = sat(rint(y * qs)); x_scale = amax / 127.
+// rint is round-half-even; |y * qs| <= 127 up to rounding, and the clamp to
+// [-127, 127] only removes that overshoot.  amax == 0 gives q = 0 and
+// x_scale = 0.
+template <int MODE, bool GAMMA>
+__global__ void __launch_bounds__(kWarps * 32)
+    norm_quant_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                      int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                      uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const uint4* xr = x + row * nvec;
+  const float rstd = row_rstd_exactsum<MODE>(xr, nvec, inv_d, eps);
+
+  float amax = 0.f;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(ldg16(xr + v), f);
+    float g[8];
+    if (GAMMA) unpack8(ldg16(gamma + v), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y = __fmul_rn(f[j], rstd);
+      if (GAMMA) y = __fmul_rn(y, g[j]);
+      amax = fmaxf(amax, fabsf(y));
+    }
+  }
+  amax = warp_max(amax);
+  const bool zero_row = !(amax > 0.f);
+  const float qs = zero_row ? 0.f : __fdiv_rn(127.0f, amax);
+  if (lane == 0) x_scale[row] = zero_row ? 0.f : __fdiv_rn(amax, 127.0f);
+
+  uint4* ar = A + row * nvec;
+  uint2* qr = q_out != nullptr ? q_out + row * nvec : nullptr;
+  for (int v = lane; v < nvec; v += 32) {
+    float f[8];
+    unpack8(ldg16(xr + v), f);
+    float g[8];
+    if (GAMMA) unpack8(ldg16(gamma + v), g);
+    float c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y = __fmul_rn(f[j], rstd);
+      if (GAMMA) y = __fmul_rn(y, g[j]);
+      float r = rintf(__fmul_rn(y, qs));
+      c[j] = fminf(fmaxf(r, -127.f), 127.f);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(c[0], c[1]);  // small integers are exact in bf16
+    o.y = pack_bf16x2(c[2], c[3]);
+    o.z = pack_bf16x2(c[4], c[5]);
+    o.w = pack_bf16x2(c[6], c[7]);
+    ar[v] = o;
+    if (qr != nullptr) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= (static_cast<uint32_t>(static_cast<int>(c[j])) & 0xFFu) << (8 * j);
+        hi |= (static_cast<uint32_t>(static_cast<int>(c[4 + j])) & 0xFFu) << (8 * j);
+      }
+      qr[v] = make_uint2(lo, hi);
+    }
+  }
+}
+
+// int8 -> bf16, 16 elements per thread per step.
+__global__ void __launch_bounds__(256)
+    s8_to_bf16_kernel(const uint4* __restrict__ src, int64_t nvec16, uint4* __restrict__ dst) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 u = __ldg(src + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
+      const float b = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
+      const float c = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
+      const float d = static_cast<float>(static_cast<int8_t>((w[k] >> 24) & 0xFF));
+      o[2 * k] = pack_bf16x2(a, b);
+      o[2 * k + 1] = pack_bf16x2(c, d);
+    }
+    dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+inline unsigned row_blocks(int64_t T) { return static_cast<unsigned>((T + kWarps - 1) / kWarps); }
+
+inline rnl_status launched(cudaStream_t s, const char* name) {
+  trace_after(s, name);
+  return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+}
+
+}  // namespace
+
+rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                            int mode, void* A, float* rstd_out, cudaStream_t s) {
+  if (T == 0) return RNL_OK;
+  const int nvec = static_cast<int>(K / 8);
+  const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
+  const auto* xp = static_cast<const uint4*>(x);
+  const auto* gp = static_cast<const uint4*>(gamma);
+  auto* ap = static_cast<uint4*>(A);
+  trace_before(s);
+  if (mode == RNL_NORM_RSQRT) {
+    if (gamma)
+      norm_cast_kernel<0, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
+    else
+      norm_cast_kernel<0, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
+  } else {
+    if (gamma)
+      norm_cast_kernel<1, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
+    else
+      norm_cast_kernel<1, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
+  }
+  return launched(s, "norm_cast");
+}
+
+rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int mode, float* rstd,
+                           cudaStream_t s) {
+  if (T == 0) return RNL_OK;
+  const int nvec = static_cast<int>(K / 8);
+  const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
+  const auto* xp = static_cast<const uint4*>(x);
+  trace_before(s);
+  if (mode == RNL_NORM_RSQRT)
+    row_rstd_kernel<0><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+  else
+    row_rstd_kernel<1><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+  return launched(s, "row_rstd");
+}
+
+rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                             int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s) {
+  if (T == 0) return RNL_OK;
+  const int nvec = static_cast<int>(K / 8);
+  const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
+  const auto* xp = static_cast<const uint4*>(x);
+  const auto* gp = static_cast<const uint4*>(gamma);
+  auto* ap = static_cast<uint4*>(A);
+  auto* qp = reinterpret_cast<uint2*>(q_out);
+  trace_before(s);
+  if (mode == RNL_NORM_RSQRT) {
+    if (gamma)
+      norm_quant_kernel<0, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+    else
+      norm_quant_kernel<0, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+  } else {
+    if (gamma)
+      norm_quant_kernel<1, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+    else
+      norm_quant_kernel<1, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+  }
+  return launched(s, "norm_quant");
+}
+
+rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s) {
+  if (n == 0) return RNL_OK;
+  const int64_t nvec16 = n / 16;
+  const int64_t want = (nvec16 + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < 4096 ? want : 4096);
+  trace_before(s);
+  s8_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), nvec16,
+                                           static_cast<uint4*>(dst));
+  return launched(s, "s8_to_bf16");
+}
+
+rnl_status read_clear_error_rowwise(unsigned int* word) {
+  *word = 0;  // these kernels never wait on anything
+  return RNL_OK;
+}
+
+}  // namespace rnl

@@ -1,0 +1,144 @@
+"""The C-ABI library on the host, without a GPU: it builds, loads, exports
+every function include/rnl.h declares, sizes workspaces and rejects bad
+arguments with the documented status codes before touching a device.
+
+The argument checks run in a child process with CUDA_VISIBLE_DEVICES="" so
+that, whatever the machine, no call can reach a GPU."""
+import json
+import os
+import re
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rnl.h")
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from rmsnorm_linear_projection_gb300 import build
+    return build.build()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)
+    keywords = {"typedef", "enum", "struct", "sizeof", "defined"}
+    return sorted({n for n in names if n not in keywords and (n.startswith("rnl_") or
+                                                              n in ("rmsnorm_linear_bf16",
+                                                                    "rmsnorm_linear_w8a8",
+                                                                    "mla_q_chain"))})
+
+
+def test_exports_every_declared_symbol(lib_path):
+    import ctypes
+    lib = ctypes.CDLL(lib_path)
+    declared = header_functions()
+    assert "rmsnorm_linear_bf16" in declared and "rnl_workspace_size" in declared
+    missing = [n for n in declared if not hasattr(lib, n)]
+    assert not missing, missing
+    from rmsnorm_linear_projection_gb300 import EXPORTS
+    assert sorted(EXPORTS) == declared
+
+
+CHILD = textwrap.dedent("""
+    import ctypes, json, sys
+    sys.path.insert(0, {root!r})
+    from rmsnorm_linear_projection_gb300 import _native as nat
+    lib = nat.load({lib!r})
+    P = ctypes.c_void_p
+    A = P(0x10000)        # a 16-byte aligned fake address: never dereferenced,
+    B = P(0x10008)        # every call below fails validation first
+    ws = P(0x20000)
+    r = {{}}
+    r["version"] = lib.rnl_version()
+    r["ws_bf16_qkv"] = lib.rnl_workspace_size(0, 4096, 4096, 6144, 0)
+    r["ws_bf16_skinny"] = lib.rnl_workspace_size(0, 16384, 28672, 24, 1)
+    r["ws_w8a8"] = lib.rnl_workspace_size(1, 8192, 4096, 4096, 0)
+    r["ws_mla"] = lib.rnl_workspace_size(2, 2048, 7168, 1536, 24576)
+    r["ws_bad_op"] = lib.rnl_workspace_size(9, 1, 8, 8, 0)
+    r["ws_neg"] = lib.rnl_workspace_size(0, -1, 8, 8, 0)
+    big = 1 << 40
+    f = lib.rmsnorm_linear_bf16
+    r["bf16_null_x"] = f(None, None, A, 4, 64, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_null_out"] = f(A, None, A, 4, 64, 8, 1e-6, 0, None, 0, ws, 1 << 20, None)
+    r["bf16_neg_T"] = f(A, None, A, -1, 64, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_zero_K"] = f(A, None, A, 4, 0, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_huge_N"] = f(A, None, A, 4, 64, big, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_K_not_mult8"] = f(A, None, A, 4, 60, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_misaligned_x"] = f(B, None, A, 4, 64, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_bad_mode"] = f(A, None, A, 4, 64, 8, 1e-6, 7, A, 0, ws, 1 << 20, None)
+    r["bf16_bad_eps"] = f(A, None, A, 4, 64, 8, float("nan"), 0, A, 0, ws, 1 << 20, None)
+    r["bf16_neg_eps"] = f(A, None, A, 4, 64, 8, -1.0, 0, A, 0, ws, 1 << 20, None)
+    r["bf16_bad_dtype"] = f(A, None, A, 4, 64, 8, 1e-6, 0, A, 5, ws, 1 << 20, None)
+    r["bf16_fp32_gamma"] = f(A, A, A, 4, 64, 8, 1e-6, 0, A, 1, ws, 1 << 20, None)
+    r["bf16_small_ws"] = f(A, None, A, 4, 64, 8, 1e-6, 0, A, 0, ws, 16, None)
+    r["bf16_null_ws"] = f(A, None, A, 4, 64, 8, 1e-6, 0, A, 0, None, 0, None)
+    r["bf16_T0"] = f(None, None, None, 0, 64, 8, 1e-6, 0, None, 0, None, 0, None)
+    r["bf16_no_device"] = f(A, None, A, 4, 64, 8, 1e-6, 0, A, 0, ws, 1 << 20, None)
+    g = lib.rmsnorm_linear_w8a8
+    r["w8a8_null_scale"] = g(A, None, A, None, 4, 64, 8, 1e-6, 0, A, None, None, ws, 1 << 20, None)
+    r["w8a8_K_not_mult16"] = g(A, None, A, A, 4, 72, 8, 1e-6, 0, A, None, None, ws, 1 << 20, None)
+    r["w8a8_small_ws"] = g(A, None, A, A, 4, 64, 8, 1e-6, 0, A, None, None, ws, 64, None)
+    m = lib.mla_q_chain
+    r["mla_null_gamma"] = m(A, A, None, A, 4, 64, 16, 8, 1e-6, 1, A, None, ws, 1 << 20, None)
+    r["mla_N1_not_mult8"] = m(A, A, A, A, 4, 64, 12, 8, 1e-6, 1, A, None, ws, 1 << 20, None)
+    s8 = lib.rnl_gemm_s8s8s32
+    r["s8_K_not_mult16"] = s8(A, A, A, 4, 8, 24, ws, 1 << 20, None)
+    r["s8_M0"] = s8(None, None, None, 0, 8, 32, None, 0, None)
+    r["status_strings"] = [lib.rnl_status_string(i).decode() for i in range(10)]
+    r["trace_enable"] = lib.rnl_trace_enable(1)
+    r["trace_read_empty"] = lib.rnl_trace_read(None, (ctypes.c_float * 4)(), 4)
+    lib.rnl_trace_enable(0)
+    print(json.dumps(r))
+""")
+
+
+@pytest.fixture(scope="module")
+def host_results(lib_path):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    code = CHILD.format(root=ROOT, lib=lib_path)
+    p = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert p.returncode == 0, p.stderr
+    return json.loads(p.stdout.strip().splitlines()[-1])
+
+
+OK, NULL, SHAPE, ALIGN, ARG, WORKSPACE, LAUNCH, TIMEOUT, UNSUP, DEVICE = range(10)
+
+
+def test_workspace_sizes(host_results):
+    r = host_results
+    assert r["version"] >= 100
+    assert r["ws_bf16_qkv"] == 4096 * 4096 * 2
+    assert r["ws_w8a8"] == 8192 * 4096 * 2 + 4096 * 4096 * 2 + 8192 * 4
+    assert r["ws_mla"] == 2 * 2048 * 1536 * 2
+    # skinny partial records: (T/128 + 512) records of 128 rows x (32 + 1) floats
+    assert r["ws_bf16_skinny"] == (16384 // 128 + 512) * 128 * 33 * 4
+    max_size = (1 << 64) - 1
+    assert r["ws_bad_op"] == max_size and r["ws_neg"] == max_size
+
+
+@pytest.mark.parametrize("key,want", [
+    ("bf16_null_x", NULL), ("bf16_null_out", NULL), ("bf16_neg_T", SHAPE),
+    ("bf16_zero_K", SHAPE), ("bf16_huge_N", SHAPE), ("bf16_K_not_mult8", ALIGN),
+    ("bf16_misaligned_x", ALIGN), ("bf16_bad_mode", ARG), ("bf16_bad_eps", ARG),
+    ("bf16_neg_eps", ARG), ("bf16_bad_dtype", ARG), ("bf16_fp32_gamma", UNSUP),
+    ("bf16_small_ws", WORKSPACE), ("bf16_null_ws", WORKSPACE), ("bf16_T0", OK),
+    ("bf16_no_device", DEVICE),
+    ("w8a8_null_scale", NULL), ("w8a8_K_not_mult16", ALIGN), ("w8a8_small_ws", WORKSPACE),
+    ("mla_null_gamma", NULL), ("mla_N1_not_mult8", ALIGN),
+    ("s8_K_not_mult16", ALIGN), ("s8_M0", OK),
+    ("trace_enable", OK), ("trace_read_empty", 0),
+])
+def test_argument_checks(host_results, key, want):
+    assert host_results[key] == want
+
+
+def test_status_strings(host_results):
+    s = host_results["status_strings"]
+    assert s[0] == "ok" and len(set(s)) == 10

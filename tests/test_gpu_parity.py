@@ -1,0 +1,241 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Small shapes span several 128x256 tiles with ragged tails in T, N and K and
+are compared in full; the five workload sizes are run in the configuration
+the benchmark times and compared on sampled rows (rows are independent, so
+a sampled row is checked exactly as in a full comparison).
+
+Bounds: bf16 outputs |gpu - oracle| <= 1e-2 * max(1, |oracle|); fp32
+outputs (mhc_pre form) the fp32-accumulation bound of gpu_util; the INT8
+matmul and the INT8 codes bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+from gpu_util import (assert_bf16_close, assert_fp32_close, dev, dev_bf16, host_bits,
+                      sample_rows)
+from oracle import bf16_bits_to_f64
+
+pytestmark = pytest.mark.gpu
+
+rnl = pytest.importorskip("rmsnorm_linear_projection_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from rmsnorm_linear_projection_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    yield
+    rnl.rnl_check_device_error()
+
+
+def _rand_case(seed, T, K, N, gamma=True):
+    c = dict(seed=seed, T=T, K=K, N=N, has_gamma=gamma)
+    return si.make_projection(c)
+
+
+# ----------------------------------------------------------------- AT-10
+@pytest.mark.parametrize("T,K,N,mode,gamma", [
+    (16, 256, 128, 0, True),     # the tiny workload's shape
+    (1, 8, 1, 0, True),          # smallest everything
+    (130, 72, 300, 0, True),     # T, K (64 + 8) and N (256 + 44) tails
+    (300, 520, 520, 1, True),    # sqrt+div form, N not a multiple of 8
+    (257, 1024, 768, 0, False),  # no gamma, three N tiles
+    (1000, 256, 100, 1, True),
+    (640, 4096, 512, 0, True),   # long K
+])
+def test_bf16_small(orc, T, K, N, mode, gamma):
+    d = _rand_case(7 + T + K + N, T, K, N, gamma)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]) if gamma else None,
+                                  dev_bf16(d["W"]), eps=1e-6, norm_mode=mode)
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, mode, 0)
+    assert_bf16_close(host_bits(out), want, f"bf16 {T}x{K}x{N}")
+
+
+def test_tiny_workload_and_golden(orc):
+    c = si.CONFIGS["tiny"]
+    d = si.make_projection(c)
+    out = host_bits(rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]),
+                                            eps=c["eps"], norm_mode=c["norm_mode"]))
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], c["eps"], c["norm_mode"], 0)
+    assert_bf16_close(out, want, "tiny")
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny_rmsnorm_linear_bf16.txt")
+    stored = np.array([[int(v, 16) for v in ln.split()] for ln in open(path) if not ln.startswith("#")],
+                      np.uint16)
+    assert_bf16_close(out, stored, "tiny vs stored oracle output")
+
+
+def test_qkv_full_sampled(orc):
+    c = si.CONFIGS["qkv"]
+    d = si.make_projection(c)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]),
+                                  eps=c["eps"], norm_mode=c["norm_mode"])
+    rows = sample_rows(c["T"], 48)
+    got = host_bits(out)[rows]
+    _, want = orc.rmsnorm_linear(d["x"][rows], d["gamma"], d["W"], c["eps"], c["norm_mode"], 0)
+    assert_bf16_close(got, want, "qkv sampled rows")
+
+
+# ------------------------------------------------------- mhc_pre FP32 form
+def _fp32_check(orc, d, mode, out, rows=None):
+    x = d["x"] if rows is None else d["x"][rows]
+    got = out.cpu().numpy() if rows is None else out.cpu().numpy()[rows]
+    ref, _ = orc.rmsnorm_linear(x, None, d["W"], 1e-6, mode, 1)
+    y, _ = orc.rmsnorm_f64(x, None, 1e-6, mode)
+    abs_sum = np.abs(y) @ np.abs(bf16_bits_to_f64(d["W"])).T
+    return assert_fp32_close(got, ref, abs_sum, "fp32 form")
+
+
+@pytest.mark.parametrize("T,K,N,mode", [
+    (300, 20480, 24, 0),   # skinny kernel: 3 row tiles (ragged), split across CTAs
+    (129, 16384, 64, 1),   # N = 64, sqrt+div form
+    (1, 512, 1, 0),        # one row, one output
+    (700, 4160, 33, 0),    # N just above 32 (64-wide MMA), K tail
+    (500, 1024, 200, 0),   # N > 64: row rstd pass + GEMM with row-scale epilogue
+    (200, 2048, 600, 1),
+])
+def test_fp32_form_small(orc, T, K, N, mode):
+    d = _rand_case(11 + T + K + N, T, K, N, gamma=False)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), None, dev_bf16(d["W"]), eps=1e-6,
+                                  norm_mode=mode, out_dtype=rnl.OUT_FP32)
+    _fp32_check(orc, d, mode, out)
+
+
+def test_skinny_full_sampled(orc):
+    c = si.CONFIGS["skinny"]
+    d = si.make_projection(c)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), None, dev_bf16(d["W"]), eps=c["eps"],
+                                  norm_mode=c["norm_mode"], out_dtype=rnl.OUT_FP32)
+    rows = sample_rows(c["T"], 64)
+    _fp32_check(orc, d, c["norm_mode"], out, rows)
+
+
+# -------------------------------------------------------------- MLA chain
+@pytest.mark.parametrize("T,K,N1,N2,mode", [
+    (200, 1024, 512, 1000, 1),
+    (129, 520, 136, 264, 0),
+])
+def test_mla_small(orc, T, K, N1, N2, mode):
+    c = dict(seed=T + K, T=T, K=K, N1=N1, N2=N2)
+    d = si.make_mla(c)
+    qa = torch.empty((T, N1), dtype=torch.bfloat16, device="cuda")
+    out = rnl.mla_q_chain(dev_bf16(d["x"]), dev_bf16(d["W_qa"]), dev_bf16(d["gamma_cq"]),
+                          dev_bf16(d["W_qb"]), eps=1e-6, norm_mode=mode, qa_out=qa)
+    want_qa, _, want = orc.mla_q_chain(d["x"], d["W_qa"], d["gamma_cq"], d["W_qb"], 1e-6, mode)
+    assert_bf16_close(host_bits(qa), want_qa, "mla stage 1")
+    assert_bf16_close(host_bits(out), want, "mla out")
+
+
+def test_mla_full_sampled(orc):
+    c = si.CONFIGS["mla"]
+    d = si.make_mla(c)
+    out = rnl.mla_q_chain(dev_bf16(d["x"]), dev_bf16(d["W_qa"]), dev_bf16(d["gamma_cq"]),
+                          dev_bf16(d["W_qb"]), eps=c["eps"], norm_mode=c["norm_mode"])
+    rows = sample_rows(c["T"], 24)
+    _, _, want = orc.mla_q_chain(d["x"][rows], d["W_qa"], d["gamma_cq"], d["W_qb"], c["eps"],
+                                 c["norm_mode"])
+    assert_bf16_close(host_bits(out)[rows], want, "mla sampled rows")
+
+
+# ------------------------------------------------------------------ W8A8
+@pytest.mark.parametrize("M,N,K", [(300, 300, 4096), (1, 1, 16), (129, 257, 1040)])
+def test_gemm_s8_bit_exact_random(orc, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    B = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    C = rnl.rnl_gemm_s8s8s32(dev(A), dev(B)).cpu().numpy()
+    want, ovf = orc.gemm_s8(A, B)
+    assert not ovf
+    assert np.array_equal(C, want)
+
+
+def test_gemm_s8_bit_exact_worst_case(orc):
+    # all entries +-127: partial sums reach 127*127*K = 66,064,384 > 2^24 for
+    # K = 4096, which fp32 accumulation without the exact 1024-chunks would round
+    M, N, K = 130, 260, 4096
+    A = np.full((M, K), 127, np.int8)
+    A[1::2] = -127
+    B = np.full((N, K), 127, np.int8)
+    B[::3] = -127
+    B[5, ::2] = -127  # mixed signs in one row
+    C = rnl.rnl_gemm_s8s8s32(dev(A), dev(B)).cpu().numpy()
+    want, ovf = orc.gemm_s8(A, B)
+    assert not ovf
+    assert int(np.abs(want).max()) == 127 * 127 * K
+    assert np.array_equal(C, want)
+
+
+def _w8a8_run(d, eps, mode):
+    T, K = d["x"].shape
+    q = torch.empty((T, K), dtype=torch.int8, device="cuda")
+    xs = torch.empty((T,), dtype=torch.float32, device="cuda")
+    out = rnl.rmsnorm_linear_w8a8(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev(d["Wq"]),
+                                  dev(d["w_scale"]), eps=eps, norm_mode=mode, q_out=q,
+                                  x_scale_out=xs)
+    return host_bits(out), q.cpu().numpy(), xs.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,K,N,mode", [(200, 2048, 300, 0), (130, 4096, 520, 1), (5, 16, 7, 0)])
+def test_w8a8_small(orc, T, K, N, mode):
+    c = dict(seed=3 + T + N, T=T, K=K, N=N)
+    d = si.make_w8a8(c)
+    out, q, xs = _w8a8_run(d, 1e-6, mode)
+    r = orc.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], 1e-6, mode)
+    assert np.array_equal(q, r["q"]), "INT8 codes differ"
+    assert np.array_equal(xs, r["x_scale"]), "x_scale differs"
+    assert_bf16_close(out, r["out"], "w8a8 out")
+
+
+def test_w8a8_zero_row(orc):
+    c = dict(seed=5, T=4, K=64, N=16)
+    d = si.make_w8a8(c)
+    d["x"][2] = 0
+    out, q, xs = _w8a8_run(d, 1e-6, 0)
+    assert not q[2].any() and xs[2] == 0.0
+    assert not bf16_bits_to_f64(out[2]).any()
+    r = orc.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], 1e-6, 0)
+    assert np.array_equal(q, r["q"])
+    assert_bf16_close(out, r["out"], "w8a8 zero row")
+
+
+def test_w8a8_full_sampled(orc):
+    c = si.CONFIGS["w8a8"]
+    d = si.make_w8a8(c)
+    out, q, xs = _w8a8_run(d, c["eps"], c["norm_mode"])
+    rows = sample_rows(c["T"], 48)
+    r = orc.rmsnorm_linear_w8a8(d["x"][rows], d["gamma"], d["Wq"], d["w_scale"], c["eps"],
+                                c["norm_mode"])
+    assert np.array_equal(q[rows], r["q"])
+    assert np.array_equal(xs[rows], r["x_scale"])
+    assert_bf16_close(out[rows], r["out"], "w8a8 sampled rows")
+    # the int32 accumulation of the full-size run is exact: recompute the
+    # sampled rows' products from the oracle's own codes through the INT8 hook
+    C = rnl.rnl_gemm_s8s8s32(dev(r["q"]), dev(d["Wq"])).cpu().numpy()
+    assert np.array_equal(C, r["acc"])
+
+
+# ------------------------------------------------------------- edge cases
+def test_empty_T_is_noop():
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    out = rnl.rmsnorm_linear_bf16(x, None, W)
+    assert out.shape == (0, 8)
+
+
+def test_misaligned_pointer_rejected():
+    buf = torch.zeros((17, 64), dtype=torch.bfloat16, device="cuda")
+    x = buf.view(-1)[1:1 + 16 * 64].view(16, 64)  # 2-byte offset
+    W = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rnl.RnlError) as e:
+        rnl.rmsnorm_linear_bf16(x, None, W)
+    assert e.value.status == 3
+
+
+def test_device_error_word_clean():
+    rnl.rnl_check_device_error()
