@@ -146,6 +146,48 @@ rnl_status mla_q_chain(const void *x, const void *W_qa, const void *gamma_cq, co
                        void *out, void *qa_out, void *workspace, size_t workspace_bytes,
                        rnl_stream_t stream);
 
+/* Size of the scratch array built into the library for the call below. */
+#define RNL_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * rmsnorm_linear_skinny_noalloc -- the mhc_pre FP32 form (the same result as
+ * rmsnorm_linear_bf16 with gamma = NULL, out_dtype = RNL_OUT_FP32 and
+ * N <= 64) without any workspace and without allocating device memory.
+ * The source pages have no counterpart of this call; it exists for how the
+ * library is embedded, not for the method.
+ *
+ * Who needs it: callers that cannot call cudaMalloc, such as code running
+ * inside a host program that owns every device allocation (a serving
+ * engine with a fixed memory pool, or a plugin that is handed only its
+ * input and output buffers).  They have no scratch buffer to pass, and a
+ * cudaMalloc of their own could synchronise the device and grow the
+ * process's memory behind the owner's back.
+ *
+ * How: the split-K scratch lives in a RNL_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * array inside the library, which every GPU that loads the library holds
+ * until the process exits.  The call makes no cudaMalloc, cudaFree or other
+ * allocating call.  It needs (ceil(T/128) + G) * 128 * (NP + 1) * 4 bytes of
+ * that array, G = min(SM count, work blocks), NP = 32 for N <= 32 and 64
+ * for N <= 64: on a 152-SM GB300 up to T = 107,520 rows (N <= 32) or
+ * T = 45,056 rows (N <= 64).  Larger T returns RNL_ERR_WORKSPACE with
+ * nothing enqueued; N > 64 returns RNL_ERR_UNSUPPORTED.
+ *
+ * Sharing: all calls on a device use the same array.  Calls whose GPU work
+ * can overlap (other streams, other host threads) race on it; serialise
+ * them.  The array keeps the previous call's contents; every value the
+ * kernels read is written earlier in the same call, so nothing is cleared.
+ *
+ * Set-up: the first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture.
+ *
+ * Arguments as rmsnorm_linear_bf16: x bf16 [T, K], W bf16 [N, K],
+ * out fp32 [T, N], 16-byte aligned, K % 8 == 0, eps >= 0, norm_mode.
+ */
+rnl_status rmsnorm_linear_skinny_noalloc(const void *x, const void *W, int64_t T, int64_t K,
+                                         int64_t N, float eps, int norm_mode, float *out,
+                                         rnl_stream_t stream);
+
 /*
  * The exact integer matmul of the W8A8 path on its own (AT-09 INT8 mode):
  * C[m, n] = sum_k A[m, k] * B[n, k], int8 inputs in [-127, 127], int32 out

@@ -23,6 +23,7 @@ from ._native import (  # noqa: F401
     load,
     mla_q_chain,
     rmsnorm_linear_bf16,
+    rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
     rnl_gemm_s8s8s32,

@@ -30,7 +30,7 @@ STATUS = {
 
 EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
            "rmsnorm_linear_w8a8", "mla_q_chain", "rnl_gemm_s8s8s32", "rnl_check_device_error",
-           "rnl_trace_enable", "rnl_trace_read")
+           "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc")
 
 
 class RnlError(RuntimeError):
@@ -56,6 +56,7 @@ def _declare(lib):
         "rnl_check_device_error": (I, [P, ctypes.POINTER(I)]),
         "rnl_trace_enable": (I, [I]),
         "rnl_trace_read": (I, [P, ctypes.POINTER(F), I]),
+        "rmsnorm_linear_skinny_noalloc": (I, [P, P, I64, I64, I64, F, I, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -189,6 +190,24 @@ def mla_q_chain(x, W_qa, gamma_cq, W_qb, eps=1e-6, norm_mode=NORM_SQRT_DIV, out=
                               float(eps), int(norm_mode), _ptr(out), _ptr(qa_out), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(dev, stream)),
            "mla_q_chain")
+    return out
+
+
+def rmsnorm_linear_skinny_noalloc(x, W, eps=1e-6, norm_mode=NORM_RSQRT, out=None, stream=None):
+    """mhc_pre FP32 form (no gamma, N <= 64) with no workspace: for callers that
+    cannot allocate device memory.  The scratch is an array built into the
+    library, shared by every call on the device (overlapping calls race)."""
+    T, K = x.shape
+    N = W.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W, "W", torch.bfloat16, (N, K), dev)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.float32, (T, N), dev)
+    _check(load().rmsnorm_linear_skinny_noalloc(_ptr(x), _ptr(W), T, K, N, float(eps),
+                                                int(norm_mode), _ptr(out), _stream(dev, stream)),
+           "rmsnorm_linear_skinny_noalloc")
     return out
 
 

@@ -23,6 +23,8 @@
 // (deterministic) and applies rstd.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -343,3 +345,78 @@ rnl_status read_clear_error_skinny(unsigned int* word) {
 }
 
 }  // namespace rnl
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the mhc_pre path (rmsnorm_linear_skinny_noalloc).
+//
+// Its scratch (the split-K partial records) lives in this file-scope device
+// array instead of a caller-provided workspace.  Every GPU that loads the
+// library holds the array until the process exits; all calls on a device
+// share it, so it keeps the previous call's contents (every record the
+// reduce kernel reads is written earlier in the same call, so nothing has
+// to be cleared), and calls that overlap on the GPU race on it.
+// ---------------------------------------------------------------------------
+namespace rnl {
+namespace {
+
+constexpr size_t kStaticScratchBytes = RNL_NOALLOC_SCRATCH_BYTES;  // 16 MiB
+static __device__ __align__(256) unsigned char g_skinny_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_skinny_scratch for the current device, looked up once
+// per device (with that device current) and cached.
+rnl_status static_scratch(int device, void** ptr) {
+  if (device < 0 || device >= 64) return RNL_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_skinny_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return RNL_ERR_DEVICE;
+    }
+    g_scratch_ptr[device] = p;
+  }
+  *ptr = g_scratch_ptr[device];
+  return RNL_OK;
+}
+
+}  // namespace
+}  // namespace rnl
+
+extern "C" rnl_status rmsnorm_linear_skinny_noalloc(const void* x, const void* W, int64_t T,
+                                                    int64_t K, int64_t N, float eps,
+                                                    int norm_mode, float* out,
+                                                    rnl_stream_t stream) {
+  using namespace rnl;
+  constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+  if (T < 0 || K <= 0 || N <= 0 || T > kMaxDim || K > kMaxDim) return RNL_ERR_SHAPE;
+  if (N > 64) return RNL_ERR_UNSUPPORTED;
+  if ((norm_mode != RNL_NORM_RSQRT && norm_mode != RNL_NORM_SQRT_DIV) || !(eps >= 0.f) ||
+      !(eps <= 3.4e38f))
+    return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!x || !W || !out) return RNL_ERR_NULL;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (K % 8 != 0 || misaligned(x) || misaligned(W) || misaligned(out)) return RNL_ERR_ALIGN;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  // records actually used: one per (CTA, row tile) pair, at most tiles + G
+  const int G = grid_for(T, K, dev.sm_count);
+  const int64_t np = N <= 32 ? 32 : 64;
+  const int64_t records = (T + SM_ROWS - 1) / SM_ROWS + G;
+  const size_t need = static_cast<size_t>(records * SM_ROWS * (np + 1) * sizeof(float));
+  if (need > kStaticScratchBytes) return RNL_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = static_scratch(dev.device, &scratch);
+  if (st != RNL_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* part = static_cast<float*>(scratch);
+  if (N <= 32)
+    return norm_mode == RNL_NORM_RSQRT ? launch_np<32, 0>(x, W, T, K, N, eps, out, part, G, dev, s)
+                                       : launch_np<32, 1>(x, W, T, K, N, eps, out, part, G, dev, s);
+  return norm_mode == RNL_NORM_RSQRT ? launch_np<64, 0>(x, W, T, K, N, eps, out, part, G, dev, s)
+                                     : launch_np<64, 1>(x, W, T, K, N, eps, out, part, G, dev, s);
+}

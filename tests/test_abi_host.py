@@ -28,10 +28,8 @@ def header_functions():
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)
     keywords = {"typedef", "enum", "struct", "sizeof", "defined"}
-    return sorted({n for n in names if n not in keywords and (n.startswith("rnl_") or
-                                                              n in ("rmsnorm_linear_bf16",
-                                                                    "rmsnorm_linear_w8a8",
-                                                                    "mla_q_chain"))})
+    prefixes = ("rnl_", "rmsnorm_linear_", "mla_")
+    return sorted({n for n in names if n not in keywords and n.startswith(prefixes)})
 
 
 def test_exports_every_declared_symbol(lib_path):
