@@ -16,6 +16,8 @@ namespace {
 
 constexpr int kWarps = 8;  // rows per block
 
+inline unsigned row_blocks(int64_t T) { return static_cast<unsigned>((T + kWarps - 1) / kWarps); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -286,29 +288,165 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// int8 -> bf16, 16 elements per thread per step.
-__global__ void __launch_bounds__(256)
-    s8_to_bf16_kernel(const uint4* __restrict__ src, int64_t nvec16, uint4* __restrict__ dst) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec16;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 u = __ldg(src + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[8];
+// The same W8A8 front end with the whole row in registers (used up to
+// K = 4096): x is read from memory once, and the three passes (sum of
+// squares, amax, codes) run on the registers.  The sum of squares visits the
+// elements in the same order as norm_quant_kernel.
+template <int MODE, bool GAMMA, int VPL>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    norm_quant_regs_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                           int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                           uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const uint4* xr = x + row * nvec;
+  uint4 u[VPL];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float a = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
-      const float b = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
-      const float c = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
-      const float d = static_cast<float>(static_cast<int8_t>((w[k] >> 24) & 0xFF));
-      o[2 * k] = pack_bf16x2(a, b);
-      o[2 * k + 1] = pack_bf16x2(c, d);
+  for (int i = 0; i < VPL; ++i) {
+    const int v = lane + 32 * i;
+    u[i] = v < nvec ? ldg16(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // sum of squares: float-float accumulation, one rounding (see row_rstd_exactsum)
+  float hi = 0.f, lo = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float t = __fmul_rn(f[j], f[j]);
+      if (MODE == 1) t = __fmul_rn(t, inv_d);
+      float sum, e;
+      two_sum(hi, t, sum, e);
+      hi = sum;
+      lo = __fadd_rn(lo, e);
     }
-    dst[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    float sum, e;
+    two_sum(hi, h2, sum, e);
+    lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    hi = sum;
+  }
+  const float ss = __fadd_rn(hi, lo);
+  const float rstd = (MODE == 0)
+                         ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_d), eps)))
+                         : __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ss, eps)));
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int v = lane + 32 * i;
+    if (v >= nvec) break;
+    float f[8];
+    unpack8(u[i], f);
+    float g[8];
+    if (GAMMA) unpack8(ldg16(gamma + v), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y = __fmul_rn(f[j], rstd);
+      if (GAMMA) y = __fmul_rn(y, g[j]);
+      amax = fmaxf(amax, fabsf(y));
+    }
+  }
+  amax = warp_max(amax);
+  const bool zero_row = !(amax > 0.f);
+  const float qs = zero_row ? 0.f : __fdiv_rn(127.0f, amax);
+  if (lane == 0) x_scale[row] = zero_row ? 0.f : __fdiv_rn(amax, 127.0f);
+  uint4* ar = A + row * nvec;
+  uint2* qr = q_out != nullptr ? q_out + row * nvec : nullptr;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int v = lane + 32 * i;
+    if (v >= nvec) break;
+    float f[8];
+    unpack8(u[i], f);
+    float g[8];
+    if (GAMMA) unpack8(ldg16(gamma + v), g);
+    float c[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float y = __fmul_rn(f[j], rstd);
+      if (GAMMA) y = __fmul_rn(y, g[j]);
+      const float r = rintf(__fmul_rn(y, qs));
+      c[j] = fminf(fmaxf(r, -127.f), 127.f);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(c[0], c[1]);
+    o.y = pack_bf16x2(c[2], c[3]);
+    o.z = pack_bf16x2(c[4], c[5]);
+    o.w = pack_bf16x2(c[6], c[7]);
+    ar[v] = o;
+    if (qr != nullptr) {
+      uint32_t q_lo = 0, q_hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        q_lo |= (static_cast<uint32_t>(static_cast<int>(c[j])) & 0xFFu) << (8 * j);
+        q_hi |= (static_cast<uint32_t>(static_cast<int>(c[4 + j])) & 0xFFu) << (8 * j);
+      }
+      qr[v] = make_uint2(q_lo, q_hi);
+    }
   }
 }
 
-inline unsigned row_blocks(int64_t T) { return static_cast<unsigned>((T + kWarps - 1) / kWarps); }
+template <int MODE, bool GAMMA>
+void norm_quant_dispatch(const uint4* xp, const uint4* gp, int64_t T, int nvec, float inv_d,
+                         float eps, uint4* ap, uint2* qp, float* xs, cudaStream_t s) {
+  const unsigned blocks = row_blocks(T);
+  constexpr unsigned kT = kWarps * 32;
+  const int vpl = (nvec + 31) / 32;
+  if (vpl <= 1)
+    norm_quant_regs_kernel<MODE, GAMMA, 1><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+  else if (vpl <= 2)
+    norm_quant_regs_kernel<MODE, GAMMA, 2><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+  else if (vpl <= 4)
+    norm_quant_regs_kernel<MODE, GAMMA, 4><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+  else if (vpl <= 8)
+    norm_quant_regs_kernel<MODE, GAMMA, 8><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+  else if (vpl <= 16)
+    norm_quant_regs_kernel<MODE, GAMMA, 16><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+  else
+    norm_quant_kernel<MODE, GAMMA><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
+}
+
+// int8 -> bf16 (exact): each thread widens 4 x 16 elements, issuing its four
+// 16-byte loads before converting.
+constexpr int kS8Vec = 4;
+
+__device__ __forceinline__ void widen16(const uint4& u, uint4* dst) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float a = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
+    const float b = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
+    const float c = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
+    const float d = static_cast<float>(static_cast<int8_t>((w[k] >> 24) & 0xFF));
+    o[2 * k] = pack_bf16x2(a, b);
+    o[2 * k + 1] = pack_bf16x2(c, d);
+  }
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void __launch_bounds__(256)
+    s8_to_bf16_kernel(const uint4* __restrict__ src, int64_t nvec16, uint4* __restrict__ dst) {
+  const int64_t base = (static_cast<int64_t>(blockIdx.x) * blockDim.x) * kS8Vec + threadIdx.x;
+  uint4 u[kS8Vec];
+#pragma unroll
+  for (int i = 0; i < kS8Vec; ++i) {
+    const int64_t v = base + static_cast<int64_t>(i) * blockDim.x;
+    u[i] = v < nvec16 ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kS8Vec; ++i) {
+    const int64_t v = base + static_cast<int64_t>(i) * blockDim.x;
+    if (v < nvec16) widen16(u[i], dst + 2 * v);
+  }
+}
 
 inline rnl_status launched(cudaStream_t s, const char* name) {
   trace_after(s, name);
@@ -386,14 +524,14 @@ rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_
   trace_before(s);
   if (mode == RNL_NORM_RSQRT) {
     if (gamma)
-      norm_quant_kernel<0, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+      norm_quant_dispatch<0, true>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, s);
     else
-      norm_quant_kernel<0, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+      norm_quant_dispatch<0, false>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, s);
   } else {
     if (gamma)
-      norm_quant_kernel<1, true><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+      norm_quant_dispatch<1, true>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, s);
     else
-      norm_quant_kernel<1, false><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale);
+      norm_quant_dispatch<1, false>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, s);
   }
   return launched(s, "norm_quant");
 }
@@ -401,8 +539,8 @@ rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s) {
   if (n == 0) return RNL_OK;
   const int64_t nvec16 = n / 16;
-  const int64_t want = (nvec16 + 255) / 256;
-  const unsigned blocks = static_cast<unsigned>(want < 4096 ? want : 4096);
+  const int64_t per_block = 256 * kS8Vec;
+  const unsigned blocks = static_cast<unsigned>((nvec16 + per_block - 1) / per_block);
   trace_before(s);
   s8_to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(src), nvec16,
                                            static_cast<uint4*>(dst));

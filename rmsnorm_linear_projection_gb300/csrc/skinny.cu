@@ -185,12 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // the row's 128 bytes (their 16-byte chunks are permuted by the
-        // swizzle, which does not matter for a sum)
+        // the row's 128 bytes.  Thread i starts at 16-byte chunk i % 8 so the
+        // eight threads served by one shared-memory wavefront hit eight
+        // different bank groups (the order of the chunks does not matter for
+        // a sum).
         const uint4* rowp = reinterpret_cast<const uint4*>(smem + stage * kStage + row_local * 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 u = rowp[c];
+          const uint4 u = rowp[c ^ (row_local & 7)];
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -260,9 +262,13 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
   for (int j = 0; j < NP; ++j) acc[j] = 0.f;
   float ss = 0.f;
-  for (int c = 0; c < G; ++c) {
+  // CTA c covers steps [floor(total*c/G), floor(total*(c+1)/G)); the CTA
+  // holding step s is ceil((s+1)*G/total) - 1.
+  const int c_first = static_cast<int>(((f0 + 1) * G + total - 1) / total) - 1;
+  const int c_last = static_cast<int>((f1 * G + total - 1) / total) - 1;
+  for (int c = c_first; c <= c_last && c < G; ++c) {
     const int64_t b = range_begin(c, total, G), e = range_begin(c + 1, total, G);
-    if (e <= f0 || b >= f1 || b == e) continue;
+    if (e <= f0 || b >= f1) continue;
     const float* rec = part + ((static_cast<int64_t>(r) + c) * SM_ROWS + (t - r * SM_ROWS)) * kRec;
 #pragma unroll
     for (int j = 0; j < NP; ++j) acc[j] += rec[j];
