@@ -204,7 +204,6 @@ def oracle_sample(work_name: str, target_s: float = 12.0):
     o = oracle.Oracle()
     c = si.CONFIGS[work_name]
     T = c["T"]
-    probe_rows = np.arange(min(4, T))
 
     def run(rows):
         if work_name in ("qkv", "tiny", "skinny"):
@@ -223,11 +222,14 @@ def oracle_sample(work_name: str, target_s: float = 12.0):
         r = o.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], c["eps"], c["norm_mode"])
         return time.perf_counter() - t, r["out"]
 
-    dt, _ = run(probe_rows)
-    per_row = max(dt / probe_rows.size, 1e-6)
-    n = int(min(T, max(probe_rows.size, target_s / per_row)))
-    rows = np.linspace(0, T - 1, n).round().astype(np.int64)
-    rows = np.unique(rows)
+    # two probes separate the per-row cost from the fixed cost (weight decode)
+    n1, n2 = min(4, T), min(16, T)
+    t1, _ = run(np.arange(n1))
+    t2, _ = run(np.arange(n2)) if n2 > n1 else (t1, None)
+    per_row = max((t2 - t1) / (n2 - n1), 1e-7) if n2 > n1 else max(t1 / n1, 1e-7)
+    fixed = max(t1 - n1 * per_row, 0.0)
+    n = int(min(T, max(n2, (target_s - fixed) / per_row)))
+    rows = np.unique(np.linspace(0, T - 1, n).round().astype(np.int64))
     dt, out = run(rows)
     frac = rows.size / T
     if work_name in ("qkv", "tiny", "skinny"):

@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -74,8 +75,8 @@ struct Carve {
 
 // Workspace layouts (a null base just measures).
 struct BF16Layout {
-  void* A = nullptr;      // bf16 [T, K] normed activations (bf16 out)
-  float* rstd = nullptr;  // [T] (fp32 out, N > 64)
+  void* A = nullptr;      // bf16 [T, K] normed activations (bf16 out, two-kernel form)
+  float* rstd = nullptr;  // [T] (bf16 out; fp32 out with N > 64)
   void* part = nullptr;   // skinny partials (fp32 out, N <= 64)
   size_t bytes = 0;
 };
@@ -83,7 +84,8 @@ BF16Layout bf16_layout(void* ws, int64_t T, int64_t K, int64_t N, int out_dtype)
   BF16Layout l;
   Carve c(ws);
   if (out_dtype == RNL_OUT_BF16) {
-    l.A = c.take(static_cast<size_t>(T) * K * 2);
+    l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+    l.A = c.take(static_cast<size_t>(T) * K * 2);  // only the two-kernel form uses it
   } else if (N <= 64) {
     l.part = c.take(skinny_workspace_bytes(T, K, N, 0));
   } else {
@@ -110,8 +112,9 @@ W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
 }
 
 struct MLALayout {
-  void* qa = nullptr;  // bf16 [T, N1] stage-1 output when the caller passes none
-  void* z = nullptr;   // bf16 [T, N1] normed * gamma_cq
+  void* qa = nullptr;     // bf16 [T, N1] stage-1 output when the caller passes none
+  void* z = nullptr;      // bf16 [T, N1] normed * gamma_cq (two-kernel form)
+  float* rstd = nullptr;  // [T] rstd of the stage-1 rows
   size_t bytes = 0;
 };
 MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
@@ -119,6 +122,7 @@ MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
   Carve c(ws);
   l.qa = c.take(static_cast<size_t>(T) * N1 * 2);
   l.z = c.take(static_cast<size_t>(T) * N1 * 2);
+  l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
   l.bytes = c.used;
   return l;
 }
@@ -138,6 +142,20 @@ S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
 }
 
 inline cudaStream_t cs(rnl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Two forms of the normalise-and-cast step compute the same values:
+//   two-kernel (default): a row pass writes the bf16 A operand [T, K], the
+//     GEMM streams it by TMA;
+//   fused (RNL_FUSED_NORM=1): a row pass writes only rstd [T]; four
+//     transform warps in the GEMM rewrite each TMA-loaded x stage in shared
+//     memory as bf16((x * rstd) * gamma) before the MMA reads it.
+// The fused form redoes the transform for every N tile of a row block (32
+// times for a 6144-wide output with 192-wide tiles) and measured 2.7x slower
+// on GB300, so it is opt-in.
+bool fused_norm() {
+  const char* e = std::getenv("RNL_FUSED_NORM");
+  return e != nullptr && e[0] == '1';
+}
 
 }  // namespace
 
@@ -263,16 +281,24 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
   cudaStream_t s = cs(stream);
 
   if (out_dtype == RNL_OUT_BF16) {
-    st = launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
-    if (st != RNL_OK) return st;
     GemmArgs g;
-    g.A = l.A;
     g.B = W;
     g.M = T;
     g.N = N;
     g.K = K;
     g.out = out;
     g.epi = Epi::kBf16;
+    if (fused_norm()) {
+      st = launch_row_rstd(x, T, K, eps, norm_mode, l.rstd, s);
+      if (st != RNL_OK) return st;
+      g.A = x;
+      g.a_rstd = l.rstd;
+      g.a_gamma = gamma;
+    } else {
+      st = launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
+      if (st != RNL_OK) return st;
+      g.A = l.A;
+    }
     return launch_gemm(g, s);
   }
   if (N <= 64)
@@ -360,10 +386,18 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   g1.epi = Epi::kBf16;
   st = launch_gemm(g1, s);
   if (st != RNL_OK) return st;
-  st = launch_norm_cast(qa, gamma_cq, T, N1, eps, norm_mode, l.z, nullptr, s);
-  if (st != RNL_OK) return st;
   GemmArgs g2;
-  g2.A = l.z;
+  if (fused_norm()) {
+    st = launch_row_rstd(qa, T, N1, eps, norm_mode, l.rstd, s);
+    if (st != RNL_OK) return st;
+    g2.A = qa;
+    g2.a_rstd = l.rstd;
+    g2.a_gamma = gamma_cq;
+  } else {
+    st = launch_norm_cast(qa, gamma_cq, T, N1, eps, norm_mode, l.z, nullptr, s);
+    if (st != RNL_OK) return st;
+    g2.A = l.z;
+  }
   g2.B = W_qb;
   g2.M = T;
   g2.N = N2;

@@ -2,13 +2,17 @@
 // 5th-generation tensor cores (tcgen05), AT-09 "Linear" of the AT-10 pattern
 // page (sec. 4: matmul(x, w, dtype, b_trans=True), W stored [N, K]).
 //
-// Persistent, warp-specialised kernel, one CTA per SM:
-//   warp 0      TMA producer: 128x64 A tile and 256x64 B tile per stage
-//               (128-byte swizzle), 4-stage ring of 48 KB stages.
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and one thread issues tcgen05.mma (M=128, N=256, K=16).
+// Persistent, warp-specialised kernel, one CTA per SM, output tiles of
+// 128 x BN (BN = 256, 192 or 128, chosen per shape so the last wave of
+// tiles is as full as possible):
+//   warp 0      TMA producer: 128x64 A box and BNx64 B box per stage
+//               (128-byte swizzle), a ring of 4 (BN=256), 5 (192) or 7 (128)
+//               stages filling the 227 KB of shared memory.
+//   warp 1      allocates 512 TMEM columns (two fp32 accumulators, 256
+//               columns apart) and one thread issues tcgen05.mma
+//               (M=128, N=BN, K=16).
 //   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp one 32-lane
-//               quarter x 128 columns), convert, store to global memory.
+//               quarter x BN/2 columns), convert, store to global memory.
 // Both operands are K-major, the layout the MMA reads directly, so the
 // weight needs no transpose (the pages pre-transpose it on the host for the
 // same reason).  The two accumulators let the epilogue of tile i overlap the
@@ -23,6 +27,8 @@
 // adds it in registers.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,29 +38,43 @@ namespace {
 __device__ unsigned int g_err_gemm;
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kThreads = 320;  // producer + MMA + 8 epilogue warps, or 4 epilogue + 4 transform
 constexpr uint32_t kABytes = BM * BK * 2;
-constexpr uint32_t kBBytes = BN * BK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kChunkKBlocks = 16;  // 1024 products per exact chunk
-constexpr int kColsPerEpiWarp = BN / 2;
-constexpr int kGroups = kColsPerEpiWarp / 32;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kAccStride = 256;  // TMEM column offset between the two accumulators
+constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in shared memory per block
+
+// Tile-width dependent constants (BN = 128, 192 or 256 output columns).
+template <int BN>
+struct Tile {
+  static constexpr uint32_t kBBytes = BN * BK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages =
+      static_cast<int>((kSmemLimit - 1024 - 256) / kStageBytes) < kMaxStages
+          ? static_cast<int>((kSmemLimit - 1024 - 256) / kStageBytes)
+          : kMaxStages;
+  static constexpr uint32_t kTmemCols = 512;  // two accumulators of BN <= 256 columns
+};
 
 struct __align__(8) Ctrl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t xform_full[kMaxStages];  // A stage normalised in place (fused-norm mode)
+  uint64_t empty[kMaxStages];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctrl);
+template <int BN>
+constexpr size_t smem_bytes() {
+  return 1024 + static_cast<size_t>(Tile<BN>::kStages) * Tile<BN>::kStageBytes + sizeof(Ctrl);
+}
+static_assert(smem_bytes<256>() <= kSmemLimit && smem_bytes<192>() <= kSmemLimit &&
+                  smem_bytes<128>() <= kSmemLimit,
+              "shared memory budget");
 
 // Tile order: groups of 8 M-tiles, N fastest within a group column, so the
 // CTAs running at the same time share A panels and B panels in L2.
@@ -75,13 +95,26 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <int EPI>
+// NORM_A: A is the raw activation x; four transform warps turn each A stage
+// into bf16((x * rstd[m]) * gamma[k]) in place before the MMA reads it (the
+// AT-10 V stage fused into the C stage's operand path).
+template <int EPI, int BN, bool NORM_A>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 int M, int N, int K, void* __restrict__ out, const float* __restrict__ row_scale,
-                const float* __restrict__ col_scale) {
+                const float* __restrict__ col_scale, const float* __restrict__ a_rstd,
+                const uint4* __restrict__ a_gamma) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
+  static_assert(!(NORM_A && kInt), "the fused norm feeds the bf16 GEMM only");
+  constexpr int kStages = Tile<BN>::kStages;
+  constexpr uint32_t kStageBytes = Tile<BN>::kStageBytes;
+  constexpr uint32_t kTmemCols = Tile<BN>::kTmemCols;
+  constexpr int kEpiWarps = NORM_A ? 4 : 8;
+  constexpr int kXformWarps = NORM_A ? 4 : 0;
+  static_assert(64 + 32 * (kEpiWarps + kXformWarps) == kThreads, "warp roles");
+  constexpr int kColsPerEpiWarp = BN * 4 / kEpiWarps;  // 8 warps: BN/2 each; 4 warps: BN
+  constexpr int kGroups = kColsPerEpiWarp / 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -100,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctrl->full[s]), 1);
+      mbar_init(smem_u32(&ctrl->xform_full[s]), kXformWarps > 0 ? kXformWarps : 1);
       mbar_init(smem_u32(&ctrl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -163,11 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + buf * BN;
+          const uint32_t d_tmem = tmem_base + buf * kAccStride;
           const int kb0 = u * kb_per_unit;
           const int kb1 = min(num_kb, kb0 + kb_per_unit);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort, &g_err_gemm, 3)) {
+            const uint32_t ready = NORM_A ? smem_u32(&ctrl->xform_full[stage]) : smem_u32(&ctrl->full[stage]);
+            if (!mbar_wait(ready, phase, abort, &g_err_gemm, 3)) {
               ok = false;
               break;
             }
@@ -193,11 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int half = ew >> 2;      // which 128 columns of the 256
+    const int half = ew >> 2;      // which half of the columns (8 epilogue warps)
     const int row_local = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t unit = 0;
@@ -229,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kGroups; ++c) {
           uint32_t r[32];
-          tmem_ld_32cols(tmem_base + lane_addr + buf * BN + half * kColsPerEpiWarp + c * 32, r);
+          tmem_ld_32cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32, r);
           tmem_ld_wait();
           const int n0 = n_base + c * 32;
           if constexpr (kInt) {
@@ -327,6 +362,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if constexpr (NORM_A) {
+    // ------------------------------------------------- A transform (fused norm)
+    // Thread t owns row t of every A stage: 64 bf16 in eight 16-byte chunks,
+    // logical chunk c stored at chunk c ^ (t % 8) by the 128-byte swizzle.
+    // Visiting logical chunks in order keeps the eight threads of a
+    // shared-memory wavefront on eight different bank groups.
+    const int t = (warp - 2 - kEpiWarps) * 32 + lane;
+    const int sw = t & 7;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      const int m = mb * BM + t;
+      const float rs = m < M ? __ldg(a_rstd + m) : 0.f;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const bool got = mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort, &g_err_gemm, 5);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        uint4* rowp = reinterpret_cast<uint4*>(smem + stage * kStageBytes + t * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int k = kb * BK + c * 8;
+          uint4* q = rowp + (c ^ sw);
+          const uint4 u = *q;
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          uint32_t gw[4] = {0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u};  // bf16 1.0
+          if (a_gamma != nullptr && k < K) {
+            const uint4 gv = __ldg(a_gamma + (k >> 3));
+            gw[0] = gv.x;
+            gw[1] = gv.y;
+            gw[2] = gv.z;
+            gw[3] = gv.w;
+          }
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xFFFF0000u);
+            const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xFFFF0000u);
+            __nv_bfloat162 h = __floats2bfloat162_rn((x0 * rs) * g0, (x1 * rs) * g1);
+            o[i] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          *q = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->xform_full[stage]));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -337,14 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, int BN, bool NORM_A>
 rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<EPI>;
+  auto kern = gemm_kernel<EPI, BN, NORM_A>;
   if (dev.device < 0 || dev.device >= 64) return RNL_ERR_DEVICE;
   if (!attr_set[dev.device]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+                             static_cast<int>(smem_bytes<BN>())) != cudaSuccess)
       return RNL_ERR_LAUNCH;
     attr_set[dev.device] = true;
   }
@@ -356,10 +446,48 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
   const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const unsigned grid = static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count);
   trace_before(s);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, static_cast<int>(g.M), static_cast<int>(g.N),
-                                          static_cast<int>(g.K), g.out, g.row_scale, g.col_scale);
+  kern<<<grid, kThreads, smem_bytes<BN>(), s>>>(ma, mb, static_cast<int>(g.M), static_cast<int>(g.N),
+                                                static_cast<int>(g.K), g.out, g.row_scale, g.col_scale,
+                                                g.a_rstd, static_cast<const uint4*>(g.a_gamma));
   trace_after(s, name);
   return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+}
+
+// Output tile width: the one whose last wave of tiles is fullest, measured as
+// waves x BN (the work one SM does along N), ties to the wider tile.
+int pick_bn(int64_t M, int64_t N, int sm_count) {
+  const int cand[3] = {256, 192, 128};
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int bn : cand) {
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sm_count - 1) / sm_count;
+    const int64_t cost = waves * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+// RNL_GEMM_BN=128|192|256 in the environment overrides the choice (tuning and
+// tests); any other value is ignored.
+int tile_width(int64_t M, int64_t N, int sm_count) {
+  if (const char* e = std::getenv("RNL_GEMM_BN")) {
+    const int v = std::atoi(e);
+    if (v == 128 || v == 192 || v == 256) return v;
+  }
+  return pick_bn(M, N, sm_count);
+}
+
+template <int EPI>
+rnl_status launch_bn(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
+  switch (tile_width(g.M, g.N, dev.sm_count)) {
+    case 128: return launch_epi<EPI, 128, false>(g, dev, s, name);
+    case 192: return launch_epi<EPI, 192, false>(g, dev, s, name);
+    default: return launch_epi<EPI, 256, false>(g, dev, s, name);
+  }
 }
 
 }  // namespace
@@ -369,11 +497,19 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
   DeviceInfo dev;
   rnl_status st = current_device(&dev);
   if (st != RNL_OK) return st;
+  if (g.a_rstd != nullptr) {  // fused norm: bf16 epilogue only
+    if (g.epi != Epi::kBf16) return RNL_ERR_ARG;
+    switch (tile_width(g.M, g.N, dev.sm_count)) {
+      case 128: return launch_epi<0, 128, true>(g, dev, s, "gemm_bf16_fused_norm");
+      case 192: return launch_epi<0, 192, true>(g, dev, s, "gemm_bf16_fused_norm");
+      default: return launch_epi<0, 256, true>(g, dev, s, "gemm_bf16_fused_norm");
+    }
+  }
   switch (g.epi) {
-    case Epi::kBf16: return launch_epi<0>(g, dev, s, "gemm_bf16");
-    case Epi::kRowScaleF32: return launch_epi<1>(g, dev, s, "gemm_rowscale_f32");
-    case Epi::kDequantBf16: return launch_epi<2>(g, dev, s, "gemm_int_dequant");
-    case Epi::kInt32: return launch_epi<3>(g, dev, s, "gemm_int_s32");
+    case Epi::kBf16: return launch_bn<0>(g, dev, s, "gemm_bf16");
+    case Epi::kRowScaleF32: return launch_bn<1>(g, dev, s, "gemm_rowscale_f32");
+    case Epi::kDequantBf16: return launch_bn<2>(g, dev, s, "gemm_int_dequant");
+    case Epi::kInt32: return launch_bn<3>(g, dev, s, "gemm_int_s32");
   }
   return RNL_ERR_ARG;
 }

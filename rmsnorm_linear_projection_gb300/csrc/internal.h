@@ -64,6 +64,10 @@ struct GemmArgs {
   const float* row_scale = nullptr;
   const float* col_scale = nullptr;
   Epi epi = Epi::kBf16;
+  // fused norm (bf16 epilogue only): A is raw x; the kernel feeds the MMA
+  // bf16((x * a_rstd[m]) * a_gamma[k]) (a_gamma may be null)
+  const float* a_rstd = nullptr;
+  const void* a_gamma = nullptr;
 };
 rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s);
 

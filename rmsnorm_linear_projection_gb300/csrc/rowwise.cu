@@ -164,6 +164,39 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
 }
 
+// rstd only, whole row in registers (K <= 32 * 8 * VPL): all loads first.
+template <int MODE, int VPL>
+__global__ void __launch_bounds__(kWarps * 32)
+    row_rstd_regs_kernel(const uint4* __restrict__ x, int64_t T, int nvec, float inv_d, float eps,
+                         float* __restrict__ rstd_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= T) return;
+  const uint4* xr = x + row * nvec;
+  uint4 u[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int v = lane + 32 * i;
+    u[i] = v < nvec ? ldg16(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    float f[8];
+    unpack8(u[i], f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (MODE == 0)
+        s = fmaf(f[j], f[j], s);
+      else
+        s = fmaf(f[j] * f[j], inv_d, s);
+    }
+  }
+  s = warp_sum(s);
+  const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
+  if (lane == 0) rstd_out[row] = rstd;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kWarps * 32)
     row_rstd_kernel(const uint4* __restrict__ x, int64_t T, int nvec, float inv_d, float eps,
@@ -307,8 +340,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int v = lane + 32 * i;
     u[i] = v < nvec ? ldg16(xr + v) : make_uint4(0u, 0u, 0u, 0u);
   }
-  // sum of squares: float-float accumulation, one rounding (see row_rstd_exactsum)
-  float hi = 0.f, lo = 0.f;
+  // sum of squares: float-float accumulation, one rounding (see
+  // row_rstd_exactsum), in eight independent chains (one per element of the
+  // 16-byte vector) so the TwoSum latency overlaps; the chains are merged
+  // with the same error-free additions.
+  float hs[8], ls[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) hs[j] = ls[j] = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     float f[8];
@@ -318,10 +356,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       float t = __fmul_rn(f[j], f[j]);
       if (MODE == 1) t = __fmul_rn(t, inv_d);
       float sum, e;
-      two_sum(hi, t, sum, e);
-      hi = sum;
-      lo = __fadd_rn(lo, e);
+      two_sum(hs[j], t, sum, e);
+      hs[j] = sum;
+      ls[j] = __fadd_rn(ls[j], e);
     }
+  }
+  float hi = hs[0], lo = ls[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) {
+    float sum, e;
+    two_sum(hi, hs[j], sum, e);
+    lo = __fadd_rn(__fadd_rn(lo, ls[j]), e);
+    hi = sum;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -505,10 +551,28 @@ rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int m
   const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
   const auto* xp = static_cast<const uint4*>(x);
   trace_before(s);
-  if (mode == RNL_NORM_RSQRT)
-    row_rstd_kernel<0><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
-  else
-    row_rstd_kernel<1><<<row_blocks(T), kWarps * 32, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+  const unsigned blocks = row_blocks(T);
+  constexpr unsigned kT = kWarps * 32;
+  const int vpl = (nvec + 31) / 32;
+  if (mode == RNL_NORM_RSQRT) {
+    if (vpl <= 4)
+      row_rstd_regs_kernel<0, 4><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else if (vpl <= 8)
+      row_rstd_regs_kernel<0, 8><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else if (vpl <= 16)
+      row_rstd_regs_kernel<0, 16><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else
+      row_rstd_kernel<0><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+  } else {
+    if (vpl <= 4)
+      row_rstd_regs_kernel<1, 4><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else if (vpl <= 8)
+      row_rstd_regs_kernel<1, 8><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else if (vpl <= 16)
+      row_rstd_regs_kernel<1, 16><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+    else
+      row_rstd_kernel<1><<<blocks, kT, 0, s>>>(xp, T, nvec, inv_d, eps, rstd);
+  }
   return launched(s, "row_rstd");
 }
 

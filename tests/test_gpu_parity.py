@@ -57,6 +57,49 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
     assert_bf16_close(host_bits(out), want, f"bf16 {T}x{K}x{N}")
 
 
+@pytest.mark.parametrize("bn", [128, 192, 256])
+@pytest.mark.parametrize("T,K,N", [(300, 520, 600), (129, 4096, 256)])
+def test_bf16_each_tile_width(orc, monkeypatch, bn, T, K, N):
+    monkeypatch.setenv("RNL_GEMM_BN", str(bn))
+    d = _rand_case(bn + T + N, T, K, N, True)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, 0, 0)
+    assert_bf16_close(host_bits(out), want, f"bf16 BN={bn} {T}x{K}x{N}")
+
+
+@pytest.mark.parametrize("bn", [128, 192, 256])
+def test_gemm_s8_each_tile_width(orc, monkeypatch, bn):
+    monkeypatch.setenv("RNL_GEMM_BN", str(bn))
+    rng = np.random.default_rng(bn)
+    A = rng.integers(-127, 128, (260, 2064)).astype(np.int8)
+    B = rng.integers(-127, 128, (520, 2064)).astype(np.int8)
+    C = rnl.rnl_gemm_s8s8s32(dev(A), dev(B)).cpu().numpy()
+    want, _ = orc.gemm_s8(A, B)
+    assert np.array_equal(C, want)
+
+
+@pytest.mark.parametrize("T,K,N,mode,gamma", [(130, 72, 300, 0, True), (640, 4096, 512, 1, False)])
+def test_bf16_fused_norm_form(orc, monkeypatch, T, K, N, mode, gamma):
+    """RNL_FUSED_NORM=1: transform warps normalise the A stages inside the GEMM."""
+    monkeypatch.setenv("RNL_FUSED_NORM", "1")
+    d = _rand_case(3 + T + K + N, T, K, N, gamma)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]) if gamma else None,
+                                  dev_bf16(d["W"]), eps=1e-6, norm_mode=mode)
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, mode, 0)
+    assert_bf16_close(host_bits(out), want, f"fused-norm bf16 {T}x{K}x{N}")
+
+
+def test_fused_and_two_kernel_forms_agree(monkeypatch):
+    """Both forms compute bf16((x * rstd) * gamma) with the same arithmetic."""
+    d = _rand_case(99, 520, 2048, 700, True)
+    args = (dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
+    monkeypatch.setenv("RNL_FUSED_NORM", "1")
+    a = host_bits(rnl.rmsnorm_linear_bf16(*args))
+    monkeypatch.setenv("RNL_FUSED_NORM", "0")
+    b = host_bits(rnl.rmsnorm_linear_bf16(*args))
+    assert np.array_equal(a, b)
+
+
 def test_tiny_workload_and_golden(orc):
     c = si.CONFIGS["tiny"]
     d = si.make_projection(c)
@@ -117,11 +160,13 @@ def test_skinny_full_sampled(orc):
 
 
 # -------------------------------------------------------------- MLA chain
+@pytest.mark.parametrize("fused", ["1", "0"])
 @pytest.mark.parametrize("T,K,N1,N2,mode", [
     (200, 1024, 512, 1000, 1),
     (129, 520, 136, 264, 0),
 ])
-def test_mla_small(orc, T, K, N1, N2, mode):
+def test_mla_small(orc, monkeypatch, fused, T, K, N1, N2, mode):
+    monkeypatch.setenv("RNL_FUSED_NORM", fused)
     c = dict(seed=T + K, T=T, K=K, N1=N1, N2=N2)
     d = si.make_mla(c)
     qa = torch.empty((T, N1), dtype=torch.bfloat16, device="cuda")
