@@ -75,9 +75,10 @@ struct Carve {
 
 // Workspace layouts (a null base just measures).
 struct BF16Layout {
+  void* part = nullptr;   // gemm K-split partial sums (bf16 out; fp32 out with N > 64)
   void* A = nullptr;      // bf16 [T, K] normed activations (bf16 out, two-kernel form)
   float* rstd = nullptr;  // [T] (bf16 out; fp32 out with N > 64)
-  void* part = nullptr;   // skinny partials (fp32 out, N <= 64)
+  void* skinny = nullptr; // skinny partials (fp32 out, N <= 64)
   size_t bytes = 0;
 };
 BF16Layout bf16_layout(void* ws, int64_t T, int64_t K, int64_t N, int out_dtype) {
@@ -86,10 +87,12 @@ BF16Layout bf16_layout(void* ws, int64_t T, int64_t K, int64_t N, int out_dtype)
   if (out_dtype == RNL_OUT_BF16) {
     l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
     l.A = c.take(static_cast<size_t>(T) * K * 2);  // only the two-kernel form uses it
+    l.part = c.take(kGemmPartialBytes);
   } else if (N <= 64) {
-    l.part = c.take(skinny_workspace_bytes(T, K, N, 0));
+    l.skinny = c.take(skinny_workspace_bytes(T, K, N, 0));
   } else {
     l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+    l.part = c.take(kGemmPartialBytes);
   }
   l.bytes = c.used;
   return l;
@@ -99,6 +102,7 @@ struct W8A8Layout {
   void* A = nullptr;        // bf16 [T, K] integer codes
   void* Wb = nullptr;       // bf16 [N, K] widened weight
   float* xs = nullptr;      // [T] x_scale when the caller passes none
+  void* part = nullptr;     // gemm K-split partial sums
   size_t bytes = 0;
 };
 W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
@@ -107,6 +111,7 @@ W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
   l.A = c.take(static_cast<size_t>(T) * K * 2);
   l.Wb = c.take(static_cast<size_t>(N) * K * 2);
   l.xs = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.part = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -115,6 +120,7 @@ struct MLALayout {
   void* qa = nullptr;     // bf16 [T, N1] stage-1 output when the caller passes none
   void* z = nullptr;      // bf16 [T, N1] normed * gamma_cq (two-kernel form)
   float* rstd = nullptr;  // [T] rstd of the stage-1 rows
+  void* part = nullptr;   // gemm K-split partial sums (both stages, one after the other)
   size_t bytes = 0;
 };
 MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
@@ -123,6 +129,7 @@ MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
   l.qa = c.take(static_cast<size_t>(T) * N1 * 2);
   l.z = c.take(static_cast<size_t>(T) * N1 * 2);
   l.rstd = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.part = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -130,6 +137,7 @@ MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
 struct S8Layout {
   void* A = nullptr;
   void* B = nullptr;
+  void* part = nullptr;
   size_t bytes = 0;
 };
 S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
@@ -137,6 +145,7 @@ S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
   Carve c(ws);
   l.A = c.take(static_cast<size_t>(M) * K * 2);
   l.B = c.take(static_cast<size_t>(N) * K * 2);
+  l.part = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -288,6 +297,8 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
     g.K = K;
     g.out = out;
     g.epi = Epi::kBf16;
+    g.partial_ws = l.part;
+    g.partial_ws_bytes = kGemmPartialBytes;
     if (fused_norm()) {
       st = launch_row_rstd(x, T, K, eps, norm_mode, l.rstd, s);
       if (st != RNL_OK) return st;
@@ -295,15 +306,16 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
       g.a_rstd = l.rstd;
       g.a_gamma = gamma;
     } else {
-      st = launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
+      st = norm_cast_stream_fits(K) ? launch_norm_cast_stream(x, gamma, T, K, eps, norm_mode, l.A, s)
+                                    : launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
       if (st != RNL_OK) return st;
       g.A = l.A;
     }
     return launch_gemm(g, s);
   }
   if (N <= 64)
-    return launch_skinny(x, W, T, K, N, eps, norm_mode, static_cast<float*>(out), l.part,
-                         workspace_bytes, dev.sm_count, s);
+    return launch_skinny(x, W, T, K, N, eps, norm_mode, static_cast<float*>(out), l.skinny,
+                         skinny_workspace_bytes(T, K, N, dev.sm_count), dev.sm_count, s);
   st = launch_row_rstd(x, T, K, eps, norm_mode, l.rstd, s);
   if (st != RNL_OK) return st;
   GemmArgs g;
@@ -315,6 +327,8 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
   g.out = out;
   g.row_scale = l.rstd;
   g.epi = Epi::kRowScaleF32;
+  g.partial_ws = l.part;
+  g.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
 }
 
@@ -352,6 +366,8 @@ rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* W
   g.row_scale = xs;
   g.col_scale = w_scale;
   g.epi = Epi::kDequantBf16;
+  g.partial_ws = l.part;
+  g.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
 }
 
@@ -384,6 +400,8 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   g1.K = K;
   g1.out = qa;
   g1.epi = Epi::kBf16;
+  g1.partial_ws = l.part;
+  g1.partial_ws_bytes = kGemmPartialBytes;
   st = launch_gemm(g1, s);
   if (st != RNL_OK) return st;
   GemmArgs g2;
@@ -394,7 +412,9 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
     g2.a_rstd = l.rstd;
     g2.a_gamma = gamma_cq;
   } else {
-    st = launch_norm_cast(qa, gamma_cq, T, N1, eps, norm_mode, l.z, nullptr, s);
+    st = norm_cast_stream_fits(N1)
+             ? launch_norm_cast_stream(qa, gamma_cq, T, N1, eps, norm_mode, l.z, s)
+             : launch_norm_cast(qa, gamma_cq, T, N1, eps, norm_mode, l.z, nullptr, s);
     if (st != RNL_OK) return st;
     g2.A = l.z;
   }
@@ -404,6 +424,8 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   g2.K = N1;
   g2.out = out;
   g2.epi = Epi::kBf16;
+  g2.partial_ws = l.part;
+  g2.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g2, s);
 }
 
@@ -435,6 +457,8 @@ rnl_status rnl_gemm_s8s8s32(const int8_t* A, const int8_t* B, int32_t* C, int64_
   g.K = K;
   g.out = C;
   g.epi = Epi::kInt32;
+  g.partial_ws = l.part;
+  g.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
 }
 
@@ -443,9 +467,10 @@ rnl_status rnl_check_device_error(rnl_stream_t stream, int* site) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
   }
-  unsigned int words[3] = {0, 0, 0};
+  unsigned int words[5] = {0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
-      read_clear_error_skinny(&words[2]) != RNL_OK)
+      read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
+      read_clear_error_norm(&words[4]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {

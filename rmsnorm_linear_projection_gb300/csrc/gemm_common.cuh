@@ -1,0 +1,109 @@
+// gemm_common.cuh -- pieces shared by the one-CTA (gemm_tc.cu) and CTA-pair
+// (gemm_pair.cu) tcgen05 GEMM kernels: tile geometry, tile order and the
+// epilogue stores of one thread's 32 consecutive output columns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+namespace rnl {
+namespace gemm {
+
+constexpr int BM = 128;     // rows of A per CTA (and TMEM lanes)
+constexpr int BK = 64;      // 64 bf16 = one 128-byte swizzle row
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr int kChunkKBlocks = 16;       // 1024 products per exact integer chunk
+constexpr int kMaxStages = 8;
+constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in shared memory per block
+constexpr uint32_t kAccStride = 256;    // TMEM column offset between the two accumulators
+constexpr int kThreads = 320;           // producer + MMA + 8 epilogue warps (or 4 + 4 transform)
+
+// Tile order: groups of G row blocks, row block fastest within a group column,
+// so the CTAs running at the same time share A panels and B panels in L2.  G
+// is chosen on the host: all row blocks when A fits comfortably in L2 (then
+// every B panel is fetched from HBM once), else 8.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int G, int& mb,
+                                            int& nb) {
+  const int group_tiles = G * num_n;
+  const int group = tile / group_tiles;
+  const int first_m = group * G;
+  const int gm = min(num_m - first_m, G);
+  const int r = tile - group * group_tiles;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// out[m, n0 .. n0+31] = bf16(v), v given as fp32 bit patterns (TMEM words).
+__device__ __forceinline__ void store_bf16_32(void* out, int64_t m, int n0, int N,
+                                              const uint32_t (&r)[32]) {
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
+  if (n0 + 32 <= N && (N & 7) == 0) {
+    uint4* dst = reinterpret_cast<uint4*>(orow + n0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[j] = make_uint4(bf16x2_bits(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
+                          bf16x2_bits(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                          bf16x2_bits(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                          bf16x2_bits(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+  }
+}
+
+// out[m, n0 .. n0+31] = fp32(v) * rs.
+__device__ __forceinline__ void store_f32_scaled_32(void* out, int64_t m, int n0, int N,
+                                                    const uint32_t (&r)[32], float rs) {
+  float* orow = static_cast<float*>(out) + m * N;
+  if (n0 + 32 <= N && (N & 3) == 0) {
+    float4* dst = reinterpret_cast<float4*>(orow + n0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      dst[j] = make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                           __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < N) orow[n0 + j] = __uint_as_float(r[j]) * rs;
+  }
+}
+
+// out[m, n0 .. n0+31] = the exact int32 sums.
+__device__ __forceinline__ void store_i32_32(void* out, int64_t m, int n0, int N,
+                                             const int (&a)[32]) {
+  int* orow = static_cast<int*>(out) + m * N;
+  if (n0 + 32 <= N && (N & 3) == 0) {
+    int4* dst = reinterpret_cast<int4*>(orow + n0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[j] = make_int4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < N) orow[n0 + j] = a[j];
+  }
+}
+
+// AT-06 dequant in the order of the SK-14 skeleton page (QuantMatMulReduceSum):
+// float(acc) * (x_scale[m] * w_scale[n]), then bf16.
+__device__ __forceinline__ void store_dequant_32(void* out, int64_t m, int n0, int N,
+                                                 const int (&a)[32], float xs,
+                                                 const float* __restrict__ w_scale) {
+  uint32_t v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    const float ws = n < N ? __ldg(w_scale + n) : 0.f;
+    v[j] = __float_as_uint(static_cast<float>(a[j]) * (xs * ws));
+  }
+  store_bf16_32(out, m, n0, N, v);
+}
+
+}  // namespace gemm
+}  // namespace rnl

@@ -29,6 +29,7 @@
 
 #include <cstdlib>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,14 +38,7 @@ namespace {
 
 __device__ unsigned int g_err_gemm;
 
-constexpr int BM = 128;
-constexpr int BK = 64;  // 64 bf16 = one 128-byte swizzle row
-constexpr int kThreads = 320;  // producer + MMA + 8 epilogue warps, or 4 epilogue + 4 transform
-constexpr uint32_t kABytes = BM * BK * 2;
-constexpr int kChunkKBlocks = 16;  // 1024 products per exact chunk
-constexpr int kMaxStages = 8;
-constexpr uint32_t kAccStride = 256;  // TMEM column offset between the two accumulators
-constexpr size_t kSmemLimit = 232448;  // 227 KB opt-in shared memory per block
+using namespace gemm;
 
 // Tile-width dependent constants (BN = 128, 192 or 256 output columns).
 template <int BN>
@@ -76,19 +70,6 @@ static_assert(smem_bytes<256>() <= kSmemLimit && smem_bytes<192>() <= kSmemLimit
                   smem_bytes<128>() <= kSmemLimit,
               "shared memory budget");
 
-// Tile order: groups of 8 M-tiles, N fastest within a group column, so the
-// CTAs running at the same time share A panels and B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-  constexpr int G = 8;
-  const int group_tiles = G * num_n;
-  const int group = tile / group_tiles;
-  const int first_m = group * G;
-  const int gm = min(num_m - first_m, G);
-  const int r = tile - group * group_tiles;
-  mb = first_m + r % gm;
-  nb = r / gm;
-}
-
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t site) {
   const bool ok = mbar_wait(bar, parity, abort, &g_err_gemm, site);
@@ -101,9 +82,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int EPI, int BN, bool NORM_A>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                int M, int N, int K, void* __restrict__ out, const float* __restrict__ row_scale,
-                const float* __restrict__ col_scale, const float* __restrict__ a_rstd,
-                const uint4* __restrict__ a_gamma) {
+                int M, int N, int K, int group_m, void* __restrict__ out,
+                const float* __restrict__ row_scale, const float* __restrict__ col_scale,
+                const float* __restrict__ a_rstd, const uint4* __restrict__ a_gamma) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
   static_assert(!(NORM_A && kInt), "the fused norm feeds the bf16 GEMM only");
@@ -150,6 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The set-up above overlaps the previous kernel when launched as its
+  // programmatic dependent; from here on its outputs (A, row scales) are read.
+  grid_launch_dependents();
+  grid_dependency_wait();
   const uint32_t tmem_base = ctrl->tmem_base;
   volatile int* abort = &ctrl->abort;
 
@@ -161,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, mb, nb);
+        tile_coords(tile, num_m, num_n, group_m, mb, nb);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_gemm, 1)) {
@@ -239,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int mb, nb;
-      tile_coords(tile, num_m, num_n, mb, nb);
+      tile_coords(tile, num_m, num_n, group_m, mb, nb);
       const int m = mb * BM + row_local;
       const int n_base = nb * BN + half * kColsPerEpiWarp;
       const bool row_ok = m < M;
@@ -271,41 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) iacc[c][j] += __float2int_rn(__uint_as_float(r[j]));
           } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-            if (row_ok) {
-              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(m) * N;
-              if (n0 + 32 <= N && (N & 7) == 0) {
-                uint32_t p[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]),
-                                                           __uint_as_float(r[2 * j + 1]));
-                  p[j] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(orow + n0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(__uint_as_float(r[j]));
-              }
-            }
+            if (row_ok) store_bf16_32(out, m, n0, N, r);
           } else {  // kRowScaleF32
-            if (row_ok) {
-              float* orow = static_cast<float*>(out) + static_cast<int64_t>(m) * N;
-              if (n0 + 32 <= N && (N & 3) == 0) {
-                float4* dst = reinterpret_cast<float4*>(orow + n0);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  dst[j] = make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
-                                       __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (n0 + j < N) orow[n0 + j] = __uint_as_float(r[j]) * rs;
-              }
-            }
+            if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
           }
         }
         tc_fence_before();
@@ -317,47 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok) {
 #pragma unroll
           for (int c = 0; c < kGroups; ++c) {
-            const int n0 = n_base + c * 32;
-            if constexpr (EPI == static_cast<int>(Epi::kInt32)) {
-              int* orow = static_cast<int*>(out) + static_cast<int64_t>(m) * N;
-              if (n0 + 32 <= N && (N & 3) == 0) {
-                int4* dst = reinterpret_cast<int4*>(orow + n0);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  dst[j] = make_int4(iacc[c][4 * j], iacc[c][4 * j + 1], iacc[c][4 * j + 2], iacc[c][4 * j + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (n0 + j < N) orow[n0 + j] = iacc[c][j];
-              }
-            } else {
-              // AT-06 dequant, SK-14 skeleton page (QuantMatMulReduceSum):
-              // float(acc) * (x_scale * w_scale), then bf16.
-              __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(m) * N;
-              float v[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int n = n0 + j;
-                const float ws = n < N ? __ldg(col_scale + n) : 0.f;
-                v[j] = static_cast<float>(iacc[c][j]) * (rs * ws);
-              }
-              if (n0 + 32 <= N && (N & 7) == 0) {
-                uint32_t p[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-                  p[j] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(orow + n0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(v[j]);
-              }
-            }
+            if constexpr (EPI == static_cast<int>(Epi::kInt32))
+              store_i32_32(out, m, n_base + c * 32, N, iacc[c]);
+            else
+              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale);
           }
         }
       }
@@ -374,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       int mb, nb;
-      tile_coords(tile, num_m, num_n, mb, nb);
+      tile_coords(tile, num_m, num_n, group_m, mb, nb);
       const int m = mb * BM + t;
       const float rs = m < M ? __ldg(a_rstd + m) : 0.f;
       for (int kb = 0; kb < num_kb; ++kb) {
@@ -446,25 +362,51 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
   const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
   const unsigned grid = static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count);
   trace_before(s);
-  kern<<<grid, kThreads, smem_bytes<BN>(), s>>>(ma, mb, static_cast<int>(g.M), static_cast<int>(g.N),
-                                                static_cast<int>(g.K), g.out, g.row_scale, g.col_scale,
-                                                g.a_rstd, static_cast<const uint4*>(g.a_gamma));
+  const int num_m = static_cast<int>((g.M + BM - 1) / BM);
+  const int group_m = (g.M * g.K * 2 <= (int64_t{48} << 20)) ? num_m : (num_m < 8 ? num_m : 8);
+  // programmatic dependent launch: the CTAs' set-up overlaps the previous kernel
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<BN>();
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
+                                           static_cast<int>(g.N), static_cast<int>(g.K), group_m,
+                                           g.out, g.row_scale, g.col_scale, g.a_rstd,
+                                           static_cast<const uint4*>(g.a_gamma));
   trace_after(s, name);
-  return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RNL_ERR_LAUNCH;
+  }
+  return RNL_OK;
 }
 
-// Output tile width: the one whose last wave of tiles is fullest, measured as
-// waves x BN (the work one SM does along N), ties to the wider tile.
-int pick_bn(int64_t M, int64_t N, int sm_count) {
+// Per-SM throughput of the one-CTA kernel in full waves on GB300 (measured:
+// 1627 and 1594 TFLOP/s over 152 SMs at BN = 256 and 192; 128 estimated).
+double one_cta_rate(int bn) { return bn == 256 ? 10.70e12 : (bn == 192 ? 10.49e12 : 9.4e12); }
+
+// Predicted one-CTA time (microseconds) at tile width bn: whole waves of tiles.
+double predict_one_cta_us(int64_t M, int64_t N, int64_t K, int sm_count, int bn) {
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const int64_t waves = (tiles + sm_count - 1) / sm_count;
+  return waves * (2.0 * BM * bn * static_cast<double>(K) / one_cta_rate(bn)) * 1e6;
+}
+
+// Output tile width of the one-CTA kernel: the fastest by predict_one_cta_us.
+int pick_bn(int64_t M, int64_t N, int64_t K, int sm_count) {
   const int cand[3] = {256, 192, 128};
   int best = 256;
-  int64_t best_cost = -1;
+  double best_t = -1.0;
   for (int bn : cand) {
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
-    const int64_t waves = (tiles + sm_count - 1) / sm_count;
-    const int64_t cost = waves * bn;
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
+    const double t = predict_one_cta_us(M, N, K, sm_count, bn);
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
       best = bn;
     }
   }
@@ -473,17 +415,17 @@ int pick_bn(int64_t M, int64_t N, int sm_count) {
 
 // RNL_GEMM_BN=128|192|256 in the environment overrides the choice (tuning and
 // tests); any other value is ignored.
-int tile_width(int64_t M, int64_t N, int sm_count) {
+int tile_width(int64_t M, int64_t N, int64_t K, int sm_count) {
   if (const char* e = std::getenv("RNL_GEMM_BN")) {
     const int v = std::atoi(e);
     if (v == 128 || v == 192 || v == 256) return v;
   }
-  return pick_bn(M, N, sm_count);
+  return pick_bn(M, N, K, sm_count);
 }
 
 template <int EPI>
 rnl_status launch_bn(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
-  switch (tile_width(g.M, g.N, dev.sm_count)) {
+  switch (tile_width(g.M, g.N, g.K, dev.sm_count)) {
     case 128: return launch_epi<EPI, 128, false>(g, dev, s, name);
     case 192: return launch_epi<EPI, 192, false>(g, dev, s, name);
     default: return launch_epi<EPI, 256, false>(g, dev, s, name);
@@ -497,9 +439,28 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
   DeviceInfo dev;
   rnl_status st = current_device(&dev);
   if (st != RNL_OK) return st;
+  // Kernel choice for plain GEMMs: the CTA-pair kernel (gemm_pair.cu) when its
+  // predicted time beats the best one-CTA tile width.  The exact-integer mode
+  // stays on one CTA (measured faster there: its per-chunk accumulator
+  // hand-off waits on both CTAs of a pair).  RNL_GEMM_PAIR=0/1 forces the
+  // choice; the fused-norm form always runs here.
+  if (g.a_rstd == nullptr) {
+    const char* e = std::getenv("RNL_GEMM_PAIR");
+    bool pair;
+    if (e != nullptr && (e[0] == '0' || e[0] == '1')) {
+      pair = e[0] == '1';
+    } else {
+      const bool integer = g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32;
+      const int bn = pick_bn(g.M, g.N, g.K, dev.sm_count);
+      pair = !integer && g.N >= 256 &&
+             predict_pair_us(g.M, g.N, g.K, dev.sm_count, resident_pairs_for(dev)) <
+                 predict_one_cta_us(g.M, g.N, g.K, dev.sm_count, bn);
+    }
+    if (pair) return launch_gemm_pair(g, s);
+  }
   if (g.a_rstd != nullptr) {  // fused norm: bf16 epilogue only
     if (g.epi != Epi::kBf16) return RNL_ERR_ARG;
-    switch (tile_width(g.M, g.N, dev.sm_count)) {
+    switch (tile_width(g.M, g.N, g.K, dev.sm_count)) {
       case 128: return launch_epi<0, 128, true>(g, dev, s, "gemm_bf16_fused_norm");
       case 192: return launch_epi<0, 192, true>(g, dev, s, "gemm_bf16_fused_norm");
       default: return launch_epi<0, 256, true>(g, dev, s, "gemm_bf16_fused_norm");

@@ -38,6 +38,11 @@ void trace_after(cudaStream_t s, const char* name);
 // y = (x * rstd) * gamma cast to bf16 into A [T, K]; rstd_out optional.
 rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                             int mode, void* A, float* rstd_out, cudaStream_t s);
+// The same as a persistent bulk-copy stream (normstream.cu), for K <= 4096;
+// launched as a programmatic dependent.
+bool norm_cast_stream_fits(int64_t K);
+rnl_status launch_norm_cast_stream(const void* x, const void* gamma, int64_t T, int64_t K,
+                                   float eps, int mode, void* A, cudaStream_t s);
 // rstd only.
 rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int mode, float* rstd,
                            cudaStream_t s);
@@ -68,8 +73,21 @@ struct GemmArgs {
   // bf16((x * a_rstd[m]) * a_gamma[k]) (a_gamma may be null)
   const float* a_rstd = nullptr;
   const void* a_gamma = nullptr;
+  // partial sums of the CTA-pair GEMM's K-split tail (see gemm_pair.cu);
+  // without it the leftover tiles run whole
+  void* partial_ws = nullptr;
+  size_t partial_ws_bytes = 0;
 };
+
+// At most this many K-split pieces of 2 x 128 x 256 32-bit partial sums.
+constexpr int kMaxPartialSlots = 128;
+constexpr size_t kGemmPartialBytes = static_cast<size_t>(kMaxPartialSlots) * 2 * 128 * 256 * 4;
 rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s);
+// The same GEMM on CTA pairs (tcgen05 cta_group::2, gemm_pair.cu); no fused norm.
+rnl_status launch_gemm_pair(const GemmArgs& g, cudaStream_t s);
+// Predicted pair-kernel time (microseconds) and resident CTA pairs (gemm_pair.cu).
+double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs);
+int resident_pairs_for(const DeviceInfo& dev);
 
 // ---- skinny split-K streaming kernel (skinny.cu) ----
 size_t skinny_workspace_bytes(int64_t T, int64_t K, int64_t N, int sm_count);
@@ -81,5 +99,7 @@ rnl_status launch_skinny(const void* x, const void* W, int64_t T, int64_t K, int
 rnl_status read_clear_error_rowwise(unsigned int* word);
 rnl_status read_clear_error_gemm(unsigned int* word);
 rnl_status read_clear_error_skinny(unsigned int* word);
+rnl_status read_clear_error_pair(unsigned int* word);
+rnl_status read_clear_error_norm(unsigned int* word);
 
 }  // namespace rnl

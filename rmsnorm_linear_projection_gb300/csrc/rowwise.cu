@@ -103,67 +103,6 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// Same computation with the whole row held in registers (K <= 32 * 8 * VPL,
-// used up to K = 4096):
-// all of a lane's 16-byte loads are issued before any arithmetic, and the
-// normalise pass reuses the registers instead of re-reading x.  The sum runs
-// in the same order as in norm_cast_kernel, so the results are identical.
-template <int MODE, bool GAMMA, int VPL>
-__global__ void __launch_bounds__(kWarps * 32, 2)
-    norm_cast_regs_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
-                          int nvec, float inv_d, float eps, uint4* __restrict__ A,
-                          float* __restrict__ rstd_out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (row >= T) return;
-  const uint4* xr = x + row * nvec;
-  uint4 u[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int v = lane + 32 * i;
-    u[i] = v < nvec ? ldg16(xr + v) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    float f[8];
-    unpack8(u[i], f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (MODE == 0)
-        s = fmaf(f[j], f[j], s);
-      else
-        s = fmaf(f[j] * f[j], inv_d, s);
-    }
-  }
-  s = warp_sum(s);
-  const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
-  if (rstd_out != nullptr && lane == 0) rstd_out[row] = rstd;
-  uint4* ar = A + row * nvec;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int v = lane + 32 * i;
-    if (v >= nvec) break;
-    float f[8];
-    unpack8(u[i], f);
-    if (GAMMA) {
-      float g[8];
-      unpack8(ldg16(gamma + v), g);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = (f[j] * rstd) * g[j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = f[j] * rstd;
-    }
-    uint4 o;
-    o.x = pack_bf16x2(f[0], f[1]);
-    o.y = pack_bf16x2(f[2], f[3]);
-    o.z = pack_bf16x2(f[4], f[5]);
-    o.w = pack_bf16x2(f[6], f[7]);
-    ar[v] = o;
-  }
-}
-
 // rstd only, whole row in registers (K <= 32 * 8 * VPL): all loads first.
 template <int MODE, int VPL>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -499,26 +438,6 @@ inline rnl_status launched(cudaStream_t s, const char* name) {
   return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
 }
 
-template <int MODE, bool GAMMA>
-void norm_cast_dispatch(const uint4* xp, const uint4* gp, int64_t T, int nvec, float inv_d,
-                        float eps, uint4* ap, float* rstd_out, cudaStream_t s) {
-  const unsigned blocks = row_blocks(T);
-  constexpr unsigned kT = kWarps * 32;
-  const int vpl = (nvec + 31) / 32;
-  if (vpl <= 1)
-    norm_cast_regs_kernel<MODE, GAMMA, 1><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-  else if (vpl <= 2)
-    norm_cast_regs_kernel<MODE, GAMMA, 2><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-  else if (vpl <= 4)
-    norm_cast_regs_kernel<MODE, GAMMA, 4><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-  else if (vpl <= 8)
-    norm_cast_regs_kernel<MODE, GAMMA, 8><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-  else if (vpl <= 16)
-    norm_cast_regs_kernel<MODE, GAMMA, 16><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-  else
-    norm_cast_kernel<MODE, GAMMA><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
-}
-
 }  // namespace
 
 rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
@@ -530,16 +449,18 @@ rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t
   const auto* gp = static_cast<const uint4*>(gamma);
   auto* ap = static_cast<uint4*>(A);
   trace_before(s);
+  const unsigned blocks = row_blocks(T);
+  constexpr unsigned kT = kWarps * 32;
   if (mode == RNL_NORM_RSQRT) {
     if (gamma)
-      norm_cast_dispatch<0, true>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out, s);
+      norm_cast_kernel<0, true><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
     else
-      norm_cast_dispatch<0, false>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out, s);
+      norm_cast_kernel<0, false><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
   } else {
     if (gamma)
-      norm_cast_dispatch<1, true>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out, s);
+      norm_cast_kernel<1, true><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
     else
-      norm_cast_dispatch<1, false>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out, s);
+      norm_cast_kernel<1, false><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, rstd_out);
   }
   return launched(s, "norm_cast");
 }

@@ -48,6 +48,8 @@ def _rand_case(seed, T, K, N, gamma=True):
     (257, 1024, 768, 0, False),  # no gamma, three N tiles
     (1000, 256, 100, 1, True),
     (640, 4096, 512, 0, True),   # long K
+    (100, 8200, 300, 0, True),   # K beyond the streamed norm pass (row-loop kernel)
+    (3000, 1536, 256, 1, True),  # many row groups per CTA in the streamed norm pass
 ])
 def test_bf16_small(orc, T, K, N, mode, gamma):
     d = _rand_case(7 + T + K + N, T, K, N, gamma)
@@ -60,6 +62,8 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
 @pytest.mark.parametrize("bn", [128, 192, 256])
 @pytest.mark.parametrize("T,K,N", [(300, 520, 600), (129, 4096, 256)])
 def test_bf16_each_tile_width(orc, monkeypatch, bn, T, K, N):
+    """The one-CTA GEMM (RNL_GEMM_PAIR=0) at each output tile width."""
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
     monkeypatch.setenv("RNL_GEMM_BN", str(bn))
     d = _rand_case(bn + T + N, T, K, N, True)
     out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
@@ -69,6 +73,7 @@ def test_bf16_each_tile_width(orc, monkeypatch, bn, T, K, N):
 
 @pytest.mark.parametrize("bn", [128, 192, 256])
 def test_gemm_s8_each_tile_width(orc, monkeypatch, bn):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
     monkeypatch.setenv("RNL_GEMM_BN", str(bn))
     rng = np.random.default_rng(bn)
     A = rng.integers(-127, 128, (260, 2064)).astype(np.int8)
@@ -112,6 +117,20 @@ def test_tiny_workload_and_golden(orc):
     stored = np.array([[int(v, 16) for v in ln.split()] for ln in open(path) if not ln.startswith("#")],
                       np.uint16)
     assert_bf16_close(out, stored, "tiny vs stored oracle output")
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_one_cta_and_pair_gemm_agree_qkv(monkeypatch, pair):
+    """Full qkv size through both GEMM kernels: identical bf16 results are not
+    required (different accumulation splits), closeness to each other is."""
+    c = si.CONFIGS["qkv"]
+    d = si.make_projection(c)
+    args = (dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
+    monkeypatch.setenv("RNL_GEMM_PAIR", pair)
+    a = host_bits(rnl.rmsnorm_linear_bf16(*args))
+    monkeypatch.setenv("RNL_GEMM_PAIR", "1" if pair == "0" else "0")
+    b = host_bits(rnl.rmsnorm_linear_bf16(*args))
+    assert_bf16_close(a, b, "one-CTA vs pair GEMM")
 
 
 def test_qkv_full_sampled(orc):
