@@ -45,6 +45,19 @@ DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny":
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of the
+# roofline stage per step, from the ncu captures summarised under profiles/;
+# only for kernels unchanged since the capture.
+TRAFFIC = {
+    # gemm_pair_kernel<0,256> 123.22 MB + gemm_pair_fixup_kernel 16.79 MB
+    # (profiles/qkv_step_kernels_4096x6144x4096.md)
+    "qkv": 140.01e6,
+    # skinny_kernel<32,0>: 123.03 MB at T = 2048, scaled by rows to T = 16384
+    # (profiles/skinny_stream_mhc_pre.md)
+    "skinny": 984.2e6,
+}
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -364,7 +377,8 @@ def run_ours(args):
             achieved, peak, punit = dom_amount / per_step_s / 1e12, peaks["bf16"], "TFLOP/s"
         roofline = {"bound": bound, "kernel": dom_name, "achieved": achieved, "peak": peak,
                     "peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
-                    "unit": punit, "frac": achieved / peak, "traffic": None,
+                    "unit": punit, "frac": achieved / peak,
+                    "traffic": TRAFFIC.get(w.name) if not args.T else None,
                     "stage_ms_per_step": per_step_s * 1e3}
     kernels = {k: {"launches": len(v), "total_ms": sum(v), "avg_ms": statistics.mean(v)}
                for k, v in per_kernel.items()}
