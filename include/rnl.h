@@ -206,6 +206,17 @@ rnl_status rnl_gemm_s8s8s32(const int8_t *A, const int8_t *B, int32_t *C, int64_
 rnl_status rnl_check_device_error(rnl_stream_t stream, int *site);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages).  Enqueues one
+ * small kernel that waits, with a 1 ms limit, on a barrier nothing arrives
+ * on -- the bounded wait every kernel of the library uses.  The wait gives
+ * up and records wait site 99 in a device error word; the kernel then
+ * returns normally.  A following rnl_check_device_error() reports
+ * RNL_ERR_TIMEOUT with *site == 99 and clears the word; the CUDA context
+ * stays usable.  Returns RNL_OK when the kernel was enqueued.
+ */
+rnl_status rnl_selftest_wait_timeout(rnl_stream_t stream);
+
+/*
  * Kernel timing trace.  While enabled, every kernel launch made by the
  * library is bracketed by two CUDA events recorded on the launch stream
  * (up to 16384 launches between reads).  rnl_trace_read() waits for the recorded

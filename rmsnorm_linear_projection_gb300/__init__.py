@@ -27,6 +27,7 @@ from ._native import (  # noqa: F401
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
     rnl_gemm_s8s8s32,
+    rnl_selftest_wait_timeout,
     rnl_trace_enable,
     rnl_trace_read,
     workspace_size,

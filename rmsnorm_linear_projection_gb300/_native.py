@@ -30,7 +30,8 @@ STATUS = {
 
 EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
            "rmsnorm_linear_w8a8", "mla_q_chain", "rnl_gemm_s8s8s32", "rnl_check_device_error",
-           "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc")
+           "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc",
+           "rnl_selftest_wait_timeout")
 
 
 class RnlError(RuntimeError):
@@ -57,6 +58,7 @@ def _declare(lib):
         "rnl_trace_enable": (I, [I]),
         "rnl_trace_read": (I, [P, ctypes.POINTER(F), I]),
         "rmsnorm_linear_skinny_noalloc": (I, [P, P, I64, I64, I64, F, I, P, P]),
+        "rnl_selftest_wait_timeout": (I, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -226,6 +228,12 @@ def rnl_gemm_s8s8s32(A, B, out=None, workspace=None, stream=None):
                                    ws.numel() * ws.element_size(), _stream(dev, stream)),
            "rnl_gemm_s8s8s32")
     return out
+
+
+def rnl_selftest_wait_timeout(stream=None, device=None):
+    """Enqueue the failure-detection self-test (a 1 ms bounded wait that must give up)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(load().rnl_selftest_wait_timeout(_stream(dev, stream)), "rnl_selftest_wait_timeout")
 
 
 def rnl_check_device_error(stream=None, device=None):

@@ -467,10 +467,10 @@ rnl_status rnl_check_device_error(rnl_stream_t stream, int* site) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
   }
-  unsigned int words[5] = {0, 0, 0, 0, 0};
+  unsigned int words[6] = {0, 0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
       read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
-      read_clear_error_norm(&words[4]) != RNL_OK)
+      read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {

@@ -101,5 +101,6 @@ rnl_status read_clear_error_gemm(unsigned int* word);
 rnl_status read_clear_error_skinny(unsigned int* word);
 rnl_status read_clear_error_pair(unsigned int* word);
 rnl_status read_clear_error_norm(unsigned int* word);
+rnl_status read_clear_error_selftest(unsigned int* word);
 
 }  // namespace rnl

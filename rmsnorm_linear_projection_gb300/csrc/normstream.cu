@@ -35,7 +35,7 @@ constexpr int kMaxNsStages = 16;
 constexpr size_t kRingBytes = 200 * 1024;
 
 struct __align__(8) NsCtrl {
-  uint64_t full[kMaxNsStages];
+  uint64_t full[kMaxNsStages][kGroupRows];  // one barrier per row slot: a warp starts on its row
   uint64_t empty[kMaxNsStages];
   int abort;
 };
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
   grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&ctrl->full[s]), 1);
+      for (int r = 0; r < kGroupRows; ++r) mbar_init(smem_u32(&ctrl->full[s][r]), 1);
       mbar_init(smem_u32(&ctrl->empty[s]), kConsumerWarps);
     }
     ctrl->abort = 0;
@@ -111,11 +111,12 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_norm, 31)) break;
         const int64_t row0 = g * kGroupRows;
         const int rows = static_cast<int>(T - row0 < kGroupRows ? T - row0 : kGroupRows);
-        const uint32_t bar = smem_u32(&ctrl->full[stage]);
         const uint32_t dst = base + stage * stage_bytes;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * row_bytes);
-        for (int r = 0; r < rows; ++r)
+        for (int r = 0; r < rows; ++r) {
+          const uint32_t bar = smem_u32(&ctrl->full[stage][r]);
+          mbar_arrive_expect_tx(bar, row_bytes);
           bulk_copy_g2s(dst + r * row_bytes, x + (row0 + r) * row_bytes, row_bytes, bar);
+        }
         if (++stage == static_cast<uint32_t>(stages)) {
           stage = 0;
           phase ^= 1u;
@@ -131,10 +132,10 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
     }
     uint32_t stage = 0, phase = 0;
     for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
-      const bool got = mbar_wait(smem_u32(&ctrl->full[stage]), phase, abort, &g_err_norm, 32);
-      if (!__all_sync(0xFFFFFFFFu, got)) break;
       const int64_t row = g * kGroupRows + warp;
       if (row < T) {
+        const bool got = mbar_wait(smem_u32(&ctrl->full[stage][warp]), phase, abort, &g_err_norm, 32);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint4* rp = reinterpret_cast<const uint4*>(smem + stage * stage_bytes + warp * row_bytes);
         uint4 xv[VPL];
 #pragma unroll

@@ -64,15 +64,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Returns false
 // (after raising *abort and recording `site` in *err) when the time limit
 // passes, or at once when another warp of the CTA has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* err, uint32_t site) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                unsigned int* err, uint32_t site,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 31u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicCAS(err, 0u, kErrTimeout | (site << 8));
         atomicOr(err, kErrTimeout);
@@ -80,6 +81,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* err, uint32_t site) {
+  return mbar_wait_limit(bar, parity, abort, err, site, kWaitLimitNs);
 }
 
 // Make this thread's generic-proxy writes to shared memory visible to the
