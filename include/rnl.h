@@ -33,7 +33,9 @@
  *   - Every tensor pointer is a DEVICE pointer of the current CUDA device,
  *     contiguous and row-major, owned by the caller.  The library allocates
  *     no device memory: scratch space comes from the caller's `workspace`,
- *     sized by rnl_workspace_size().
+ *     sized by rnl_workspace_size().  (Exception: the host-buffer pipeline
+ *     at the end, which takes host pointers for x and out and owns its
+ *     device staging.)
  *   - bf16 data are passed as `const void*` (IEEE bfloat16 bit patterns).
  *   - Base pointers (tensors and workspace) must be 16-byte aligned; K must
  *     be a multiple of 8 (bf16 rows) -- the TMA copy engine moves rows whose
@@ -215,6 +217,62 @@ rnl_status rnl_check_device_error(rnl_stream_t stream, int *site);
  * stays usable.  Returns RNL_OK when the kernel was enqueued.
  */
 rnl_status rnl_selftest_wait_timeout(rnl_stream_t stream);
+
+/*
+ * Host-buffer pipeline (no counterpart on the pages: how the projection is
+ * fed when its activations live in host memory).  The calls above take
+ * device pointers; a pipeline takes the activations x from, and returns the
+ * output to, PAGE-LOCKED host memory (cudaHostAlloc / cudaHostRegister),
+ * while the weights stay device pointers, resident across calls.
+ *
+ * A pipeline owns two slots of device staging (x and output buffers), one
+ * workspace and three non-blocking streams: a host-to-device copy stream, a
+ * kernel stream and a device-to-host copy stream.  Submitted call i uses
+ * slot i % 2; its input copy overlaps the kernels of call i - 1 and the
+ * output copy of call i - 2, so a stream of calls runs at the rate of the
+ * slowest of the three (on GB300 usually the host link).  Submitting never
+ * blocks the host.
+ *
+ * rnl_pipeline_create(op, T, K, N, N2, &pipe): sizes as rnl_workspace_size
+ *   (RNL_OP_BF16: N2 = out_dtype; RNL_OP_W8A8: N2 ignored; RNL_OP_MLA:
+ *   N = N1, N2).  Binds the pipeline to the current device and allocates
+ *   2 * (T*K*2 + T*out_width*out_bytes) bytes of staging plus the workspace
+ *   (cudaMalloc; RNL_ERR_WORKSPACE if that fails).  Every call is checked
+ *   against these sizes only; the shape rules of the matching entry point
+ *   apply (K % 8, K % 16 for W8A8, N1 % 8 for MLA).
+ * rnl_pipeline_submit_*: the arguments of rmsnorm_linear_bf16 /
+ *   rmsnorm_linear_w8a8 / mla_q_chain, with x_host and out_host host
+ *   pointers (page-locked, else RNL_ERR_ARG) of T*K bf16 and of the output
+ *   size; the weights, gamma and w_scale are device pointers that must stay
+ *   valid and unchanged until the call completes.  x_host may be reused and
+ *   out_host read only after rnl_pipeline_wait(ticket) returns.  *ticket
+ *   receives the call's number (0, 1, 2, ...).  Argument errors return
+ *   before anything is enqueued and leave the pipeline usable; a CUDA error
+ *   while enqueuing makes every later submit return that status.  The
+ *   W8A8 and MLA calls write no q_out / x_scale_out / qa_out.
+ * rnl_pipeline_wait(pipe, ticket, &site): blocks until call `ticket` has
+ *   written out_host (it may also wait for the next call of the same slot,
+ *   if that one was already submitted), then reads the device error words
+ *   as rnl_check_device_error does, without synchronising anything else.
+ *   RNL_ERR_ARG for a ticket never issued.
+ * rnl_pipeline_destroy(pipe): waits for everything submitted, frees the
+ *   staging, workspace, streams and events.  NULL is a no-op.
+ * A pipeline is not thread-safe; use one per host thread.
+ */
+typedef struct rnl_pipeline rnl_pipeline;
+rnl_status rnl_pipeline_create(int op, int64_t T, int64_t K, int64_t N, int64_t N2,
+                               rnl_pipeline **pipe);
+rnl_status rnl_pipeline_submit_bf16(rnl_pipeline *pipe, const void *x_host, const void *gamma,
+                                    const void *W, float eps, int norm_mode, void *out_host,
+                                    int64_t *ticket);
+rnl_status rnl_pipeline_submit_w8a8(rnl_pipeline *pipe, const void *x_host, const void *gamma,
+                                    const int8_t *Wq, const float *w_scale, float eps,
+                                    int norm_mode, void *out_host, int64_t *ticket);
+rnl_status rnl_pipeline_submit_mla(rnl_pipeline *pipe, const void *x_host, const void *W_qa,
+                                   const void *gamma_cq, const void *W_qb, float eps,
+                                   int norm_mode, void *out_host, int64_t *ticket);
+rnl_status rnl_pipeline_wait(rnl_pipeline *pipe, int64_t ticket, int *site);
+rnl_status rnl_pipeline_destroy(rnl_pipeline *pipe);
 
 /*
  * Kernel timing trace.  While enabled, every kernel launch made by the

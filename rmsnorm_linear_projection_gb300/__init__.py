@@ -8,6 +8,8 @@ arguments; the computation runs in the library's CUDA kernels.
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
+    rnl_pipeline_*        host-buffer pipeline: calls fed from and answering into
+                          pinned host memory, copies overlapped with the kernels
 """
 from ._native import (  # noqa: F401
     EXPORTS,
@@ -19,6 +21,7 @@ from ._native import (  # noqa: F401
     OP_W8A8,
     OUT_BF16,
     OUT_FP32,
+    PipelineHandle,
     RnlError,
     load,
     mla_q_chain,
@@ -27,6 +30,12 @@ from ._native import (  # noqa: F401
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
     rnl_gemm_s8s8s32,
+    rnl_pipeline_create,
+    rnl_pipeline_destroy,
+    rnl_pipeline_submit_bf16,
+    rnl_pipeline_submit_mla,
+    rnl_pipeline_submit_w8a8,
+    rnl_pipeline_wait,
     rnl_selftest_wait_timeout,
     rnl_trace_enable,
     rnl_trace_read,

@@ -31,7 +31,9 @@ STATUS = {
 EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
            "rmsnorm_linear_w8a8", "mla_q_chain", "rnl_gemm_s8s8s32", "rnl_check_device_error",
            "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc",
-           "rnl_selftest_wait_timeout")
+           "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
+           "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
+           "rnl_pipeline_destroy")
 
 
 class RnlError(RuntimeError):
@@ -59,6 +61,12 @@ def _declare(lib):
         "rnl_trace_read": (I, [P, ctypes.POINTER(F), I]),
         "rmsnorm_linear_skinny_noalloc": (I, [P, P, I64, I64, I64, F, I, P, P]),
         "rnl_selftest_wait_timeout": (I, [P]),
+        "rnl_pipeline_create": (I, [I, I64, I64, I64, I64, ctypes.POINTER(P)]),
+        "rnl_pipeline_submit_bf16": (I, [P, P, P, P, F, I, P, ctypes.POINTER(I64)]),
+        "rnl_pipeline_submit_w8a8": (I, [P, P, P, P, P, F, I, P, ctypes.POINTER(I64)]),
+        "rnl_pipeline_submit_mla": (I, [P, P, P, P, P, F, I, P, ctypes.POINTER(I64)]),
+        "rnl_pipeline_wait": (I, [P, I64, ctypes.POINTER(I)]),
+        "rnl_pipeline_destroy": (I, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -255,3 +263,95 @@ def rnl_trace_read(max_records: int = 16384):
     ms = (ctypes.c_float * max_records)()
     n = load().rnl_trace_read(ctypes.cast(names, ctypes.c_void_p), ms, max_records)
     return [(bytes(names[i]).split(b"\0", 1)[0].decode(), float(ms[i])) for i in range(n)]
+
+
+# ---------------------------------------------------------------- host-buffer pipeline
+class PipelineHandle:
+    """An rnl_pipeline* plus the sizes it was created for."""
+
+    def __init__(self, ptr, op, T, K, N, N2, device):
+        self.ptr, self.op, self.T, self.K, self.N, self.N2, self.device = ptr, op, T, K, N, N2, device
+
+    def out_shape_dtype(self):
+        if self.op == OP_MLA:
+            return (self.T, self.N2), torch.bfloat16
+        if self.op == OP_BF16 and self.N2 == OUT_FP32:
+            return (self.T, self.N), torch.float32
+        return (self.T, self.N), torch.bfloat16
+
+
+def _host(t, name, dtype, shape):
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned (page-locked) CPU tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+
+
+def rnl_pipeline_create(op, T, K, N, N2=0, device=None):
+    """Create a host-buffer pipeline on `device` (default: current) for calls of
+    one op and size; N2 = out_dtype for OP_BF16, the stage-2 width for OP_MLA."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ptr = ctypes.c_void_p(None)
+    with torch.cuda.device(dev):
+        _check(load().rnl_pipeline_create(int(op), T, K, N, N2, ctypes.byref(ptr)),
+               "rnl_pipeline_create")
+    return PipelineHandle(ptr, op, T, K, N, N2, dev)
+
+
+def _submit(pipe, name, x_host, out_host, call):
+    _host(x_host, "x_host", torch.bfloat16, (pipe.T, pipe.K))
+    shape, dt = pipe.out_shape_dtype()
+    _host(out_host, "out_host", dt, shape)
+    ticket = ctypes.c_int64(-1)
+    _check(call(ctypes.byref(ticket)), name)
+    return ticket.value
+
+
+def rnl_pipeline_submit_bf16(pipe, x_host, gamma, W, out_host, eps=1e-6, norm_mode=NORM_RSQRT):
+    """Enqueue one rmsnorm_linear_bf16 call fed from pinned host x_host into
+    pinned host out_host; returns its ticket."""
+    dev = pipe.device
+    _need(W, "W", torch.bfloat16, (pipe.N, pipe.K), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (pipe.K,), dev)
+    return _submit(pipe, "rnl_pipeline_submit_bf16", x_host, out_host, lambda t: load().rnl_pipeline_submit_bf16(
+        pipe.ptr, _ptr(x_host), _ptr(gamma), _ptr(W), float(eps), int(norm_mode), _ptr(out_host), t))
+
+
+def rnl_pipeline_submit_w8a8(pipe, x_host, gamma, Wq, w_scale, out_host, eps=1e-6, norm_mode=NORM_RSQRT):
+    """Enqueue one rmsnorm_linear_w8a8 call (host x_host -> host out_host)."""
+    dev = pipe.device
+    _need(Wq, "Wq", torch.int8, (pipe.N, pipe.K), dev)
+    _need(w_scale, "w_scale", torch.float32, (pipe.N,), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (pipe.K,), dev)
+    return _submit(pipe, "rnl_pipeline_submit_w8a8", x_host, out_host, lambda t: load().rnl_pipeline_submit_w8a8(
+        pipe.ptr, _ptr(x_host), _ptr(gamma), _ptr(Wq), _ptr(w_scale), float(eps), int(norm_mode),
+        _ptr(out_host), t))
+
+
+def rnl_pipeline_submit_mla(pipe, x_host, W_qa, gamma_cq, W_qb, out_host, eps=1e-6, norm_mode=NORM_SQRT_DIV):
+    """Enqueue one mla_q_chain call (host x_host -> host out_host)."""
+    dev = pipe.device
+    _need(W_qa, "W_qa", torch.bfloat16, (pipe.N, pipe.K), dev)
+    _need(gamma_cq, "gamma_cq", torch.bfloat16, (pipe.N,), dev)
+    _need(W_qb, "W_qb", torch.bfloat16, (pipe.N2, pipe.N), dev)
+    return _submit(pipe, "rnl_pipeline_submit_mla", x_host, out_host, lambda t: load().rnl_pipeline_submit_mla(
+        pipe.ptr, _ptr(x_host), _ptr(W_qa), _ptr(gamma_cq), _ptr(W_qb), float(eps), int(norm_mode),
+        _ptr(out_host), t))
+
+
+def rnl_pipeline_wait(pipe, ticket):
+    """Block until call `ticket` has written its host output; raises RnlError on a
+    device timeout."""
+    site = ctypes.c_int(0)
+    st = load().rnl_pipeline_wait(pipe.ptr, int(ticket), ctypes.byref(site))
+    if st != 0:
+        raise RnlError(st, f"rnl_pipeline_wait (wait site {site.value})")
+
+
+def rnl_pipeline_destroy(pipe):
+    """Wait for all submitted calls and free the pipeline."""
+    if pipe.ptr:
+        _check(load().rnl_pipeline_destroy(pipe.ptr), "rnl_pipeline_destroy")
+        pipe.ptr = ctypes.c_void_p(None)

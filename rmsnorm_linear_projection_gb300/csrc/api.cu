@@ -230,6 +230,22 @@ void trace_after(cudaStream_t s, const char* name) {
   g_trace_pending = false;
 }
 
+rnl_status read_device_errors(int* site) {
+  unsigned int words[6] = {0, 0, 0, 0, 0, 0};
+  if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
+      read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
+      read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK)
+    return RNL_ERR_LAUNCH;
+  for (unsigned int w : words) {
+    if (w != 0) {
+      if (site) *site = static_cast<int>((w >> 8) & 0xFFu);
+      return RNL_ERR_TIMEOUT;
+    }
+  }
+  if (site) *site = 0;
+  return RNL_OK;
+}
+
 }  // namespace rnl
 
 using namespace rnl;
@@ -467,19 +483,7 @@ rnl_status rnl_check_device_error(rnl_stream_t stream, int* site) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
   }
-  unsigned int words[6] = {0, 0, 0, 0, 0, 0};
-  if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
-      read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
-      read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK)
-    return RNL_ERR_LAUNCH;
-  for (unsigned int w : words) {
-    if (w != 0) {
-      if (site) *site = static_cast<int>((w >> 8) & 0xFFu);
-      return RNL_ERR_TIMEOUT;
-    }
-  }
-  if (site) *site = 0;
-  return RNL_OK;
+  return read_device_errors(site);
 }
 
 rnl_status rnl_trace_enable(int on) {

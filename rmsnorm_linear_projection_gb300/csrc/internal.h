@@ -102,5 +102,8 @@ rnl_status read_clear_error_skinny(unsigned int* word);
 rnl_status read_clear_error_pair(unsigned int* word);
 rnl_status read_clear_error_norm(unsigned int* word);
 rnl_status read_clear_error_selftest(unsigned int* word);
+// Reads and clears all of them without synchronising (api.cu): RNL_OK, or
+// RNL_ERR_TIMEOUT with the first recorded wait site in *site (optional).
+rnl_status read_device_errors(int* site);
 
 }  // namespace rnl

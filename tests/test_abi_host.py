@@ -88,6 +88,20 @@ CHILD = textwrap.dedent("""
     s8 = lib.rnl_gemm_s8s8s32
     r["s8_K_not_mult16"] = s8(A, A, A, 4, 8, 24, ws, 1 << 20, None)
     r["s8_M0"] = s8(None, None, None, 0, 8, 32, None, 0, None)
+    pp = ctypes.c_void_p(None)
+    r["pipe_null_out"] = lib.rnl_pipeline_create(0, 4, 64, 8, 0, None)
+    r["pipe_bad_op"] = lib.rnl_pipeline_create(3, 4, 64, 8, 0, ctypes.byref(pp))
+    r["pipe_zero_K"] = lib.rnl_pipeline_create(0, 4, 0, 8, 0, ctypes.byref(pp))
+    r["pipe_bad_dtype"] = lib.rnl_pipeline_create(0, 4, 64, 8, 7, ctypes.byref(pp))
+    r["pipe_no_device"] = lib.rnl_pipeline_create(0, 4, 64, 8, 0, ctypes.byref(pp))
+    r["pipe_handle_after_fail"] = pp.value
+    tk = ctypes.c_int64(-1)
+    r["pipe_submit_null"] = lib.rnl_pipeline_submit_bf16(None, A, None, A, 1e-6, 0, A, ctypes.byref(tk))
+    r["pipe_submit_null_W"] = lib.rnl_pipeline_submit_bf16(None, A, None, None, 1e-6, 0, A, ctypes.byref(tk))
+    r["pipe_submit_bad_eps"] = lib.rnl_pipeline_submit_w8a8(None, A, None, A, A, -1.0, 0, A, ctypes.byref(tk))
+    r["pipe_submit_mla_bad_mode"] = lib.rnl_pipeline_submit_mla(None, A, A, A, A, 1e-6, 5, A, ctypes.byref(tk))
+    r["pipe_wait_null"] = lib.rnl_pipeline_wait(None, 0, None)
+    r["pipe_destroy_null"] = lib.rnl_pipeline_destroy(None)
     r["status_strings"] = [lib.rnl_status_string(i).decode() for i in range(10)]
     r["trace_enable"] = lib.rnl_trace_enable(1)
     r["trace_read_empty"] = lib.rnl_trace_read(None, (ctypes.c_float * 4)(), 4)
@@ -133,6 +147,10 @@ def test_workspace_sizes(host_results):
     ("mla_null_gamma", NULL), ("mla_N1_not_mult8", ALIGN),
     ("s8_K_not_mult16", ALIGN), ("s8_M0", OK),
     ("trace_enable", OK), ("trace_read_empty", 0),
+    ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
+    ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
+    ("pipe_submit_null", NULL), ("pipe_submit_null_W", NULL), ("pipe_submit_bad_eps", ARG),
+    ("pipe_submit_mla_bad_mode", ARG), ("pipe_wait_null", NULL), ("pipe_destroy_null", OK),
 ])
 def test_argument_checks(host_results, key, want):
     assert host_results[key] == want
