@@ -62,6 +62,7 @@ def _declare(lib):
         "orc_rmsnorm_f64": (C, [P, P, I64, I64, D, C, P, P]),
         "orc_rmsnorm_linear": (C, [P, P, P, I64, I64, I64, D, C, C, P, P]),
         "orc_mla_q_chain": (C, [P, P, P, P, I64, I64, I64, I64, D, C, P, P, P]),
+        "orc_rmsnorm_linear_ex": (C, [P, P, P, P, P, P, I64, I64, I64, D, C, P, P, P, P]),
         "orc_quant_rows_f32": (C, [P, P, I64, I64, F, C, P, P, P, P]),
         "orc_gemm_s8": (C, [P, P, I64, I64, I64, P]),
         "orc_dequant_bf16": (C, [P, P, P, I64, I64, P, P]),
@@ -145,6 +146,25 @@ class Oracle:
                                            float(eps), int(variant), int(form), _ptr(ref),
                                            _ptr(out)), "rmsnorm_linear")
         return ref, out
+
+    def rmsnorm_linear_ex(self, x, residual, gamma, beta, W, bias, eps, variant):
+        """AT-10 with residual add, norm bias, projection bias; returns
+        (ref, out, x_sum, rstd)."""
+        x, W = _c(x, np.uint16), _c(W, np.uint16)
+        T, K = x.shape
+        N = W.shape[0]
+        assert W.shape[1] == K
+        res = _c(residual, np.uint16)
+        assert res is None or res.shape == (T, K)
+        ref = np.empty((T, N), np.float64)
+        out = np.empty((T, N), np.uint16)
+        x_sum = np.empty((T, K), np.uint16)
+        rstd = np.empty((T,), np.float64)
+        _check(self.lib.orc_rmsnorm_linear_ex(
+            _ptr(x), _ptr(res), _ptr(_c(gamma, np.uint16)), _ptr(_c(beta, np.uint16)), _ptr(W),
+            _ptr(_c(bias, np.uint16)), T, K, N, float(eps), int(variant), _ptr(ref), _ptr(out),
+            _ptr(x_sum), _ptr(rstd)), "rmsnorm_linear_ex")
+        return ref, out, x_sum, rstd
 
     # -- MLA q chain ----------------------------------------------------------
     def mla_q_chain(self, x, W_qa, gamma_cq, W_qb, eps, variant):

@@ -247,6 +247,86 @@ int orc_rmsnorm_linear(const uint16_t *x, const uint16_t *gamma, const uint16_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* AT-10 with the options of its two atoms.                                  */
+/*   [AT10] sec. 6 (Qwen3PreAttn): the norm is applied to x_add, the input   */
+/*          after the residual add: x_add = bf16(x + residual), the sum of   */
+/*          two bf16 values rounded once (exact in binary64 before that).    */
+/*   [AT10] sec. 3, AT-03 parameter table: has_bias (a bias added to the     */
+/*          normed row, after gamma: y = x_add * rstd * gamma + beta) and    */
+/*          output_rstd (rstd per row, as InplaceAddRmsNorm returns it).     */
+/*   [AT10] sec. 4, AT-09 parameters: has_bias of the projection, added to   */
+/*          the accumulator before the output cast:                          */
+/*          out = bf16(sum_k a[k] * W[n,k] + bias[n]).                        */
+/* residual, gamma, beta, bias may each be NULL (option off).  x_sum (bf16   */
+/* bits of x_add, [T,K]), rstd ([T]) and ref ([T,N], binary64 before the     */
+/* output cast) are optional outputs.                                        */
+/* ------------------------------------------------------------------------ */
+
+int orc_rmsnorm_linear_ex(const uint16_t *x, const uint16_t *residual, const uint16_t *gamma,
+                          const uint16_t *beta, const uint16_t *W, const uint16_t *bias,
+                          int64_t T, int64_t K, int64_t N, double eps, int variant,
+                          double *ref, uint16_t *out, uint16_t *x_sum, double *rstd)
+{
+    if (!x || !W || T < 0 || K <= 0 || N <= 0 || (variant != 0 && variant != 1))
+        return ORC_EARG;
+    double *wd = decode_matrix(W, N * K);
+    if (!wd)
+        return ORC_ENOMEM;
+    int status = ORC_OK;
+#pragma omp parallel
+    {
+        uint16_t *xa = (uint16_t *)malloc((size_t)K * sizeof(uint16_t));
+        double *a = (double *)malloc((size_t)K * sizeof(double));
+        if (!xa || !a) {
+#pragma omp atomic write
+            status = ORC_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!xa || !a)
+                continue;
+            const uint16_t *xr = x + t * K;
+            for (int64_t k = 0; k < K; ++k) {
+                if (residual)
+                    xa[k] = orc_bf16_rne(orc_bf16_value(xr[k]) +
+                                         orc_bf16_value(residual[t * K + k]));
+                else
+                    xa[k] = xr[k];
+                if (x_sum)
+                    x_sum[t * K + k] = xa[k];
+            }
+            double r = row_rstd_f64(xa, K, eps, variant);
+            if (rstd)
+                rstd[t] = r;
+            for (int64_t k = 0; k < K; ++k) {
+                double v = orc_bf16_value(xa[k]) * r;
+                if (gamma)
+                    v = v * orc_bf16_value(gamma[k]);
+                if (beta)
+                    v = v + orc_bf16_value(beta[k]);
+                a[k] = orc_bf16_value(orc_bf16_rne(v));
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                const double *wr = wd + n * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += a[k] * wr[k];
+                if (bias)
+                    acc = acc + orc_bf16_value(bias[n]);
+                if (ref)
+                    ref[t * N + n] = acc;
+                if (out)
+                    out[t * N + n] = orc_bf16_rne(acc);
+            }
+        }
+        free(xa);
+        free(a);
+    }
+    free(wd);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
 /* MLA two-stage q chain.  [AT10] sec. 5 (MLAProlog) and sec. 9 (the golden  */
 /* chain): q = bf16(matmul(x, wq_a)); qr = rms_norm(q) (variant B in the     */
 /* page's code); qr = qr * gamma_cq (FP32); qr = bf16(qr);                   */

@@ -396,8 +396,201 @@ def pin_w8a8_composition(orc):
     assert np.allclose(r["ref"], full, rtol=0, atol=0.02 * np.abs(full).max())
 
 
+# ---------------------------------------------------------------------------
+# AT-10 with the residual add (x_add), the AT-03 norm bias and output_rstd,
+# and the AT-09 projection bias
+# ---------------------------------------------------------------------------
+
+def pin_ex_reduces_to_base(orc):
+    """With every option off the extended form is the AT-10 form itself."""
+    rng = _rng(20)
+    T, K, N = 9, 72, 30
+    x = _rand_bf16(rng, (T, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    W = _rand_bf16(rng, (N, K), 0.05)
+    for variant in (0, 1):
+        ref, out = orc.rmsnorm_linear(x, g, W, 1e-6, variant, 0)
+        ref2, out2, xs, r = orc.rmsnorm_linear_ex(x, None, g, None, W, None, 1e-6, variant)
+        _, r_base = orc.rmsnorm_f64(x, g, 1e-6, variant)
+        assert np.array_equal(out, out2) and np.array_equal(ref, ref2)
+        assert np.array_equal(xs, x) and np.array_equal(r, r_base)
+
+
+def pin_ex_residual_sum_exact(orc):
+    """x_add = bf16(x + residual) with one rounding of the exact sum: random
+    pairs against brute force, constructed ties (to even), a summand far
+    below half an ulp, and cancellation to zero."""
+    rng = _rng(21)
+    K = 64
+    x = _rand_bf16(rng, (4, K))
+    res = _rand_bf16(rng, (4, K), 0.7)
+    # constructed rows: 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7 -> 1 (even);
+    # (1 + 2^-7) + 2^-8 is the midpoint of 1 + 2^-7 and 1 + 2^-6 -> 1 + 2^-6;
+    # 1 + 2^-30 -> 1; x + (-x) -> 0
+    one = _bf16_bits_of_f32(np.float32(1.0))
+    x[0, :4] = [one, _bf16_bits_of_f32(np.float32(1 + 2**-7)), one, x[0, 3]]
+    res[0, :4] = [_bf16_bits_of_f32(np.float32(2**-8)), _bf16_bits_of_f32(np.float32(2**-8)),
+                  _bf16_bits_of_f32(np.float32(2**-30)), x[0, 3] ^ np.uint16(0x8000)]
+    W = _rand_bf16(rng, (8, K), 0.05)
+    _, _, xs, _ = orc.rmsnorm_linear_ex(x, res, None, None, W, None, 1e-6, 0)
+    for t in range(4):
+        for k in range(K):
+            want, _ = exact.bf16_round_exact(Fraction(exact.bf16_value(x[t, k])) +
+                                             Fraction(exact.bf16_value(res[t, k])))
+            assert int(xs[t, k]) & 0x7FFF == want & 0x7FFF, (t, k)
+            if want & 0x7FFF:
+                assert int(xs[t, k]) == want, (t, k)
+    assert bf16_bits_to_f64(xs[0, :4]).tolist() == [1.0, 1 + 2**-6, 1.0, 0.0]
+
+
+def pin_ex_residual_composition(orc):
+    """The norm and projection see x_add: the extended form on (x, residual)
+    equals the AT-10 form on the x_sum it reports, rstd included; swapping x
+    and residual changes nothing (the sum commutes)."""
+    rng = _rng(22)
+    T, K, N = 7, 96, 20
+    x = _rand_bf16(rng, (T, K))
+    res = _rand_bf16(rng, (T, K), 2.0)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    W = _rand_bf16(rng, (N, K), 0.05)
+    for variant in (0, 1):
+        ref, out, xs, r = orc.rmsnorm_linear_ex(x, res, g, None, W, None, 1e-6, variant)
+        ref_b, out_b = orc.rmsnorm_linear(xs, g, W, 1e-6, variant, 0)
+        _, r_b = orc.rmsnorm_f64(xs, g, 1e-6, variant)
+        assert np.array_equal(out, out_b) and np.array_equal(ref, ref_b) and np.array_equal(r, r_b)
+        ref_s, out_s, xs_s, r_s = orc.rmsnorm_linear_ex(res, x, g, None, W, None, 1e-6, variant)
+        assert np.array_equal(out, out_s) and np.array_equal(xs, xs_s) and np.array_equal(r, r_s)
+    # rstd of a row whose x_add is constant c: 1/sqrt(c^2 + eps)
+    xc = np.full((1, K), _bf16_bits_of_f32(np.float32(1.5)), np.uint16)
+    rc = np.full((1, K), _bf16_bits_of_f32(np.float32(0.5)), np.uint16)
+    _, _, _, r = orc.rmsnorm_linear_ex(xc, rc, None, None, W, None, 1e-6, 0)
+    assert exact.rel_close(r[0], exact.dec_sqrt_recip(Fraction(4) + Fraction(1e-6)), 1e-15)
+
+
+def pin_ex_norm_bias_closed_form(orc):
+    """Constant row c with gamma g and norm bias b, W = I:
+    out_k = bf16(bf16(c / sqrt(c^2 + eps) * g_k + b_k)) -- the bias comes after
+    gamma and before the bf16 cast."""
+    rng = _rng(23)
+    K = 16
+    one = _bf16_bits_of_f32(np.float32(1.0))
+    W = np.zeros((K, K), np.uint16)
+    W[np.arange(K), np.arange(K)] = one
+    for c in (0.75, -3.0):
+        x = np.full((1, K), _bf16_bits_of_f32(np.float32(c)), np.uint16)
+        g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+        b = _bf16_bits_of_f32(rng.uniform(-2.0, 2.0, K).astype(np.float32))
+        for variant in (0, 1):
+            _, out, _, _ = orc.rmsnorm_linear_ex(x, None, g, b, W, None, 1e-6, variant)
+            cf = Fraction(exact.bf16_value(x[0, 0]))
+            rr = exact.dec_sqrt_recip(cf * cf + Fraction(1e-6))
+            for k in range(K):
+                y = cf * rr * Fraction(exact.bf16_value(g[k])) + Fraction(exact.bf16_value(b[k]))
+                a_bits, near = exact.bf16_round_exact(y)
+                assert near or int(out[0, k]) == a_bits, (c, variant, k)
+
+
+def pin_ex_projection_bias(orc):
+    """W = 0 gives out = bias exactly; with two unit weights per row,
+    out = bf16(a_i + a_j + bias) rounded once (not bf16(bf16(a_i + a_j) + bias))."""
+    rng = _rng(24)
+    T, K, N = 5, 40, 12
+    x = _rand_bf16(rng, (T, K))
+    bias = _rand_bf16(rng, (N,), 3.0)
+    W0 = np.zeros((N, K), np.uint16)
+    _, out, _, _ = orc.rmsnorm_linear_ex(x, None, None, None, W0, bias, 1e-6, 0)
+    assert np.array_equal(out, np.tile(bias, (T, 1)))
+    one = _bf16_bits_of_f32(np.float32(1.0))
+    W = np.zeros((N, K), np.uint16)
+    pairs = [(rng.integers(0, K), rng.integers(0, K)) for _ in range(N)]
+    for n, (i, j) in enumerate(pairs):
+        W[n, i] = one
+        W[n, j] = one if i != j else _bf16_bits_of_f32(np.float32(2.0))
+    y, _ = orc.rmsnorm_f64(x, None, 1e-6, 0)
+    a = [[Fraction(exact.bf16_value(exact.bf16_round_exact(Fraction(float(v)))[0])) for v in row] for row in y]
+    _, out, _, _ = orc.rmsnorm_linear_ex(x, None, None, None, W, bias, 1e-6, 0)
+    for t in range(T):
+        for n, (i, j) in enumerate(pairs):
+            s = a[t][i] + a[t][j] + Fraction(exact.bf16_value(bias[n]))
+            want, near = exact.bf16_round_exact(s)
+            assert near or int(out[t, n]) == want, (t, n)
+
+
+def pin_ex_exact_small(orc):
+    """Brute force of the whole extended row, every option on, in exact
+    rationals (fractions + 60-digit square root)."""
+    rng = _rng(25)
+    for (T, K, N) in ((2, 3, 2), (3, 8, 5)):
+        x = _rand_bf16(rng, (T, K))
+        res = _rand_bf16(rng, (T, K), 0.5)
+        g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+        b = _rand_bf16(rng, (K,), 0.3)
+        W = _rand_bf16(rng, (N, K), 0.5)
+        bias = _rand_bf16(rng, (N,), 0.3)
+        for variant in (0, 1):
+            ref, out, xs, r = orc.rmsnorm_linear_ex(x, res, g, b, W, bias, 1e-6, variant)
+            for t in range(T):
+                xa = []
+                for k in range(K):
+                    bits, _ = exact.bf16_round_exact(Fraction(exact.bf16_value(x[t, k])) +
+                                                     Fraction(exact.bf16_value(res[t, k])))
+                    assert int(xs[t, k]) == bits
+                    xa.append(Fraction(exact.bf16_value(bits)))
+                rr = exact.dec_sqrt_recip(sum(v * v for v in xa) / K + Fraction(1e-6))
+                assert exact.rel_close(r[t], rr, 1e-15)
+                a = []
+                for k in range(K):
+                    y = xa[k] * rr * Fraction(exact.bf16_value(g[k])) + Fraction(exact.bf16_value(b[k]))
+                    bits, near = exact.bf16_round_exact(y)
+                    assert not near
+                    a.append(Fraction(exact.bf16_value(bits)))
+                for n in range(N):
+                    sacc = sum(a[k] * Fraction(exact.bf16_value(W[n, k])) for k in range(K))
+                    sacc += Fraction(exact.bf16_value(bias[n]))
+                    assert exact.rel_close(ref[t, n], sacc, 1e-15) or abs(float(sacc)) < 1e-300
+                    bits, near = exact.bf16_round_exact(sacc)
+                    assert near or int(out[t, n]) == bits, (T, K, N, variant, t, n)
+
+
+def pin_ex_torch(orc):
+    """Library cross-check: torch (float64) add, rms_norm, + beta, bf16 cast,
+    matmul + bias."""
+    import torch
+    rng = _rng(26)
+    T, K, N = 10, 256, 24
+    x = _rand_bf16(rng, (T, K))
+    res = _rand_bf16(rng, (T, K), 1.5)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    b = _rand_bf16(rng, (K,), 0.1)
+    W = _rand_bf16(rng, (N, K), 0.02)
+    bias = _rand_bf16(rng, (N,), 0.5)
+    ref, out, xs, r = orc.rmsnorm_linear_ex(x, res, g, b, W, bias, 1e-6, 0)
+    xa = (torch.from_numpy(bf16_bits_to_f64(x)) + torch.from_numpy(bf16_bits_to_f64(res)))
+    # the f64 sum is exact; so is its float32 copy while the two exponents are
+    # within 16 of each other (true of these draws), so this rounds once
+    xa_b = xa.to(torch.float32).to(torch.bfloat16)
+    assert np.array_equal(xa_b.view(torch.int16).numpy().view(np.uint16), xs)
+    xa_d = xa_b.to(torch.float64)
+    y = torch.nn.functional.rms_norm(xa_d, (K,), weight=torch.from_numpy(bf16_bits_to_f64(g)), eps=1e-6)
+    y = y + torch.from_numpy(bf16_bits_to_f64(b))
+    rstd = 1.0 / torch.sqrt((xa_d * xa_d).mean(dim=1) + 1e-6)
+    assert np.allclose(r, rstd.numpy(), rtol=1e-14, atol=0)
+    a = y.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    wt = torch.from_numpy(bf16_bits_to_f64(W))
+    want = a @ wt.T + torch.from_numpy(bf16_bits_to_f64(bias))
+    scale = (a.abs() @ wt.abs().T).numpy() + np.abs(bf16_bits_to_f64(bias))
+    assert np.all(np.abs(ref - want.numpy()) <= 2.0**-7 * scale * 0.05 + 1e-12 * scale)
+
+
 ALL_PINS = [
     pin_bf16_codec,
+    pin_ex_reduces_to_base,
+    pin_ex_residual_sum_exact,
+    pin_ex_residual_composition,
+    pin_ex_norm_bias_closed_form,
+    pin_ex_projection_bias,
+    pin_ex_exact_small,
+    pin_ex_torch,
     pin_rmsnorm_variants_agree,
     pin_rmsnorm_closed_forms,
     pin_rmsnorm_scale_invariance,

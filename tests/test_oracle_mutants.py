@@ -23,9 +23,9 @@ MUTANTS = [
     ("drop_gamma_at10", "                if (gamma)\n                    v = v * orc_bf16_value(gamma[k]);\n                a[k]",
      "                a[k]"),
     ("drop_bf16_cast_of_normed", "a[k] = (form == 0) ? orc_bf16_value(orc_bf16_rne(v)) : v;", "a[k] = v;"),
-    ("transposed_weight", "const double *wr = wd + n * K;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[k];",
-     "const double *wr = wd + n;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[(k % N) * K + (k / N) % K];"),
-    ("wrong_sign_accumulate", "acc += a[k] * wr[k];", "acc -= a[k] * wr[k];"),
+    ("transposed_weight", "const double *wr = wd + n * K;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[k];\n                if (ref)",
+     "const double *wr = wd + n;\n                double acc = 0.0;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += a[k] * wr[(k % N) * K + (k / N) % K];\n                if (ref)"),
+    ("wrong_sign_accumulate", "acc += a[k] * wr[k];\n                if (ref)", "acc -= a[k] * wr[k];\n                if (ref)"),
     ("mla_drop_gamma", "v = v * orc_bf16_value(gamma_cq[j]);", "v = v * 1.0;"),
     ("mla_stage2_unrounded_input", "z[j] = orc_bf16_value(orc_bf16_rne(v));", "z[j] = v;"),
     ("quant_round_half_away", "float r = rintf(v);", "float r = roundf(v);"),
@@ -39,6 +39,20 @@ MUTANTS = [
      "double scale = (double)x_scale[m] * (double)w_scale[m % N];"),
     ("bf16_ties_away", "double r = nearbyint(m * 256.0);", "double r = round(m * 256.0);"),
     ("bf16_truncate", "double r = nearbyint(m * 256.0);", "double r = floor(m * 256.0);"),
+    # AT-10 with residual add, norm bias, output_rstd and projection bias
+    ("ex_drop_residual", "xa[k] = orc_bf16_rne(orc_bf16_value(xr[k]) +\n                                         orc_bf16_value(residual[t * K + k]));",
+     "xa[k] = xr[k];"),
+    ("ex_residual_subtracted", "orc_bf16_value(xr[k]) +\n                                         orc_bf16_value(residual",
+     "orc_bf16_value(xr[k]) -\n                                         orc_bf16_value(residual"),
+    ("ex_rstd_of_x_not_x_add", "double r = row_rstd_f64(xa, K, eps, variant);",
+     "double r = row_rstd_f64(xr, K, eps, variant);"),
+    ("ex_norm_bias_before_gamma",
+     "                if (gamma)\n                    v = v * orc_bf16_value(gamma[k]);\n                if (beta)\n                    v = v + orc_bf16_value(beta[k]);",
+     "                if (beta)\n                    v = v + orc_bf16_value(beta[k]);\n                if (gamma)\n                    v = v * orc_bf16_value(gamma[k]);"),
+    ("ex_drop_norm_bias", "                if (beta)\n                    v = v + orc_bf16_value(beta[k]);", ""),
+    ("ex_projection_bias_after_rounding", "acc = acc + orc_bf16_value(bias[n]);",
+     "acc = orc_bf16_value(orc_bf16_rne(acc)) + orc_bf16_value(bias[n]);"),
+    ("ex_drop_projection_bias", "acc = acc + orc_bf16_value(bias[n]);", "acc = acc;"),
 ]
 
 CHILD = textwrap.dedent("""
