@@ -9,7 +9,8 @@ bf16 out); the metric is TFLOP/s of the projection (2*T*N*K per step), or
 GB/s for the HBM-bound workloads (skinny, tiny), TOPS for W8A8.
 
 A step is one call of the library's C entry point on inputs already resident
-in HBM.  Each step is timed with CUDA events on the launch stream; the L2
+in HBM (its arguments marshalled once, so the host's Python work stays off
+the GPU's critical path).  Each step is timed with CUDA events on the launch stream; the L2
 (129 MB) is flushed between steps, outside the timed events, by writing a
 256 MB buffer and then reading it (so the flush's own dirty lines are
 written back before the step starts).  The dominant kernel's own duration comes from the library's
@@ -40,8 +41,8 @@ sys.path.insert(0, ROOT)
 
 import synth_inputs as si  # noqa: E402
 
-WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny")
-DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600}
+WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex")
+DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600, "qkv_ex": 2000}
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
@@ -74,10 +75,21 @@ class Work:
     def __init__(self, name: str, device, T=None):
         import torch
         self.name = name
-        self.cfg = c = si.scaled(si.CONFIGS[name], T=T) if T else si.CONFIGS[name]
+        base = "qkv" if name == "qkv_ex" else name
+        self.cfg = c = si.scaled(si.CONFIGS[base], T=T) if T else si.CONFIGS[base]
         self.device = device
         self.torch = torch
-        if name in ("qkv", "tiny", "skinny"):
+        if name == "qkv_ex":
+            # the qkv projection with the residual add, norm bias, output_rstd,
+            # the residual sum written back and the projection bias
+            self.h = si.make_projection(c)
+            T, K, N = c["T"], c["K"], c["N"]
+            self.h["residual"] = si.normal_bf16(c["seed"], "residual", (T, K), 1.0)
+            self.h["beta"] = si.normal_bf16(c["seed"], "beta", (K,), 0.1)
+            self.h["bias"] = si.normal_bf16(c["seed"], "bias", (N,), 0.5)
+            self.flops = 2.0 * T * N * K
+            self.bytes = 4.0 * T * K + 2.0 * N * K + 4.0 * K + 2.0 * N + 2.0 * T * N + 2.0 * T * K + 4.0 * T
+        elif name in ("qkv", "tiny", "skinny"):
             self.h = si.make_projection(c)
             T, K, N = c["T"], c["K"], c["N"]
             self.flops = 2.0 * T * N * K
@@ -125,6 +137,16 @@ class Work:
         d = self.d if d is None else d
         out = self.out if out is None else out
         c = self.cfg
+        if self.name == "qkv_ex":
+            if self.ws is None:
+                self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_BF16, c["T"], c["K"], c["N"], rnl.OUT_BF16),
+                                           dtype=self.torch.uint8, device=self.device)
+                self.x_sum = self.torch.empty_like(d["x"])
+                self.rstd = self.torch.empty(c["T"], dtype=self.torch.float32, device=self.device)
+            return rnl.rmsnorm_linear_bf16_ex(d["x"], d["gamma"], d["W"], residual=d["residual"],
+                                              x_sum_out=self.x_sum, beta=d["beta"], bias=d["bias"],
+                                              eps=c["eps"], norm_mode=c["norm_mode"], out=out,
+                                              rstd_out=self.rstd, workspace=self.ws, stream=stream)
         if self.name in ("qkv", "tiny", "skinny"):
             odt = rnl.OUT_FP32 if c["out_dtype"] == "fp32" else rnl.OUT_BF16
             if self.ws is None:
@@ -143,6 +165,48 @@ class Work:
                                        dtype=self.torch.uint8, device=self.device)
         return rnl.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], eps=c["eps"],
                                        norm_mode=c["norm_mode"], out=out, workspace=self.ws, stream=stream)
+
+    def prepared(self, stream):
+        """The same call as call() on the default inputs, with its C arguments
+        marshalled once: the returned function makes only the C call.  The
+        binding's per-call checks cost tens of microseconds of Python on the
+        host; in the timed loop they would leave the GPU waiting for launches
+        instead of measuring the kernels."""
+        import ctypes
+        import rmsnorm_linear_projection_gb300 as rnl
+        self.call(stream=stream)  # allocates the workspace (and the ex outputs) once
+        lib, c, d, out = rnl.load(), self.cfg, self.d, self.out
+        P = ctypes.c_void_p
+
+        def ptr(t):
+            return None if t is None else P(t.data_ptr())
+
+        s = P(stream.cuda_stream)
+        nbytes = self.ws.numel() * self.ws.element_size()
+        if self.name == "qkv_ex":
+            fn = lib.rmsnorm_linear_bf16_ex
+            args = (ptr(d["x"]), ptr(d["residual"]), ptr(self.x_sum), ptr(d["gamma"]), ptr(d["beta"]),
+                    ptr(d["W"]), ptr(d["bias"]), c["T"], c["K"], c["N"], c["eps"], c["norm_mode"],
+                    ptr(out), ptr(self.rstd), ptr(self.ws), nbytes, s)
+        elif self.name in ("qkv", "tiny", "skinny"):
+            odt = rnl.OUT_FP32 if c["out_dtype"] == "fp32" else rnl.OUT_BF16
+            fn = lib.rmsnorm_linear_bf16
+            args = (ptr(d["x"]), ptr(d["gamma"]), ptr(d["W"]), c["T"], c["K"], c["N"], c["eps"],
+                    c["norm_mode"], ptr(out), odt, ptr(self.ws), nbytes, s)
+        elif self.name == "mla":
+            fn = lib.mla_q_chain
+            args = (ptr(d["x"]), ptr(d["W_qa"]), ptr(d["gamma_cq"]), ptr(d["W_qb"]), c["T"], c["K"],
+                    c["N1"], c["N2"], c["eps"], c["norm_mode"], ptr(out), None, ptr(self.ws), nbytes, s)
+        else:
+            fn = lib.rmsnorm_linear_w8a8
+            args = (ptr(d["x"]), ptr(d["gamma"]), ptr(d["Wq"]), ptr(d["w_scale"]), c["T"], c["K"], c["N"],
+                    c["eps"], c["norm_mode"], ptr(out), None, None, ptr(self.ws), nbytes, s)
+
+        def go():
+            st = fn(*args)
+            if st != 0:
+                raise rnl.RnlError(st, self.name)
+        return go
 
     def dominant(self):
         """(stage name, kernel-name prefix, algorithmic amount per step, bound) of the
@@ -322,10 +386,13 @@ def run_ours(args):
         flush.zero_()
         flush.sum()
 
+    # the timed loop makes the C call with arguments marshalled once
+    step = w.prepared(stream)
+
     # warm-up
     for _ in range(args.warmup):
         flush_l2()
-        w.call()
+        step()
     torch.cuda.synchronize()
     rnl.rnl_check_device_error()
 
@@ -341,7 +408,7 @@ def run_ours(args):
     for i in range(args.steps):
         flush_l2()
         starts[i].record(stream)
-        w.call()
+        step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -392,7 +459,7 @@ def run_ours(args):
     # i-1's output copy; the timed region runs from the first submit until the
     # last step's output is in host memory.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.name != "qkv_ex":  # the host-buffer pipeline has no ex form
         c = w.cfg
         host_x = torch.empty(w.d["x"].shape, dtype=w.d["x"].dtype, pin_memory=True)
         host_x.copy_(w.d["x"])
@@ -467,7 +534,7 @@ def run_ours(args):
         del graph
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not args.T:
+    if rank == 0 and world == 1 and not args.no_cpu and not args.T and w.name != "qkv_ex":
         v, u, cores, sample, rows, ref_out, _ = oracle_sample(args.workload, target_s=args.cpu_seconds)
         got = w.out.cpu()
         got = got.view(torch.int16).numpy().view(np.uint16) if got.dtype == torch.bfloat16 else got.numpy()

@@ -119,6 +119,33 @@ rnl_status rmsnorm_linear_bf16(const void *x, const void *gamma, const void *W, 
                                rnl_stream_t stream);
 
 /*
+ * AT-10 with the options of its two atoms and the residual add in front
+ * (AT-10 pattern page: sec. 3, the AT-03 parameter table -- has_bias,
+ * output_rstd; sec. 4, the AT-09 parameters -- has_bias; sec. 6,
+ * Qwen3PreAttn -- the norm is applied to x_add, the input after the
+ * residual add).  bf16 output.
+ *   x         bf16 [T, K]
+ *   residual  bf16 [T, K] or NULL: x_add = bf16(x + residual), rounded once
+ *             (the correctly rounded bf16 of the exact sum); NULL: x_add = x
+ *   x_sum_out bf16 [T, K] or NULL: receives x_add (needs residual, else
+ *             RNL_ERR_ARG).  It may be x or residual itself (the in-place
+ *             add of InplaceAddRmsNorm); any other overlap with them is
+ *             RNL_ERR_ARG.
+ *   gamma     bf16 [K] or NULL;  beta bf16 [K] or NULL (AT-03 has_bias)
+ *   W         bf16 [N, K];  bias bf16 [N] or NULL (AT-09 has_bias)
+ *   out       bf16 [T, N]:  out = bf16(sum_k a[t,k] * W[n,k] + bias[n]),
+ *             a = bf16((x_add * rstd) * gamma + beta), FP32 arithmetic
+ *   rstd_out  fp32 [T] or NULL (AT-03 output_rstd): rstd of x_add's row
+ * Workspace: rnl_workspace_size(RNL_OP_BF16, T, K, N, RNL_OUT_BF16).
+ * Alignment: 16 bytes for every tensor except rstd_out (4 bytes); K % 8.
+ */
+rnl_status rmsnorm_linear_bf16_ex(const void *x, const void *residual, void *x_sum_out,
+                                  const void *gamma, const void *beta, const void *W,
+                                  const void *bias, int64_t T, int64_t K, int64_t N, float eps,
+                                  int norm_mode, void *out, float *rstd_out, void *workspace,
+                                  size_t workspace_bytes, rnl_stream_t stream);
+
+/*
  * AT-11 RMSNorm + per-token INT8 quant + exact INT8 x INT8 -> INT32 matmul +
  * FP32 dequant, BF16 out.
  *   x        bf16 [T, K];  gamma bf16 [K] or NULL

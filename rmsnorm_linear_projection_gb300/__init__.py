@@ -5,6 +5,8 @@ The functions carry the names of the C entry points and only marshal
 arguments; the computation runs in the library's CUDA kernels.
 
     rmsnorm_linear_bf16   AT-10 RMSNorm + Linear (bf16 out) / mhc_pre FP32 form
+    rmsnorm_linear_bf16_ex  the same with residual add, norm bias, output_rstd and
+                          projection bias
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
@@ -26,6 +28,7 @@ from ._native import (  # noqa: F401
     load,
     mla_q_chain,
     rmsnorm_linear_bf16,
+    rmsnorm_linear_bf16_ex,
     rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,
     rnl_check_device_error,

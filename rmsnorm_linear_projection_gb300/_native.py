@@ -33,7 +33,7 @@ EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_li
            "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc",
            "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
-           "rnl_pipeline_destroy")
+           "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex")
 
 
 class RnlError(RuntimeError):
@@ -67,6 +67,7 @@ def _declare(lib):
         "rnl_pipeline_submit_mla": (I, [P, P, P, P, P, F, I, P, ctypes.POINTER(I64)]),
         "rnl_pipeline_wait": (I, [P, I64, ctypes.POINTER(I)]),
         "rnl_pipeline_destroy": (I, [P]),
+        "rmsnorm_linear_bf16_ex": (I, [P, P, P, P, P, P, P, I64, I64, I64, F, I, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -150,6 +151,35 @@ def rmsnorm_linear_bf16(x, gamma, W, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
                                       int(norm_mode), _ptr(out), int(out_dtype), _ptr(ws),
                                       ws.numel() * ws.element_size(), _stream(dev, stream)),
            "rmsnorm_linear_bf16")
+    return out
+
+
+def rmsnorm_linear_bf16_ex(x, gamma, W, residual=None, x_sum_out=None, beta=None, bias=None,
+                           eps=1e-6, norm_mode=NORM_RSQRT, out=None, rstd_out=None,
+                           workspace=None, stream=None):
+    """AT-10 with the residual add (x_add = bf16(x + residual)), the AT-03
+    norm bias beta and output_rstd, and the AT-09 projection bias; bf16 out.
+    x_sum_out may be x or residual (in-place add)."""
+    T, K = x.shape
+    N = W.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W, "W", torch.bfloat16, (N, K), dev)
+    for t, name, shape in ((residual, "residual", (T, K)), (x_sum_out, "x_sum_out", (T, K)),
+                           (gamma, "gamma", (K,)), (beta, "beta", (K,)), (bias, "bias", (N,))):
+        if t is not None:
+            _need(t, name, torch.bfloat16, shape, dev)
+    if rstd_out is not None:
+        _need(rstd_out, "rstd_out", torch.float32, (T,), dev)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, N), dev)
+    ws = _workspace(workspace_size(OP_BF16, T, K, N, OUT_BF16), dev, workspace)
+    _check(load().rmsnorm_linear_bf16_ex(_ptr(x), _ptr(residual), _ptr(x_sum_out), _ptr(gamma),
+                                         _ptr(beta), _ptr(W), _ptr(bias), T, K, N, float(eps),
+                                         int(norm_mode), _ptr(out), _ptr(rstd_out), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "rmsnorm_linear_bf16_ex")
     return out
 
 

@@ -348,6 +348,62 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
   return launch_gemm(g, s);
 }
 
+rnl_status rmsnorm_linear_bf16_ex(const void* x, const void* residual, void* x_sum_out,
+                                  const void* gamma, const void* beta, const void* W,
+                                  const void* bias, int64_t T, int64_t K, int64_t N, float eps,
+                                  int norm_mode, void* out, float* rstd_out, void* workspace,
+                                  size_t workspace_bytes, rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps)) return RNL_ERR_ARG;
+  if (x_sum_out && !residual) return RNL_ERR_ARG;  // nothing to write back
+  if (x_sum_out && x_sum_out != x && x_sum_out != residual) {
+    // x_sum_out is either one of the inputs (in place) or disjoint from both
+    const uintptr_t o = reinterpret_cast<uintptr_t>(x_sum_out);
+    const uintptr_t n = static_cast<uintptr_t>(T) * static_cast<uintptr_t>(K) * 2;
+    for (const void* in : {x, residual}) {
+      const uintptr_t i = reinterpret_cast<uintptr_t>(in);
+      if (in && o < i + n && i < o + n) return RNL_ERR_ARG;
+    }
+  }
+  if (T == 0) return RNL_OK;
+  if (!x || !W || !out) return RNL_ERR_NULL;
+  if (K % 8 != 0 || !aligned16(x) || !aligned16(W) || !aligned16(out) ||
+      (residual && !aligned16(residual)) || (x_sum_out && !aligned16(x_sum_out)) ||
+      (gamma && !aligned16(gamma)) || (beta && !aligned16(beta)) || (bias && !aligned16(bias)) ||
+      (rstd_out && (reinterpret_cast<uintptr_t>(rstd_out) & 3u)) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const BF16Layout need = bf16_layout(nullptr, T, K, N, RNL_OUT_BF16);
+  if (need.bytes > 0 && (!workspace || workspace_bytes < need.bytes)) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const BF16Layout l = bf16_layout(workspace, T, K, N, RNL_OUT_BF16);
+  cudaStream_t s = cs(stream);
+  // with no residual, beta or rstd output this is the plain AT-10 V stage
+  if (!residual && !beta && !rstd_out && norm_cast_stream_fits(K))
+    st = launch_norm_cast_stream(x, gamma, T, K, eps, norm_mode, l.A, s);
+  else if (norm_cast_stream_fits(K))
+    st = launch_add_norm_cast_stream(x, residual, x_sum_out, gamma, beta, T, K, eps, norm_mode,
+                                     l.A, rstd_out, s);
+  else
+    st = launch_add_norm_cast(x, residual, x_sum_out, gamma, beta, T, K, eps, norm_mode, l.A,
+                              rstd_out, s);
+  if (st != RNL_OK) return st;
+  GemmArgs g;
+  g.A = l.A;
+  g.B = W;
+  g.M = T;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.epi = Epi::kBf16;
+  g.bias = bias;
+  g.partial_ws = l.part;
+  g.partial_ws_bytes = kGemmPartialBytes;
+  return launch_gemm(g, s);
+}
+
 rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* Wq,
                                const float* w_scale, int64_t T, int64_t K, int64_t N, float eps,
                                int norm_mode, void* out, int8_t* q_out, float* x_scale_out,

@@ -58,6 +58,35 @@ __device__ __forceinline__ void store_bf16_32(void* out, int64_t m, int n0, int 
   }
 }
 
+// out[m, n0 .. n0+31] = bf16(v + bias[n]) (AT-09 has_bias; bias bf16 [N],
+// 16-byte aligned; n0 is a multiple of 32).  Each 16-byte chunk of the bias
+// is loaded next to the 8 outputs it feeds, so few registers stay live.
+__device__ __forceinline__ void store_bf16_bias_32(void* out, int64_t m, int n0, int N,
+                                                   const uint32_t (&r)[32],
+                                                   const __nv_bfloat16* __restrict__ bias) {
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
+  if (n0 + 32 <= N && (N & 7) == 0) {
+    uint4* dst = reinterpret_cast<uint4*>(orow + n0);
+    const uint4* b = reinterpret_cast<const uint4*>(bias + n0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 u = __ldg(b + j);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = bf16x2_bits(__fadd_rn(__uint_as_float(r[8 * j + 2 * i]), __uint_as_float(w[i] << 16)),
+                           __fadd_rn(__uint_as_float(r[8 * j + 2 * i + 1]), __uint_as_float(w[i] & 0xFFFF0000u)));
+      dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < N)
+        orow[n0 + j] = __float2bfloat16_rn(__fadd_rn(__uint_as_float(r[j]), __bfloat162float(bias[n0 + j])));
+  }
+}
+
 // out[m, n0 .. n0+31] = fp32(v) * rs.
 __device__ __forceinline__ void store_f32_scaled_32(void* out, int64_t m, int n0, int N,
                                                     const uint32_t (&r)[32], float rs) {
@@ -91,10 +120,11 @@ __device__ __forceinline__ void store_i32_32(void* out, int64_t m, int n0, int N
 }
 
 // AT-06 dequant in the order of the SK-14 skeleton page (QuantMatMulReduceSum):
-// float(acc) * (x_scale[m] * w_scale[n]), then bf16.
+// float(acc) * (x_scale[m] * w_scale[n]) (+ bias[n] when given), then bf16.
 __device__ __forceinline__ void store_dequant_32(void* out, int64_t m, int n0, int N,
                                                  const int (&a)[32], float xs,
-                                                 const float* __restrict__ w_scale) {
+                                                 const float* __restrict__ w_scale,
+                                                 const __nv_bfloat16* __restrict__ bias) {
   uint32_t v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -102,7 +132,10 @@ __device__ __forceinline__ void store_dequant_32(void* out, int64_t m, int n0, i
     const float ws = n < N ? __ldg(w_scale + n) : 0.f;
     v[j] = __float_as_uint(static_cast<float>(a[j]) * (xs * ws));
   }
-  store_bf16_32(out, m, n0, N, v);
+  if (bias != nullptr)
+    store_bf16_bias_32(out, m, n0, N, v, bias);
+  else
+    store_bf16_32(out, m, n0, N, v);
 }
 
 }  // namespace gemm

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap map_b, int M, int N, int K, int group_m,
                      int dp_waves, int tail_tiles, int splits, void* __restrict__ out,
                      const float* __restrict__ row_scale, const float* __restrict__ col_scale,
-                     uint32_t* __restrict__ partial) {
+                     uint32_t* __restrict__ partial, const __nv_bfloat16* __restrict__ bias) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
   constexpr int kStages = PairTile<BN>::kStages;
@@ -290,7 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
           } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-            if (row_ok) store_bf16_32(out, m, n0, N, r);
+            if (row_ok) {
+              if (bias != nullptr)
+                store_bf16_bias_32(out, m, n0, N, r, bias);
+              else
+                store_bf16_32(out, m, n0, N, r);
+            }
           } else {
             if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
           }
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (EPI == static_cast<int>(Epi::kInt32))
               store_i32_32(out, m, n_base + c * 32, N, iacc[c]);
             else
-              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale);
+              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale, bias);
           }
         }
       }
@@ -345,7 +350,8 @@ template <int EPI, int BN>
 __global__ void __launch_bounds__(256)
     gemm_pair_fixup_kernel(int M, int N, int group_m, int dp_tiles, int tail_tiles, int splits,
                            const uint32_t* __restrict__ partial, void* __restrict__ out,
-                           const float* __restrict__ row_scale, const float* __restrict__ col_scale) {
+                           const float* __restrict__ row_scale, const float* __restrict__ col_scale,
+                           const __nv_bfloat16* __restrict__ bias) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
   constexpr int kQuadsPerRow = BN / 4;
@@ -400,8 +406,11 @@ __global__ void __launch_bounds__(256)
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (n0 + j < N)
-          orow[n0 + j] = __float2bfloat16_rn(static_cast<float>(a[j]) * (xs * __ldg(col_scale + n0 + j)));
+        if (n0 + j < N) {
+          float v = static_cast<float>(a[j]) * (xs * __ldg(col_scale + n0 + j));
+          if (bias != nullptr) v = __fadd_rn(v, __bfloat162float(bias[n0 + j]));
+          orow[n0 + j] = __float2bfloat16_rn(v);
+        }
     }
     (void)acc_bits;
   } else {
@@ -424,8 +433,13 @@ __global__ void __launch_bounds__(256)
       a2 += __uint_as_float(v.z);
       a3 += __uint_as_float(v.w);
     }
-    const float a[4] = {a0, a1, a2, a3};
+    float a[4] = {a0, a1, a2, a3};
     if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
+      if (bias != nullptr) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (n0 + j < N) a[j] = __fadd_rn(a[j], __bfloat162float(bias[n0 + j]));
+      }
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
       if (n0 + 4 <= N && (N & 3) == 0) {
         uint2 o;
@@ -517,7 +531,8 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
                                      static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                      pl.dp_waves, pl.tail_tiles, pl.splits, g.out, g.row_scale,
-                                     g.col_scale, static_cast<uint32_t*>(g.partial_ws));
+                                     g.col_scale, static_cast<uint32_t*>(g.partial_ws),
+                                     static_cast<const __nv_bfloat16*>(g.bias));
   trace_after(s, name);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -535,7 +550,7 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
     e = cudaLaunchKernelEx(&fc, gemm_pair_fixup_kernel<EPI, BN>, static_cast<int>(g.M),
                            static_cast<int>(g.N), group_m, pl.dp_waves * pairs, pl.tail_tiles,
                            pl.splits, static_cast<const uint32_t*>(g.partial_ws), g.out,
-                           g.row_scale, g.col_scale);
+                           g.row_scale, g.col_scale, static_cast<const __nv_bfloat16*>(g.bias));
     trace_after(s, "gemm_pair_fixup");
     if (e != cudaSuccess) {
       cudaGetLastError();

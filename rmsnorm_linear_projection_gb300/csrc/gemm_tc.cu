@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 int M, int N, int K, int group_m, void* __restrict__ out,
                 const float* __restrict__ row_scale, const float* __restrict__ col_scale,
-                const float* __restrict__ a_rstd, const uint4* __restrict__ a_gamma) {
+                const float* __restrict__ a_rstd, const uint4* __restrict__ a_gamma,
+                const __nv_bfloat16* __restrict__ bias) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
   static_assert(!(NORM_A && kInt), "the fused norm feeds the bf16 GEMM only");
@@ -256,7 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) iacc[c][j] += __float2int_rn(__uint_as_float(r[j]));
           } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-            if (row_ok) store_bf16_32(out, m, n0, N, r);
+            if (row_ok) {
+              if (bias != nullptr)
+                store_bf16_bias_32(out, m, n0, N, r, bias);
+              else
+                store_bf16_32(out, m, n0, N, r);
+            }
           } else {  // kRowScaleF32
             if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
           }
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (EPI == static_cast<int>(Epi::kInt32))
               store_i32_32(out, m, n_base + c * 32, N, iacc[c]);
             else
-              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale);
+              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale, bias);
           }
         }
       }
@@ -378,7 +384,8 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
                                            static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                            g.out, g.row_scale, g.col_scale, g.a_rstd,
-                                           static_cast<const uint4*>(g.a_gamma));
+                                           static_cast<const uint4*>(g.a_gamma),
+                                           static_cast<const __nv_bfloat16*>(g.bias));
   trace_after(s, name);
   if (e != cudaSuccess) {
     cudaGetLastError();

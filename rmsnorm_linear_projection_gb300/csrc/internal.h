@@ -43,6 +43,18 @@ rnl_status launch_norm_cast(const void* x, const void* gamma, int64_t T, int64_t
 bool norm_cast_stream_fits(int64_t K);
 rnl_status launch_norm_cast_stream(const void* x, const void* gamma, int64_t T, int64_t K,
                                    float eps, int mode, void* A, cudaStream_t s);
+// The same with the residual add in front and the AT-03 options (addnorm.cu,
+// any K): x_add = bf16(x + residual) (residual may be null), written to
+// x_sum_out when not null (may be x or residual); A = bf16((x_add * rstd) *
+// gamma + beta) (gamma, beta may be null); rstd_out optional.
+rnl_status launch_add_norm_cast(const void* x, const void* residual, void* x_sum_out,
+                                const void* gamma, const void* beta, int64_t T, int64_t K,
+                                float eps, int mode, void* A, float* rstd_out, cudaStream_t s);
+// The same options on the streamed pass (normstream.cu), K <= 4096.
+rnl_status launch_add_norm_cast_stream(const void* x, const void* residual, void* x_sum_out,
+                                       const void* gamma, const void* beta, int64_t T, int64_t K,
+                                       float eps, int mode, void* A, float* rstd_out,
+                                       cudaStream_t s);
 // rstd only.
 rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int mode, float* rstd,
                            cudaStream_t s);
@@ -73,6 +85,9 @@ struct GemmArgs {
   // bf16((x * a_rstd[m]) * a_gamma[k]) (a_gamma may be null)
   const float* a_rstd = nullptr;
   const void* a_gamma = nullptr;
+  // AT-09 has_bias: bf16 [N] added to the accumulator before the output cast
+  // (bf16 and dequant epilogues; may be null)
+  const void* bias = nullptr;
   // partial sums of the CTA-pair GEMM's K-split tail (see gemm_pair.cu);
   // without it the leftover tiles run whole
   void* partial_ws = nullptr;

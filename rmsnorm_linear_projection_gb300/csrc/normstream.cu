@@ -40,6 +40,21 @@ struct __align__(8) NsCtrl {
   int abort;
 };
 
+// Options of the extended form (EXT = true; every pointer may be null): the
+// residual row is added first (x_add = bf16(x + residual)), x_add is written
+// to x_sum, beta is added after gamma, rstd is written per row.  Each
+// consumer warp loads its residual row from global memory before it waits
+// for the x row, so the load overlaps the bulk copy (the ring holds x rows
+// only and keeps its depth).  x_add then replaces the x row in the warp's ring
+// slot and the output pass reads it from there, so no row is held in
+// registers across the two passes.
+struct NsExt {
+  const uint4* residual;
+  uint4* x_sum;
+  const uint4* beta;
+  float* rstd_out;
+};
+
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                               uint32_t bar) {
   asm volatile(
@@ -72,19 +87,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // VPL = 16-byte vectors per lane (row of up to 32 * 8 * VPL elements).  Each
 // consumer lane keeps its share of the current row in registers between the
 // two passes; gamma is staged once per CTA in shared memory.
-template <int MODE, bool GAMMA, int VPL>
+template <int MODE, bool GAMMA, int VPL, bool EXT>
 __global__ void __launch_bounds__(kThreadsNS, 1)
-    norm_cast_stream_kernel(const uint8_t* __restrict__ x, const uint4* __restrict__ gamma,
-                            int64_t T, int nvec, int stages, float inv_d, float eps,
-                            uint4* __restrict__ A) {
+    norm_cast_stream_kernel(const uint8_t* x, const uint4* __restrict__ gamma, int64_t T,
+                            int nvec, int stages, float inv_d, float eps, uint4* __restrict__ A,
+                            const NsExt ext) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 127u) & ~127u;
   uint8_t* smem = smem_raw + (base - raw_addr);
   const uint32_t row_bytes = static_cast<uint32_t>(nvec) * 16u;
   const uint32_t stage_bytes = kGroupRows * row_bytes;
+  const bool has_res = EXT && ext.residual != nullptr;
+  const bool has_beta = EXT && ext.beta != nullptr;
   uint4* gamma_s = reinterpret_cast<uint4*>(smem + static_cast<size_t>(stages) * stage_bytes);
-  NsCtrl* ctrl = reinterpret_cast<NsCtrl*>(smem + static_cast<size_t>(stages) * stage_bytes + row_bytes);
+  uint4* beta_s = gamma_s + nvec;  // EXT only
+  NsCtrl* ctrl = reinterpret_cast<NsCtrl*>(smem + static_cast<size_t>(stages) * stage_bytes +
+                                           (EXT ? 2 : 1) * row_bytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -126,14 +145,89 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ consumers
-    if (GAMMA) {  // gamma staged once in shared memory for all rows
-      for (int v = threadIdx.x; v < nvec; v += kConsumerWarps * 32) gamma_s[v] = __ldg(gamma + v);
+    if (GAMMA || has_beta) {  // gamma (and beta) staged once in shared memory for all rows
+      for (int v = threadIdx.x; v < nvec; v += kConsumerWarps * 32) {
+        if (GAMMA) gamma_s[v] = __ldg(gamma + v);
+        if (has_beta) beta_s[v] = __ldg(ext.beta + v);
+      }
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
     uint32_t stage = 0, phase = 0;
     for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
       const int64_t row = g * kGroupRows + warp;
-      if (row < T) {
+      if (row < T && EXT) {
+        uint4 rv[EXT ? VPL : 1];
+        if (has_res) {  // plain loads: x_sum may be the residual itself
+          const uint4* qr = ext.residual + row * nvec;
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) {
+            const int v = lane + 32 * i;
+            rv[i] = v < nvec ? qr[v] : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        const bool got = mbar_wait(smem_u32(&ctrl->full[stage][warp]), phase, abort, &g_err_norm, 32);
+        if (!__all_sync(0xFFFFFFFFu, got)) break;
+        uint4* rp = reinterpret_cast<uint4*>(smem + stage * stage_bytes + warp * row_bytes);
+        uint4* sr = ext.x_sum != nullptr ? ext.x_sum + row * nvec : nullptr;
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int v = lane + 32 * i;
+          if (v < nvec) {
+            uint4 u = rp[v];
+            if (has_res) {  // x_add = bf16(x + residual), one rounding of the exact sum
+              float a[8], b[8];
+              unpack8(u, a);
+              unpack8(rv[i], b);
+              u = make_uint4(pack_bf16x2(__fadd_rn(a[0], b[0]), __fadd_rn(a[1], b[1])),
+                             pack_bf16x2(__fadd_rn(a[2], b[2]), __fadd_rn(a[3], b[3])),
+                             pack_bf16x2(__fadd_rn(a[4], b[4]), __fadd_rn(a[5], b[5])),
+                             pack_bf16x2(__fadd_rn(a[6], b[6]), __fadd_rn(a[7], b[7])));
+              rp[v] = u;
+            }
+            if (sr != nullptr) sr[v] = u;
+            float f[8];
+            unpack8(u, f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (MODE == 0)
+                s = fmaf(f[j], f[j], s);
+              else
+                s = fmaf(f[j] * f[j], inv_d, s);
+            }
+          }
+        }
+        s = warp_sum(s);
+        const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
+        if (ext.rstd_out != nullptr && lane == 0) ext.rstd_out[row] = rstd;
+        uint4* ar = A + row * nvec;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int v = lane + 32 * i;  // the elements this lane wrote above
+          if (v >= nvec) break;
+          float f[8];
+          unpack8(rp[v], f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = f[j] * rstd;
+          if (GAMMA) {
+            float gg[8];
+            unpack8(gamma_s[v], gg);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = f[j] * gg[j];
+          }
+          if (has_beta) {
+            float bb[8];
+            unpack8(beta_s[v], bb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __fadd_rn(f[j], bb[j]);
+          }
+          ar[v] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                             pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        }
+        // the slot was written through the generic proxy; order that before
+        // the next bulk copy (async proxy) refills it
+        if (has_res) fence_proxy_async_shared();
+      } else if (row < T) {
         const bool got = mbar_wait(smem_u32(&ctrl->full[stage][warp]), phase, abort, &g_err_norm, 32);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint4* rp = reinterpret_cast<const uint4*>(smem + stage * stage_bytes + warp * row_bytes);
@@ -192,14 +286,16 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
   }
 }
 
-template <int MODE, bool GAMMA, int VPL>
+template <int MODE, bool GAMMA, int VPL, bool EXT>
 rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int stages, float inv_d,
-                     float eps, void* A, size_t smem, const DeviceInfo& dev, cudaStream_t s) {
+                     float eps, void* A, const NsExt& ext, size_t smem, const DeviceInfo& dev,
+                     cudaStream_t s) {
   static bool attr_set[64] = {};
-  auto kern = norm_cast_stream_kernel<MODE, GAMMA, VPL>;
+  auto kern = norm_cast_stream_kernel<MODE, GAMMA, VPL, EXT>;
   if (!attr_set[dev.device]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kRingBytes + 128 + 8192 + sizeof(NsCtrl))) != cudaSuccess)
+                             static_cast<int>(kRingBytes + 128 + 2 * 8192 + sizeof(NsCtrl))) !=
+        cudaSuccess)
       return RNL_ERR_LAUNCH;
     attr_set[dev.device] = true;
   }
@@ -216,7 +312,7 @@ rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int 
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(x),
                                            static_cast<const uint4*>(gamma), T, nvec, stages,
-                                           inv_d, eps, static_cast<uint4*>(A));
+                                           inv_d, eps, static_cast<uint4*>(A), ext);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
@@ -224,24 +320,30 @@ rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int 
   return RNL_OK;
 }
 
-template <int VPL>
+template <int VPL, bool EXT>
 rnl_status dispatch_mode(const void* x, const void* gamma, int64_t T, int nvec, int stages,
-                         float inv_d, float eps, void* A, size_t smem, const DeviceInfo& dev,
-                         cudaStream_t s, int mode) {
+                         float inv_d, float eps, void* A, const NsExt& ext, size_t smem,
+                         const DeviceInfo& dev, cudaStream_t s, int mode) {
   if (mode == RNL_NORM_RSQRT)
-    return gamma ? launch_ns<0, true, VPL>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s)
-                 : launch_ns<0, false, VPL>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s);
-  return gamma ? launch_ns<1, true, VPL>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s)
-               : launch_ns<1, false, VPL>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s);
+    return gamma ? launch_ns<0, true, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s)
+                 : launch_ns<0, false, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s);
+  return gamma ? launch_ns<1, true, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s)
+               : launch_ns<1, false, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s);
 }
 
-}  // namespace
+template <bool EXT>
+rnl_status dispatch_vpl(const void* x, const void* gamma, int64_t T, int nvec, int stages,
+                        float inv_d, float eps, void* A, const NsExt& ext, size_t smem,
+                        const DeviceInfo& dev, cudaStream_t s, int mode) {
+  const int vpl = (nvec + 31) / 32;
+  if (vpl <= 2) return dispatch_mode<2, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
+  if (vpl <= 4) return dispatch_mode<4, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
+  if (vpl <= 8) return dispatch_mode<8, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
+  return dispatch_mode<16, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
+}
 
-// Rows of up to 4096 elements (16 vectors per lane in registers).
-bool norm_cast_stream_fits(int64_t K) { return K % 8 == 0 && K <= 4096; }
-
-rnl_status launch_norm_cast_stream(const void* x, const void* gamma, int64_t T, int64_t K,
-                                   float eps, int mode, void* A, cudaStream_t s) {
+rnl_status launch_stream(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                         int mode, void* A, const NsExt* ext, cudaStream_t s) {
   if (T == 0) return RNL_OK;
   if (!norm_cast_stream_fits(K)) return RNL_ERR_UNSUPPORTED;
   DeviceInfo dev;
@@ -251,21 +353,39 @@ rnl_status launch_norm_cast_stream(const void* x, const void* gamma, int64_t T, 
   const size_t stage = static_cast<size_t>(kGroupRows) * static_cast<size_t>(K) * 2;
   int stages = static_cast<int>(kRingBytes / stage);
   if (stages > kMaxNsStages) stages = kMaxNsStages;
-  const size_t smem = 128 + static_cast<size_t>(stages) * stage + static_cast<size_t>(K) * 2 +
-                      sizeof(NsCtrl);
+  // ring, then gamma [, beta] rows, then the barriers
+  const size_t smem = 128 + static_cast<size_t>(stages) * stage +
+                      static_cast<size_t>(ext ? 2 : 1) * static_cast<size_t>(K) * 2 + sizeof(NsCtrl);
   const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
   trace_before(s);
-  const int vpl = (nvec + 31) / 32;
-  if (vpl <= 2)
-    st = dispatch_mode<2>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s, mode);
-  else if (vpl <= 4)
-    st = dispatch_mode<4>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s, mode);
-  else if (vpl <= 8)
-    st = dispatch_mode<8>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s, mode);
+  if (ext)
+    st = dispatch_vpl<true>(x, gamma, T, nvec, stages, inv_d, eps, A, *ext, smem, dev, s, mode);
   else
-    st = dispatch_mode<16>(x, gamma, T, nvec, stages, inv_d, eps, A, smem, dev, s, mode);
-  trace_after(s, "norm_cast");
+    st = dispatch_vpl<false>(x, gamma, T, nvec, stages, inv_d, eps, A, NsExt{}, smem, dev, s, mode);
+  trace_after(s, ext ? "add_norm_cast" : "norm_cast");
   return st;
+}
+
+}  // namespace
+
+// Rows of up to 4096 elements (16 vectors per lane in registers).
+bool norm_cast_stream_fits(int64_t K) { return K % 8 == 0 && K <= 4096; }
+
+rnl_status launch_norm_cast_stream(const void* x, const void* gamma, int64_t T, int64_t K,
+                                   float eps, int mode, void* A, cudaStream_t s) {
+  return launch_stream(x, gamma, T, K, eps, mode, A, nullptr, s);
+}
+
+rnl_status launch_add_norm_cast_stream(const void* x, const void* residual, void* x_sum_out,
+                                       const void* gamma, const void* beta, int64_t T, int64_t K,
+                                       float eps, int mode, void* A, float* rstd_out,
+                                       cudaStream_t s) {
+  NsExt ext;
+  ext.residual = static_cast<const uint4*>(residual);
+  ext.x_sum = static_cast<uint4*>(x_sum_out);
+  ext.beta = static_cast<const uint4*>(beta);
+  ext.rstd_out = rstd_out;
+  return launch_stream(x, gamma, T, K, eps, mode, A, &ext, s);
 }
 
 rnl_status read_clear_error_norm(unsigned int* word) {

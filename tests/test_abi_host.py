@@ -88,6 +88,16 @@ CHILD = textwrap.dedent("""
     s8 = lib.rnl_gemm_s8s8s32
     r["s8_K_not_mult16"] = s8(A, A, A, 4, 8, 24, ws, 1 << 20, None)
     r["s8_M0"] = s8(None, None, None, 0, 8, 32, None, 0, None)
+    e = lib.rmsnorm_linear_bf16_ex
+    C = P(0x30000)
+    r["ex_sum_without_residual"] = e(A, None, C, None, None, A, None, 4, 64, 8, 1e-6, 0, A, None, ws, 1 << 20, None)
+    r["ex_sum_partial_overlap"] = e(A, C, P(0x10010), None, None, A, None, 4, 64, 8, 1e-6, 0, A, None, ws, 1 << 20, None)
+    r["ex_misaligned_bias"] = e(A, None, None, None, None, A, B, 4, 64, 8, 1e-6, 0, A, None, ws, 1 << 20, None)
+    r["ex_misaligned_rstd"] = e(A, None, None, None, None, A, None, 4, 64, 8, 1e-6, 0, A, P(0x10002), ws, 1 << 20, None)
+    r["ex_null_W"] = e(A, None, None, None, None, None, None, 4, 64, 8, 1e-6, 0, A, None, ws, 1 << 20, None)
+    r["ex_bad_mode"] = e(A, None, None, None, None, A, None, 4, 64, 8, 1e-6, 3, A, None, ws, 1 << 20, None)
+    r["ex_small_ws"] = e(A, None, None, None, None, A, None, 4, 64, 8, 1e-6, 0, A, None, ws, 16, None)
+    r["ex_in_place_no_device"] = e(A, C, C, A, A, A, A, 4, 64, 8, 1e-6, 0, A, P(0x40000), ws, 1 << 30, None)
     pp = ctypes.c_void_p(None)
     r["pipe_null_out"] = lib.rnl_pipeline_create(0, 4, 64, 8, 0, None)
     r["pipe_bad_op"] = lib.rnl_pipeline_create(3, 4, 64, 8, 0, ctypes.byref(pp))
@@ -147,6 +157,9 @@ def test_workspace_sizes(host_results):
     ("mla_null_gamma", NULL), ("mla_N1_not_mult8", ALIGN),
     ("s8_K_not_mult16", ALIGN), ("s8_M0", OK),
     ("trace_enable", OK), ("trace_read_empty", 0),
+    ("ex_sum_without_residual", ARG), ("ex_sum_partial_overlap", ARG), ("ex_misaligned_bias", ALIGN),
+    ("ex_misaligned_rstd", ALIGN), ("ex_null_W", NULL), ("ex_bad_mode", ARG), ("ex_small_ws", WORKSPACE),
+    ("ex_in_place_no_device", DEVICE),
     ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
     ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
     ("pipe_submit_null", NULL), ("pipe_submit_null_W", NULL), ("pipe_submit_bad_eps", ARG),
