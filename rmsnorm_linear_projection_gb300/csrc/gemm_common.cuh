@@ -39,11 +39,46 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 256-bit global store / load (one full 32-byte sector per thread); p must
+// be 32-byte aligned.  The load is a plain (coherent) load.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_global_v8(const void* p, uint32_t (&v)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                 "=r"(v[6]), "=r"(v[7])
+               : "l"(p)
+               : "memory");
+}
+
+// Whether a thread's 32 consecutive outputs of row m starting at column n0
+// (a multiple of 32) can go out as 32-byte stores: the row pitch and the base
+// are multiples of 32 bytes.
+__device__ __forceinline__ bool rows_32b_aligned(const void* out, int N, int elem_bytes) {
+  return ((static_cast<int64_t>(N) * elem_bytes) & 31) == 0 &&
+         (reinterpret_cast<uintptr_t>(out) & 31) == 0;
+}
+
 // out[m, n0 .. n0+31] = bf16(v), v given as fp32 bit patterns (TMEM words).
+// Each thread writes its own row, so full 32-byte sectors (256-bit stores)
+// halve the number of memory transactions against 16-byte stores.
 __device__ __forceinline__ void store_bf16_32(void* out, int64_t m, int n0, int N,
                                               const uint32_t (&r)[32]) {
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
-  if (n0 + 32 <= N && (N & 7) == 0) {
+  if (n0 + 32 <= N && rows_32b_aligned(out, N, 2)) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        o[i] = bf16x2_bits(__uint_as_float(r[16 * h + 2 * i]), __uint_as_float(r[16 * h + 2 * i + 1]));
+      st_global_v8(orow + n0 + 16 * h, o);
+    }
+  } else if (n0 + 32 <= N && (N & 7) == 0) {
     uint4* dst = reinterpret_cast<uint4*>(orow + n0);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -65,7 +100,25 @@ __device__ __forceinline__ void store_bf16_bias_32(void* out, int64_t m, int n0,
                                                    const uint32_t (&r)[32],
                                                    const __nv_bfloat16* __restrict__ bias) {
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
-  if (n0 + 32 <= N && (N & 7) == 0) {
+  if (n0 + 32 <= N && rows_32b_aligned(out, N, 2)) {
+    const uint4* b = reinterpret_cast<const uint4*>(bias + n0);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t o[8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint4 u = __ldg(b + 2 * h + q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int k = 16 * h + 8 * q + 2 * i;
+          o[4 * q + i] = bf16x2_bits(__fadd_rn(__uint_as_float(r[k]), __uint_as_float(w[i] << 16)),
+                                     __fadd_rn(__uint_as_float(r[k + 1]), __uint_as_float(w[i] & 0xFFFF0000u)));
+        }
+      }
+      st_global_v8(orow + n0 + 16 * h, o);
+    }
+  } else if (n0 + 32 <= N && (N & 7) == 0) {
     uint4* dst = reinterpret_cast<uint4*>(orow + n0);
     const uint4* b = reinterpret_cast<const uint4*>(bias + n0);
 #pragma unroll
@@ -91,7 +144,15 @@ __device__ __forceinline__ void store_bf16_bias_32(void* out, int64_t m, int n0,
 __device__ __forceinline__ void store_f32_scaled_32(void* out, int64_t m, int n0, int N,
                                                     const uint32_t (&r)[32], float rs) {
   float* orow = static_cast<float*>(out) + m * N;
-  if (n0 + 32 <= N && (N & 3) == 0) {
+  if (n0 + 32 <= N && rows_32b_aligned(out, N, 4)) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = __float_as_uint(__uint_as_float(r[8 * h + i]) * rs);
+      st_global_v8(orow + n0 + 8 * h, o);
+    }
+  } else if (n0 + 32 <= N && (N & 3) == 0) {
     float4* dst = reinterpret_cast<float4*>(orow + n0);
 #pragma unroll
     for (int j = 0; j < 8; ++j)

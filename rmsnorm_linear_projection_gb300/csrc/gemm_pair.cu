@@ -19,15 +19,25 @@
 // CTA's epilogue warps arrive on the even CTA's "accumulator empty" barrier.
 // Every wait is bounded (ptx.cuh).
 //
-// Work list (persistent, one CTA pair per two SMs): with P pairs and T tiles,
-// the first floor(T/P) * P tiles run data-parallel (pair p takes tiles p,
-// p+P, ...).  The R = T mod P tiles left over would leave most pairs idle in a
-// last partial wave, so each of them is cut along K into S = P / R pieces and
-// every pair takes one piece: its partial sums (fp32, or exact int32 in the
-// integer mode) go to a workspace, and gemm_pair_fixup_kernel adds the S
-// pieces of each tile in a fixed order and applies the epilogue.
+// Work list (persistent, one CTA pair per two SMs; P pairs, T tiles): a
+// hybrid of data-parallel waves and stream-K.  The first (floor(T/P) - 1) * P
+// tiles run data-parallel (pair p takes tiles p, p+P, ..., in the grouped
+// order that keeps A and W L2-resident).  The last P to 2P tiles would leave
+// most pairs idle in a partial wave, so their k-blocks, flattened tile by
+// tile, are cut into P equal contiguous ranges, one per pair (stream-K).  A
+// range that starts inside a tile computes a partial sum of that tile (fp32,
+// or exact int32 in the integer mode), stores it to its pair's slot of the
+// workspace and publishes it with a per-warp flag (a GPU-scope release of a
+// per-launch epoch); the pair whose range holds the tile's first k-blocks
+// processes that fragment last, waits (bounded) for the flags of the pairs
+// that hold the rest and adds their partial sums in its epilogue, in pair
+// order.  All pairs of the grid are resident at once (the grid is sized from
+// the occupancy of the cluster launch), and a pair only waits for pairs of
+// higher index, which never wait on it.
 #include <cuda_bf16.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstdlib>
 
 #include "gemm_common.cuh"
@@ -42,7 +52,6 @@ using namespace gemm;
 __device__ unsigned int g_err_pair;
 
 constexpr int kEpiWarps = 8;
-constexpr int kMaxSplits = 16;  // K pieces per leftover tile (partial volume vs tail length)
 
 template <int BN>
 struct PairTile {
@@ -70,39 +79,81 @@ constexpr size_t pair_smem_bytes() {
          sizeof(PairCtrl);
 }
 
-struct Work {
-  int tile;  // index in the grouped tile order
-  int kb0;   // k-block range [kb0, kb1)
-  int kb1;
-  int slot;  // partial-sum slot, or -1 for a whole tile written to the output
+// The work list shape (identical in every role and CTA).
+struct Sched {
+  int num_pairs;
+  int dp_tiles;  // tiles [0, dp_tiles) data-parallel, whole
+  int sk_tiles;  // tiles [dp_tiles, dp_tiles + sk_tiles) stream-K
+  int num_kb;
+  __device__ __forceinline__ int dp_items(int pair) const {
+    return pair < dp_tiles ? (dp_tiles - pair + num_pairs - 1) / num_pairs : 0;
+  }
+  // first stream-K unit (k-block of the flattened stream-K tiles) of a pair
+  __device__ __forceinline__ int64_t sk_start(int pair) const {
+    return static_cast<int64_t>(pair) * sk_tiles * num_kb / num_pairs;
+  }
+  __device__ __forceinline__ int sk_items(int pair) const {
+    const int64_t u0 = sk_start(pair), u1 = sk_start(pair + 1);
+    if (u1 <= u0) return 0;
+    return static_cast<int>((u1 - 1) / num_kb - u0 / num_kb + 1);
+  }
+  __device__ __forceinline__ int items(int pair) const { return dp_items(pair) + sk_items(pair); }
 };
 
-// Item `it` of pair `pair`'s work list (identical in every role).
-__device__ __forceinline__ Work work_item(int pair, int it, int num_pairs, int dp_waves,
-                                          int splits, int num_kb) {
+enum : int {
+  kWhole = 0,    // the whole tile: epilogue to the output
+  kFinish = 1,   // the tile's first k-blocks: add the other pairs' partial sums, then epilogue
+  kPartial = 2,  // a later part of the tile: partial sums to this pair's slot, then the flag
+};
+
+struct Work {
+  int tile;     // index in the grouped tile order
+  int kb0;      // k-block range [kb0, kb1)
+  int kb1;
+  int kind;
+  int sk_tile;  // index among the stream-K tiles, or -1
+};
+
+// Item `it` of pair `pair`'s work list.
+__device__ __forceinline__ Work work_item(const Sched& sc, int pair, int it) {
   Work w;
-  if (it < dp_waves) {
-    w.tile = pair + it * num_pairs;
+  const int ndp = sc.dp_items(pair);
+  if (it < ndp) {
+    w.tile = pair + it * sc.num_pairs;
     w.kb0 = 0;
-    w.kb1 = num_kb;
-    w.slot = -1;
-  } else {
-    const int j = pair % splits;
-    w.tile = dp_waves * num_pairs + pair / splits;
-    w.kb0 = static_cast<int>((static_cast<int64_t>(j) * num_kb) / splits);
-    w.kb1 = static_cast<int>((static_cast<int64_t>(j + 1) * num_kb) / splits);
-    w.slot = splits > 1 ? pair : -1;
+    w.kb1 = sc.num_kb;
+    w.kind = kWhole;
+    w.sk_tile = -1;
+    return w;
   }
+  const int64_t u0 = sc.sk_start(pair), u1 = sc.sk_start(pair + 1);
+  const int t = static_cast<int>(u0 / sc.num_kb) + (it - ndp);
+  const int64_t ts = static_cast<int64_t>(t) * sc.num_kb;
+  w.kb0 = static_cast<int>(u0 > ts ? u0 - ts : 0);
+  w.kb1 = static_cast<int>(u1 < ts + sc.num_kb ? u1 - ts : sc.num_kb);
+  w.tile = sc.dp_tiles + t;
+  w.sk_tile = t;
+  w.kind = w.kb0 > 0 ? kPartial : (w.kb1 < sc.num_kb ? kFinish : kWhole);
   return w;
+}
+
+// One past the last pair whose partial sums the finisher `pair` of stream-K
+// tile t adds: the pairs after it whose ranges start inside tile t.
+__device__ __forceinline__ int partners_end(const Sched& sc, int pair, int t) {
+  const int64_t tile_end = static_cast<int64_t>(t + 1) * sc.num_kb;
+  int q = pair + 1;
+  while (q < sc.num_pairs && sc.sk_start(q) < tile_end) ++q;
+  return q;
 }
 
 template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b, int M, int N, int K, int group_m,
-                     int dp_waves, int tail_tiles, int splits, void* __restrict__ out,
+                     int dp_tiles, int sk_tiles, void* __restrict__ out,
                      const float* __restrict__ row_scale, const float* __restrict__ col_scale,
-                     uint32_t* __restrict__ partial, const __nv_bfloat16* __restrict__ bias) {
+                     uint32_t* partial, uint64_t* flags, uint64_t epoch,
+                     const __nv_bfloat16* __restrict__ bias) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
   constexpr int kStages = PairTile<BN>::kStages;
@@ -125,7 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_m = (M + 2 * BM - 1) / (2 * BM);  // 256-row blocks
   const int num_n = (N + BN - 1) / BN;
   const int num_kb = (K + BK - 1) / BK;
-  const int n_items = dp_waves + (pair < tail_tiles * splits ? 1 : 0);
+  Sched sc;
+  sc.num_pairs = num_pairs;
+  sc.dp_tiles = dp_tiles;
+  sc.sk_tiles = sk_tiles;
+  sc.num_kb = num_kb;
+  const int n_items = sc.items(pair);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -162,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int it = 0; it < n_items && ok; ++it) {
-        const Work w = work_item(pair, it, num_pairs, dp_waves, splits, num_kb);
+        const Work w = work_item(sc, pair, it);
         int mb, nb;
         tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -192,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, unit = 0;
       bool ok = true;
       for (int it = 0; it < n_items && ok; ++it) {
-        const Work w = work_item(pair, it, num_pairs, dp_waves, splits, num_kb);
+        const Work w = work_item(sc, pair, it);
         const int kb_per_unit = kInt ? kChunkKBlocks : (w.kb1 - w.kb0);
         const int units = (w.kb1 - w.kb0 + kb_per_unit - 1) / kb_per_unit;
         for (int u = 0; u < units && ok; ++u, ++unit) {
@@ -244,12 +300,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t unit = 0;
     bool ok = true;
     for (int it = 0; it < n_items && ok; ++it) {
-      const Work w = work_item(pair, it, num_pairs, dp_waves, splits, num_kb);
+      const Work w = work_item(sc, pair, it);
       const int kb_per_unit = kInt ? kChunkKBlocks : (w.kb1 - w.kb0);
       const int units = (w.kb1 - w.kb0 + kb_per_unit - 1) / kb_per_unit;
-      // partial slot of this CTA: [slot][rank][128 rows][BN] 32-bit words
-      uint32_t* prow = w.slot >= 0 ? partial + ((static_cast<int64_t>(w.slot) * 2 + rank) * BM + row_local) * BN
-                                   : nullptr;
+      // partial slots: [pair][rank][epilogue warp][32-byte chunk][lane] words,
+      // lane-major so that one warp instruction moves 1 KB of contiguous
+      // memory; only the same warp and lane of the finisher read a chunk back
+      const int64_t slot_words = static_cast<int64_t>(2) * BM * BN;
+      const int64_t warp_off = (static_cast<int64_t>(rank) * kEpiWarps + ew) * 32 * kColsPerEpiWarp +
+                               lane * 8;
+      uint32_t* prow = w.kind == kPartial ? partial + pair * slot_words + warp_off : nullptr;
+      // a finisher adds the partial sums of pairs [pair + 1, q_end)
+      const int q_end = w.kind == kFinish ? partners_end(sc, pair, w.sk_tile) : pair + 1;
+      if (w.kind == kFinish) {
+        // this warp reads only the words the same warp of each partner wrote
+        bool got = true;
+        for (int q = pair + 1; q < q_end && got; ++q)
+          got = flag_wait(flags + (static_cast<int64_t>(q) * 2 + rank) * kEpiWarps + ew, epoch, abort,
+                          &g_err_pair, 25);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+      }
       int mb, nb;
       tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
       const int64_t m = static_cast<int64_t>(mb) * 2 * BM + rank * BM + row_local;
@@ -286,18 +359,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) iacc[c][j] += __float2int_rn(__uint_as_float(r[j]));
           } else if (prow != nullptr) {
-            uint4* dst = reinterpret_cast<uint4*>(prow + half * kColsPerEpiWarp + c * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-          } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-            if (row_ok) {
-              if (bias != nullptr)
-                store_bf16_bias_32(out, m, n0, N, r, bias);
-              else
-                store_bf16_32(out, m, n0, N, r);
+            for (int j = 0; j < 4; ++j) {
+              uint32_t v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = r[8 * j + i];
+              st_global_v8(prow + (c * 4 + j) * 256, v);
             }
           } else {
-            if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
+            if (row_ok) {
+              // the partners' fp32 partial sums, added in pair order (plain
+              // loads: they were written during this grid)
+              for (int q = pair + 1; q < q_end; ++q) {
+                const uint32_t* src = partial + q * slot_words + warp_off;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t v[8];
+                  ld_global_v8(src + (c * 4 + j) * 256, v);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    r[8 * j + i] = __float_as_uint(__uint_as_float(r[8 * j + i]) + __uint_as_float(v[i]));
+                }
+              }
+            }
+            if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
+              if (row_ok) {
+                if (bias != nullptr)
+                  store_bf16_bias_32(out, m, n0, N, r, bias);
+                else
+                  store_bf16_32(out, m, n0, N, r);
+              }
+            } else {
+              if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
+            }
           }
         }
         tc_fence_before();
@@ -314,12 +408,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (prow != nullptr) {
 #pragma unroll
           for (int c = 0; c < kGroups; ++c) {
-            int4* dst = reinterpret_cast<int4*>(prow + half * kColsPerEpiWarp + c * 32);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_int4(iacc[c][4 * j], iacc[c][4 * j + 1], iacc[c][4 * j + 2], iacc[c][4 * j + 3]);
+            for (int j = 0; j < 4; ++j) {
+              uint32_t v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = static_cast<uint32_t>(iacc[c][8 * j + i]);
+              st_global_v8(prow + (c * 4 + j) * 256, v);
+            }
           }
         } else if (row_ok) {
+          // the partners' exact int32 partial sums
+          for (int q = pair + 1; q < q_end; ++q) {
+            const uint32_t* src = partial + q * slot_words + warp_off;
+#pragma unroll
+            for (int c = 0; c < kGroups; ++c) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t v[8];
+                ld_global_v8(src + (c * 4 + j) * 256, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) iacc[c][8 * j + i] += static_cast<int>(v[i]);
+              }
+            }
+          }
 #pragma unroll
           for (int c = 0; c < kGroups; ++c) {
             if constexpr (EPI == static_cast<int>(Epi::kInt32))
@@ -328,6 +439,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale, bias);
           }
         }
+      }
+      if (w.kind == kPartial) {
+        // every lane orders its partial stores, then one lane publishes this
+        // warp's flag (release)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+          flag_release(flags + (static_cast<int64_t>(pair) * 2 + rank) * kEpiWarps + ew, epoch);
       }
     }
   }
@@ -346,142 +465,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Adds the S partial pieces of each split tile (in piece order) and applies
 // the epilogue.  Thread = (tile, 256-row position, 4 consecutive columns);
 // the piece loads are unrolled so several are in flight per thread.
-template <int EPI, int BN>
-__global__ void __launch_bounds__(256)
-    gemm_pair_fixup_kernel(int M, int N, int group_m, int dp_tiles, int tail_tiles, int splits,
-                           const uint32_t* __restrict__ partial, void* __restrict__ out,
-                           const float* __restrict__ row_scale, const float* __restrict__ col_scale,
-                           const __nv_bfloat16* __restrict__ bias) {
-  constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
-                         EPI == static_cast<int>(Epi::kInt32));
-  constexpr int kQuadsPerRow = BN / 4;
-  grid_dependency_wait();
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = static_cast<int64_t>(tail_tiles) * 2 * BM * kQuadsPerRow;
-  if (idx >= total) return;
-  const int q = static_cast<int>(idx % kQuadsPerRow);
-  const int row = static_cast<int>((idx / kQuadsPerRow) % (2 * BM));  // 0..255 in the pair tile
-  const int r = static_cast<int>(idx / (kQuadsPerRow * 2 * BM));
-  const int num_m = (M + 2 * BM - 1) / (2 * BM);
-  const int num_n = (N + BN - 1) / BN;
-  int mb, nb;
-  tile_coords(dp_tiles + r, num_m, num_n, group_m, mb, nb);
-  const int64_t m = static_cast<int64_t>(mb) * 2 * BM + row;
-  const int n0 = nb * BN + q * 4;
-  if (m >= M || n0 >= N) return;
-  const int rank = row / BM;
-  const int row_local = row % BM;
-  // word offset of this thread's 4 columns in piece sidx
-  const int64_t stride = static_cast<int64_t>(2) * BM * BN;  // words per piece
-  const uint4* src = reinterpret_cast<const uint4*>(
-      partial + ((static_cast<int64_t>(r) * splits * 2 + rank) * BM + row_local) * BN + q * 4);
-  const int64_t vstride = stride / 4;  // in uint4
-  uint4 acc_bits;
-  if constexpr (kInt) {
-    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-    int sidx = 0;
-    for (; sidx + 4 <= splits; sidx += 4) {
-      const uint4 v0 = src[(sidx + 0) * vstride], v1 = src[(sidx + 1) * vstride];
-      const uint4 v2 = src[(sidx + 2) * vstride], v3 = src[(sidx + 3) * vstride];
-      a0 += static_cast<int>(v0.x) + static_cast<int>(v1.x) + static_cast<int>(v2.x) + static_cast<int>(v3.x);
-      a1 += static_cast<int>(v0.y) + static_cast<int>(v1.y) + static_cast<int>(v2.y) + static_cast<int>(v3.y);
-      a2 += static_cast<int>(v0.z) + static_cast<int>(v1.z) + static_cast<int>(v2.z) + static_cast<int>(v3.z);
-      a3 += static_cast<int>(v0.w) + static_cast<int>(v1.w) + static_cast<int>(v2.w) + static_cast<int>(v3.w);
-    }
-    for (; sidx < splits; ++sidx) {
-      const uint4 v = src[sidx * vstride];
-      a0 += static_cast<int>(v.x);
-      a1 += static_cast<int>(v.y);
-      a2 += static_cast<int>(v.z);
-      a3 += static_cast<int>(v.w);
-    }
-    const int a[4] = {a0, a1, a2, a3};
-    if constexpr (EPI == static_cast<int>(Epi::kInt32)) {
-      int* orow = static_cast<int*>(out) + m * N;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (n0 + j < N) orow[n0 + j] = a[j];
-    } else {
-      const float xs = __ldg(row_scale + m);
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (n0 + j < N) {
-          float v = static_cast<float>(a[j]) * (xs * __ldg(col_scale + n0 + j));
-          if (bias != nullptr) v = __fadd_rn(v, __bfloat162float(bias[n0 + j]));
-          orow[n0 + j] = __float2bfloat16_rn(v);
-        }
-    }
-    (void)acc_bits;
-  } else {
-    // fp32 partial sums added in piece order (pairwise within a group of
-    // four pieces, then sequentially), the same order on every run
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int sidx = 0;
-    for (; sidx + 4 <= splits; sidx += 4) {
-      const uint4 v0 = src[(sidx + 0) * vstride], v1 = src[(sidx + 1) * vstride];
-      const uint4 v2 = src[(sidx + 2) * vstride], v3 = src[(sidx + 3) * vstride];
-      a0 += (__uint_as_float(v0.x) + __uint_as_float(v1.x)) + (__uint_as_float(v2.x) + __uint_as_float(v3.x));
-      a1 += (__uint_as_float(v0.y) + __uint_as_float(v1.y)) + (__uint_as_float(v2.y) + __uint_as_float(v3.y));
-      a2 += (__uint_as_float(v0.z) + __uint_as_float(v1.z)) + (__uint_as_float(v2.z) + __uint_as_float(v3.z));
-      a3 += (__uint_as_float(v0.w) + __uint_as_float(v1.w)) + (__uint_as_float(v2.w) + __uint_as_float(v3.w));
-    }
-    for (; sidx < splits; ++sidx) {
-      const uint4 v = src[sidx * vstride];
-      a0 += __uint_as_float(v.x);
-      a1 += __uint_as_float(v.y);
-      a2 += __uint_as_float(v.z);
-      a3 += __uint_as_float(v.w);
-    }
-    float a[4] = {a0, a1, a2, a3};
-    if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-      if (bias != nullptr) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n0 + j < N) a[j] = __fadd_rn(a[j], __bfloat162float(bias[n0 + j]));
-      }
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out) + m * N;
-      if (n0 + 4 <= N && (N & 3) == 0) {
-        uint2 o;
-        o.x = bf16x2_bits(a[0], a[1]);
-        o.y = bf16x2_bits(a[2], a[3]);
-        *reinterpret_cast<uint2*>(orow + n0) = o;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (n0 + j < N) orow[n0 + j] = __float2bfloat16_rn(a[j]);
-      }
-    } else {
-      const float rs = __ldg(row_scale + m);
-      float* orow = static_cast<float*>(out) + m * N;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (n0 + j < N) orow[n0 + j] = a[j] * rs;
-    }
-    (void)acc_bits;
-  }
-}
-
-// Work-list shape for T tiles on P pairs: full data-parallel waves, then the
-// leftover tiles cut along K into `splits` pieces (one per pair).
+// Work-list shape for T tiles on P pairs: (floor(T/P) - 1) full data-parallel
+// waves, the remaining P .. 2P - 1 tiles stream-K (every tile then spans at
+// most two pairs' ranges, so a finisher adds at most one partner's partial
+// sums).  Fewer than 2P tiles: all stream-K.  Without a workspace for the
+// partial sums: every tile whole, data-parallel.
 struct Plan {
-  int dp_waves = 0;
-  int tail_tiles = 0;
-  int splits = 1;
+  int dp_tiles = 0;
+  int sk_tiles = 0;
 };
 
-Plan make_plan(int64_t tiles, int pairs, int num_kb) {
+Plan make_plan(int64_t tiles, int pairs, bool have_partials) {
   Plan pl;
-  pl.dp_waves = static_cast<int>(tiles / pairs);
-  pl.tail_tiles = static_cast<int>(tiles - static_cast<int64_t>(pl.dp_waves) * pairs);
-  if (pl.tail_tiles > 0) {
-    int sp = pairs / pl.tail_tiles;
-    if (sp > kMaxSplits) sp = kMaxSplits;
-    if (sp > num_kb) sp = num_kb;
-    if (sp * pl.tail_tiles > kMaxPartialSlots) sp = kMaxPartialSlots / pl.tail_tiles;
-    pl.splits = sp < 1 ? 1 : sp;
+  if (!have_partials) {
+    pl.dp_tiles = static_cast<int>(tiles);
+    return pl;
   }
+  const int64_t waves = tiles / pairs;
+  const int64_t dp_waves = waves > 1 ? waves - 1 : 0;
+  pl.dp_tiles = static_cast<int>(dp_waves * pairs);
+  pl.sk_tiles = static_cast<int>(tiles - pl.dp_tiles);
   return pl;
+}
+
+// Pairs to launch: with stream-K every resident pair, as long as each range
+// keeps at least 8 k-blocks (fewer pairs for tiny problems); without partial
+// sums at most one pair per tile.
+int grid_pairs(int64_t tiles, int num_kb, int max_pairs, bool have_partials) {
+  int64_t p = tiles;
+  if (have_partials) {
+    const int64_t by_units = tiles * num_kb / 8;
+    p = by_units > tiles ? by_units : tiles;
+  }
+  if (p > max_pairs) p = max_pairs;
+  if (p > kMaxPartialSlots - 1) p = kMaxPartialSlots - 1;
+  return static_cast<int>(p < 1 ? 1 : p);
+}
+
+// Epoch of each launch: a per-process start value from the clock, then one
+// step per launch, so a flag left in a reused workspace by an earlier launch
+// (or process) never matches.
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> counter{
+      static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) * 2654435761ull};
+  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 template <int EPI, int BN>
@@ -505,12 +532,17 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   const int num_m = static_cast<int>((g.M + 2 * BM - 1) / (2 * BM));
   const int num_kb = static_cast<int>((g.K + BK - 1) / BK);
   const int64_t tiles = static_cast<int64_t>(num_m) * ((g.N + BN - 1) / BN);
-  const int pairs = static_cast<int>(tiles < max_pairs ? tiles : max_pairs);
-  Plan pl = make_plan(tiles, pairs, num_kb);
-  if (pl.splits > 1 && (g.partial_ws == nullptr ||
-                        g.partial_ws_bytes < static_cast<size_t>(pl.tail_tiles) * pl.splits * 2 *
-                                                 BM * BN * 4))
-    pl.splits = 1;  // no room for partial sums: the leftover tiles run whole
+  // partial sums: one slot of 2 x 128 x BN words per pair, the flags in the
+  // last slot of the workspace (room for kMaxPartialSlots - 1 pairs)
+  const size_t slot_bytes = static_cast<size_t>(2) * BM * BN * 4;
+  const bool have_partials = g.partial_ws != nullptr &&
+                             g.partial_ws_bytes >= kMaxPartialSlots * slot_bytes;
+  const int pairs = grid_pairs(tiles, num_kb, max_pairs, have_partials);
+  const Plan pl = make_plan(tiles, pairs, have_partials);
+  uint32_t* partial = static_cast<uint32_t*>(g.partial_ws);
+  uint64_t* flags = have_partials ? reinterpret_cast<uint64_t*>(static_cast<char*>(g.partial_ws) +
+                                                                (kMaxPartialSlots - 1) * slot_bytes)
+                                  : nullptr;
   const int group_m = (g.M * g.K * 2 <= (int64_t{48} << 20)) ? num_m : (num_m < 4 ? num_m : 4);
 
   cudaLaunchAttribute attr[2];
@@ -528,34 +560,15 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   trace_before(s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
-                                     static_cast<int>(g.N), static_cast<int>(g.K), group_m,
-                                     pl.dp_waves, pl.tail_tiles, pl.splits, g.out, g.row_scale,
-                                     g.col_scale, static_cast<uint32_t*>(g.partial_ws),
-                                     static_cast<const __nv_bfloat16*>(g.bias));
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
+                                           static_cast<int>(g.N), static_cast<int>(g.K), group_m,
+                                           pl.dp_tiles, pl.sk_tiles, g.out, g.row_scale,
+                                           g.col_scale, partial, flags, next_epoch(),
+                                           static_cast<const __nv_bfloat16*>(g.bias));
   trace_after(s, name);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
-  }
-  if (pl.splits > 1) {
-    const int64_t threads = static_cast<int64_t>(pl.tail_tiles) * 2 * BM * (BN / 4);
-    cudaLaunchConfig_t fc = {};
-    fc.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256), 1, 1);
-    fc.blockDim = dim3(256, 1, 1);
-    fc.stream = s;
-    fc.attrs = &attr[1];
-    fc.numAttrs = 1;
-    trace_before(s);
-    e = cudaLaunchKernelEx(&fc, gemm_pair_fixup_kernel<EPI, BN>, static_cast<int>(g.M),
-                           static_cast<int>(g.N), group_m, pl.dp_waves * pairs, pl.tail_tiles,
-                           pl.splits, static_cast<const uint32_t*>(g.partial_ws), g.out,
-                           g.row_scale, g.col_scale, static_cast<const __nv_bfloat16*>(g.bias));
-    trace_after(s, "gemm_pair_fixup");
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return RNL_ERR_LAUNCH;
-    }
   }
   return RNL_OK;
 }
@@ -605,27 +618,21 @@ rnl_status launch_pair_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_
 
 }  // namespace
 
-// Predicted time of the pair kernel (256-wide tiles, K-split tail) in
-// microseconds, from the per-SM rate it sustained on GB300 in full waves
-// (1909 TFLOP/s over 152 SMs) plus the tail piece (1/S of a tile and about
-// 0.15 of a tile of fill, drain and partial stores) and the fix-up pass.
+// Predicted time of the pair kernel (256-wide tiles) in microseconds, from
+// the per-SM rate it sustained on GB300 in full waves (1909 TFLOP/s over 152
+// SMs): every pair's share of the k-blocks, plus about 2 us for the stream-K
+// partial sums (written early by one pair, read by another at its end) when
+// the tiles do not fill whole waves.
 double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs_hint) {
   const int pairs = pairs_hint > 0 ? pairs_hint : sm_count / 2;
   const int64_t num_m = (M + 2 * BM - 1) / (2 * BM);
   const int64_t tiles = num_m * ((N + 255) / 256);
-  const int p = static_cast<int>(tiles < pairs ? tiles : pairs);
   const int num_kb = static_cast<int>((K + BK - 1) / BK);
-  const Plan pl = make_plan(tiles, p, num_kb);
+  const int p = grid_pairs(tiles, num_kb, pairs, true);
   const double tile_us = 2.0 * BM * 256 * static_cast<double>(K) / 12.56e12 * 1e6;
-  double t = pl.dp_waves * tile_us;
-  if (pl.tail_tiles > 0) {
-    if (pl.splits > 1) {
-      const double part_bytes = static_cast<double>(pl.tail_tiles) * pl.splits * 2 * BM * 256 * 4;
-      t += (1.0 / pl.splits + 0.15) * tile_us + 3.0 + 2.0 * part_bytes / 6.0e12 * 1e6;
-    } else {
-      t += tile_us;
-    }
-  }
+  const Plan pl = make_plan(tiles, p, true);
+  double t = (static_cast<double>(pl.dp_tiles) / p + static_cast<double>(pl.sk_tiles) / p) * tile_us;
+  if (pl.sk_tiles % p != 0) t += 2.0;
   return t;
 }
 

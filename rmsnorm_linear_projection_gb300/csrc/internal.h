@@ -88,13 +88,14 @@ struct GemmArgs {
   // AT-09 has_bias: bf16 [N] added to the accumulator before the output cast
   // (bf16 and dequant epilogues; may be null)
   const void* bias = nullptr;
-  // partial sums of the CTA-pair GEMM's K-split tail (see gemm_pair.cu);
-  // without it the leftover tiles run whole
+  // partial sums and flags of the CTA-pair GEMM's stream-K tiles (see
+  // gemm_pair.cu); without it every tile runs whole
   void* partial_ws = nullptr;
   size_t partial_ws_bytes = 0;
 };
 
-// At most this many K-split pieces of 2 x 128 x 256 32-bit partial sums.
+// Partial-sum slots of the CTA-pair GEMM's stream-K tiles (2 x 128 x 256
+// 32-bit words each): one per pair, the last one holding the hand-off flags.
 constexpr int kMaxPartialSlots = 128;
 constexpr size_t kGemmPartialBytes = static_cast<size_t>(kMaxPartialSlots) * 2 * 128 * 256 * 4;
 rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s);

@@ -88,6 +88,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_limit(bar, parity, abort, err, site, kWaitLimitNs);
 }
 
+// ---------------------------------------------------------- global flags
+// A 64-bit flag in global memory, published with a GPU-scope release store
+// and read with GPU-scope acquire loads: the hand-off of partial sums between
+// CTAs of one grid (stream-K GEMM).
+__device__ __forceinline__ void flag_release(uint64_t* f, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t flag_acquire(const uint64_t* f) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+  return v;
+}
+
+// Wait until *f == v, bounded like mbar_wait (same abort flag, error word and
+// time limit).
+__device__ __forceinline__ bool flag_wait(const uint64_t* f, uint64_t v, volatile int* abort,
+                                          unsigned int* err, uint32_t site) {
+  if (flag_acquire(f) == v) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(64);
+    if (flag_acquire(f) == v) return true;
+    if ((n & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicCAS(err, 0u, kErrTimeout | (site << 8));
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (TMA, tensor core) before a barrier hands the buffer over.
 __device__ __forceinline__ void fence_proxy_async_shared() {
