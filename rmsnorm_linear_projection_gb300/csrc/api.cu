@@ -474,6 +474,7 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   g1.epi = Epi::kBf16;
   g1.partial_ws = l.part;
   g1.partial_ws_bytes = kGemmPartialBytes;
+  g1.trace_name = "gemm_mla_stage1";
   st = launch_gemm(g1, s);
   if (st != RNL_OK) return st;
   GemmArgs g2;
@@ -498,6 +499,7 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   g2.epi = Epi::kBf16;
   g2.partial_ws = l.part;
   g2.partial_ws_bytes = kGemmPartialBytes;
+  g2.trace_name = "gemm_mla_stage2";
   return launch_gemm(g2, s);
 }
 

@@ -565,7 +565,7 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
                                            pl.dp_tiles, pl.sk_tiles, g.out, g.row_scale,
                                            g.col_scale, partial, flags, next_epoch(),
                                            static_cast<const __nv_bfloat16*>(g.bias));
-  trace_after(s, name);
+  trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;

@@ -386,7 +386,7 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
                                            g.out, g.row_scale, g.col_scale, g.a_rstd,
                                            static_cast<const uint4*>(g.a_gamma),
                                            static_cast<const __nv_bfloat16*>(g.bias));
-  trace_after(s, name);
+  trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;

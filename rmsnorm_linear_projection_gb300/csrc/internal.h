@@ -92,6 +92,8 @@ struct GemmArgs {
   // gemm_pair.cu); without it every tile runs whole
   void* partial_ws = nullptr;
   size_t partial_ws_bytes = 0;
+  // name of the launch in the kernel trace (default: the kernel's kind)
+  const char* trace_name = nullptr;
 };
 
 // Partial-sum slots of the CTA-pair GEMM's stream-K tiles (2 x 128 x 256
