@@ -424,9 +424,7 @@ rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* W
   const W8A8Layout l = w8a8_layout(workspace, T, K, N);
   cudaStream_t s = cs(stream);
   float* xs = x_scale_out ? x_scale_out : l.xs;
-  st = launch_norm_quant(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
-  if (st != RNL_OK) return st;
-  st = launch_s8_to_bf16(Wq, N * K, l.Wb, s);
+  st = launch_w8a8_front(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, Wq, N, l.Wb, s);
   if (st != RNL_OK) return st;
   GemmArgs g;
   g.A = l.A;

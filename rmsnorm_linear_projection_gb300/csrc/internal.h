@@ -62,6 +62,12 @@ rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int m
 // q_out (optional) as int8, x_scale = amax / 127.
 rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                              int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
+// Both of the above in one launch (norm-quantise rows of x and widening of
+// the N x K weight run side by side); rows longer than 4096 fall back to the
+// two launches.
+rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                             int mode, void* A, int8_t* q_out, float* x_scale, const int8_t* Wq,
+                             int64_t N, void* Wb, cudaStream_t s);
 // int8 -> bf16 (exact), n elements, n % 16 == 0.
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
 

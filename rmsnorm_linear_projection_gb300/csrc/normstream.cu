@@ -4,7 +4,8 @@
 // operand of the GEMM.
 //
 // The kernel is HBM-bound (read x once, write A once).  One CTA per SM walks
-// groups of 8 rows; one producer thread copies each row of a group into a
+// its own contiguous range of about T / (number of SMs) rows (equal bytes per
+// SM) in groups of 8 rows; one producer thread copies each row of a group into a
 // shared-memory ring with one bulk copy per row (cp.async.bulk, completion
 // counted on the stage's mbarrier), and 8 consumer warps each normalise one
 // row of the group from shared memory and store it with coalesced 16-byte
@@ -107,7 +108,12 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t groups = (T + kGroupRows - 1) / kGroupRows;
+  // this CTA's rows: a contiguous range of T / gridDim.x rows (rounded), so
+  // every SM moves the same number of bytes; groups of 8 within the range,
+  // the last one possibly partial
+  const int64_t r_begin = static_cast<int64_t>(blockIdx.x) * T / gridDim.x;
+  const int64_t r_end = static_cast<int64_t>(blockIdx.x + 1) * T / gridDim.x;
+  const int64_t groups = (r_end - r_begin + kGroupRows - 1) / kGroupRows;
 
   grid_launch_dependents();
   if (threadIdx.x == 0) {
@@ -126,10 +132,10 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
+      for (int64_t g = 0; g < groups; ++g) {
         if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_norm, 31)) break;
-        const int64_t row0 = g * kGroupRows;
-        const int rows = static_cast<int>(T - row0 < kGroupRows ? T - row0 : kGroupRows);
+        const int64_t row0 = r_begin + g * kGroupRows;
+        const int rows = static_cast<int>(r_end - row0 < kGroupRows ? r_end - row0 : kGroupRows);
         const uint32_t dst = base + stage * stage_bytes;
         for (int r = 0; r < rows; ++r) {
           const uint32_t bar = smem_u32(&ctrl->full[stage][r]);
@@ -153,9 +159,9 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
     uint32_t stage = 0, phase = 0;
-    for (int64_t g = blockIdx.x; g < groups; g += gridDim.x) {
-      const int64_t row = g * kGroupRows + warp;
-      if (row < T && EXT) {
+    for (int64_t g = 0; g < groups; ++g) {
+      const int64_t row = r_begin + g * kGroupRows + warp;
+      if (row < r_end && EXT) {
         uint4 rv[EXT ? VPL : 1];
         if (has_res) {  // plain loads: x_sum may be the residual itself
           const uint4* qr = ext.residual + row * nvec;
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         // the slot was written through the generic proxy; order that before
         // the next bulk copy (async proxy) refills it
         if (has_res) fence_proxy_async_shared();
-      } else if (row < T) {
+      } else if (row < r_end) {
         const bool got = mbar_wait(smem_u32(&ctrl->full[stage][warp]), phase, abort, &g_err_norm, 32);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         const uint4* rp = reinterpret_cast<const uint4*>(smem + stage * stage_bytes + warp * row_bytes);

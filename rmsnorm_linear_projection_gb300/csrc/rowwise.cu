@@ -265,12 +265,14 @@ __global__ void __launch_bounds__(kWarps * 32)
 // squares, amax, codes) run on the registers.  The sum of squares visits the
 // elements in the same order as norm_quant_kernel.
 template <int MODE, bool GAMMA, int VPL>
-__global__ void __launch_bounds__(kWarps * 32, 2)
-    norm_quant_regs_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
-                           int nvec, float inv_d, float eps, uint4* __restrict__ A,
-                           uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+__device__ __forceinline__ void norm_quant_regs_rows(unsigned block, const uint4* __restrict__ x,
+                                                     const uint4* __restrict__ gamma, int64_t T,
+                                                     int nvec, float inv_d, float eps,
+                                                     uint4* __restrict__ A,
+                                                     uint2* __restrict__ q_out,
+                                                     float* __restrict__ x_scale) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t row = static_cast<int64_t>(block) * kWarps + (threadIdx.x >> 5);
   if (row >= T) return;
   const uint4* xr = x + row * nvec;
   uint4 u[VPL];
@@ -377,6 +379,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
 }
 
+template <int MODE, bool GAMMA, int VPL>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    norm_quant_regs_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                           int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                           uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+  norm_quant_regs_rows<MODE, GAMMA, VPL>(blockIdx.x, x, gamma, T, nvec, inv_d, eps, A, q_out,
+                                         x_scale);
+}
+
 template <int MODE, bool GAMMA>
 void norm_quant_dispatch(const uint4* xp, const uint4* gp, int64_t T, int nvec, float inv_d,
                          float eps, uint4* ap, uint2* qp, float* xs, cudaStream_t s) {
@@ -417,9 +428,9 @@ __device__ __forceinline__ void widen16(const uint4& u, uint4* dst) {
   dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-__global__ void __launch_bounds__(256)
-    s8_to_bf16_kernel(const uint4* __restrict__ src, int64_t nvec16, uint4* __restrict__ dst) {
-  const int64_t base = (static_cast<int64_t>(blockIdx.x) * blockDim.x) * kS8Vec + threadIdx.x;
+__device__ __forceinline__ void widen_block(unsigned block, const uint4* __restrict__ src,
+                                            int64_t nvec16, uint4* __restrict__ dst) {
+  const int64_t base = (static_cast<int64_t>(block) * blockDim.x) * kS8Vec + threadIdx.x;
   uint4 u[kS8Vec];
 #pragma unroll
   for (int i = 0; i < kS8Vec; ++i) {
@@ -431,6 +442,39 @@ __global__ void __launch_bounds__(256)
     const int64_t v = base + static_cast<int64_t>(i) * blockDim.x;
     if (v < nvec16) widen16(u[i], dst + 2 * v);
   }
+}
+
+__global__ void __launch_bounds__(256)
+    s8_to_bf16_kernel(const uint4* __restrict__ src, int64_t nvec16, uint4* __restrict__ dst) {
+  widen_block(blockIdx.x, src, nvec16, dst);
+}
+
+// The W8A8 front end in one launch: the norm-and-quantise rows of x (ALU
+// bound) and the int8 -> bf16 widening of the weight (HBM bound) share no
+// data, so their blocks are interleaved in one grid (even / odd while both
+// last) and run side by side on every SM instead of one after the other.
+template <int MODE, bool GAMMA, int VPL>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    w8a8_front_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                      int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                      uint2* __restrict__ q_out, float* __restrict__ x_scale,
+                      const uint4* __restrict__ w_src, int64_t w_nvec16, uint4* __restrict__ w_dst,
+                      unsigned quant_blocks, unsigned widen_blocks) {
+  const unsigned b = blockIdx.x;
+  const unsigned both = quant_blocks < widen_blocks ? quant_blocks : widen_blocks;
+  bool quant;
+  unsigned idx;
+  if (b < 2 * both) {
+    quant = (b & 1u) == 0;
+    idx = b >> 1;
+  } else {
+    quant = quant_blocks > widen_blocks;
+    idx = b - both;
+  }
+  if (quant)
+    norm_quant_regs_rows<MODE, GAMMA, VPL>(idx, x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale);
+  else
+    widen_block(idx, w_src, w_nvec16, w_dst);
 }
 
 inline rnl_status launched(cudaStream_t s, const char* name) {
@@ -519,6 +563,66 @@ rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_
       norm_quant_dispatch<1, false>(xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, s);
   }
   return launched(s, "norm_quant");
+}
+
+namespace {
+template <int MODE, bool GAMMA, int VPL>
+void front_launch(unsigned grid, const uint4* xp, const uint4* gp, int64_t T, int nvec,
+                  float inv_d, float eps, uint4* ap, uint2* qp, float* xs, const uint4* wp,
+                  int64_t w_nvec16, uint4* wd, unsigned qb, unsigned wb, cudaStream_t s) {
+  w8a8_front_kernel<MODE, GAMMA, VPL><<<grid, kWarps * 32, 0, s>>>(
+      xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb);
+}
+
+template <int MODE, bool GAMMA>
+void front_vpl(int vpl, unsigned grid, const uint4* xp, const uint4* gp, int64_t T, int nvec,
+               float inv_d, float eps, uint4* ap, uint2* qp, float* xs, const uint4* wp,
+               int64_t w_nvec16, uint4* wd, unsigned qb, unsigned wb, cudaStream_t s) {
+  if (vpl <= 2)
+    front_launch<MODE, GAMMA, 2>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+  else if (vpl <= 4)
+    front_launch<MODE, GAMMA, 4>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+  else if (vpl <= 8)
+    front_launch<MODE, GAMMA, 8>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+  else
+    front_launch<MODE, GAMMA, 16>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+}
+}  // namespace
+
+rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                             int mode, void* A, int8_t* q_out, float* x_scale, const int8_t* Wq,
+                             int64_t N, void* Wb, cudaStream_t s) {
+  const int nvec = static_cast<int>(K / 8);
+  const int vpl = (nvec + 31) / 32;
+  if (T == 0 || vpl > 16) {  // long rows: the two kernels one after the other
+    rnl_status st = launch_norm_quant(x, gamma, T, K, eps, mode, A, q_out, x_scale, s);
+    if (st != RNL_OK) return st;
+    return launch_s8_to_bf16(Wq, N * K, Wb, s);
+  }
+  const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
+  const int64_t w_nvec16 = N * K / 16;
+  const unsigned qb = row_blocks(T);
+  const unsigned wb = static_cast<unsigned>((w_nvec16 + 256 * kS8Vec - 1) / (256 * kS8Vec));
+  const unsigned grid = qb + wb;
+  const auto* xp = static_cast<const uint4*>(x);
+  const auto* gp = static_cast<const uint4*>(gamma);
+  auto* ap = static_cast<uint4*>(A);
+  auto* qp = reinterpret_cast<uint2*>(q_out);
+  const auto* wp = reinterpret_cast<const uint4*>(Wq);
+  auto* wd = static_cast<uint4*>(Wb);
+  trace_before(s);
+  if (mode == RNL_NORM_RSQRT) {
+    if (gamma)
+      front_vpl<0, true>(vpl, grid, xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, wp, w_nvec16, wd, qb, wb, s);
+    else
+      front_vpl<0, false>(vpl, grid, xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, wp, w_nvec16, wd, qb, wb, s);
+  } else {
+    if (gamma)
+      front_vpl<1, true>(vpl, grid, xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, wp, w_nvec16, wd, qb, wb, s);
+    else
+      front_vpl<1, false>(vpl, grid, xp, gp, T, nvec, inv_d, eps, ap, qp, x_scale, wp, w_nvec16, wd, qb, wb, s);
+  }
+  return launched(s, "w8a8_front");
 }
 
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s) {
