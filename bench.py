@@ -51,9 +51,15 @@ METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 # roofline stage per step, from the ncu captures summarised under profiles/;
 # only for kernels unchanged since the capture.
 TRAFFIC = {
-    # gemm_pair_kernel<0,256> 123.22 MB + gemm_pair_fixup_kernel 16.79 MB
+    # gemm_pair_kernel<0,256>: 98.13 MB read + 39.87 MB written
     # (profiles/qkv_step_kernels_4096x6144x4096.md)
-    "qkv": 140.01e6,
+    "qkv": 138.00e6,
+    # both MLA GEMM stages: 59.92 MB + 155.11 MB
+    # (profiles/mla_gemm_stages_2048x7168x1536x24576.md)
+    "mla": 215.03e6,
+    # gemm_kernel<2,256,0>: 125.17 MB read + 46.38 MB written
+    # (profiles/w8a8_front_and_int_gemm_8192x4096x4096.md)
+    "w8a8": 171.55e6,
     # skinny_kernel<32,0>: 123.03 MB at T = 2048, scaled by rows to T = 16384
     # (profiles/skinny_stream_mhc_pre.md)
     "skinny": 984.2e6,
