@@ -63,6 +63,7 @@ def _declare(lib):
         "orc_rmsnorm_linear": (C, [P, P, P, I64, I64, I64, D, C, C, P, P]),
         "orc_mla_q_chain": (C, [P, P, P, P, I64, I64, I64, I64, D, C, P, P, P]),
         "orc_rmsnorm_linear_ex": (C, [P, P, P, P, P, P, I64, I64, I64, D, C, P, P, P, P]),
+        "orc_qkv_rope": (C, [P, I64, I64, I64, I64, P, P, D, P, P, I64, P, P, P]),
         "orc_quant_rows_f32": (C, [P, P, I64, I64, F, C, P, P, P, P]),
         "orc_gemm_s8": (C, [P, P, I64, I64, I64, P]),
         "orc_dequant_bf16": (C, [P, P, P, I64, I64, P, P]),
@@ -165,6 +166,23 @@ class Oracle:
             _ptr(_c(bias, np.uint16)), T, K, N, float(eps), int(variant), _ptr(ref), _ptr(out),
             _ptr(x_sum), _ptr(rstd)), "rmsnorm_linear_ex")
         return ref, out, x_sum, rstd
+
+    def qkv_rope(self, y, Hq, Hkv, D, q_gamma, k_gamma, eps, pos, cs):
+        """QKV split + per-head RMSNorm + RoPE of a projection output y (bf16
+        bits [T, (Hq + 2 Hkv) D]); cs: fp32 [P, D] cos | sin table.  Returns
+        (q, k, v) bf16 bits [T, H, D]."""
+        y = _c(y, np.uint16)
+        T = y.shape[0]
+        assert y.shape[1] == (Hq + 2 * Hkv) * D
+        pos = _c(pos, np.int32)
+        cs = _c(cs, np.float32)
+        q = np.empty((T, Hq, D), np.uint16)
+        k = np.empty((T, Hkv, D), np.uint16)
+        v = np.empty((T, Hkv, D), np.uint16)
+        _check(self.lib.orc_qkv_rope(_ptr(y), T, Hq, Hkv, D, _ptr(_c(q_gamma, np.uint16)),
+                                     _ptr(_c(k_gamma, np.uint16)), float(eps), _ptr(pos), _ptr(cs),
+                                     cs.shape[0], _ptr(q), _ptr(k), _ptr(v)), "qkv_rope")
+        return q, k, v
 
     # -- MLA q chain ----------------------------------------------------------
     def mla_q_chain(self, x, W_qa, gamma_cq, W_qb, eps, variant):

@@ -327,6 +327,74 @@ int orc_rmsnorm_linear_ex(const uint16_t *x, const uint16_t *residual, const uin
 }
 
 /* ------------------------------------------------------------------------ */
+/* The V stage after the QKV projection.  [AT10] sec. 6 (Qwen3PreAttn): the  */
+/* projection output is split into Q, K and V, and Q and K each get a        */
+/* per-head RMSNorm (their own gamma over head_dim) and RoPE.                */
+/*   y [T, (Hq + 2 Hkv) * D] bf16: columns [0, Hq D) are the q heads,        */
+/*     [Hq D, (Hq + Hkv) D) the k heads, the rest the v heads.               */
+/*   q / k head row h (D values): ms = mean(h^2) (binary64), r = 1/sqrt(ms   */
+/*     + eps), z = bf16(h * r * gamma) (the norm's bf16 output); RoPE with   */
+/*     the rotate-half pairing, angle table cs [P, D] (cos in [0, D/2), sin  */
+/*     in [D/2, D)) at position pos[t]:                                      */
+/*       o[i]       = bf16(z[i] * c_i - z[i + D/2] * s_i)                    */
+/*       o[i + D/2] = bf16(z[i + D/2] * c_i + z[i] * s_i),  i < D/2          */
+/*   v heads are copied unchanged.                                           */
+/* Outputs q [T, Hq, D], k [T, Hkv, D], v [T, Hkv, D] (bf16 bits).           */
+/* Returns ORC_EARG for a position outside [0, P).                           */
+/* ------------------------------------------------------------------------ */
+
+int orc_qkv_rope(const uint16_t *y, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                 const uint16_t *q_gamma, const uint16_t *k_gamma, double eps,
+                 const int32_t *pos, const float *cs, int64_t P, uint16_t *q, uint16_t *k,
+                 uint16_t *v)
+{
+    if (!y || !q_gamma || !k_gamma || !pos || !cs || !q || !k || !v || T < 0 || Hq < 0 ||
+        Hkv < 0 || D <= 0 || (D % 2) != 0 || P <= 0)
+        return ORC_EARG;
+    const int64_t N = (Hq + 2 * Hkv) * D;
+    const int64_t half = D / 2;
+    for (int64_t t = 0; t < T; ++t) {
+        if (pos[t] < 0 || pos[t] >= P)
+            return ORC_EARG;
+        const float *c = cs + (int64_t)pos[t] * D;
+        const float *s = c + half;
+        for (int64_t h = 0; h < Hq + 2 * Hkv; ++h) {
+            const uint16_t *yh = y + t * N + h * D;
+            uint16_t *dst;
+            const uint16_t *g;
+            if (h < Hq) {
+                dst = q + (t * Hq + h) * D;
+                g = q_gamma;
+            } else if (h < Hq + Hkv) {
+                dst = k + (t * Hkv + (h - Hq)) * D;
+                g = k_gamma;
+            } else {
+                dst = v + (t * Hkv + (h - Hq - Hkv)) * D;
+                for (int64_t i = 0; i < D; ++i)
+                    dst[i] = yh[i];
+                continue;
+            }
+            double ss = 0.0;
+            for (int64_t i = 0; i < D; ++i) {
+                double a = orc_bf16_value(yh[i]);
+                ss += a * a;
+            }
+            double r = 1.0 / sqrt(ss / (double)D + eps);
+            for (int64_t i = 0; i < half; ++i) {
+                double z0 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[i]) * r *
+                                                        orc_bf16_value(g[i])));
+                double z1 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[i + half]) * r *
+                                                        orc_bf16_value(g[i + half])));
+                double ci = (double)c[i], si = (double)s[i];
+                dst[i] = orc_bf16_rne(z0 * ci - z1 * si);
+                dst[i + half] = orc_bf16_rne(z1 * ci + z0 * si);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* MLA two-stage q chain.  [AT10] sec. 5 (MLAProlog) and sec. 9 (the golden  */
 /* chain): q = bf16(matmul(x, wq_a)); qr = rms_norm(q) (variant B in the     */
 /* page's code); qr = qr * gamma_cq (FP32); qr = bf16(qr);                   */

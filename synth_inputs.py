@@ -51,6 +51,11 @@ CONFIGS = {
                  seed=1003),
     "skinny": dict(T=16384, K=28672, N=24, eps=1e-6, norm_mode=0,
                    has_gamma=False, out_dtype="fp32", seed=1004),
+    # the qkv projection followed by the QKV split + per-head RMSNorm + RoPE
+    # stage (Qwen3 layout: 32 query heads and 8 key/value heads of 128)
+    "qkv_rope": dict(T=4096, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
+                     out_dtype="bf16", seed=1001, n_q_heads=32, n_kv_heads=8, head_dim=128,
+                     head_eps=1e-6, max_pos=4096, rope_base=1.0e6),
 }
 
 
@@ -210,6 +215,30 @@ def make_w8a8(cfg: dict, rows=None, with_x: bool = True) -> dict:
     d["Wq"] = uniform_int8(s, "Wq", (N, K), -127, 127)
     d["w_scale"] = uniform_f32(s, "w_scale", (N,), 1e-3, 1e-2)
     return d
+
+
+def rope_table(P: int, D: int, base: float = 1.0e6) -> np.ndarray:
+    """A rotary-embedding angle table, as a model precomputes it: fp32 [P, D],
+    row p = [cos(p * f_0) .. cos(p * f_{D/2-1}), sin(p * f_0) .. sin(p * f_{D/2-1})]
+    with f_i = base^(-2i/D) (base 1e6 as in Qwen3).  Computed in binary64 and
+    rounded to fp32; both the oracle and the GPU path receive the same table."""
+    i = np.arange(D // 2, dtype=np.float64)
+    f = base ** (-2.0 * i / D)
+    ang = np.arange(P, dtype=np.float64)[:, None] * f[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def make_qkv_rope(cfg: dict) -> dict:
+    """Per-head norm weights, positions and angle table for the QKV split +
+    per-head RMSNorm + RoPE stage after the qkv projection (Hq query heads,
+    Hkv key/value heads of D; tokens of one sequence at positions 0..T-1)."""
+    s, T, D = cfg["seed"], cfg["T"], cfg["head_dim"]
+    return {
+        "q_gamma": uniform_bf16(s, "q_gamma", (D,), 0.5, 1.5),
+        "k_gamma": uniform_bf16(s, "k_gamma", (D,), 0.5, 1.5),
+        "positions": (np.arange(T, dtype=np.int64) % cfg["max_pos"]).astype(np.int32),
+        "cos_sin": rope_table(cfg["max_pos"], D, cfg.get("rope_base", 1.0e6)),
+    }
 
 
 def scaled(cfg: dict, **over) -> dict:

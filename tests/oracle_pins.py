@@ -582,8 +582,173 @@ def pin_ex_torch(orc):
     assert np.all(np.abs(ref - want.numpy()) <= 2.0**-7 * scale * 0.05 + 1e-12 * scale)
 
 
+# ---------------------------------------------------------------------------
+# QKV split + per-head RMSNorm + RoPE after the qkv projection (AT-10 page,
+# sec. 6, Qwen3PreAttn)
+# ---------------------------------------------------------------------------
+
+def _qkv_case(rng, T=3, Hq=2, Hkv=1, D=8):
+    y = _rand_bf16(rng, (T, (Hq + 2 * Hkv) * D))
+    qg = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    kg = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    return y, qg, kg
+
+
+def _table(cos, sin, D, P=1):
+    """A one-row-per-position table with the same angle for every pair."""
+    t = np.empty((P, D), np.float32)
+    t[:, : D // 2] = cos
+    t[:, D // 2:] = sin
+    return t
+
+
+def pin_rope_angle_zero_is_head_norm(orc):
+    """At angle 0 (cos 1, sin 0) the rotation is the identity: q and k are the
+    bf16 per-head RMSNorm of their column ranges (the pinned rmsnorm_f64 on the
+    reshaped heads), v is y's last columns unchanged."""
+    rng = _rng(30)
+    T, Hq, Hkv, D = 5, 4, 2, 16
+    y, qg, kg = _qkv_case(rng, T, Hq, Hkv, D)
+    q, k, v = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, np.zeros(T, np.int32), _table(1.0, 0.0, D))
+    yq = y[:, : Hq * D].reshape(T * Hq, D)
+    yk = y[:, Hq * D:(Hq + Hkv) * D].reshape(T * Hkv, D)
+    for got, heads, g in ((q, yq, qg), (k, yk, kg)):
+        ref, _ = orc.rmsnorm_f64(heads, g, 1e-6, 0)
+        want = orc.bf16_rne(ref.ravel()).reshape(got.shape)
+        diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+        assert diff.max() <= 1 and (diff == 0).mean() > 0.99
+    assert np.array_equal(v.reshape(T, -1), y[:, (Hq + Hkv) * D:])
+
+
+def pin_rope_quarter_and_half_turn(orc):
+    """cos 0, sin 1: o[i] = -z[i + D/2], o[i + D/2] = z[i] exactly (rotate-half
+    pairing, sign); cos -1, sin 0: o = -z exactly."""
+    rng = _rng(31)
+    T, Hq, Hkv, D = 4, 2, 2, 16
+    y, qg, kg = _qkv_case(rng, T, Hq, Hkv, D)
+    pos = np.zeros(T, np.int32)
+    z, zk, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, _table(1.0, 0.0, D))
+    q, k, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, _table(0.0, 1.0, D))
+    h = D // 2
+    for got, base in ((q, z), (k, zk)):
+        assert np.array_equal(got[..., :h], base[..., h:] ^ np.uint16(0x8000))
+        assert np.array_equal(got[..., h:], base[..., :h])
+    q2, _, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, _table(-1.0, 0.0, D))
+    assert np.array_equal(q2, z ^ np.uint16(0x8000))
+
+
+def pin_rope_positions_index_the_table(orc):
+    """Each token uses its own table row: a token at position p gives the same
+    output as the same token alone with a one-row table holding row p."""
+    rng = _rng(32)
+    T, Hq, Hkv, D = 6, 2, 1, 8
+    y, qg, kg = _qkv_case(rng, T, Hq, Hkv, D)
+    P = 9
+    ang = rng.uniform(-3, 3, (P, D // 2))
+    cs = np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+    pos = rng.integers(0, P, T).astype(np.int32)
+    q, k, v = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, cs)
+    for t in range(T):
+        q1, k1, _ = orc.qkv_rope(y[t:t + 1], Hq, Hkv, D, qg, kg, 1e-6, np.zeros(1, np.int32),
+                                 cs[pos[t]:pos[t] + 1])
+        assert np.array_equal(q1[0], q[t]) and np.array_equal(k1[0], k[t])
+
+
+def pin_rope_exact_small(orc):
+    """Brute force in exact rationals: the head norm (60-digit square root),
+    the bf16 cast of the normed values, the rotation with the fp32 table
+    values, the final bf16 cast."""
+    rng = _rng(33)
+    T, Hq, Hkv, D = 2, 1, 1, 8
+    y, qg, kg = _qkv_case(rng, T, Hq, Hkv, D)
+    P = 3
+    ang = rng.uniform(-3, 3, (P, D // 2))
+    cs = np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+    pos = np.array([2, 1], np.int32)
+    q, k, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, cs)
+    h = D // 2
+    for t in range(T):
+        for got, col0, g in ((q[t, 0], 0, qg), (k[t, 0], Hq * D, kg)):
+            row = [Fraction(exact.bf16_value(b)) for b in y[t, col0:col0 + D]]
+            r = exact.dec_sqrt_recip(sum(a * a for a in row) / D + Fraction(1e-6))
+            z = []
+            for i in range(D):
+                bits, near = exact.bf16_round_exact(row[i] * r * Fraction(exact.bf16_value(g[i])))
+                assert not near
+                z.append(Fraction(exact.bf16_value(bits)))
+            c = [Fraction(float(x)) for x in cs[pos[t], :h]]
+            sn = [Fraction(float(x)) for x in cs[pos[t], h:]]
+            for i in range(h):
+                for val, idx in ((z[i] * c[i] - z[i + h] * sn[i], i), (z[i + h] * c[i] + z[i] * sn[i], i + h)):
+                    bits, near = exact.bf16_round_exact(val)
+                    assert near or int(got[idx]) == bits, (t, idx)
+
+
+def pin_rope_torch(orc):
+    """Library cross-check: torch float64 rms_norm per head, bf16 cast, the
+    rotate-half rotation (x * cos + rotate_half(x) * sin)."""
+    import torch
+    rng = _rng(34)
+    T, Hq, Hkv, D = 8, 4, 2, 64
+    y, qg, kg = _qkv_case(rng, T, Hq, Hkv, D)
+    import synth_inputs as si
+    cs = si.rope_table(16, D)
+    pos = rng.integers(0, 16, T).astype(np.int32)
+    q, k, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, pos, cs)
+    yt = torch.from_numpy(bf16_bits_to_f64(y))
+    cos = torch.from_numpy(cs[pos, : D // 2].astype(np.float64))
+    sin = torch.from_numpy(cs[pos, D // 2:].astype(np.float64))
+    cos = torch.cat([cos, cos], dim=1)[:, None, :]
+    sin = torch.cat([sin, sin], dim=1)[:, None, :]
+    for got, lo, H, g in ((q, 0, Hq, qg), (k, Hq * D, Hkv, kg)):
+        heads = yt[:, lo:lo + H * D].reshape(T, H, D)
+        z = torch.nn.functional.rms_norm(heads, (D,), weight=torch.from_numpy(bf16_bits_to_f64(g)), eps=1e-6)
+        z = z.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+        rot = torch.cat([-z[..., D // 2:], z[..., : D // 2]], dim=-1)
+        want = z * cos + rot * sin
+        err = np.abs(bf16_bits_to_f64(got) - want.numpy())
+        assert np.all(err <= 2.0**-7 * np.abs(want.numpy()) + 1e-6), err.max()
+
+
+def pin_rope_small_rows_closed_form(orc):
+    """A constant head row c with c^2 of the order of eps: at angle 0 the
+    output is bf16(c * gamma / sqrt(c^2 + eps)), far from +-gamma, so the eps
+    of the per-head norm is visible."""
+    D, Hq, Hkv = 8, 1, 1
+    qg = _bf16_bits_of_f32(np.linspace(0.5, 1.5, D).astype(np.float32))
+    kg = _bf16_bits_of_f32(np.linspace(1.5, 0.5, D).astype(np.float32))
+    for c in (2.0**-10, -(2.0**-11)):
+        cb = _bf16_bits_of_f32(np.float32(c))
+        y = np.full((1, (Hq + 2 * Hkv) * D), cb, np.uint16)
+        q, k, _ = orc.qkv_rope(y, Hq, Hkv, D, qg, kg, 1e-6, np.zeros(1, np.int32), _table(1.0, 0.0, D))
+        cf = Fraction(c)
+        r = exact.dec_sqrt_recip(cf * cf + Fraction(1e-6))
+        for got, g in ((q[0, 0], qg), (k[0, 0], kg)):
+            for i in range(D):
+                bits, near = exact.bf16_round_exact(cf * r * Fraction(exact.bf16_value(g[i])))
+                assert near or int(got[i]) == bits, (c, i)
+
+
+def pin_rope_rejects_bad_position(orc):
+    rng = _rng(35)
+    y, qg, kg = _qkv_case(rng, 2, 1, 1, 8)
+    for bad in (-1, 4):
+        try:
+            orc.qkv_rope(y, 1, 1, 8, qg, kg, 1e-6, np.array([0, bad], np.int32), _table(1.0, 0.0, 8, P=4))
+        except RuntimeError:
+            continue
+        raise AssertionError(f"position {bad} accepted")
+
+
 ALL_PINS = [
     pin_bf16_codec,
+    pin_rope_angle_zero_is_head_norm,
+    pin_rope_quarter_and_half_turn,
+    pin_rope_positions_index_the_table,
+    pin_rope_exact_small,
+    pin_rope_torch,
+    pin_rope_small_rows_closed_form,
+    pin_rope_rejects_bad_position,
     pin_ex_reduces_to_base,
     pin_ex_residual_sum_exact,
     pin_ex_residual_composition,

@@ -53,6 +53,18 @@ MUTANTS = [
     ("ex_projection_bias_after_rounding", "acc = acc + orc_bf16_value(bias[n]);",
      "acc = orc_bf16_value(orc_bf16_rne(acc)) + orc_bf16_value(bias[n]);"),
     ("ex_drop_projection_bias", "acc = acc + orc_bf16_value(bias[n]);", "acc = acc;"),
+    # QKV split + per-head RMSNorm + RoPE
+    ("rope_sign_of_sine", "dst[i] = orc_bf16_rne(z0 * ci - z1 * si);", "dst[i] = orc_bf16_rne(z0 * ci + z1 * si);"),
+    ("rope_cos_sin_swapped", "const float *c = cs + (int64_t)pos[t] * D;\n        const float *s = c + half;",
+     "const float *s = cs + (int64_t)pos[t] * D;\n        const float *c = s + half;"),
+    ("rope_k_heads_use_q_gamma", "                g = k_gamma;", "                g = q_gamma;"),
+    ("rope_unrounded_norm", "double z0 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[i]) * r *\n                                                        orc_bf16_value(g[i])));",
+     "double z0 = orc_bf16_value(yh[i]) * r * orc_bf16_value(g[i]);"),
+    ("rope_adjacent_pairing", "double z1 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[i + half]) * r *",
+     "double z1 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[(i + 1) % D]) * r *"),
+    ("rope_head_norm_drops_eps", "double r = 1.0 / sqrt(ss / (double)D + eps);", "double r = 1.0 / sqrt(ss / (double)D);"),
+    ("rope_split_off_by_one_head", "            if (h < Hq) {\n                dst = q + (t * Hq + h) * D;",
+     "            if (h <= Hq && h < Hq + Hkv) {\n                dst = q + (t * Hq + (h < Hq ? h : 0)) * D;"),
 ]
 
 CHILD = textwrap.dedent("""
