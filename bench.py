@@ -42,8 +42,9 @@ sys.path.insert(0, ROOT)
 
 import synth_inputs as si  # noqa: E402
 
-WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex")
-DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600, "qkv_ex": 2000}
+WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex", "qkv_rope")
+DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600, "qkv_ex": 2000,
+                 "qkv_rope": 2000}
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
@@ -96,6 +97,13 @@ class Work:
             self.h["bias"] = si.normal_bf16(c["seed"], "bias", (N,), 0.5)
             self.flops = 2.0 * T * N * K
             self.bytes = 4.0 * T * K + 2.0 * N * K + 4.0 * K + 2.0 * N + 2.0 * T * N + 2.0 * T * K + 4.0 * T
+        elif name == "qkv_rope":
+            # the qkv projection, then the QKV split + per-head RMSNorm + RoPE
+            self.h = si.make_projection(c)
+            self.h.update(si.make_qkv_rope(c))
+            T, K, N = c["T"], c["K"], c["N"]
+            self.flops = 2.0 * T * N * K
+            self.bytes = 2.0 * T * K + 2.0 * N * K + 2.0 * K + 2.0 * T * N
         elif name in ("qkv", "tiny", "skinny"):
             self.h = si.make_projection(c)
             T, K, N = c["T"], c["K"], c["N"]
@@ -120,6 +128,8 @@ class Work:
         torch = self.torch
         if a is None:
             return None
+        if a.dtype in (np.int32, np.float32):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
         if a.dtype == np.uint16:
             t = t.view(torch.bfloat16)
@@ -127,6 +137,11 @@ class Work:
 
     def _alloc_out(self):
         torch, c = self.torch, self.cfg
+        if self.name == "qkv_rope":
+            T, Hq, Hkv, D = c["T"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
+            self.qkv = tuple(torch.empty((T, H, D), dtype=torch.bfloat16, device=self.device)
+                             for H in (Hq, Hkv, Hkv))
+            return self.qkv[0]
         if self.name == "mla":
             return torch.empty((c["T"], c["N2"]), dtype=torch.bfloat16, device=self.device)
         dt = torch.float32 if c.get("out_dtype") == "fp32" else torch.bfloat16
@@ -144,6 +159,16 @@ class Work:
         d = self.d if d is None else d
         out = self.out if out is None else out
         c = self.cfg
+        if self.name == "qkv_rope":
+            if self.ws is None:
+                self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_QKV_ROPE, c["T"], c["K"], c["N"]),
+                                           dtype=self.torch.uint8, device=self.device)
+            q, k, v = self.qkv
+            return rnl.rmsnorm_linear_qkv_rope(d["x"], d["gamma"], d["W"], c["n_q_heads"], c["n_kv_heads"],
+                                               c["head_dim"], d["q_gamma"], d["k_gamma"], d["positions"],
+                                               d["cos_sin"], eps=c["eps"], norm_mode=c["norm_mode"],
+                                               head_eps=c["head_eps"], q_out=q, k_out=k, v_out=v,
+                                               workspace=self.ws, stream=stream)
         if self.name == "qkv_ex":
             if self.ws is None:
                 self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_BF16, c["T"], c["K"], c["N"], rnl.OUT_BF16),
@@ -190,7 +215,14 @@ class Work:
 
         s = P(stream.cuda_stream)
         nbytes = self.ws.numel() * self.ws.element_size()
-        if self.name == "qkv_ex":
+        if self.name == "qkv_rope":
+            fn = lib.rmsnorm_linear_qkv_rope
+            q, k, v = self.qkv
+            args = (ptr(d["x"]), ptr(d["gamma"]), ptr(d["W"]), c["T"], c["K"], c["n_q_heads"], c["n_kv_heads"],
+                    c["head_dim"], c["eps"], c["norm_mode"], ptr(d["q_gamma"]), ptr(d["k_gamma"]),
+                    c["head_eps"], ptr(d["positions"]), ptr(d["cos_sin"]), c["max_pos"], ptr(q), ptr(k),
+                    ptr(v), ptr(self.ws), nbytes, s)
+        elif self.name == "qkv_ex":
             fn = lib.rmsnorm_linear_bf16_ex
             args = (ptr(d["x"]), ptr(d["residual"]), ptr(self.x_sum), ptr(d["gamma"]), ptr(d["beta"]),
                     ptr(d["W"]), ptr(d["bias"]), c["T"], c["K"], c["N"], c["eps"], c["norm_mode"],
@@ -478,7 +510,7 @@ def run_ours(args):
     # i-1's output copy; the timed region runs from the first submit until the
     # last step's output is in host memory.
     e2e = None
-    if not args.no_e2e and w.name != "qkv_ex":  # the host-buffer pipeline has no ex form
+    if not args.no_e2e and w.name not in ("qkv_ex", "qkv_rope"):  # no host-buffer pipeline form
         c = w.cfg
         host_x = torch.empty(w.d["x"].shape, dtype=w.d["x"].dtype, pin_memory=True)
         host_x.copy_(w.d["x"])
@@ -553,7 +585,7 @@ def run_ours(args):
         del graph
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not args.T and w.name != "qkv_ex":
+    if rank == 0 and world == 1 and not args.no_cpu and not args.T and w.name not in ("qkv_ex", "qkv_rope"):
         v, u, cores, sample, rows, ref_out, _ = oracle_sample(args.workload, target_s=args.cpu_seconds)
         got = w.out.cpu()
         got = got.view(torch.int16).numpy().view(np.uint16) if got.dtype == torch.bfloat16 else got.numpy()

@@ -80,7 +80,7 @@ enum { RNL_NORM_RSQRT = 0, RNL_NORM_SQRT_DIV = 1 };
 /* AT-09 out_dtype */
 enum { RNL_OUT_BF16 = 0, RNL_OUT_FP32 = 1 };
 /* operation ids for rnl_workspace_size */
-enum { RNL_OP_BF16 = 0, RNL_OP_W8A8 = 1, RNL_OP_MLA = 2, RNL_OP_GEMM_S8 = 3 };
+enum { RNL_OP_BF16 = 0, RNL_OP_W8A8 = 1, RNL_OP_MLA = 2, RNL_OP_GEMM_S8 = 3, RNL_OP_QKV_ROPE = 4 };
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int rnl_version(void);
@@ -94,6 +94,7 @@ const char *rnl_status_string(rnl_status s);
  *   RNL_OP_W8A8:    T, K, N; N2 ignored
  *   RNL_OP_MLA:     T, K, N = N1, N2
  *   RNL_OP_GEMM_S8: T = M, K, N; N2 ignored
+ *   RNL_OP_QKV_ROPE: T, K, N = (n_q_heads + 2 * n_kv_heads) * head_dim; N2 ignored
  * Returns (size_t)-1 for invalid sizes.  Host-only; needs no GPU.
  */
 size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
@@ -144,6 +145,47 @@ rnl_status rmsnorm_linear_bf16_ex(const void *x, const void *residual, void *x_s
                                   const void *bias, int64_t T, int64_t K, int64_t N, float eps,
                                   int norm_mode, void *out, float *rstd_out, void *workspace,
                                   size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * The V stage after the qkv projection (AT-10 pattern page, sec. 6,
+ * Qwen3PreAttn: the projection output is split into Q, K and V, then Q and K
+ * get a per-head RMSNorm and the rotary embedding).
+ *   y         bf16 [T, (n_q_heads + 2 * n_kv_heads) * head_dim]: the q heads,
+ *             then the k heads, then the v heads (column ranges)
+ *   head_dim  64, 128 or 256 (else RNL_ERR_UNSUPPORTED)
+ *   q_gamma, k_gamma  bf16 [head_dim]: the per-head norms' weights
+ *   eps       of the per-head norms (rsqrt form, FP32):
+ *             z = bf16((h * rsqrt(mean(h^2) + eps)) * gamma)
+ *   positions int32 [T]: each token's row of the angle table; a value outside
+ *             [0, max_pos) leaves that token's q / k rows unwritten and makes
+ *             the next rnl_check_device_error() return RNL_ERR_ARG
+ *   cos_sin   fp32 [max_pos, head_dim]: row p = cos of the head_dim / 2
+ *             angles, then their sin (a model's rotary cache); rotate-half
+ *             pairing: o[i] = z[i] c_i - z[i + D/2] s_i,
+ *             o[i + D/2] = z[i + D/2] c_i + z[i] s_i, bf16 out
+ *   q_out bf16 [T, n_q_heads, head_dim];  k_out, v_out bf16 [T, n_kv_heads,
+ *             head_dim] (v heads copied unchanged)
+ * 16-byte aligned tensors (positions: 4 bytes).  No workspace.
+ */
+rnl_status rnl_qkv_rope(const void *y, int64_t T, int64_t n_q_heads, int64_t n_kv_heads,
+                        int64_t head_dim, const void *q_gamma, const void *k_gamma, float eps,
+                        const int32_t *positions, const float *cos_sin, int64_t max_pos,
+                        void *q_out, void *k_out, void *v_out, rnl_stream_t stream);
+
+/*
+ * rmsnorm_linear_bf16 (AT-10, bf16 out, N = (n_q_heads + 2 * n_kv_heads) *
+ * head_dim) followed by rnl_qkv_rope on its output, which lives in the
+ * workspace: rnl_workspace_size(RNL_OP_QKV_ROPE, T, K, N, 0) bytes.
+ * head_eps is the per-head norms' eps.  Arguments of both stages are checked
+ * before anything is enqueued.
+ */
+rnl_status rmsnorm_linear_qkv_rope(const void *x, const void *gamma, const void *W, int64_t T,
+                                   int64_t K, int64_t n_q_heads, int64_t n_kv_heads,
+                                   int64_t head_dim, float eps, int norm_mode,
+                                   const void *q_gamma, const void *k_gamma, float head_eps,
+                                   const int32_t *positions, const float *cos_sin,
+                                   int64_t max_pos, void *q_out, void *k_out, void *v_out,
+                                   void *workspace, size_t workspace_bytes, rnl_stream_t stream);
 
 /*
  * AT-11 RMSNorm + per-token INT8 quant + exact INT8 x INT8 -> INT32 matmul +
@@ -228,9 +270,11 @@ rnl_status rnl_gemm_s8s8s32(const int8_t *A, const int8_t *B, int32_t *C, int64_
 
 /*
  * Synchronises `stream`, then reads and clears the device error words of
- * every kernel module.  RNL_OK if no kernel gave up on a wait,
- * RNL_ERR_TIMEOUT otherwise (*site, if not NULL, receives the first
- * recorded wait site), RNL_ERR_LAUNCH if the synchronisation itself failed.
+ * every kernel module.  RNL_OK if no kernel gave up on a wait or met a bad
+ * argument, RNL_ERR_TIMEOUT for a wait that gave up, RNL_ERR_ARG for a bad
+ * argument seen on the device (a rotary position outside its table); *site,
+ * if not NULL, receives the first recorded site.  RNL_ERR_LAUNCH if the
+ * synchronisation itself failed.
  */
 rnl_status rnl_check_device_error(rnl_stream_t stream, int *site);
 

@@ -10,6 +10,8 @@ arguments; the computation runs in the library's CUDA kernels.
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
+    rnl_qkv_rope / rmsnorm_linear_qkv_rope
+                          QKV split + per-head RMSNorm + RoPE after the qkv projection
     rnl_pipeline_*        host-buffer pipeline: calls fed from and answering into
                           pinned host memory, copies overlapped with the kernels
 """
@@ -20,6 +22,7 @@ from ._native import (  # noqa: F401
     OP_BF16,
     OP_GEMM_S8,
     OP_MLA,
+    OP_QKV_ROPE,
     OP_W8A8,
     OUT_BF16,
     OUT_FP32,
@@ -29,6 +32,7 @@ from ._native import (  # noqa: F401
     mla_q_chain,
     rmsnorm_linear_bf16,
     rmsnorm_linear_bf16_ex,
+    rmsnorm_linear_qkv_rope,
     rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
@@ -39,6 +43,7 @@ from ._native import (  # noqa: F401
     rnl_pipeline_submit_mla,
     rnl_pipeline_submit_w8a8,
     rnl_pipeline_wait,
+    rnl_qkv_rope,
     rnl_selftest_wait_timeout,
     rnl_trace_enable,
     rnl_trace_read,

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "librnl.so")
 
 NORM_RSQRT, NORM_SQRT_DIV = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8 = 0, 1, 2, 3
+OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE = 0, 1, 2, 3, 4
 
 STATUS = {
     0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
@@ -33,7 +33,8 @@ EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_li
            "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc",
            "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
-           "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex")
+           "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex", "rnl_qkv_rope",
+           "rmsnorm_linear_qkv_rope")
 
 
 class RnlError(RuntimeError):
@@ -68,6 +69,9 @@ def _declare(lib):
         "rnl_pipeline_wait": (I, [P, I64, ctypes.POINTER(I)]),
         "rnl_pipeline_destroy": (I, [P]),
         "rmsnorm_linear_bf16_ex": (I, [P, P, P, P, P, P, P, I64, I64, I64, F, I, P, P, P, SZ, P]),
+        "rnl_qkv_rope": (I, [P, I64, I64, I64, I64, P, P, F, P, P, I64, P, P, P, P]),
+        "rmsnorm_linear_qkv_rope": (I, [P, P, P, I64, I64, I64, I64, I64, F, I, P, P, F, P, P, I64,
+                                        P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -183,6 +187,65 @@ def rmsnorm_linear_bf16_ex(x, gamma, W, residual=None, x_sum_out=None, beta=None
     return out
 
 
+def _qkv_outputs(T, Hq, Hkv, D, dev, q_out, k_out, v_out):
+    q_out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) if q_out is None else q_out
+    k_out = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev) if k_out is None else k_out
+    v_out = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev) if v_out is None else v_out
+    _need(q_out, "q_out", torch.bfloat16, (T, Hq, D), dev)
+    _need(k_out, "k_out", torch.bfloat16, (T, Hkv, D), dev)
+    _need(v_out, "v_out", torch.bfloat16, (T, Hkv, D), dev)
+    return q_out, k_out, v_out
+
+
+def rnl_qkv_rope(y, n_q_heads, n_kv_heads, head_dim, q_gamma, k_gamma, positions, cos_sin,
+                 eps=1e-6, q_out=None, k_out=None, v_out=None, stream=None):
+    """QKV split + per-head RMSNorm + RoPE of a bf16 projection output y
+    [T, (Hq + 2 Hkv) * D]; returns (q, k, v)."""
+    T = y.shape[0]
+    Hq, Hkv, D = n_q_heads, n_kv_heads, head_dim
+    dev = y.device
+    _need(y, "y", torch.bfloat16, (T, (Hq + 2 * Hkv) * D), dev)
+    _need(q_gamma, "q_gamma", torch.bfloat16, (D,), dev)
+    _need(k_gamma, "k_gamma", torch.bfloat16, (D,), dev)
+    _need(positions, "positions", torch.int32, (T,), dev)
+    P = cos_sin.shape[0]
+    _need(cos_sin, "cos_sin", torch.float32, (P, D), dev)
+    q_out, k_out, v_out = _qkv_outputs(T, Hq, Hkv, D, dev, q_out, k_out, v_out)
+    _check(load().rnl_qkv_rope(_ptr(y), T, Hq, Hkv, D, _ptr(q_gamma), _ptr(k_gamma), float(eps),
+                               _ptr(positions), _ptr(cos_sin), P, _ptr(q_out), _ptr(k_out),
+                               _ptr(v_out), _stream(dev, stream)), "rnl_qkv_rope")
+    return q_out, k_out, v_out
+
+
+def rmsnorm_linear_qkv_rope(x, gamma, W, n_q_heads, n_kv_heads, head_dim, q_gamma, k_gamma,
+                            positions, cos_sin, eps=1e-6, norm_mode=NORM_RSQRT, head_eps=1e-6,
+                            q_out=None, k_out=None, v_out=None, workspace=None, stream=None):
+    """AT-10 RMSNorm + Linear into the qkv projection, then the QKV split +
+    per-head RMSNorm + RoPE stage; returns (q, k, v)."""
+    T, K = x.shape
+    Hq, Hkv, D = n_q_heads, n_kv_heads, head_dim
+    N = (Hq + 2 * Hkv) * D
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W, "W", torch.bfloat16, (N, K), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (K,), dev)
+    _need(q_gamma, "q_gamma", torch.bfloat16, (D,), dev)
+    _need(k_gamma, "k_gamma", torch.bfloat16, (D,), dev)
+    _need(positions, "positions", torch.int32, (T,), dev)
+    P = cos_sin.shape[0]
+    _need(cos_sin, "cos_sin", torch.float32, (P, D), dev)
+    q_out, k_out, v_out = _qkv_outputs(T, Hq, Hkv, D, dev, q_out, k_out, v_out)
+    ws = _workspace(workspace_size(OP_QKV_ROPE, T, K, N), dev, workspace)
+    _check(load().rmsnorm_linear_qkv_rope(_ptr(x), _ptr(gamma), _ptr(W), T, K, Hq, Hkv, D,
+                                          float(eps), int(norm_mode), _ptr(q_gamma), _ptr(k_gamma),
+                                          float(head_eps), _ptr(positions), _ptr(cos_sin), P,
+                                          _ptr(q_out), _ptr(k_out), _ptr(v_out), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "rmsnorm_linear_qkv_rope")
+    return q_out, k_out, v_out
+
+
 def rmsnorm_linear_w8a8(x, gamma, Wq, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
                         q_out=None, x_scale_out=None, workspace=None, stream=None):
     """AT-11 RMSNorm + per-token INT8 quant + exact INT8 matmul + dequant (bf16 out)."""
@@ -280,7 +343,7 @@ def rnl_check_device_error(stream=None, device=None):
     site = ctypes.c_int(0)
     st = load().rnl_check_device_error(_stream(dev, stream), ctypes.byref(site))
     if st != 0:
-        raise RnlError(st, f"device error (wait site {site.value})")
+        raise RnlError(st, f"device error (site {site.value})")
 
 
 def rnl_trace_enable(on: bool = True):

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace rnl {
 namespace {
@@ -231,15 +232,16 @@ void trace_after(cudaStream_t s, const char* name) {
 }
 
 rnl_status read_device_errors(int* site) {
-  unsigned int words[6] = {0, 0, 0, 0, 0, 0};
+  unsigned int words[7] = {0, 0, 0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
       read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
-      read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK)
+      read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK ||
+      read_clear_error_rope(&words[6]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {
       if (site) *site = static_cast<int>((w >> 8) & 0xFFu);
-      return RNL_ERR_TIMEOUT;
+      return (w & kErrTimeout) ? RNL_ERR_TIMEOUT : RNL_ERR_ARG;
     }
   }
   if (site) *site = 0;
@@ -279,6 +281,8 @@ size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2) {
     case RNL_OP_W8A8: return w8a8_layout(nullptr, T, K, N).bytes;
     case RNL_OP_MLA: return mla_layout(nullptr, T, N).bytes;
     case RNL_OP_GEMM_S8: return s8_layout(nullptr, T, K, N).bytes;
+    case RNL_OP_QKV_ROPE:
+      return bf16_layout(nullptr, T, K, N, RNL_OUT_BF16).bytes + round_up(static_cast<size_t>(T) * N * 2);
   }
   return static_cast<size_t>(-1);
 }
@@ -402,6 +406,65 @@ rnl_status rmsnorm_linear_bf16_ex(const void* x, const void* residual, void* x_s
   g.partial_ws = l.part;
   g.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
+}
+
+rnl_status rnl_qkv_rope(const void* y, int64_t T, int64_t n_q_heads, int64_t n_kv_heads,
+                        int64_t head_dim, const void* q_gamma, const void* k_gamma, float eps,
+                        const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                        void* q_out, void* k_out, void* v_out, rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(n_q_heads) || bad_dim(n_kv_heads) || bad_dim(max_pos) ||
+      n_q_heads + 2 * n_kv_heads == 0 || max_pos == 0 || bad_dim(T * (n_q_heads + 2 * n_kv_heads)))
+    return RNL_ERR_SHAPE;
+  if (!qkv_rope_head_dim_ok(head_dim)) return RNL_ERR_UNSUPPORTED;
+  if (bad_eps(eps)) return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!y || !positions || !cos_sin || (n_q_heads && (!q_gamma || !q_out)) ||
+      (n_kv_heads && (!k_gamma || !k_out || !v_out)))
+    return RNL_ERR_NULL;
+  if (!aligned16(y) || !aligned16(cos_sin) || (q_gamma && !aligned16(q_gamma)) ||
+      (k_gamma && !aligned16(k_gamma)) || (q_out && !aligned16(q_out)) ||
+      (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return RNL_ERR_ALIGN;
+  DeviceInfo dev;
+  const rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  return launch_qkv_rope(y, T, n_q_heads, n_kv_heads, head_dim, q_gamma, k_gamma, eps, positions,
+                         cos_sin, max_pos, q_out, k_out, v_out, cs(stream));
+}
+
+rnl_status rmsnorm_linear_qkv_rope(const void* x, const void* gamma, const void* W, int64_t T,
+                                   int64_t K, int64_t n_q_heads, int64_t n_kv_heads,
+                                   int64_t head_dim, float eps, int norm_mode,
+                                   const void* q_gamma, const void* k_gamma, float head_eps,
+                                   const int32_t* positions, const float* cos_sin,
+                                   int64_t max_pos, void* q_out, void* k_out, void* v_out,
+                                   void* workspace, size_t workspace_bytes, rnl_stream_t stream) {
+  if (bad_dim(n_q_heads) || bad_dim(n_kv_heads) || bad_dim(head_dim)) return RNL_ERR_SHAPE;
+  const int64_t N = (n_q_heads + 2 * n_kv_heads) * head_dim;
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0 || bad_dim(max_pos) || max_pos == 0)
+    return RNL_ERR_SHAPE;
+  if (!qkv_rope_head_dim_ok(head_dim)) return RNL_ERR_UNSUPPORTED;
+  if (bad_mode(norm_mode) || bad_eps(eps) || bad_eps(head_eps)) return RNL_ERR_ARG;
+  const size_t need = rnl_workspace_size(RNL_OP_QKV_ROPE, T, K, N, 0);
+  if (T == 0) return RNL_OK;
+  if (!workspace || workspace_bytes < need) return RNL_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return RNL_ERR_ALIGN;
+  const size_t proj = bf16_layout(nullptr, T, K, N, RNL_OUT_BF16).bytes;
+  void* y = static_cast<char*>(workspace) + proj;
+  // check the V-stage arguments before anything is enqueued
+  if (!positions || !cos_sin || (n_q_heads && (!q_gamma || !q_out)) ||
+      (n_kv_heads && (!k_gamma || !k_out || !v_out)))
+    return RNL_ERR_NULL;
+  if (!aligned16(cos_sin) || (q_gamma && !aligned16(q_gamma)) || (k_gamma && !aligned16(k_gamma)) ||
+      (q_out && !aligned16(q_out)) || (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return RNL_ERR_ALIGN;
+  rnl_status st = rmsnorm_linear_bf16(x, gamma, W, T, K, N, eps, norm_mode, y, RNL_OUT_BF16,
+                                      workspace, proj, stream);
+  if (st != RNL_OK) return st;
+  return rnl_qkv_rope(y, T, n_q_heads, n_kv_heads, head_dim, q_gamma, k_gamma, head_eps,
+                      positions, cos_sin, max_pos, q_out, k_out, v_out, stream);
 }
 
 rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* Wq,

@@ -71,6 +71,13 @@ rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_
 // int8 -> bf16 (exact), n elements, n % 16 == 0.
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
 
+// ---- QKV split + per-head RMSNorm + RoPE (qkvrope.cu) ----
+bool qkv_rope_head_dim_ok(int64_t D);
+rnl_status launch_qkv_rope(const void* y, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                           const void* q_gamma, const void* k_gamma, float eps,
+                           const int32_t* positions, const float* cos_sin, int64_t max_pos,
+                           void* q, void* k, void* v, cudaStream_t s);
+
 // ---- tcgen05 GEMM (gemm_tc.cu) ----
 enum class Epi : int {
   kBf16 = 0,         // out bf16 = acc
@@ -126,8 +133,10 @@ rnl_status read_clear_error_skinny(unsigned int* word);
 rnl_status read_clear_error_pair(unsigned int* word);
 rnl_status read_clear_error_norm(unsigned int* word);
 rnl_status read_clear_error_selftest(unsigned int* word);
+rnl_status read_clear_error_rope(unsigned int* word);
 // Reads and clears all of them without synchronising (api.cu): RNL_OK, or
-// RNL_ERR_TIMEOUT with the first recorded wait site in *site (optional).
+// RNL_ERR_TIMEOUT / RNL_ERR_ARG with the first recorded site in *site
+// (optional).
 rnl_status read_device_errors(int* site);
 
 }  // namespace rnl

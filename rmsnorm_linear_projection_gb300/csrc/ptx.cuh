@@ -14,9 +14,11 @@
 
 namespace rnl {
 
-// Error word layout (per module): bit 0 = a wait timed out; bits 8..15 = the
-// site id of the first timeout.
+// Error word layout (per module): bit 0 = a wait timed out; bit 1 = a bad
+// argument seen on the device; bits 8..15 = the site id of the first error.
 constexpr uint32_t kErrTimeout = 1u;
+// bit 1: an argument found bad on the device (e.g. a position outside its table)
+constexpr uint32_t kErrArg = 2u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
