@@ -64,6 +64,7 @@ def _declare(lib):
         "orc_mla_q_chain": (C, [P, P, P, P, I64, I64, I64, I64, D, C, P, P, P]),
         "orc_rmsnorm_linear_ex": (C, [P, P, P, P, P, P, I64, I64, I64, D, C, P, P, P, P]),
         "orc_qkv_rope": (C, [P, I64, I64, I64, I64, P, P, D, P, P, I64, P, P, P]),
+        "orc_quant_matmul_reduce_sum": (C, [P, P, P, P, I64, I64, I64, I64, P, P]),
         "orc_quant_rows_f32": (C, [P, P, I64, I64, F, C, P, P, P, P]),
         "orc_gemm_s8": (C, [P, P, I64, I64, I64, P]),
         "orc_dequant_bf16": (C, [P, P, P, I64, I64, P, P]),
@@ -183,6 +184,24 @@ class Oracle:
                                      _ptr(_c(k_gamma, np.uint16)), float(eps), _ptr(pos), _ptr(cs),
                                      cs.shape[0], _ptr(q), _ptr(k), _ptr(v)), "qkv_rope")
         return q, k, v
+
+    def quant_matmul_reduce_sum(self, x1, x2, x1_scale, x2_scale):
+        """QuantMatMulReduceSum: x1 int8 [B,M,K], x2 int8 [B,K,N], x1_scale fp32
+        [B,M], x2_scale bf16 bits [N].  Returns (ref fp32 [M,N], out bf16 bits)."""
+        x1, x2 = _c(x1, np.int8), _c(x2, np.int8)
+        B, M, K = x1.shape
+        N = x2.shape[2]
+        assert x2.shape == (B, K, N)
+        xs, ws = _c(x1_scale, np.float32), _c(x2_scale, np.uint16)
+        assert xs.shape == (B, M) and ws.shape == (N,)
+        ref = np.empty((M, N), np.float32)
+        out = np.empty((M, N), np.uint16)
+        st = self.lib.orc_quant_matmul_reduce_sum(_ptr(x1), _ptr(x2), _ptr(xs), _ptr(ws), B, M, K, N,
+                                                  _ptr(ref), _ptr(out))
+        _check(st, "quant_matmul_reduce_sum")
+        if st == 1:
+            raise OverflowError("int32 accumulator overflow")
+        return ref, out
 
     # -- MLA q chain ----------------------------------------------------------
     def mla_q_chain(self, x, W_qa, gamma_cq, W_qb, eps, variant):

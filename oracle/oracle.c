@@ -34,6 +34,7 @@
  *
  * bf16 values are passed as their 16-bit patterns (uint16_t).
  */
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -392,6 +393,54 @@ int orc_qkv_rope(const uint16_t *y, int64_t T, int64_t Hq, int64_t Hkv, int64_t 
         }
     }
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* QuantMatMulReduceSum.  [SK14] "variant A in practice: QuantMatMulReduceSum" */
+/* (and its parameter table): x1 int8 [B, M, K], x2 int8 [B, K, N] (ND),      */
+/* x1_scale fp32 [B, M], x2_scale bf16 [N], out bf16 [M, N]:                  */
+/*   acc_b = x1[b] @ x2[b]                  exact integers (int64 here)       */
+/*   mm_b = fp32(acc_b)                     the page's cast to DT_FP32        */
+/*   sc_b = fp32(x1_scale[b, m] * fp32(x2_scale[n]))   (scale product, FP32)  */
+/*   scaled_b = fp32(mm_b * sc_b)                                             */
+/*   out = bf16(sum_b scaled_b)             FP32 sum over the batch, b = 0..  */
+/* The page fixes FP32 for every step after the integer matmul, so this one   */
+/* is computed in binary32 (each step one correctly rounded operation, the    */
+/* batch sum in increasing b), not binary64.  ref receives the fp32 sum.      */
+/* Returns ORC_OVERFLOW if an acc leaves the int32 range (the page's INT32).  */
+/* ------------------------------------------------------------------------ */
+
+int orc_quant_matmul_reduce_sum(const int8_t *x1, const int8_t *x2, const float *x1_scale,
+                                const uint16_t *x2_scale, int64_t B, int64_t M, int64_t K,
+                                int64_t N, float *ref, uint16_t *out)
+{
+    if (!x1 || !x2 || !x1_scale || !x2_scale || !out || B <= 0 || M < 0 || K <= 0 || N <= 0)
+        return ORC_EARG;
+    int overflow = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : overflow)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            float sum = 0.0f;
+            const float ws = bf16_as_float(x2_scale[n]);
+            for (int64_t b = 0; b < B; ++b) {
+                int64_t acc = 0;
+                const int8_t *ar = x1 + (b * M + m) * K;
+                const int8_t *bc = x2 + b * K * N + n;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += (int64_t)ar[k] * (int64_t)bc[k * N];
+                if (acc > INT32_MAX || acc < INT32_MIN)
+                    overflow = 1;
+                const float mm = (float)(int32_t)acc;
+                const float sc = x1_scale[b * M + m] * ws;
+                const float scaled = mm * sc;
+                sum = sum + scaled;
+            }
+            if (ref)
+                ref[m * N + n] = sum;
+            out[m * N + n] = orc_bf16_rne((double)sum);
+        }
+    }
+    return overflow ? ORC_OVERFLOW : ORC_OK;
 }
 
 /* ------------------------------------------------------------------------ */

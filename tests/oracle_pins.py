@@ -740,8 +740,128 @@ def pin_rope_rejects_bad_position(orc):
         raise AssertionError(f"position {bad} accepted")
 
 
+# ---------------------------------------------------------------------------
+# QuantMatMulReduceSum (SK-14 skeleton page, variant A)
+# ---------------------------------------------------------------------------
+
+def _qmrs_case(rng, B, M, K, N, lo=-127, hi=127):
+    x1 = rng.integers(lo, hi + 1, (B, M, K)).astype(np.int8)
+    x2 = rng.integers(lo, hi + 1, (B, K, N)).astype(np.int8)
+    return x1, x2
+
+
+def pin_qmrs_unit_scales_exact(orc):
+    """Unit scales: every step is exact while the sums stay below 2^24, so the
+    output is the bf16 rounding of the exact integer sum over the batch
+    (Python integers, x2 read as [K, N])."""
+    rng = _rng(40)
+    for (B, M, K, N) in ((1, 3, 5, 4), (3, 4, 16, 6)):
+        x1, x2 = _qmrs_case(rng, B, M, K, N)
+        xs = np.ones((B, M), np.float32)
+        ws = np.full(N, _bf16_bits_of_f32(np.float32(1.0)), np.uint16)
+        _, out = orc.quant_matmul_reduce_sum(x1, x2, xs, ws)
+        for m in range(M):
+            for n in range(N):
+                tot = sum(int(x1[b, m, k]) * int(x2[b, k, n]) for b in range(B) for k in range(K))
+                bits, near = exact.bf16_round_exact(tot)
+                assert near or int(out[m, n]) == bits, (B, m, n)
+
+
+def pin_qmrs_x2_is_k_by_n(orc):
+    """x2[b] a permutation matrix of ones (K = N): out[m, n] sums x1[b, m, k]
+    over the batch at the k with x2[b, k, n] = 1 (catches a transposed x2)."""
+    rng = _rng(41)
+    B, M, K = 2, 5, 12
+    x1, _ = _qmrs_case(rng, B, M, K, K, -10, 10)
+    x2 = np.zeros((B, K, K), np.int8)
+    perms = [rng.permutation(K) for _ in range(B)]
+    for b in range(B):
+        x2[b, perms[b], np.arange(K)] = 1  # x2[b, perm[n], n] = 1
+    xs = np.ones((B, M), np.float32)
+    ws = np.full(K, _bf16_bits_of_f32(np.float32(1.0)), np.uint16)
+    _, out = orc.quant_matmul_reduce_sum(x1, x2, xs, ws)
+    want = sum(x1[b][:, perms[b]].astype(np.float64) for b in range(B))
+    assert np.array_equal(bf16_bits_to_f64(out), want)
+
+
+def pin_qmrs_power_of_two_scales(orc):
+    """Multiplying x1_scale by 4 and x2_scale by 1/2 doubles every FP32 step
+    exactly, so the output doubles bit for bit."""
+    rng = _rng(42)
+    B, M, K, N = 3, 6, 64, 10
+    x1, x2 = _qmrs_case(rng, B, M, K, N)
+    xs = rng.uniform(1e-3, 1e-2, (B, M)).astype(np.float32)
+    ws = _bf16_bits_of_f32(rng.uniform(1e-3, 1e-2, N).astype(np.float32))
+    ref, out = orc.quant_matmul_reduce_sum(x1, x2, xs, ws)
+    ws_half = _bf16_bits_of_f32((bf16_bits_to_f64(ws) / 2).astype(np.float32))
+    ref2, out2 = orc.quant_matmul_reduce_sum(x1, x2, xs * np.float32(4), ws_half)
+    assert np.array_equal(ref2, ref * np.float32(2))
+    assert np.array_equal(bf16_bits_to_f64(out2), 2 * bf16_bits_to_f64(out))
+
+
+def pin_qmrs_batch_structure(orc):
+    """Two batches in either order give the same sum (a + b = b + a in IEEE);
+    a trailing batch of zeros changes nothing; batch b uses x1_scale[b]."""
+    rng = _rng(43)
+    B, M, K, N = 2, 4, 32, 8
+    x1, x2 = _qmrs_case(rng, B, M, K, N)
+    xs = rng.uniform(1e-3, 1e-2, (B, M)).astype(np.float32)
+    ws = _bf16_bits_of_f32(rng.uniform(1e-3, 1e-2, N).astype(np.float32))
+    ref, out = orc.quant_matmul_reduce_sum(x1, x2, xs, ws)
+    ref_s, _ = orc.quant_matmul_reduce_sum(x1[::-1], x2[::-1], xs[::-1], ws)
+    assert np.array_equal(ref, ref_s)
+    z1 = np.concatenate([x1, np.zeros((1, M, K), np.int8)])
+    z2 = np.concatenate([x2, x2[:1]])
+    zs = np.concatenate([xs, xs[:1]])
+    ref_z, _ = orc.quant_matmul_reduce_sum(z1, z2, zs, ws)
+    assert np.array_equal(ref_z, ref)
+    # the scale of batch 1 applies to batch 1 only: zeroing it leaves batch 0
+    xs0 = xs.copy()
+    xs0[1] = 0
+    ref0, _ = orc.quant_matmul_reduce_sum(x1, x2, xs0, ws)
+    ref_b0, _ = orc.quant_matmul_reduce_sum(x1[:1], x2[:1], xs[:1], ws)
+    assert np.array_equal(ref0, ref_b0)
+
+
+def pin_qmrs_numpy_float32(orc):
+    """Library cross-check: numpy int64 matmul per batch, then the page's
+    FP32 steps with numpy float32 scalars in the same order."""
+    rng = _rng(44)
+    B, M, K, N = 4, 5, 96, 7
+    x1, x2 = _qmrs_case(rng, B, M, K, N)
+    xs = rng.uniform(1e-3, 1e-2, (B, M)).astype(np.float32)
+    ws = _bf16_bits_of_f32(rng.uniform(1e-3, 1e-2, N).astype(np.float32))
+    wsf = bf16_bits_to_f64(ws).astype(np.float32)
+    ref, _ = orc.quant_matmul_reduce_sum(x1, x2, xs, ws)
+    acc = np.einsum("bmk,bkn->bmn", x1.astype(np.int64), x2.astype(np.int64))
+    want = np.zeros((M, N), np.float32)
+    for b in range(B):
+        sc = xs[b][:, None] * wsf[None, :]
+        want = want + acc[b].astype(np.float32) * sc
+    assert np.array_equal(ref, want)
+
+
+def pin_qmrs_overflow(orc):
+    """|acc| > 2^31 - 1 is reported (the page's INT32 result cannot hold it)."""
+    K = 133200  # 127 * 127 * K > 2^31 - 1
+    x1 = np.full((1, 1, K), 127, np.int8)
+    x2 = np.full((1, K, 1), 127, np.int8)
+    try:
+        orc.quant_matmul_reduce_sum(x1, x2, np.ones((1, 1), np.float32),
+                                    np.full(1, _bf16_bits_of_f32(np.float32(1.0)), np.uint16))
+    except OverflowError:
+        return
+    raise AssertionError("overflow not reported")
+
+
 ALL_PINS = [
     pin_bf16_codec,
+    pin_qmrs_unit_scales_exact,
+    pin_qmrs_x2_is_k_by_n,
+    pin_qmrs_power_of_two_scales,
+    pin_qmrs_batch_structure,
+    pin_qmrs_numpy_float32,
+    pin_qmrs_overflow,
     pin_rope_angle_zero_is_head_norm,
     pin_rope_quarter_and_half_turn,
     pin_rope_positions_index_the_table,

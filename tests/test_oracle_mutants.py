@@ -63,6 +63,14 @@ MUTANTS = [
     ("rope_adjacent_pairing", "double z1 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[i + half]) * r *",
      "double z1 = orc_bf16_value(orc_bf16_rne(orc_bf16_value(yh[(i + 1) % D]) * r *"),
     ("rope_head_norm_drops_eps", "double r = 1.0 / sqrt(ss / (double)D + eps);", "double r = 1.0 / sqrt(ss / (double)D);"),
+    # QuantMatMulReduceSum
+    ("qmrs_x2_transposed", "const int8_t *bc = x2 + b * K * N + n;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += (int64_t)ar[k] * (int64_t)bc[k * N];",
+     "const int8_t *bc = x2 + b * K * N + n * K;\n                for (int64_t k = 0; k < K; ++k)\n                    acc += (int64_t)ar[k] * (int64_t)bc[k % N];"),
+    ("qmrs_scale_of_batch_0", "const float sc = x1_scale[b * M + m] * ws;", "const float sc = x1_scale[m] * ws;"),
+    ("qmrs_scale_product_in_double", "const float scaled = mm * sc;", "const float scaled = (float)((double)mm * ((double)x1_scale[b * M + m] * (double)ws));"),
+    ("qmrs_batch_sum_reversed", "            for (int64_t b = 0; b < B; ++b) {\n                int64_t acc = 0;",
+     "            for (int64_t bb = 0; bb < B; ++bb) {\n                const int64_t b = B - 1 - bb;\n                int64_t acc = 0;"),
+    ("qmrs_drop_x2_scale", "const float ws = bf16_as_float(x2_scale[n]);", "const float ws = 1.0f;"),
     ("rope_split_off_by_one_head", "            if (h < Hq) {\n                dst = q + (t * Hq + h) * D;",
      "            if (h <= Hq && h < Hq + Hkv) {\n                dst = q + (t * Hq + (h < Hq ? h : 0)) * D;"),
 ]
