@@ -42,9 +42,9 @@ sys.path.insert(0, ROOT)
 
 import synth_inputs as si  # noqa: E402
 
-WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex", "qkv_rope")
+WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex", "qkv_rope", "qmrs")
 DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600, "qkv_ex": 2000,
-                 "qkv_rope": 2000}
+                 "qkv_rope": 2000, "qmrs": 1000}
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
@@ -97,6 +97,12 @@ class Work:
             self.h["bias"] = si.normal_bf16(c["seed"], "bias", (N,), 0.5)
             self.flops = 2.0 * T * N * K
             self.bytes = 4.0 * T * K + 2.0 * N * K + 4.0 * K + 2.0 * N + 2.0 * T * N + 2.0 * T * K + 4.0 * T
+        elif name == "qmrs":
+            # QuantMatMulReduceSum: B exact int8 matmuls, dequantised and summed
+            self.h = si.make_qmrs(c)
+            B, M, K, N = c["B"], c["M"], c["K"], c["N"]
+            self.flops = 2.0 * B * M * N * K
+            self.bytes = 1.0 * B * (M * K + K * N) + 4.0 * B * M + 2.0 * N + 2.0 * M * N
         elif name == "qkv_rope":
             # the qkv projection, then the QKV split + per-head RMSNorm + RoPE
             self.h = si.make_projection(c)
@@ -128,7 +134,7 @@ class Work:
         torch = self.torch
         if a is None:
             return None
-        if a.dtype in (np.int32, np.float32):
+        if a.dtype in (np.int32, np.float32, np.int8):
             return torch.from_numpy(np.ascontiguousarray(a)).to(self.device)
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a)
         if a.dtype == np.uint16:
@@ -137,6 +143,8 @@ class Work:
 
     def _alloc_out(self):
         torch, c = self.torch, self.cfg
+        if self.name == "qmrs":
+            return torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=self.device)
         if self.name == "qkv_rope":
             T, Hq, Hkv, D = c["T"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
             self.qkv = tuple(torch.empty((T, H, D), dtype=torch.bfloat16, device=self.device)
@@ -150,7 +158,7 @@ class Work:
     def unit(self):
         if self.name in ("skinny", "tiny"):
             return "GB/s", self.bytes / 1e9
-        if self.name == "w8a8":
+        if self.name in ("w8a8", "qmrs"):
             return "TOPS", self.flops / 1e12
         return "TFLOP/s", self.flops / 1e12
 
@@ -159,6 +167,12 @@ class Work:
         d = self.d if d is None else d
         out = self.out if out is None else out
         c = self.cfg
+        if self.name == "qmrs":
+            if self.ws is None:
+                self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_QMRS, c["M"], c["K"], c["N"], c["B"]),
+                                           dtype=self.torch.uint8, device=self.device)
+            return rnl.quant_matmul_reduce_sum(d["x1"], d["x2"], d["x1_scale"], d["x2_scale"], out=out,
+                                               workspace=self.ws, stream=stream)
         if self.name == "qkv_rope":
             if self.ws is None:
                 self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_QKV_ROPE, c["T"], c["K"], c["N"]),
@@ -215,7 +229,11 @@ class Work:
 
         s = P(stream.cuda_stream)
         nbytes = self.ws.numel() * self.ws.element_size()
-        if self.name == "qkv_rope":
+        if self.name == "qmrs":
+            fn = lib.quant_matmul_reduce_sum
+            args = (ptr(d["x1"]), ptr(d["x2"]), ptr(d["x1_scale"]), ptr(d["x2_scale"]), c["B"], c["M"], c["K"],
+                    c["N"], ptr(out), ptr(self.ws), nbytes, s)
+        elif self.name == "qkv_rope":
             fn = lib.rmsnorm_linear_qkv_rope
             q, k, v = self.qkv
             args = (ptr(d["x"]), ptr(d["gamma"]), ptr(d["W"]), c["T"], c["K"], c["n_q_heads"], c["n_kv_heads"],
@@ -256,6 +274,8 @@ class Work:
             return "skinny_stream", "skinny_stream", 2.0 * c["T"] * c["K"] + 2.0 * c["N"] * c["K"], "hbm"
         if self.name == "mla":
             return "gemm (both stages)", "gemm", 2.0 * c["T"] * (c["N1"] * c["K"] + c["N2"] * c["N1"]), "tensor"
+        if self.name == "qmrs":
+            return "gemm (all batches)", "gemm", 2.0 * c["B"] * c["M"] * c["N"] * c["K"], "tensor"
         return "gemm", "gemm", 2.0 * c["T"] * c["N"] * c["K"], "tensor"
 
 
@@ -510,7 +530,7 @@ def run_ours(args):
     # i-1's output copy; the timed region runs from the first submit until the
     # last step's output is in host memory.
     e2e = None
-    if not args.no_e2e and w.name not in ("qkv_ex", "qkv_rope"):  # no host-buffer pipeline form
+    if not args.no_e2e and w.name not in ("qkv_ex", "qkv_rope", "qmrs"):  # no host-buffer pipeline form
         c = w.cfg
         host_x = torch.empty(w.d["x"].shape, dtype=w.d["x"].dtype, pin_memory=True)
         host_x.copy_(w.d["x"])
@@ -585,7 +605,7 @@ def run_ours(args):
         del graph
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and not args.T and w.name not in ("qkv_ex", "qkv_rope"):
+    if rank == 0 and world == 1 and not args.no_cpu and not args.T and w.name not in ("qkv_ex", "qkv_rope", "qmrs"):
         v, u, cores, sample, rows, ref_out, _ = oracle_sample(args.workload, target_s=args.cpu_seconds)
         got = w.out.cpu()
         got = got.view(torch.int16).numpy().view(np.uint16) if got.dtype == torch.bfloat16 else got.numpy()
@@ -605,7 +625,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "u8/i32" if w.name == "w8a8" else "bf16",
+            "dtype": "s8/i32" if w.name in ("w8a8", "qmrs") else "bf16",
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": w.name, **{k: v for k, v in c.items() if k != "seed"},
                        "l2": "flushed between timed steps (256 MB written then read, outside the step events)",

@@ -80,7 +80,14 @@ enum { RNL_NORM_RSQRT = 0, RNL_NORM_SQRT_DIV = 1 };
 /* AT-09 out_dtype */
 enum { RNL_OUT_BF16 = 0, RNL_OUT_FP32 = 1 };
 /* operation ids for rnl_workspace_size */
-enum { RNL_OP_BF16 = 0, RNL_OP_W8A8 = 1, RNL_OP_MLA = 2, RNL_OP_GEMM_S8 = 3, RNL_OP_QKV_ROPE = 4 };
+enum {
+  RNL_OP_BF16 = 0,
+  RNL_OP_W8A8 = 1,
+  RNL_OP_MLA = 2,
+  RNL_OP_GEMM_S8 = 3,
+  RNL_OP_QKV_ROPE = 4,
+  RNL_OP_QMRS = 5
+};
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int rnl_version(void);
@@ -95,6 +102,7 @@ const char *rnl_status_string(rnl_status s);
  *   RNL_OP_MLA:     T, K, N = N1, N2
  *   RNL_OP_GEMM_S8: T = M, K, N; N2 ignored
  *   RNL_OP_QKV_ROPE: T, K, N = (n_q_heads + 2 * n_kv_heads) * head_dim; N2 ignored
+ *   RNL_OP_QMRS:    T = M, K, N, N2 = B (the batch)
  * Returns (size_t)-1 for invalid sizes.  Host-only; needs no GPU.
  */
 size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
@@ -186,6 +194,25 @@ rnl_status rmsnorm_linear_qkv_rope(const void *x, const void *gamma, const void 
                                    const int32_t *positions, const float *cos_sin,
                                    int64_t max_pos, void *q_out, void *k_out, void *v_out,
                                    void *workspace, size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * QuantMatMulReduceSum ("SK-14 general multi-MatMul skeleton" page, variant
+ * A and its parameter table): a batch of exact INT8 matmuls, dequantised and
+ * summed over the batch.
+ *   x1        int8 [B, M, K];  x2 int8 [B, K, N] (N contiguous, as on the page)
+ *   x1_scale  fp32 [B, M];     x2_scale bf16 [N]
+ *   out       bf16 [M, N] = bf16(sum_b fp32(acc_b) * (x1_scale[b, m] *
+ *             fp32(x2_scale[n]))), acc_b = x1[b] @ x2[b] exact in int32; every
+ *             step after the matmul is one FP32 operation, the batch summed in
+ *             increasing b (so the result does not depend on the kernel's
+ *             tiling).  |acc_b| must fit int32 (K <= 133144 always does).
+ * K % 16 == 0 and N % 16 == 0; 16-byte aligned x1, x2, out; 4-byte x1_scale.
+ * Workspace: rnl_workspace_size(RNL_OP_QMRS, M, K, N, B) bytes.
+ */
+rnl_status quant_matmul_reduce_sum(const int8_t *x1, const int8_t *x2, const float *x1_scale,
+                                   const void *x2_scale, int64_t B, int64_t M, int64_t K,
+                                   int64_t N, void *out, void *workspace, size_t workspace_bytes,
+                                   rnl_stream_t stream);
 
 /*
  * AT-11 RMSNorm + per-token INT8 quant + exact INT8 x INT8 -> INT32 matmul +

@@ -10,6 +10,8 @@ arguments; the computation runs in the library's CUDA kernels.
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
+    quant_matmul_reduce_sum  QuantMatMulReduceSum: batched exact INT8 matmul, FP32
+                          dequant and sum over the batch
     rnl_qkv_rope / rmsnorm_linear_qkv_rope
                           QKV split + per-head RMSNorm + RoPE after the qkv projection
     rnl_pipeline_*        host-buffer pipeline: calls fed from and answering into
@@ -23,6 +25,7 @@ from ._native import (  # noqa: F401
     OP_GEMM_S8,
     OP_MLA,
     OP_QKV_ROPE,
+    OP_QMRS,
     OP_W8A8,
     OUT_BF16,
     OUT_FP32,
@@ -30,6 +33,7 @@ from ._native import (  # noqa: F401
     RnlError,
     load,
     mla_q_chain,
+    quant_matmul_reduce_sum,
     rmsnorm_linear_bf16,
     rmsnorm_linear_bf16_ex,
     rmsnorm_linear_qkv_rope,

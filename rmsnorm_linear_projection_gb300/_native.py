@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "librnl.so")
 
 NORM_RSQRT, NORM_SQRT_DIV = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE = 0, 1, 2, 3, 4
+OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS = 0, 1, 2, 3, 4, 5
 
 STATUS = {
     0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
@@ -34,7 +34,7 @@ EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_li
            "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
            "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex", "rnl_qkv_rope",
-           "rmsnorm_linear_qkv_rope")
+           "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum")
 
 
 class RnlError(RuntimeError):
@@ -70,6 +70,7 @@ def _declare(lib):
         "rnl_pipeline_destroy": (I, [P]),
         "rmsnorm_linear_bf16_ex": (I, [P, P, P, P, P, P, P, I64, I64, I64, F, I, P, P, P, SZ, P]),
         "rnl_qkv_rope": (I, [P, I64, I64, I64, I64, P, P, F, P, P, I64, P, P, P, P]),
+        "quant_matmul_reduce_sum": (I, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
         "rmsnorm_linear_qkv_rope": (I, [P, P, P, I64, I64, I64, I64, I64, F, I, P, P, F, P, P, I64,
                                         P, P, P, P, SZ, P]),
     }
@@ -242,8 +243,30 @@ def rmsnorm_linear_qkv_rope(x, gamma, W, n_q_heads, n_kv_heads, head_dim, q_gamm
                                           float(head_eps), _ptr(positions), _ptr(cos_sin), P,
                                           _ptr(q_out), _ptr(k_out), _ptr(v_out), _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream(dev, stream)),
-           "rmsnorm_linear_qkv_rope")
+           "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum")
     return q_out, k_out, v_out
+
+
+def quant_matmul_reduce_sum(x1, x2, x1_scale, x2_scale, out=None, workspace=None, stream=None):
+    """QuantMatMulReduceSum: exact int8 matmuls x1[b] @ x2[b] (x1 [B,M,K],
+    x2 [B,K,N]), dequantised with x1_scale [B,M] (fp32) and x2_scale [N]
+    (bf16) and summed over the batch in FP32; bf16 out [M, N]."""
+    B, M, K = x1.shape
+    N = x2.shape[2]
+    dev = x1.device
+    _need(x1, "x1", torch.int8, (B, M, K), dev)
+    _need(x2, "x2", torch.int8, (B, K, N), dev)
+    _need(x1_scale, "x1_scale", torch.float32, (B, M), dev)
+    _need(x2_scale, "x2_scale", torch.bfloat16, (N,), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (M, N), dev)
+    ws = _workspace(workspace_size(OP_QMRS, M, K, N, B), dev, workspace)
+    _check(load().quant_matmul_reduce_sum(_ptr(x1), _ptr(x2), _ptr(x1_scale), _ptr(x2_scale), B, M, K, N,
+                                          _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(dev, stream)),
+           "quant_matmul_reduce_sum")
+    return out
 
 
 def rmsnorm_linear_w8a8(x, gamma, Wq, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, out=None,

@@ -135,6 +135,24 @@ MLALayout mla_layout(void* ws, int64_t T, int64_t N1) {
   return l;
 }
 
+struct QmrsLayout {
+  void* x1 = nullptr;     // bf16 [B*M, K] widened x1
+  void* x2 = nullptr;     // bf16 [B*N, K] transposed, widened x2
+  float* ws = nullptr;    // fp32 [N] x2_scale
+  float* acc = nullptr;   // fp32 [M, N] running sum over the batch
+  size_t bytes = 0;
+};
+QmrsLayout qmrs_layout(void* ws, int64_t B, int64_t M, int64_t K, int64_t N) {
+  QmrsLayout l;
+  Carve c(ws);
+  l.x1 = c.take(static_cast<size_t>(B) * M * K * 2);
+  l.x2 = c.take(static_cast<size_t>(B) * N * K * 2);
+  l.ws = static_cast<float*>(c.take(static_cast<size_t>(N) * 4));
+  l.acc = static_cast<float*>(c.take(B > 1 ? static_cast<size_t>(M) * N * 4 : 0));
+  l.bytes = c.used;
+  return l;
+}
+
 struct S8Layout {
   void* A = nullptr;
   void* B = nullptr;
@@ -281,6 +299,9 @@ size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2) {
     case RNL_OP_W8A8: return w8a8_layout(nullptr, T, K, N).bytes;
     case RNL_OP_MLA: return mla_layout(nullptr, T, N).bytes;
     case RNL_OP_GEMM_S8: return s8_layout(nullptr, T, K, N).bytes;
+    case RNL_OP_QMRS:
+      if (N2 <= 0) return static_cast<size_t>(-1);
+      return qmrs_layout(nullptr, N2, T, K, N).bytes;
     case RNL_OP_QKV_ROPE:
       return bf16_layout(nullptr, T, K, N, RNL_OUT_BF16).bytes + round_up(static_cast<size_t>(T) * N * 2);
   }
@@ -465,6 +486,51 @@ rnl_status rmsnorm_linear_qkv_rope(const void* x, const void* gamma, const void*
   if (st != RNL_OK) return st;
   return rnl_qkv_rope(y, T, n_q_heads, n_kv_heads, head_dim, q_gamma, k_gamma, head_eps,
                       positions, cos_sin, max_pos, q_out, k_out, v_out, stream);
+}
+
+rnl_status quant_matmul_reduce_sum(const int8_t* x1, const int8_t* x2, const float* x1_scale,
+                                   const void* x2_scale, int64_t B, int64_t M, int64_t K,
+                                   int64_t N, void* out, void* workspace, size_t workspace_bytes,
+                                   rnl_stream_t stream) {
+  if (bad_dim(B) || bad_dim(M) || bad_dim(K) || bad_dim(N) || B == 0 || K == 0 || N == 0 ||
+      bad_dim(B * M) || bad_dim(B * N))
+    return RNL_ERR_SHAPE;
+  if (M == 0) return RNL_OK;
+  if (!x1 || !x2 || !x1_scale || !x2_scale || !out) return RNL_ERR_NULL;
+  if (K % 16 != 0 || N % 16 != 0 || !aligned16(x1) || !aligned16(x2) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(x1_scale) & 3u) || (reinterpret_cast<uintptr_t>(x2_scale) & 1u) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const QmrsLayout need = qmrs_layout(nullptr, B, M, K, N);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const QmrsLayout l = qmrs_layout(workspace, B, M, K, N);
+  cudaStream_t s = cs(stream);
+  st = launch_s8_to_bf16(x1, B * M * K, l.x1, s);
+  if (st != RNL_OK) return st;
+  st = launch_s8_transpose_widen(x2, B, K, N, l.x2, s);
+  if (st != RNL_OK) return st;
+  st = launch_bf16_to_f32(x2_scale, N, l.ws, s);
+  if (st != RNL_OK) return st;
+  for (int64_t b = 0; b < B; ++b) {
+    GemmArgs g;
+    g.A = static_cast<const char*>(l.x1) + static_cast<size_t>(b) * M * K * 2;
+    g.B = static_cast<const char*>(l.x2) + static_cast<size_t>(b) * N * K * 2;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.out = l.acc;
+    g.out_final = out;
+    g.row_scale = x1_scale + b * M;
+    g.col_scale = l.ws;
+    g.epi = Epi::kDequantAccF32;
+    g.acc_mode = (b > 0 ? 1 : 0) | (b == B - 1 ? 2 : 0);
+    st = launch_gemm(g, s);
+    if (st != RNL_OK) return st;
+  }
+  return RNL_OK;
 }
 
 rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* Wq,

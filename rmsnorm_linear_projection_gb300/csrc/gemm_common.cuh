@@ -199,5 +199,62 @@ __device__ __forceinline__ void store_dequant_32(void* out, int64_t m, int n0, i
     store_bf16_32(out, m, n0, N, v);
 }
 
+// QuantMatMulReduceSum epilogue of one batch (SK-14 skeleton page, variant A)
+// for outputs [m, n0 .. n0+31]: v = fp32(acc) * (x1_scale * x2_scale), each a
+// correctly rounded FP32 operation; mode bit 0: v = acc_buf[m, n] + v (the
+// earlier batches' FP32 sum); bit 1: write bf16(v) to out_final (last batch),
+// else v to acc_buf.  The first batch adds nothing (0 + v, so -0 becomes +0 as
+// in a sum that starts at zero).
+__device__ __forceinline__ void store_dequant_acc_32(float* acc_buf, __nv_bfloat16* out_final,
+                                                     int64_t m, int n0, int N, const int (&a)[32],
+                                                     float xs, const float* __restrict__ w_scale,
+                                                     int mode) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    const float ws = n < N ? __ldg(w_scale + n) : 0.f;
+    v[j] = __fmul_rn(__int2float_rn(a[j]), __fmul_rn(xs, ws));
+  }
+  float* arow = acc_buf + m * N;
+  const bool full = n0 + 32 <= N;
+  if (mode & 1) {
+    if (full && rows_32b_aligned(acc_buf, N, 4)) {
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t p[8];
+        ld_global_v8(arow + n0 + 8 * h, p);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * h + i] = __fadd_rn(__uint_as_float(p[i]), v[8 * h + i]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j < N) v[j] = __fadd_rn(arow[n0 + j], v[j]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(0.0f, v[j]);
+  }
+  if (mode & 2) {
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+    store_bf16_32(out_final, m, n0, N, r);
+  } else if (full && rows_32b_aligned(acc_buf, N, 4)) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t p[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = __float_as_uint(v[8 * h + i]);
+      st_global_v8(arow + n0 + 8 * h, p);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n0 + j < N) arow[n0 + j] = v[j];
+  }
+}
+
 }  // namespace gemm
 }  // namespace rnl

@@ -649,6 +649,7 @@ rnl_status launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
     case Epi::kRowScaleF32: return launch_pair_epi<1>(g, dev, s, "gemm_pair_rowscale_f32");
     case Epi::kDequantBf16: return launch_pair_epi<2>(g, dev, s, "gemm_pair_int_dequant");
     case Epi::kInt32: return launch_pair_epi<3>(g, dev, s, "gemm_pair_int_s32");
+    case Epi::kDequantAccF32: return RNL_ERR_UNSUPPORTED;  // one-CTA kernel only
   }
   return RNL_ERR_ARG;
 }

@@ -85,9 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int M, int N, int K, int group_m, void* __restrict__ out,
                 const float* __restrict__ row_scale, const float* __restrict__ col_scale,
                 const float* __restrict__ a_rstd, const uint4* __restrict__ a_gamma,
-                const __nv_bfloat16* __restrict__ bias) {
+                const __nv_bfloat16* __restrict__ bias, int acc_mode, void* out_final) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
-                         EPI == static_cast<int>(Epi::kInt32));
+                         EPI == static_cast<int>(Epi::kInt32) ||
+                         EPI == static_cast<int>(Epi::kDequantAccF32));
   static_assert(!(NORM_A && kInt), "the fused norm feeds the bf16 GEMM only");
   constexpr int kStages = Tile<BN>::kStages;
   constexpr uint32_t kStageBytes = Tile<BN>::kStageBytes;
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_base = nb * BN + half * kColsPerEpiWarp;
       const bool row_ok = m < M;
       float rs = 0.f;
-      if ((EPI == static_cast<int>(Epi::kRowScaleF32) || EPI == static_cast<int>(Epi::kDequantBf16)) && row_ok)
+      if ((EPI == static_cast<int>(Epi::kRowScaleF32) || EPI == static_cast<int>(Epi::kDequantBf16) ||
+           EPI == static_cast<int>(Epi::kDequantAccF32)) && row_ok)
         rs = __ldg(row_scale + m);
       int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
       if (kInt) {
@@ -278,6 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kGroups; ++c) {
             if constexpr (EPI == static_cast<int>(Epi::kInt32))
               store_i32_32(out, m, n_base + c * 32, N, iacc[c]);
+            else if constexpr (EPI == static_cast<int>(Epi::kDequantAccF32))
+              store_dequant_acc_32(static_cast<float*>(out), static_cast<__nv_bfloat16*>(out_final), m,
+                                   n_base + c * 32, N, iacc[c], rs, col_scale, acc_mode);
             else
               store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale, bias);
           }
@@ -385,7 +390,8 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
                                            static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                            g.out, g.row_scale, g.col_scale, g.a_rstd,
                                            static_cast<const uint4*>(g.a_gamma),
-                                           static_cast<const __nv_bfloat16*>(g.bias));
+                                           static_cast<const __nv_bfloat16*>(g.bias), g.acc_mode,
+                                           g.out_final);
   trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -457,13 +463,14 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
     if (e != nullptr && (e[0] == '0' || e[0] == '1')) {
       pair = e[0] == '1';
     } else {
-      const bool integer = g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32;
+      const bool integer =
+          g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32 || g.epi == Epi::kDequantAccF32;
       const int bn = pick_bn(g.M, g.N, g.K, dev.sm_count);
       pair = !integer && g.N >= 256 &&
              predict_pair_us(g.M, g.N, g.K, dev.sm_count, resident_pairs_for(dev)) <
                  predict_one_cta_us(g.M, g.N, g.K, dev.sm_count, bn);
     }
-    if (pair) return launch_gemm_pair(g, s);
+    if (pair && g.epi != Epi::kDequantAccF32) return launch_gemm_pair(g, s);  // one CTA only
   }
   if (g.a_rstd != nullptr) {  // fused norm: bf16 epilogue only
     if (g.epi != Epi::kBf16) return RNL_ERR_ARG;
@@ -478,6 +485,7 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
     case Epi::kRowScaleF32: return launch_bn<1>(g, dev, s, "gemm_rowscale_f32");
     case Epi::kDequantBf16: return launch_bn<2>(g, dev, s, "gemm_int_dequant");
     case Epi::kInt32: return launch_bn<3>(g, dev, s, "gemm_int_s32");
+    case Epi::kDequantAccF32: return launch_bn<4>(g, dev, s, "gemm_int_dequant_acc");
   }
   return RNL_ERR_ARG;
 }

@@ -68,6 +68,11 @@ rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_
 rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                              int mode, void* A, int8_t* q_out, float* x_scale, const int8_t* Wq,
                              int64_t N, void* Wb, cudaStream_t s);
+// int8 [B, K, N] -> bf16 [B, N, K] (exact; the K-major operand of an ND int8
+// matrix), K % 16 == 0 and N % 16 == 0 (qmrs.cu); and bf16 -> fp32 of n values.
+rnl_status launch_s8_transpose_widen(const int8_t* src, int64_t B, int64_t K, int64_t N, void* dst,
+                                     cudaStream_t s);
+rnl_status launch_bf16_to_f32(const void* src, int64_t n, float* dst, cudaStream_t s);
 // int8 -> bf16 (exact), n elements, n % 16 == 0.
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
 
@@ -84,6 +89,11 @@ enum class Epi : int {
   kRowScaleF32 = 1,  // out fp32 = acc * row_scale[m]
   kDequantBf16 = 2,  // out bf16 = float(exact int acc) * (row_scale[m] * col_scale[n])
   kInt32 = 3,        // out int32 = exact int acc
+  // QuantMatMulReduceSum, one batch: v = fp32(exact int acc) * (row_scale[m] *
+  // col_scale[n]) in FP32; acc_mode bit 0 adds the FP32 running sum in `out`
+  // (earlier batches), bit 1 (last batch) writes bf16(v) to out_final instead
+  // of v to `out`
+  kDequantAccF32 = 4,
 };
 
 struct GemmArgs {
@@ -107,6 +117,9 @@ struct GemmArgs {
   size_t partial_ws_bytes = 0;
   // name of the launch in the kernel trace (default: the kernel's kind)
   const char* trace_name = nullptr;
+  // Epi::kDequantAccF32 only
+  int acc_mode = 0;
+  void* out_final = nullptr;
 };
 
 // Partial-sum slots of the CTA-pair GEMM's stream-K tiles (2 x 128 x 256

@@ -51,6 +51,9 @@ CONFIGS = {
                  seed=1003),
     "skinny": dict(T=16384, K=28672, N=24, eps=1e-6, norm_mode=0,
                    has_gamma=False, out_dtype="fp32", seed=1004),
+    # QuantMatMulReduceSum: a batch of 4 exact int8 matmuls, summed (the
+    # pages give no sizes; 275 GOP like the W8A8 workload)
+    "qmrs": dict(B=4, M=2048, K=4096, N=4096, seed=1005),
     # the qkv projection followed by the QKV split + per-head RMSNorm + RoPE
     # stage (Qwen3 layout: 32 query heads and 8 key/value heads of 128)
     "qkv_rope": dict(T=4096, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
@@ -238,6 +241,24 @@ def make_qkv_rope(cfg: dict) -> dict:
         "k_gamma": uniform_bf16(s, "k_gamma", (D,), 0.5, 1.5),
         "positions": (np.arange(T, dtype=np.int64) % cfg["max_pos"]).astype(np.int32),
         "cos_sin": rope_table(cfg["max_pos"], D, cfg.get("rope_base", 1.0e6)),
+    }
+
+
+def make_qmrs(cfg: dict, rows=None) -> dict:
+    """QuantMatMulReduceSum operands: x1 int8 [B, M, K], x2 int8 [B, K, N]
+    (uniform integers in [-127, 127]), x1_scale fp32 [B, M], x2_scale bf16 [N]
+    (uniform in [1e-3, 1e-2]).  ``rows`` restricts x1 and x1_scale to a subset
+    of M (the values are those of the full tensors)."""
+    s, B, M, K, N = cfg["seed"], cfg["B"], cfg["M"], cfg["K"], cfg["N"]
+    x1 = uniform_int8(s, "x1", (B * M, K), -127, 127).reshape(B, M, K)
+    xs = uniform_f32(s, "x1_scale", (B, M), 1e-3, 1e-2)
+    if rows is not None:
+        x1, xs = x1[:, rows, :], xs[:, rows]
+    return {
+        "x1": x1,
+        "x2": uniform_int8(s, "x2", (B * K, N), -127, 127).reshape(B, K, N),
+        "x1_scale": xs,
+        "x2_scale": uniform_bf16(s, "x2_scale", (N,), 1e-3, 1e-2),
     }
 
 

@@ -28,7 +28,7 @@ def header_functions():
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)
     keywords = {"typedef", "enum", "struct", "sizeof", "defined"}
-    prefixes = ("rnl_", "rmsnorm_linear_", "mla_")
+    prefixes = ("rnl_", "rmsnorm_linear_", "mla_", "quant_")
     return sorted({n for n in names if n not in keywords and n.startswith(prefixes)})
 
 
@@ -98,6 +98,15 @@ CHILD = textwrap.dedent("""
     r["ex_bad_mode"] = e(A, None, None, None, None, A, None, 4, 64, 8, 1e-6, 3, A, None, ws, 1 << 20, None)
     r["ex_small_ws"] = e(A, None, None, None, None, A, None, 4, 64, 8, 1e-6, 0, A, None, ws, 16, None)
     r["ex_in_place_no_device"] = e(A, C, C, A, A, A, A, 4, 64, 8, 1e-6, 0, A, P(0x40000), ws, 1 << 30, None)
+    qm = lib.quant_matmul_reduce_sum
+    r["qmrs_N_not_mult16"] = qm(A, A, A, A, 2, 4, 32, 24, A, ws, 1 << 30, None)
+    r["qmrs_B0"] = qm(A, A, A, A, 0, 4, 32, 32, A, ws, 1 << 30, None)
+    r["qmrs_M0"] = qm(None, None, None, None, 2, 0, 32, 32, None, None, 0, None)
+    r["qmrs_null_scale"] = qm(A, A, None, A, 2, 4, 32, 32, A, ws, 1 << 30, None)
+    r["qmrs_small_ws"] = qm(A, A, A, A, 2, 4, 32, 32, A, ws, 64, None)
+    r["qmrs_no_device"] = qm(A, A, A, A, 2, 4, 32, 32, A, ws, 1 << 30, None)
+    r["ws_qmrs"] = lib.rnl_workspace_size(5, 2048, 4096, 4096, 4)
+    r["ws_qmrs_b1"] = lib.rnl_workspace_size(5, 2048, 4096, 4096, 1)
     pp = ctypes.c_void_p(None)
     r["pipe_null_out"] = lib.rnl_pipeline_create(0, 4, 64, 8, 0, None)
     r["pipe_bad_op"] = lib.rnl_pipeline_create(3, 4, 64, 8, 0, ctypes.byref(pp))
@@ -142,6 +151,9 @@ def test_workspace_sizes(host_results):
     assert r["ws_mla"] == 2 * 2048 * 1536 * 2 + 2048 * 4 + part
     # skinny partial records: (T/128 + 512) records of 128 rows x (32 + 1) floats
     assert r["ws_bf16_skinny"] == (16384 // 128 + 512) * 128 * 33 * 4
+    # QuantMatMulReduceSum: widened x1 and x2, fp32 x2_scale, fp32 batch sum
+    assert r["ws_qmrs"] == 4 * 2048 * 4096 * 2 + 4 * 4096 * 4096 * 2 + 4096 * 4 + 2048 * 4096 * 4
+    assert r["ws_qmrs_b1"] == 2048 * 4096 * 2 + 4096 * 4096 * 2 + 4096 * 4  # no running sum
     max_size = (1 << 64) - 1
     assert r["ws_bad_op"] == max_size and r["ws_neg"] == max_size
 
@@ -160,6 +172,8 @@ def test_workspace_sizes(host_results):
     ("ex_sum_without_residual", ARG), ("ex_sum_partial_overlap", ARG), ("ex_misaligned_bias", ALIGN),
     ("ex_misaligned_rstd", ALIGN), ("ex_null_W", NULL), ("ex_bad_mode", ARG), ("ex_small_ws", WORKSPACE),
     ("ex_in_place_no_device", DEVICE),
+    ("qmrs_N_not_mult16", ALIGN), ("qmrs_B0", SHAPE), ("qmrs_M0", OK), ("qmrs_null_scale", NULL),
+    ("qmrs_small_ws", WORKSPACE), ("qmrs_no_device", DEVICE),
     ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
     ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
     ("pipe_submit_null", NULL), ("pipe_submit_null_W", NULL), ("pipe_submit_bad_eps", ARG),
