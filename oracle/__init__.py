@@ -65,6 +65,11 @@ def _declare(lib):
         "orc_rmsnorm_linear_ex": (C, [P, P, P, P, P, P, I64, I64, I64, D, C, P, P, P, P]),
         "orc_qkv_rope": (C, [P, I64, I64, I64, I64, P, P, D, P, P, I64, P, P, P]),
         "orc_quant_matmul_reduce_sum": (C, [P, P, P, P, I64, I64, I64, I64, P, P]),
+        "orc_e4m3_value": (D, [ctypes.c_uint8]),
+        "orc_e4m3_rne_sat": (ctypes.c_uint8, [D]),
+        "orc_e8m0_value": (D, [ctypes.c_uint8]),
+        "orc_mxfp8_quant_rows": (C, [P, P, I64, I64, ctypes.c_float, C, I64, P, P]),
+        "orc_mxfp8_scaled_mm": (C, [P, P, P, P, I64, I64, I64, I64, C, P, P]),
         "orc_quant_rows_f32": (C, [P, P, I64, I64, F, C, P, P, P, P]),
         "orc_gemm_s8": (C, [P, P, I64, I64, I64, P]),
         "orc_dequant_bf16": (C, [P, P, P, I64, I64, P, P]),
@@ -201,6 +206,38 @@ class Oracle:
         _check(st, "quant_matmul_reduce_sum")
         if st == 1:
             raise OverflowError("int32 accumulator overflow")
+        return ref, out
+
+    # -- MXFP8 ----------------------------------------------------------------
+    def e4m3_value(self, c):
+        return self.lib.orc_e4m3_value(int(c))
+
+    def e4m3_rne_sat(self, v):
+        return int(self.lib.orc_e4m3_rne_sat(float(v)))
+
+    def e8m0_value(self, s):
+        return self.lib.orc_e8m0_value(int(s))
+
+    def mxfp8_quant_rows(self, x, gamma, eps, variant, block=64):
+        """E4M3 codes [T,K] (uint8) and E8M0 scale bytes [T, K/block]."""
+        x = _c(x, np.uint16)
+        T, K = x.shape
+        codes = np.empty((T, K), np.uint8)
+        scales = np.empty((T, K // block), np.uint8)
+        _check(self.lib.orc_mxfp8_quant_rows(_ptr(x), _ptr(_c(gamma, np.uint16)), T, K, float(eps),
+                                             int(variant), int(block), _ptr(codes), _ptr(scales)),
+               "mxfp8_quant_rows")
+        return codes, scales
+
+    def mxfp8_scaled_mm(self, xq, xs, wq, ws, out_dtype=0, block=64):
+        """(ref binary64 [T,N], out bf16 bits or fp32 [T,N])."""
+        xq, xs, wq, ws = _c(xq, np.uint8), _c(xs, np.uint8), _c(wq, np.uint8), _c(ws, np.uint8)
+        T, K = xq.shape
+        N = wq.shape[0]
+        ref = np.empty((T, N), np.float64)
+        out = np.empty((T, N), np.uint16 if out_dtype == 0 else np.float32)
+        _check(self.lib.orc_mxfp8_scaled_mm(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), T, K, N, int(block),
+                                            int(out_dtype), _ptr(ref), _ptr(out)), "mxfp8_scaled_mm")
         return ref, out
 
     # -- MLA q chain ----------------------------------------------------------

@@ -444,6 +444,189 @@ int orc_quant_matmul_reduce_sum(const int8_t *x1, const int8_t *x2, const float 
 }
 
 /* ------------------------------------------------------------------------ */
+/* MXFP8 mode of AT-09 / AT-11.  [AT10] sec. 4 (AT-09 quant_mode mxfp8:      */
+/* y = scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale)); [SK14] (GMM-MXFP8:  */
+/* data E4M3FN, scale factors E8M0FNU, one scale per 64 elements).          */
+/*                                                                          */
+/* E4M3FN, written from the format: 1 sign bit, 4 exponent bits (bias 7),   */
+/* 3 mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); there is no */
+/* infinity, S.1111.111 is NaN, the largest finite value is 448.            */
+/* E8M0FNU: an unsigned biased exponent, value 2^(byte - 127), 255 = NaN.   */
+/* ------------------------------------------------------------------------ */
+
+double orc_e4m3_value(uint8_t c)
+{
+    const int sign = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 0xF && m == 7)
+        return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return sign ? -v : v;
+}
+
+/* Round to nearest, ties to even, saturating to the largest finite value
+   (the "satfinite" conversion); NaN stays NaN. */
+uint8_t orc_e4m3_rne_sat(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const uint8_t sign = (v < 0 || (v == 0 && signbit(v))) ? 0x80 : 0;
+    const double a = fabs(v);
+    if (a < ldexp(1.0, -6)) { /* subnormal range: steps of 2^-9 */
+        const double r = nearbyint(ldexp(a, 9));
+        return sign | (uint8_t)r; /* r == 8 is the smallest normal, code 0x08 */
+    }
+    int E;
+    frexp(a, &E); /* a = f * 2^E, f in [0.5, 1) */
+    int k = E - 1; /* a in [2^k, 2^(k+1)) */
+    double r = nearbyint(ldexp(a, 3 - k)); /* mantissa in eighths, [8, 16] */
+    if (r == 16.0) {
+        r = 8.0;
+        k += 1;
+    }
+    if (k > 8 || (k == 8 && r > 14.0))
+        return sign | 0x7E; /* 448 */
+    return sign | (uint8_t)(((k + 7) << 3) | ((int)r - 8));
+}
+
+double orc_e8m0_value(uint8_t s)
+{
+    return s == 255 ? NAN : ldexp(1.0, (int)s - 127);
+}
+
+/* Per-token MXFP8 front end: the norm in binary32 exactly as
+   orc_quant_rows_f32 (exact-sum rstd, y = (x * rstd) * gamma), then for each
+   block of `block` elements: amax = max |y|, shared exponent
+   X = floor(log2(amax)) - 8 (8 = the largest exponent of E4M3, so the block
+   maximum lands in [256, 512) and saturates above 448), clamped to
+   [-127, 127]; scale byte X + 127; codes = E4M3(y * 2^-X).  A block of zeros
+   gets X = -127 and zero codes. */
+int orc_mxfp8_quant_rows(const uint16_t *x, const uint16_t *gamma, int64_t T, int64_t K,
+                         float eps, int variant, int64_t block, uint8_t *codes, uint8_t *scales)
+{
+    if (!x || !codes || !scales || T < 0 || K <= 0 || block <= 0 || K % block != 0 ||
+        (variant != 0 && variant != 1))
+        return ORC_EARG;
+    const float inv_d = (float)(1.0 / (double)K);
+    int status = ORC_OK;
+#pragma omp parallel
+    {
+        float *y = (float *)malloc((size_t)K * sizeof(float));
+        if (!y) {
+#pragma omp atomic write
+            status = ORC_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!y)
+                continue;
+            const uint16_t *xr = x + t * K;
+            double s64 = 0.0;
+            float rstd;
+            if (variant == 0) {
+                for (int64_t k = 0; k < K; ++k) {
+                    float v = bf16_as_float(xr[k]);
+                    float sq = v * v;
+                    s64 += (double)sq;
+                }
+                float s = (float)s64;
+                float ms = s * inv_d;
+                float var = ms + eps;
+                rstd = 1.0f / sqrtf(var);
+            } else {
+                for (int64_t k = 0; k < K; ++k) {
+                    float v = bf16_as_float(xr[k]);
+                    float sq = v * v;
+                    float sc = sq * inv_d;
+                    s64 += (double)sc;
+                }
+                float s = (float)s64;
+                float var = s + eps;
+                float sd = sqrtf(var);
+                rstd = 1.0f / sd;
+            }
+            for (int64_t k = 0; k < K; ++k) {
+                float v = bf16_as_float(xr[k]) * rstd;
+                if (gamma)
+                    v = v * bf16_as_float(gamma[k]);
+                y[k] = v;
+            }
+            for (int64_t b0 = 0; b0 < K; b0 += block) {
+                float amax = 0.0f;
+                for (int64_t k = b0; k < b0 + block; ++k)
+                    if (fabsf(y[k]) > amax)
+                        amax = fabsf(y[k]);
+                int X = -127;
+                if (amax > 0.0f) {
+                    int E;
+                    frexpf(amax, &E);
+                    X = E - 1 - 8;
+                    if (X < -127)
+                        X = -127;
+                    if (X > 127)
+                        X = 127;
+                }
+                scales[t * (K / block) + b0 / block] = (uint8_t)(X + 127);
+                for (int64_t k = b0; k < b0 + block; ++k)
+                    codes[t * K + k] = orc_e4m3_rne_sat(ldexp((double)y[k], -X));
+            }
+        }
+        free(y);
+    }
+    return status;
+}
+
+/* scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale) with both operands stored
+   [rows, K] (b_trans): ref = sum_k x[t,k] 2^(xs[t,k/block]-127) w[n,k]
+   2^(ws[n,k/block]-127) in binary64, the FP32 result fp32(ref), and the
+   output: out_dtype 0 = bf16(fp32(ref)) (the cast after scaled_mm), 1 = fp32. */
+int orc_mxfp8_scaled_mm(const uint8_t *xq, const uint8_t *xs, const uint8_t *wq, const uint8_t *ws,
+                        int64_t T, int64_t K, int64_t N, int64_t block, int out_dtype,
+                        double *ref, void *out)
+{
+    if (!xq || !xs || !wq || !ws || T < 0 || K <= 0 || N <= 0 || block <= 0 || K % block != 0 ||
+        (out_dtype != 0 && out_dtype != 1))
+        return ORC_EARG;
+    const int64_t nb = K / block;
+    double *wd = (double *)malloc((size_t)N * K * sizeof(double));
+    if (!wd)
+        return ORC_ENOMEM;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            wd[n * K + k] = orc_e4m3_value(wq[n * K + k]) * orc_e8m0_value(ws[n * nb + k / block]);
+    int status = ORC_OK;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc((size_t)K * sizeof(double));
+        if (!a) {
+#pragma omp atomic write
+            status = ORC_ENOMEM;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            if (!a)
+                continue;
+            for (int64_t k = 0; k < K; ++k)
+                a[k] = orc_e4m3_value(xq[t * K + k]) * orc_e8m0_value(xs[t * nb + k / block]);
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += a[k] * wd[n * K + k];
+                if (ref)
+                    ref[t * N + n] = acc;
+                const float f = (float)acc;
+                if (out_dtype == 0)
+                    ((uint16_t *)out)[t * N + n] = orc_bf16_rne((double)f);
+                else
+                    ((float *)out)[t * N + n] = f;
+            }
+        }
+        free(a);
+    }
+    free(wd);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
 /* MLA two-stage q chain.  [AT10] sec. 5 (MLAProlog) and sec. 9 (the golden  */
 /* chain): q = bf16(matmul(x, wq_a)); qr = rms_norm(q) (variant B in the     */
 /* page's code); qr = qr * gamma_cq (FP32); qr = bf16(qr);                   */

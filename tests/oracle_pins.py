@@ -854,7 +854,272 @@ def pin_qmrs_overflow(orc):
     raise AssertionError("overflow not reported")
 
 
+# ---------------------------------------------------------------------------
+# MXFP8 (AT-09 quant_mode mxfp8; GMM-MXFP8 layout: E4M3FN data, E8M0FNU
+# scale factors, one scale per 64 elements)
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_decode(codes):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _torch_e4m3_encode(vals):
+    """Round to nearest even through torch's float8_e4m3fn (valid for |v| < 464,
+    where torch and a saturating conversion agree)."""
+    import torch
+    t = torch.from_numpy(np.asarray(vals, np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def pin_e4m3_codec(orc):
+    # facts of the format: bias 7, 3 mantissa bits, no infinity, S.1111.111 NaN
+    known = {0x00: 0.0, 0x01: 2.0**-9, 0x07: 7 * 2.0**-9, 0x08: 2.0**-6, 0x38: 1.0, 0x39: 1.125,
+             0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in known.items():
+        assert orc.e4m3_value(c) == v, hex(c)
+    assert np.isnan(orc.e4m3_value(0x7F)) and np.isnan(orc.e4m3_value(0xFF))
+    allc = np.arange(256, dtype=np.uint8)
+    mine = np.array([orc.e4m3_value(int(c)) for c in allc])
+    ref = _torch_e4m3_decode(allc)
+    both_nan = np.isnan(mine) & np.isnan(ref)
+    assert np.array_equal(mine[~both_nan], ref[~both_nan]) and both_nan.sum() == 2
+    pos = mine[1:0x7F]
+    assert np.all(np.diff(pos) > 0) and pos.size == 126  # monotone in the code
+    # encoding: ties to even, the subnormal range, saturation to +-448
+    enc = {1.0625: 0x38, 1.1875: 0x3A, 2.0**-10: 0x00, 3 * 2.0**-10: 0x02, 7.5 * 2.0**-9: 0x08,
+           -1.0625: 0xB8, 448.0: 0x7E, 449.0: 0x7E, 464.0: 0x7E, 480.0: 0x7E, 1e30: 0x7E,
+           -1e30: 0xFE, 0.1: 0x1D, 15.5 * 2.0**-10: 0x08}
+    for v, c in enc.items():
+        assert orc.e4m3_rne_sat(v) == c, (v, hex(orc.e4m3_rne_sat(v)), hex(c))
+    assert orc.e4m3_rne_sat(0.0) == 0x00 and orc.e4m3_rne_sat(-0.0) == 0x80
+    rng = _rng(60)
+    v = np.concatenate([rng.standard_normal(3000) * 50, rng.standard_normal(3000) * 2.0**-7,
+                        rng.uniform(-463, 463, 2000), np.ldexp(rng.uniform(-1, 1, 1000), -9)]).astype(np.float32)
+    got = np.array([orc.e4m3_rne_sat(float(a)) for a in v], np.uint8)
+    assert np.array_equal(got, _torch_e4m3_encode(v))
+    # every finite code is a fixed point; midpoints go to the even neighbour
+    for c in range(0x7F):
+        assert orc.e4m3_rne_sat(orc.e4m3_value(c)) == c
+        if c < 0x7E:
+            mid = (orc.e4m3_value(c) + orc.e4m3_value(c + 1)) / 2
+            assert orc.e4m3_rne_sat(mid) == (c if c % 2 == 0 else c + 1)
+
+
+def pin_e8m0_scale(orc):
+    assert orc.e8m0_value(127) == 1.0 and orc.e8m0_value(128) == 2.0 and orc.e8m0_value(119) == 2.0**-8
+    assert orc.e8m0_value(0) == 2.0**-127 and orc.e8m0_value(254) == 2.0**127
+    assert np.isnan(orc.e8m0_value(255))
+
+
+def _mx_expected(y, block=64):
+    """Codes and scale bytes of the MX rule for exact y (a closed form: shared
+    exponent floor(log2 amax) - 8 via numpy's frexp, codes through torch's
+    float8 conversion, saturation applied to the block maximum's range)."""
+    T, K = y.shape
+    codes = np.zeros((T, K), np.uint8)
+    scales = np.zeros((T, K // block), np.uint8)
+    for t in range(T):
+        for b in range(K // block):
+            blk = y[t, b * block:(b + 1) * block].astype(np.float64)
+            amax = np.abs(blk).max()
+            X = -127 if amax == 0 else max(-127, int(np.frexp(amax)[1]) - 1 - 8)
+            scales[t, b] = X + 127
+            v = np.ldexp(blk, -X)
+            sat = np.abs(v) > 448
+            c = _torch_e4m3_encode(np.where(sat, 0.0, v).astype(np.float32))
+            c[sat] = np.where(v[sat] > 0, 0x7E, 0xFE)
+            codes[t, b * block:(b + 1) * block] = c
+    return codes, scales
+
+
+def pin_mxfp8_constructed_ties(orc):
+    # x and eps chosen so that the binary32 mean of squares plus eps rounds to
+    # 4096 exactly (the tiny entries' squares are far below its last bit):
+    # rstd = 1/64 and y = x / 64.
+    # The block maximum y = 1.5 gives X = -8 (y * 256 = 384); the other
+    # entries land on E4M3 ties, on the subnormal range and (row 1) on
+    # saturation (y * 256 = 488 > 448).
+    base = [96.0, 17 / 64, 19 / 64, -17 / 64, 2.0**-12, 3 * 2.0**-12, 7.5 * 2.0**-11, 0.0]
+    rows = [base + [0.0] * 56, [122.0] + base[1:] + [0.0] * 56]
+    want = [[0x7C, 0x38, 0x3A, 0xB8, 0x00, 0x02, 0x08, 0x00], [0x7E, 0x38, 0x3A, 0xB8, 0x00, 0x02, 0x08, 0x00]]
+    for x, w in zip(rows, want):
+        x = np.array([x], np.float32)
+        xb = _bf16_bits_of_f32(x)
+        assert np.array_equal(bf16_bits_to_f64(xb), x.astype(np.float64))
+        ms = sum(Fraction(float(v)) ** 2 for v in x[0]) / 64
+        eps = float(np.float32(float(Fraction(4096) - ms)))
+        assert abs(Fraction(eps) + ms - 4096) <= Fraction(1, 2**13)  # within half an ulp below 4096
+        for variant in (0, 1):
+            assert orc.quant_rows_f32(xb, None, eps, variant)[2][0] == np.float32(1 / 64)
+            codes, scales = orc.mxfp8_quant_rows(xb, None, eps, variant)
+            assert scales.tolist() == [[119]]  # X = -8
+            assert codes[0, :8].tolist() == w and not codes[0, 8:].any()
+
+
+def pin_mxfp8_gamma_closed_form(orc):
+    # x = 1 everywhere and eps = 0: rstd = 1 exactly in both variants, y = gamma
+    rng = _rng(61)
+    K = 256
+    g = _bf16_bits_of_f32(rng.uniform(-3, 3, K).astype(np.float32))
+    g[64:128] = _bf16_bits_of_f32((rng.uniform(-1, 1, 64) * 2.0**-20).astype(np.float32))
+    g[128:192] = 0
+    x = np.full((2, K), 0x3F80, np.uint16)
+    x[1] = 0xC000  # -2: rstd = 1/2, y = -gamma
+    y = np.stack([bf16_bits_to_f64(g), -bf16_bits_to_f64(g)])
+    want_c, want_s = _mx_expected(y)
+    assert want_s[0, 2] == 0  # a zero block: X = -127, zero codes
+    for variant in (0, 1):
+        codes, scales = orc.mxfp8_quant_rows(x, g, 0.0, variant)
+        assert np.array_equal(scales, want_s) and np.array_equal(codes, want_c)
+
+
+def pin_mxfp8_block_structure_and_bound(orc):
+    rng = _rng(62)
+    T, K = 12, 512
+    x = _rand_bf16(rng, (T, K))
+    x[:, 64:128] = _bf16_bits_of_f32((rng.standard_normal((T, 64)) * 1e-3).astype(np.float32))  # a quiet block
+    x[2, :] = 0
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    for variant in (0, 1):
+        codes, scales = orc.mxfp8_quant_rows(x, g, 1e-6, variant)
+        assert scales.shape == (T, K // 64)
+        assert not codes[2].any() and (scales[2] == 0).all()
+        y64, _ = orc.rmsnorm_f64(x, g, 1e-6, variant)
+        for t in range(T):
+            if t == 2:
+                continue
+            for b in range(K // 64):
+                blk = y64[t, b * 64:(b + 1) * 64]
+                amax = np.abs(blk).max()
+                X = int(scales[t, b]) - 127
+                # the shared exponent puts the block maximum in [256, 512)
+                assert 256 * (1 - 1e-6) <= amax * 2.0**-X < 512 * (1 + 1e-6), (t, b)
+                dq = np.array([orc.e4m3_value(c) for c in codes[t, b * 64:(b + 1) * 64]]) * 2.0**X
+                v = blk * 2.0**-X
+                # half a step of the E4M3 grid at each magnitude (2^-10 in the
+                # subnormal range), or the saturation of values above 448
+                step = np.where(np.abs(v) < 2.0**-6, 2.0**-9,
+                                2.0 ** (np.floor(np.log2(np.maximum(np.abs(v), 2.0**-6))) - 3))
+                tol = np.where(np.abs(v) > 448, np.abs(v) - 448, step / 2) * (1 + 1e-5) + 1e-6 * np.abs(v)
+                assert np.all(np.abs(dq * 2.0**-X - v) <= tol), (t, b)
+        # the quiet block has its own, smaller scale
+        assert (scales[[0, 1, 3], 1] < scales[[0, 1, 3], 0] - 5).all()
+        # rows are independent
+        assert np.array_equal(codes[1:], orc.mxfp8_quant_rows(x[1:], g, 1e-6, variant)[0])
+    # block 32 (the OCP MX block) is the same rule on half blocks
+    c64, s64 = orc.mxfp8_quant_rows(x, g, 1e-6, 0, block=64)
+    c32, s32 = orc.mxfp8_quant_rows(x, g, 1e-6, 0, block=32)
+    assert s32.shape == (T, K // 32) and (s32.reshape(T, -1, 2).max(axis=2) == s64).all()
+
+
+def pin_mxfp8_power_of_two_invariance(orc):
+    # eps = 0: x * 2^5 leaves y, so every code and scale, unchanged
+    rng = _rng(63)
+    x = _rand_bf16(rng, (6, 192))
+    xs = _bf16_bits_of_f32((bf16_bits_to_f64(x) * 32).astype(np.float32))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, 192).astype(np.float32))
+    for variant in (0, 1):
+        a = orc.mxfp8_quant_rows(x, g, 0.0, variant)
+        b = orc.mxfp8_quant_rows(xs, g, 0.0, variant)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        # and gamma * 2 moves every scale by exactly one, codes unchanged
+        g2 = _bf16_bits_of_f32((bf16_bits_to_f64(g) * 2).astype(np.float32))
+        c = orc.mxfp8_quant_rows(x, g2, 0.0, variant)
+        assert np.array_equal(c[0], a[0]) and np.array_equal(c[1].astype(int), a[1].astype(int) + 1)
+
+
+def _mx_random(rng, rows, K, sigma=1.0):
+    codes = rng.integers(0, 256, (rows, K)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scales = rng.integers(127 - 12, 127 + 4, (rows, K // 64)).astype(np.uint8)
+    return codes, scales
+
+
+def pin_mxfp8_scaled_mm_exact_small(orc):
+    rng = _rng(64)
+    T, K, N = 3, 128, 4
+    xq, xs = _mx_random(rng, T, K)
+    wq, ws = _mx_random(rng, N, K)
+    ref, out = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 0)
+    _, out32 = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 1)
+    xv, wv = _torch_e4m3_decode(xq), _torch_e4m3_decode(wq)
+    for t in range(T):
+        for n in range(N):
+            e = sum(Fraction(float(xv[t, k])) * Fraction(2) ** (int(xs[t, k // 64]) - 127) *
+                    Fraction(float(wv[n, k])) * Fraction(2) ** (int(ws[n, k // 64]) - 127) for k in range(K))
+            assert exact.rel_close(ref[t, n], e, 1e-13) or abs(float(e)) < 1e-300
+            # the FP32 result: within half an FP32 ulp of the exact sum (plus
+            # the binary64 accumulation's own error), and the bf16 output is
+            # that FP32 value rounded once more
+            assert abs(Fraction(float(out32[t, n])) - e) <= abs(e) * Fraction(1, 2**24) * (1 + Fraction(1, 10**9))
+            bits, near = exact.bf16_round_exact(Fraction(float(out32[t, n])))
+            assert near or int(out[t, n]) == bits
+
+
+def pin_mxfp8_scaled_mm_torch(orc):
+    import torch
+    rng = _rng(65)
+    T, K, N = 9, 256, 11
+    xq, xs = _mx_random(rng, T, K)
+    wq, ws = _mx_random(rng, N, K)
+    ref, out32 = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 1)
+    xv = torch.from_numpy(_torch_e4m3_decode(xq)) * torch.pow(2.0, torch.from_numpy(xs.astype(np.float64) - 127)).repeat_interleave(64, 1)
+    wv = torch.from_numpy(_torch_e4m3_decode(wq)) * torch.pow(2.0, torch.from_numpy(ws.astype(np.float64) - 127)).repeat_interleave(64, 1)
+    want = (xv @ wv.T).numpy()
+    mag = (xv.abs() @ wv.abs().T).numpy()
+    assert np.all(np.abs(ref - want) <= 1e-14 * mag)
+    assert np.array_equal(out32, ref.astype(np.float32))
+
+
+def pin_mxfp8_scaled_mm_fp32_then_bf16(orc):
+    # exact sum 1 + 2^-8 + 2^-30: its FP32 value 1 + 2^-8 is a bf16 tie, which
+    # goes to 1.0 (even); rounding the binary64 sum straight to bf16 would give 1 + 2^-7.
+    K = 128
+    xq = np.zeros((1, K), np.uint8)
+    wq = np.zeros((1, K), np.uint8)
+    xq[0, 0] = xq[0, 1] = xq[0, 64] = 0x38  # 1.0
+    wq[0, 0] = 0x78  # 256 * 2^-8 = 1
+    wq[0, 1] = 0x38  # 1 * 2^-8
+    wq[0, 64] = 0x38  # 1 * 2^-30
+    xs = np.full((1, 2), 127, np.uint8)
+    ws = np.array([[127 - 8, 127 - 30]], np.uint8)
+    ref, out = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 0)
+    assert ref[0, 0] == 1 + 2.0**-8 + 2.0**-30
+    assert int(out[0, 0]) == 0x3F80
+    _, o32 = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 1)
+    assert o32[0, 0] == np.float32(1 + 2.0**-8)
+
+
+def pin_mxfp8_composition(orc):
+    # quantise the normed activations and a weight, then scaled_mm: close to
+    # the unquantised FP32 projection (E4M3 keeps 4 significant bits)
+    rng = _rng(66)
+    T, K, N = 5, 256, 16
+    x = _rand_bf16(rng, (T, K))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    W = rng.standard_normal((N, K)) * 0.02
+    xq, xs = orc.mxfp8_quant_rows(x, g, 1e-6, 0)
+    wq, ws = _mx_expected(W)
+    ref, _ = orc.mxfp8_scaled_mm(xq, xs, wq, ws, 1)
+    y64, _ = orc.rmsnorm_f64(x, g, 1e-6, 0)
+    full = y64 @ W.T
+    mag = np.abs(y64) @ np.abs(W).T
+    assert np.all(np.abs(ref - full) <= 2 * 2.0**-4 * mag)
+    assert np.abs(ref - full).max() < 0.1 * np.abs(full).max()
+
+
 ALL_PINS = [
+    pin_e4m3_codec,
+    pin_e8m0_scale,
+    pin_mxfp8_constructed_ties,
+    pin_mxfp8_gamma_closed_form,
+    pin_mxfp8_block_structure_and_bound,
+    pin_mxfp8_power_of_two_invariance,
+    pin_mxfp8_scaled_mm_exact_small,
+    pin_mxfp8_scaled_mm_torch,
+    pin_mxfp8_scaled_mm_fp32_then_bf16,
+    pin_mxfp8_composition,
     pin_bf16_codec,
     pin_qmrs_unit_scales_exact,
     pin_qmrs_x2_is_k_by_n,

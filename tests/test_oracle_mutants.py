@@ -71,6 +71,21 @@ MUTANTS = [
     ("qmrs_batch_sum_reversed", "            for (int64_t b = 0; b < B; ++b) {\n                int64_t acc = 0;",
      "            for (int64_t bb = 0; bb < B; ++bb) {\n                const int64_t b = B - 1 - bb;\n                int64_t acc = 0;"),
     ("qmrs_drop_x2_scale", "const float ws = bf16_as_float(x2_scale[n]);", "const float ws = 1.0f;"),
+    # MXFP8: E4M3 codec, shared block exponent, scaled_mm
+    ("e4m3_decode_wrong_bias", "ldexp(8.0 + m, e - 10)", "ldexp(8.0 + m, e - 11)"),
+    ("e4m3_ties_away", "double r = nearbyint(ldexp(a, 3 - k));", "double r = round(ldexp(a, 3 - k));"),
+    ("e4m3_overflow_to_nan", "return sign | 0x7E; /* 448 */", "return sign | 0x7F; /* 448 */"),
+    ("e4m3_subnormal_threshold", "if (a < ldexp(1.0, -6)) { /* subnormal range", "if (a < ldexp(1.0, -7)) { /* subnormal range"),
+    ("mx_exponent_off_by_one", "X = E - 1 - 8;", "X = E - 8;"),
+    ("mx_amax_over_whole_row", "for (int64_t k = b0; k < b0 + block; ++k)\n                    if (fabsf(y[k]) > amax)",
+     "for (int64_t k = 0; k < K; ++k)\n                    if (fabsf(y[k]) > amax)"),
+    ("mx_drop_gamma", "                if (gamma)\n                    v = v * bf16_as_float(gamma[k]);\n                y[k] = v;",
+     "                y[k] = v;"),
+    ("mx_scaled_mm_first_weight_scale", "orc_e8m0_value(ws[n * nb + k / block])", "orc_e8m0_value(ws[n * nb])"),
+    ("mx_scaled_mm_bf16_from_binary64", "((uint16_t *)out)[t * N + n] = orc_bf16_rne((double)f);",
+     "((uint16_t *)out)[t * N + n] = orc_bf16_rne(acc);"),
+    ("mx_scale_byte_bias", "scales[t * (K / block) + b0 / block] = (uint8_t)(X + 127);",
+     "scales[t * (K / block) + b0 / block] = (uint8_t)(X + 128);"),
     ("rope_split_off_by_one_head", "            if (h < Hq) {\n                dst = q + (t * Hq + h) * D;",
      "            if (h <= Hq && h < Hq + Hkv) {\n                dst = q + (t * Hq + (h < Hq ? h : 0)) * D;"),
 ]
