@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs = 0.f;
       if ((EPI == static_cast<int>(Epi::kRowScaleF32) ||
            EPI == static_cast<int>(Epi::kDequantBf16)) && row_ok)
-        rs = __ldg(row_scale + m);
+        rs = row_scale != nullptr ? __ldg(row_scale + m) : 1.0f;
       int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
       if (kInt) {
 #pragma unroll
@@ -620,9 +620,12 @@ rnl_status launch_pair_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_
 
 // Predicted time of the pair kernel (256-wide tiles) in microseconds, from
 // the per-SM rate it sustained on GB300 in full waves (1909 TFLOP/s over 152
-// SMs): every pair's share of the k-blocks, plus about 2 us for the stream-K
-// partial sums (written early by one pair, read by another at its end) when
-// the tiles do not fill whole waves.
+// SMs): every pair's share of the k-blocks, plus the stream-K hand-off when
+// the tiles do not fill whole waves: about 2 us after data-parallel waves (a
+// partner's partial is its first, short item), about 20 us when every tile is
+// split (fewer than 2P tiles: a partner's partial is its whole range, so the
+// finisher waits for it, then drains; measured on the MLA q_a shape,
+// 2048 x 1536 x 7168: 43 us against 39 us on one CTA).
 double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs_hint) {
   const int pairs = pairs_hint > 0 ? pairs_hint : sm_count / 2;
   const int64_t num_m = (M + 2 * BM - 1) / (2 * BM);
@@ -632,7 +635,7 @@ double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs_
   const double tile_us = 2.0 * BM * 256 * static_cast<double>(K) / 12.56e12 * 1e6;
   const Plan pl = make_plan(tiles, p, true);
   double t = (static_cast<double>(pl.dp_tiles) / p + static_cast<double>(pl.sk_tiles) / p) * tile_us;
-  if (pl.sk_tiles % p != 0) t += 2.0;
+  if (pl.sk_tiles % p != 0) t += pl.dp_tiles > 0 ? 2.0 : 20.0;
   return t;
 }
 
