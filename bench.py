@@ -1,6 +1,7 @@
 """Benchmark of the fused RMSNorm -> Linear projection on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload qkv|tiny|mla|w8a8|skinny]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload qkv|tiny|mla|w8a8|skinny|qkv_ex|qkv_rope|qmrs|mxfp8]
                     [--impl ours|reference]
 
 Prints ONE JSON line.  The default workload is the pre-attention fused QKV
@@ -42,9 +43,9 @@ sys.path.insert(0, ROOT)
 
 import synth_inputs as si  # noqa: E402
 
-WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex", "qkv_rope", "qmrs")
+WORKLOADS = ("qkv", "tiny", "mla", "w8a8", "skinny", "qkv_ex", "qkv_rope", "qmrs", "mxfp8")
 DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny": 600, "qkv_ex": 2000,
-                 "qkv_rope": 2000, "qmrs": 1000}
+                 "qkv_rope": 2000, "qmrs": 1000, "mxfp8": 2000}
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
@@ -103,6 +104,13 @@ class Work:
             B, M, K, N = c["B"], c["M"], c["K"], c["N"]
             self.flops = 2.0 * B * M * N * K
             self.bytes = 1.0 * B * (M * K + K * N) + 4.0 * B * M + 2.0 * N + 2.0 * M * N
+        elif name == "mxfp8":
+            # the qkv projection shape in MXFP8 mode: E4M3 weight codes with
+            # one E8M0 scale per 64 elements
+            self.h = si.make_mxfp8(c)
+            T, K, N = c["T"], c["K"], c["N"]
+            self.flops = 2.0 * T * N * K
+            self.bytes = 2.0 * T * K + 1.0 * N * K + N * K / c["block"] + 2.0 * K + 2.0 * T * N
         elif name == "qkv_rope":
             # the qkv projection, then the QKV split + per-head RMSNorm + RoPE
             self.h = si.make_projection(c)
@@ -183,6 +191,13 @@ class Work:
                                                d["cos_sin"], eps=c["eps"], norm_mode=c["norm_mode"],
                                                head_eps=c["head_eps"], q_out=q, k_out=k, v_out=v,
                                                workspace=self.ws, stream=stream)
+        if self.name == "mxfp8":
+            if self.ws is None:
+                self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_MXFP8, c["T"], c["K"], c["N"]),
+                                           dtype=self.torch.uint8, device=self.device)
+            return rnl.rmsnorm_linear_mxfp8(d["x"], d["gamma"], d["w_codes"], d["w_scale"], eps=c["eps"],
+                                            norm_mode=c["norm_mode"], block=c["block"], out=out,
+                                            workspace=self.ws, stream=stream)
         if self.name == "qkv_ex":
             if self.ws is None:
                 self.ws = self.torch.empty(rnl.workspace_size(rnl.OP_BF16, c["T"], c["K"], c["N"], rnl.OUT_BF16),
@@ -240,6 +255,11 @@ class Work:
                     c["head_dim"], c["eps"], c["norm_mode"], ptr(d["q_gamma"]), ptr(d["k_gamma"]),
                     c["head_eps"], ptr(d["positions"]), ptr(d["cos_sin"]), c["max_pos"], ptr(q), ptr(k),
                     ptr(v), ptr(self.ws), nbytes, s)
+        elif self.name == "mxfp8":
+            fn = lib.rmsnorm_linear_mxfp8
+            args = (ptr(d["x"]), ptr(d["gamma"]), ptr(d["w_codes"]), ptr(d["w_scale"]), c["T"], c["K"], c["N"],
+                    c["eps"], c["norm_mode"], c["block"], ptr(out), rnl.OUT_BF16, None, None, ptr(self.ws),
+                    nbytes, s)
         elif self.name == "qkv_ex":
             fn = lib.rmsnorm_linear_bf16_ex
             args = (ptr(d["x"]), ptr(d["residual"]), ptr(self.x_sum), ptr(d["gamma"]), ptr(d["beta"]),
@@ -346,6 +366,12 @@ def oracle_sample(work_name: str, target_s: float = 12.0):
             form = 1 if c["out_dtype"] == "fp32" else 0
             t = time.perf_counter()
             _, out = o.rmsnorm_linear(d["x"], d["gamma"], d["W"], c["eps"], c["norm_mode"], form)
+            return time.perf_counter() - t, out
+        if work_name == "mxfp8":
+            d = si.make_mxfp8(c, rows=rows)
+            t = time.perf_counter()
+            xq, xs = o.mxfp8_quant_rows(d["x"], d["gamma"], c["eps"], c["norm_mode"], block=c["block"])
+            _, out = o.mxfp8_scaled_mm(xq, xs, d["w_codes"], d["w_scale"], 0, block=c["block"])
             return time.perf_counter() - t, out
         if work_name == "mla":
             d = si.make_mla(c, rows=rows)
@@ -530,7 +556,7 @@ def run_ours(args):
     # i-1's output copy; the timed region runs from the first submit until the
     # last step's output is in host memory.
     e2e = None
-    if not args.no_e2e and w.name not in ("qkv_ex", "qkv_rope", "qmrs"):  # no host-buffer pipeline form
+    if not args.no_e2e and w.name not in ("qkv_ex", "qkv_rope", "qmrs", "mxfp8"):  # no host-buffer pipeline form
         c = w.cfg
         host_x = torch.empty(w.d["x"].shape, dtype=w.d["x"].dtype, pin_memory=True)
         host_x.copy_(w.d["x"])
@@ -625,7 +651,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "s8/i32" if w.name in ("w8a8", "qmrs") else "bf16",
+            "dtype": ("s8/i32" if w.name in ("w8a8", "qmrs") else
+                      "e4m3->bf16/f32" if w.name == "mxfp8" else "bf16"),
             "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": w.name, **{k: v for k, v in c.items() if k != "seed"},
                        "l2": "flushed between timed steps (256 MB written then read, outside the step events)",

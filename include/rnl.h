@@ -86,7 +86,8 @@ enum {
   RNL_OP_MLA = 2,
   RNL_OP_GEMM_S8 = 3,
   RNL_OP_QKV_ROPE = 4,
-  RNL_OP_QMRS = 5
+  RNL_OP_QMRS = 5,
+  RNL_OP_MXFP8 = 6
 };
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -103,6 +104,7 @@ const char *rnl_status_string(rnl_status s);
  *   RNL_OP_GEMM_S8: T = M, K, N; N2 ignored
  *   RNL_OP_QKV_ROPE: T, K, N = (n_q_heads + 2 * n_kv_heads) * head_dim; N2 ignored
  *   RNL_OP_QMRS:    T = M, K, N, N2 = B (the batch)
+ *   RNL_OP_MXFP8:   T, K, N; N2 ignored (rmsnorm_linear_mxfp8 and mxfp8_scaled_mm)
  * Returns (size_t)-1 for invalid sizes.  Host-only; needs no GPU.
  */
 size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
@@ -232,6 +234,47 @@ rnl_status rmsnorm_linear_w8a8(const void *x, const void *gamma, const int8_t *W
                                const float *w_scale, int64_t T, int64_t K, int64_t N, float eps,
                                int norm_mode, void *out, int8_t *q_out, float *x_scale_out,
                                void *workspace, size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * AT-11 in MXFP8 mode: RMSNorm, MX quantisation of the normed rows, and
+ * scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale) against an MXFP8 weight
+ * (AT-10 pattern page, sec. 4, AT-09 quant_mode mxfp8; SK-14 skeleton page,
+ * GMM-MXFP8: E4M3FN data, E8M0FNU scales, one scale per 64 elements).
+ *   x        bf16 [T, K];  gamma bf16 [K] or NULL
+ *   w_codes  E4M3FN bytes [N, K];  w_scale E8M0 bytes [N, K / block]
+ *            (element k of row n is value(w_codes[n, k]) * 2^(w_scale[n, k / block] - 127))
+ *   block    elements per scale along K: 64 (the page's) or 32 (OCP MX)
+ *   out      bf16 [T, N] (RNL_OUT_BF16: the FP32 result cast once) or fp32 [T, N]
+ *   x_codes_out  optional E4M3FN bytes [T, K]: the activation codes (NULL = not written)
+ *   x_scale_out  optional E8M0 bytes [T, K / block]: their scales (NULL = not written)
+ * Per block of the normed FP32 row y (the norm as in rmsnorm_linear_w8a8):
+ * X = floor(log2 max|y|) - 8 (at least -127; an all-zero block gets -127),
+ * scale byte X + 127, codes E4M3(y * 2^-X) rounded to nearest even and
+ * saturated to +-448.  Codes and scales are exact functions of x, gamma and
+ * eps (the FP32 sum of squares is the rounding of the exact sum).  The
+ * product is accumulated in FP32 on the tensor cores from the exactly
+ * dequantised operands.  K % block == 0; x, gamma, w_codes, out 16-byte
+ * aligned.  Workspace: rnl_workspace_size(RNL_OP_MXFP8, T, K, N, 0) bytes.
+ * Non-finite inputs and weights whose dequantised values exceed the bf16
+ * range give unspecified (but memory-safe) results.
+ */
+rnl_status rmsnorm_linear_mxfp8(const void *x, const void *gamma, const uint8_t *w_codes,
+                                const uint8_t *w_scale, int64_t T, int64_t K, int64_t N, float eps,
+                                int norm_mode, int64_t block, void *out, int out_dtype,
+                                uint8_t *x_codes_out, uint8_t *x_scale_out, void *workspace,
+                                size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale) on MXFP8 operands already
+ * quantised (the same page passages): out[t, n] = sum_k value(x_codes[t, k])
+ * 2^(x_scale[t, k/block] - 127) value(w_codes[n, k]) 2^(w_scale[n, k/block] - 127),
+ * FP32 accumulation, bf16 or fp32 out as above.  Layouts, alignment and
+ * workspace as rmsnorm_linear_mxfp8 (x_codes [T, K], x_scale [T, K / block]).
+ */
+rnl_status mxfp8_scaled_mm(const uint8_t *x_codes, const uint8_t *x_scale, const uint8_t *w_codes,
+                           const uint8_t *w_scale, int64_t T, int64_t K, int64_t N, int64_t block,
+                           void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                           rnl_stream_t stream);
 
 /*
  * MLA two-stage q chain.

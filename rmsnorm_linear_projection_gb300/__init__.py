@@ -12,6 +12,8 @@ arguments; the computation runs in the library's CUDA kernels.
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
     quant_matmul_reduce_sum  QuantMatMulReduceSum: batched exact INT8 matmul, FP32
                           dequant and sum over the batch
+    rmsnorm_linear_mxfp8  AT-11 in MXFP8 mode: RMSNorm + MX quant + scaled_mm
+    mxfp8_scaled_mm       scaled_mm on MXFP8 operands
     rnl_qkv_rope / rmsnorm_linear_qkv_rope
                           QKV split + per-head RMSNorm + RoPE after the qkv projection
     rnl_pipeline_*        host-buffer pipeline: calls fed from and answering into
@@ -24,6 +26,7 @@ from ._native import (  # noqa: F401
     OP_BF16,
     OP_GEMM_S8,
     OP_MLA,
+    OP_MXFP8,
     OP_QKV_ROPE,
     OP_QMRS,
     OP_W8A8,
@@ -33,9 +36,11 @@ from ._native import (  # noqa: F401
     RnlError,
     load,
     mla_q_chain,
+    mxfp8_scaled_mm,
     quant_matmul_reduce_sum,
     rmsnorm_linear_bf16,
     rmsnorm_linear_bf16_ex,
+    rmsnorm_linear_mxfp8,
     rmsnorm_linear_qkv_rope,
     rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "librnl.so")
 
 NORM_RSQRT, NORM_SQRT_DIV = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS = 0, 1, 2, 3, 4, 5
+OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS, OP_MXFP8 = 0, 1, 2, 3, 4, 5, 6
 
 STATUS = {
     0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
@@ -34,7 +34,8 @@ EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_li
            "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
            "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex", "rnl_qkv_rope",
-           "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum")
+           "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum", "rmsnorm_linear_mxfp8",
+           "mxfp8_scaled_mm")
 
 
 class RnlError(RuntimeError):
@@ -71,6 +72,8 @@ def _declare(lib):
         "rmsnorm_linear_bf16_ex": (I, [P, P, P, P, P, P, P, I64, I64, I64, F, I, P, P, P, SZ, P]),
         "rnl_qkv_rope": (I, [P, I64, I64, I64, I64, P, P, F, P, P, I64, P, P, P, P]),
         "quant_matmul_reduce_sum": (I, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
+        "rmsnorm_linear_mxfp8": (I, [P, P, P, P, I64, I64, I64, F, I, I64, P, I, P, P, P, SZ, P]),
+        "mxfp8_scaled_mm": (I, [P, P, P, P, I64, I64, I64, I64, P, I, P, SZ, P]),
         "rmsnorm_linear_qkv_rope": (I, [P, P, P, I64, I64, I64, I64, I64, F, I, P, P, F, P, P, I64,
                                         P, P, P, P, SZ, P]),
     }
@@ -243,7 +246,7 @@ def rmsnorm_linear_qkv_rope(x, gamma, W, n_q_heads, n_kv_heads, head_dim, q_gamm
                                           float(head_eps), _ptr(positions), _ptr(cos_sin), P,
                                           _ptr(q_out), _ptr(k_out), _ptr(v_out), _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream(dev, stream)),
-           "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum")
+           "rmsnorm_linear_qkv_rope")
     return q_out, k_out, v_out
 
 
@@ -293,6 +296,60 @@ def rmsnorm_linear_w8a8(x, gamma, Wq, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, o
                                       _ptr(x_scale_out), _ptr(ws), ws.numel() * ws.element_size(),
                                       _stream(dev, stream)),
            "rmsnorm_linear_w8a8")
+    return out
+
+
+def rmsnorm_linear_mxfp8(x, gamma, w_codes, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, block=64,
+                         out=None, out_dtype=OUT_BF16, x_codes_out=None, x_scale_out=None,
+                         workspace=None, stream=None):
+    """AT-11 in MXFP8 mode: RMSNorm, MX quantisation of the rows, scaled_mm
+    against E4M3 weight codes [N, K] with E8M0 scale bytes [N, K / block]."""
+    T, K = x.shape
+    N = w_codes.shape[0]
+    dev = x.device
+    nb = K // block if block else 0
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(w_codes, "w_codes", torch.uint8, (N, K), dev)
+    _need(w_scale, "w_scale", torch.uint8, (N, nb), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (K,), dev)
+    odt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+    if out is None:
+        out = torch.empty((T, N), dtype=odt, device=dev)
+    _need(out, "out", odt, (T, N), dev)
+    if x_codes_out is not None:
+        _need(x_codes_out, "x_codes_out", torch.uint8, (T, K), dev)
+    if x_scale_out is not None:
+        _need(x_scale_out, "x_scale_out", torch.uint8, (T, nb), dev)
+    ws = _workspace(workspace_size(OP_MXFP8, T, K, N), dev, workspace)
+    _check(load().rmsnorm_linear_mxfp8(_ptr(x), _ptr(gamma), _ptr(w_codes), _ptr(w_scale), T, K, N,
+                                       float(eps), int(norm_mode), int(block), _ptr(out), int(out_dtype),
+                                       _ptr(x_codes_out), _ptr(x_scale_out), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "rmsnorm_linear_mxfp8")
+    return out
+
+
+def mxfp8_scaled_mm(x_codes, x_scale, w_codes, w_scale, block=64, out=None, out_dtype=OUT_BF16,
+                    workspace=None, stream=None):
+    """scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale) on MXFP8 operands."""
+    T, K = x_codes.shape
+    N = w_codes.shape[0]
+    dev = x_codes.device
+    nb = K // block if block else 0
+    _need(x_codes, "x_codes", torch.uint8, (T, K), dev)
+    _need(x_scale, "x_scale", torch.uint8, (T, nb), dev)
+    _need(w_codes, "w_codes", torch.uint8, (N, K), dev)
+    _need(w_scale, "w_scale", torch.uint8, (N, nb), dev)
+    odt = torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32
+    if out is None:
+        out = torch.empty((T, N), dtype=odt, device=dev)
+    _need(out, "out", odt, (T, N), dev)
+    ws = _workspace(workspace_size(OP_MXFP8, T, K, N), dev, workspace)
+    _check(load().mxfp8_scaled_mm(_ptr(x_codes), _ptr(x_scale), _ptr(w_codes), _ptr(w_scale), T, K, N,
+                                  int(block), _ptr(out), int(out_dtype), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "mxfp8_scaled_mm")
     return out
 
 

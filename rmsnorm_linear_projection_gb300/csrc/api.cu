@@ -153,6 +153,40 @@ QmrsLayout qmrs_layout(void* ws, int64_t B, int64_t M, int64_t K, int64_t N) {
   return l;
 }
 
+struct MxLayout {
+  void* A = nullptr;   // bf16 [T, K] dequantised activations
+  void* Wb = nullptr;  // bf16 [N, K] dequantised weight
+  void* part = nullptr;
+  size_t bytes = 0;
+};
+MxLayout mx_layout(void* ws, int64_t T, int64_t K, int64_t N) {
+  MxLayout l;
+  Carve c(ws);
+  l.A = c.take(static_cast<size_t>(T) * K * 2);
+  l.Wb = c.take(static_cast<size_t>(N) * K * 2);
+  l.part = c.take(kGemmPartialBytes);
+  l.bytes = c.used;
+  return l;
+}
+
+// The GEMM of both MXFP8 entry points: bf16 operands, bf16 out or fp32 out
+// (the fp32 epilogue with no row scale).
+rnl_status mx_gemm(const MxLayout& l, int64_t T, int64_t K, int64_t N, void* out, int out_dtype,
+                   cudaStream_t s) {
+  GemmArgs g;
+  g.A = l.A;
+  g.B = l.Wb;
+  g.M = T;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.epi = out_dtype == RNL_OUT_BF16 ? Epi::kBf16 : Epi::kRowScaleF32;
+  g.partial_ws = l.part;
+  g.partial_ws_bytes = kGemmPartialBytes;
+  g.trace_name = "gemm_mxfp8";
+  return launch_gemm(g, s);
+}
+
 struct S8Layout {
   void* A = nullptr;
   void* B = nullptr;
@@ -302,6 +336,7 @@ size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2) {
     case RNL_OP_QMRS:
       if (N2 <= 0) return static_cast<size_t>(-1);
       return qmrs_layout(nullptr, N2, T, K, N).bytes;
+    case RNL_OP_MXFP8: return mx_layout(nullptr, T, K, N).bytes;
     case RNL_OP_QKV_ROPE:
       return bf16_layout(nullptr, T, K, N, RNL_OUT_BF16).bytes + round_up(static_cast<size_t>(T) * N * 2);
   }
@@ -568,6 +603,59 @@ rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* W
   g.partial_ws = l.part;
   g.partial_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
+}
+
+rnl_status rmsnorm_linear_mxfp8(const void* x, const void* gamma, const uint8_t* w_codes,
+                                const uint8_t* w_scale, int64_t T, int64_t K, int64_t N, float eps,
+                                int norm_mode, int64_t block, void* out, int out_dtype,
+                                uint8_t* x_codes_out, uint8_t* x_scale_out, void* workspace,
+                                size_t workspace_bytes, rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps) || !mx_block_ok(block) ||
+      (out_dtype != RNL_OUT_BF16 && out_dtype != RNL_OUT_FP32))
+    return RNL_ERR_ARG;
+  if (K % block != 0) return RNL_ERR_SHAPE;
+  if (T == 0) return RNL_OK;
+  if (!x || !w_codes || !w_scale || !out) return RNL_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w_codes) || !aligned16(out) || (gamma && !aligned16(gamma)) ||
+      (x_codes_out && !aligned16(x_codes_out)) || (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const MxLayout need = mx_layout(nullptr, T, K, N);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const MxLayout l = mx_layout(workspace, T, K, N);
+  cudaStream_t s = cs(stream);
+  st = launch_mx_front(x, gamma, T, K, eps, norm_mode, block, l.A, x_codes_out, x_scale_out,
+                       w_codes, w_scale, N, l.Wb, s);
+  if (st != RNL_OK) return st;
+  return mx_gemm(l, T, K, N, out, out_dtype, s);
+}
+
+rnl_status mxfp8_scaled_mm(const uint8_t* x_codes, const uint8_t* x_scale, const uint8_t* w_codes,
+                           const uint8_t* w_scale, int64_t T, int64_t K, int64_t N, int64_t block,
+                           void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                           rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (!mx_block_ok(block) || (out_dtype != RNL_OUT_BF16 && out_dtype != RNL_OUT_FP32))
+    return RNL_ERR_ARG;
+  if (K % block != 0) return RNL_ERR_SHAPE;
+  if (T == 0) return RNL_OK;
+  if (!x_codes || !x_scale || !w_codes || !w_scale || !out) return RNL_ERR_NULL;
+  if (!aligned16(x_codes) || !aligned16(w_codes) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const MxLayout need = mx_layout(nullptr, T, K, N);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const MxLayout l = mx_layout(workspace, T, K, N);
+  cudaStream_t s = cs(stream);
+  st = launch_mx_dequant2(x_codes, x_scale, T, w_codes, w_scale, N, K, block, l.A, l.Wb, s);
+  if (st != RNL_OK) return st;
+  return mx_gemm(l, T, K, N, out, out_dtype, s);
 }
 
 rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, const void* W_qb,

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rs = 0.f;
       if ((EPI == static_cast<int>(Epi::kRowScaleF32) || EPI == static_cast<int>(Epi::kDequantBf16) ||
            EPI == static_cast<int>(Epi::kDequantAccF32)) && row_ok)
-        rs = __ldg(row_scale + m);
+        rs = row_scale != nullptr ? __ldg(row_scale + m) : 1.0f;
       int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
       if (kInt) {
 #pragma unroll

@@ -76,6 +76,22 @@ rnl_status launch_bf16_to_f32(const void* src, int64_t n, float* dst, cudaStream
 // int8 -> bf16 (exact), n elements, n % 16 == 0.
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
 
+// ---- MXFP8 (mxfp8.cu) ----
+// block must be 32 or 64 (elements per E8M0 scale along K).
+bool mx_block_ok(int64_t block);
+// norm + MX quantisation of x's rows (A = bf16 of the dequantised codes;
+// codes [T, K] and scale bytes [T, K / block] optional) and dequantisation
+// of the E4M3 weight [N, K] with its scales [N, K / block] into Wb, in one
+// launch.  K % block == 0.
+rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                           int mode, int64_t block, void* A, uint8_t* q_out, uint8_t* s_out,
+                           const uint8_t* w_codes, const uint8_t* w_scale, int64_t N, void* Wb,
+                           cudaStream_t s);
+// Dequantisation of two MXFP8 operands [M, K] and [N, K] into bf16 A and B.
+rnl_status launch_mx_dequant2(const uint8_t* a_codes, const uint8_t* a_scale, int64_t M,
+                              const uint8_t* b_codes, const uint8_t* b_scale, int64_t N, int64_t K,
+                              int64_t block, void* A, void* B, cudaStream_t s);
+
 // ---- QKV split + per-head RMSNorm + RoPE (qkvrope.cu) ----
 bool qkv_rope_head_dim_ok(int64_t D);
 rnl_status launch_qkv_rope(const void* y, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
@@ -86,7 +102,7 @@ rnl_status launch_qkv_rope(const void* y, int64_t T, int64_t Hq, int64_t Hkv, in
 // ---- tcgen05 GEMM (gemm_tc.cu) ----
 enum class Epi : int {
   kBf16 = 0,         // out bf16 = acc
-  kRowScaleF32 = 1,  // out fp32 = acc * row_scale[m]
+  kRowScaleF32 = 1,  // out fp32 = acc * row_scale[m] (row_scale null: 1)
   kDequantBf16 = 2,  // out bf16 = float(exact int acc) * (row_scale[m] * col_scale[n])
   kInt32 = 3,        // out int32 = exact int acc
   // QuantMatMulReduceSum, one batch: v = fp32(exact int acc) * (row_scale[m] *

@@ -9,6 +9,7 @@
 // in FP32, then the result is cast to BF16 for the matmul).
 #include <cuda_bf16.h>
 
+#include "exactsum.cuh"
 #include "internal.h"
 
 namespace rnl {
@@ -146,50 +147,23 @@ __global__ void __launch_bounds__(kWarps * 32)
   if ((threadIdx.x & 31) == 0) rstd_out[row] = rstd;
 }
 
-// Error-free transformation of a sum (Knuth's TwoSum): s + e == a + b exactly.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-// rstd for the W8A8 front end, where the FP32 values decide integer codes.
-// Each term (x*x, or (x*x)*(1/K) for the sqrt+div form) is one binary32
-// product; the terms are added in float-float (hi + lo, TwoSum per term and
-// per lane merge), so the row's sum is known to about 2^-44 relative and is
-// rounded once to binary32 -- the FP32 value of the exact sum, independent of
-// the summation order.  Every later step is one correctly rounded binary32
-// operation (no fused multiply-add, no approximate reciprocal square root).
+// rstd for the W8A8 front end, where the FP32 values decide integer codes:
+// the binary32 value of the row's exact sum of squares (exactsum.cuh), then
+// one correctly rounded operation per step (no fused multiply-add, no
+// approximate reciprocal square root).
 template <int MODE>
 __device__ __forceinline__ float row_rstd_exactsum(const uint4* xr, int nvec, float inv_d,
                                                    float eps) {
   const int lane = threadIdx.x & 31;
-  float hi = 0.f, lo = 0.f;
+  float hs[8], ls[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) hs[j] = ls[j] = 0.f;
   for (int v = lane; v < nvec; v += 32) {
     float f[8];
     unpack8(ldg16(xr + v), f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float t = __fmul_rn(f[j], f[j]);
-      if (MODE == 1) t = __fmul_rn(t, inv_d);
-      float s, e;
-      two_sum(hi, t, s, e);
-      hi = s;
-      lo = __fadd_rn(lo, e);
-    }
+    ff_add_squares8<MODE>(f, inv_d, hs, ls);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    float s, e;
-    two_sum(hi, h2, s, e);
-    lo = __fadd_rn(__fadd_rn(lo, l2), e);
-    hi = s;
-  }
-  const float ss = __fadd_rn(hi, lo);
-  if (MODE == 0) return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_d), eps)));
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ss, eps)));
+  return rstd_of_sum<MODE>(ff_warp_total(hs, ls), inv_d, eps);
 }
 
 // AT-11 front end: RMSNorm, then AT-05 per-token symmetric INT8 codes
@@ -292,37 +266,9 @@ __device__ __forceinline__ void norm_quant_regs_rows(unsigned block, const uint4
   for (int i = 0; i < VPL; ++i) {
     float f[8];
     unpack8(u[i], f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float t = __fmul_rn(f[j], f[j]);
-      if (MODE == 1) t = __fmul_rn(t, inv_d);
-      float sum, e;
-      two_sum(hs[j], t, sum, e);
-      hs[j] = sum;
-      ls[j] = __fadd_rn(ls[j], e);
-    }
+    ff_add_squares8<MODE>(f, inv_d, hs, ls);
   }
-  float hi = hs[0], lo = ls[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) {
-    float sum, e;
-    two_sum(hi, hs[j], sum, e);
-    lo = __fadd_rn(__fadd_rn(lo, ls[j]), e);
-    hi = sum;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    float sum, e;
-    two_sum(hi, h2, sum, e);
-    lo = __fadd_rn(__fadd_rn(lo, l2), e);
-    hi = sum;
-  }
-  const float ss = __fadd_rn(hi, lo);
-  const float rstd = (MODE == 0)
-                         ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, inv_d), eps)))
-                         : __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ss, eps)));
+  const float rstd = rstd_of_sum<MODE>(ff_warp_total(hs, ls), inv_d, eps);
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {

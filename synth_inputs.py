@@ -26,6 +26,12 @@ Workload recipes (shapes and distributions of the five projection cases):
              on [-127,127], w_scale[4096] fp32 ~U(1e-3,1e-2), eps 1e-6.
 * ``skinny`` x[16384,28672] ~N(0,1), no gamma, W[24,28672] ~N(0,0.02),
              eps 1e-6, rsqrt form, fp32 out (mhc_pre-style).
+* ``mxfp8``  x[4096,4096] ~N(0,1), gamma ~U(0.5,1.5), an MXFP8 weight [6144,4096]
+             drawn directly as bytes: E4M3 codes with uniform sign, exponent
+             field uniform on [10, 15] and mantissa uniform (the NaN pattern
+             replaced by the largest finite magnitude), E8M0 scale bytes
+             uniform on [113, 114] per block of 64 (|w| mostly 2^-10 .. 0.05),
+             eps 1e-6, rsqrt form, bf16 out.
 """
 from __future__ import annotations
 
@@ -56,6 +62,9 @@ CONFIGS = {
     "qmrs": dict(B=4, M=2048, K=4096, N=4096, seed=1005),
     # the qkv projection followed by the QKV split + per-head RMSNorm + RoPE
     # stage (Qwen3 layout: 32 query heads and 8 key/value heads of 128)
+    # the qkv projection shape in MXFP8 mode (one E8M0 scale per 64 elements)
+    "mxfp8": dict(T=4096, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
+                  out_dtype="bf16", block=64, seed=1006),
     "qkv_rope": dict(T=4096, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
                      out_dtype="bf16", seed=1001, n_q_heads=32, n_kv_heads=8, head_dim=128,
                      head_eps=1e-6, max_pos=4096, rope_base=1.0e6),
@@ -182,6 +191,42 @@ def uniform_int8(seed: int, name: str, shape, lo: int = -127, hi: int = 127, row
     return _chunked(fn, r, cols, np.int8)
 
 
+def uniform_u8(seed: int, name: str, shape, lo: int, hi: int, rows=None) -> np.ndarray:
+    """Integers uniform on [lo, hi] as uint8."""
+    shape = tuple(shape)
+    nrows, cols = shape
+    r = _rows_arg(nrows, rows)
+    key = _key(seed, name)
+    span = hi - lo + 1
+
+    def fn(rb):
+        u = _unit(key, _flat_index(rb, cols))
+        return (np.floor(u * span).astype(np.int64) + lo).clip(lo, hi).astype(np.uint8)
+
+    return _chunked(fn, r, cols, np.uint8)
+
+
+def e4m3_codes(seed: int, name: str, shape, e_lo: int = 10, rows=None) -> np.ndarray:
+    """E4M3FN bytes drawn field by field: sign uniform, exponent field uniform
+    on [e_lo, 15], mantissa uniform on [0, 7]; the NaN pattern (exponent 15,
+    mantissa 7) becomes mantissa 6 (the largest finite magnitude)."""
+    shape = tuple(shape)
+    nrows, cols = shape
+    r = _rows_arg(nrows, rows)
+    key = _key(seed, name)
+    span = np.uint64(16 - e_lo)
+
+    def fn(rb):
+        b = _bits(key, _flat_index(rb, cols))
+        sign = (b & np.uint64(1)).astype(np.uint8)
+        mant = ((b >> np.uint64(1)) & np.uint64(7)).astype(np.uint8)
+        e = ((b >> np.uint64(4)) % span).astype(np.uint8) + np.uint8(e_lo)
+        mant = np.where((e == 15) & (mant == 7), np.uint8(6), mant)
+        return (sign << np.uint8(7)) | (e << np.uint8(3)) | mant
+
+    return _chunked(fn, r, cols, np.uint8)
+
+
 # ---------------------------------------------------------------------------
 # The five workloads.  Each returns a dict of numpy arrays; ``rows`` (optional)
 # restricts the activation to a subset of its rows (weights are always full).
@@ -217,6 +262,18 @@ def make_w8a8(cfg: dict, rows=None, with_x: bool = True) -> dict:
     d["gamma"] = uniform_bf16(s, "gamma", (K,), 0.5, 1.5)
     d["Wq"] = uniform_int8(s, "Wq", (N, K), -127, 127)
     d["w_scale"] = uniform_f32(s, "w_scale", (N,), 1e-3, 1e-2)
+    return d
+
+
+def make_mxfp8(cfg: dict, rows=None, with_x: bool = True) -> dict:
+    """x, gamma and the MXFP8 weight (codes [N, K], scale bytes [N, K/block])."""
+    s, T, K, N, blk = cfg["seed"], cfg["T"], cfg["K"], cfg["N"], cfg.get("block", 64)
+    d = {}
+    if with_x:
+        d["x"] = normal_bf16(s, "x", (T, K), 1.0, rows=rows)
+    d["gamma"] = uniform_bf16(s, "gamma", (K,), 0.5, 1.5) if cfg.get("has_gamma", True) else None
+    d["w_codes"] = e4m3_codes(s, "w_codes", (N, K))
+    d["w_scale"] = uniform_u8(s, "w_scale", (N, K // blk), 113, 114)
     return d
 
 

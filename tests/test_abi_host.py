@@ -28,7 +28,7 @@ def header_functions():
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", src)
     keywords = {"typedef", "enum", "struct", "sizeof", "defined"}
-    prefixes = ("rnl_", "rmsnorm_linear_", "mla_", "quant_")
+    prefixes = ("rnl_", "rmsnorm_linear_", "mla_", "quant_", "mxfp8_")
     return sorted({n for n in names if n not in keywords and n.startswith(prefixes)})
 
 
@@ -107,6 +107,21 @@ CHILD = textwrap.dedent("""
     r["qmrs_no_device"] = qm(A, A, A, A, 2, 4, 32, 32, A, ws, 1 << 30, None)
     r["ws_qmrs"] = lib.rnl_workspace_size(5, 2048, 4096, 4096, 4)
     r["ws_qmrs_b1"] = lib.rnl_workspace_size(5, 2048, 4096, 4096, 1)
+    mx = lib.rmsnorm_linear_mxfp8
+    #     x, gamma, w_codes, w_scale, T, K, N, eps, mode, block, out, out_dtype, codes, scales, ws, bytes, stream
+    r["mx_bad_block"] = mx(A, None, A, A, 4, 128, 8, 1e-6, 0, 48, A, 0, None, None, ws, 1 << 30, None)
+    r["mx_K_not_mult_block"] = mx(A, None, A, A, 4, 96, 8, 1e-6, 0, 64, A, 0, None, None, ws, 1 << 30, None)
+    r["mx_bad_dtype"] = mx(A, None, A, A, 4, 128, 8, 1e-6, 0, 64, A, 2, None, None, ws, 1 << 30, None)
+    r["mx_null_scale"] = mx(A, None, A, None, 4, 128, 8, 1e-6, 0, 64, A, 0, None, None, ws, 1 << 30, None)
+    r["mx_misaligned_codes_out"] = mx(A, None, A, A, 4, 128, 8, 1e-6, 0, 64, A, 0, B, None, ws, 1 << 30, None)
+    r["mx_small_ws"] = mx(A, None, A, A, 4, 128, 8, 1e-6, 0, 64, A, 0, None, None, ws, 64, None)
+    r["mx_T0"] = mx(None, None, None, None, 0, 128, 8, 1e-6, 0, 64, None, 0, None, None, None, 0, None)
+    r["mx_no_device"] = mx(A, A, A, A, 4, 128, 8, 1e-6, 0, 32, A, 1, A, A, ws, 1 << 30, None)
+    sm = lib.mxfp8_scaled_mm
+    r["mxmm_null_x_scale"] = sm(A, None, A, A, 4, 128, 8, 64, A, 0, ws, 1 << 30, None)
+    r["mxmm_bad_block"] = sm(A, A, A, A, 4, 128, 8, 16, A, 0, ws, 1 << 30, None)
+    r["mxmm_no_device"] = sm(A, A, A, A, 4, 128, 8, 64, A, 1, ws, 1 << 30, None)
+    r["ws_mxfp8"] = lib.rnl_workspace_size(6, 4096, 4096, 6144, 0)
     pp = ctypes.c_void_p(None)
     r["pipe_null_out"] = lib.rnl_pipeline_create(0, 4, 64, 8, 0, None)
     r["pipe_bad_op"] = lib.rnl_pipeline_create(3, 4, 64, 8, 0, ctypes.byref(pp))
@@ -154,6 +169,8 @@ def test_workspace_sizes(host_results):
     # QuantMatMulReduceSum: widened x1 and x2, fp32 x2_scale, fp32 batch sum
     assert r["ws_qmrs"] == 4 * 2048 * 4096 * 2 + 4 * 4096 * 4096 * 2 + 4096 * 4 + 2048 * 4096 * 4
     assert r["ws_qmrs_b1"] == 2048 * 4096 * 2 + 4096 * 4096 * 2 + 4096 * 4  # no running sum
+    # MXFP8: dequantised bf16 activations and weight, GEMM partials
+    assert r["ws_mxfp8"] == 4096 * 4096 * 2 + 6144 * 4096 * 2 + part
     max_size = (1 << 64) - 1
     assert r["ws_bad_op"] == max_size and r["ws_neg"] == max_size
 
@@ -174,6 +191,9 @@ def test_workspace_sizes(host_results):
     ("ex_in_place_no_device", DEVICE),
     ("qmrs_N_not_mult16", ALIGN), ("qmrs_B0", SHAPE), ("qmrs_M0", OK), ("qmrs_null_scale", NULL),
     ("qmrs_small_ws", WORKSPACE), ("qmrs_no_device", DEVICE),
+    ("mx_bad_block", ARG), ("mx_K_not_mult_block", SHAPE), ("mx_bad_dtype", ARG), ("mx_null_scale", NULL),
+    ("mx_misaligned_codes_out", ALIGN), ("mx_small_ws", WORKSPACE), ("mx_T0", OK), ("mx_no_device", DEVICE),
+    ("mxmm_null_x_scale", NULL), ("mxmm_bad_block", ARG), ("mxmm_no_device", DEVICE),
     ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
     ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
     ("pipe_submit_null", NULL), ("pipe_submit_null_W", NULL), ("pipe_submit_bad_eps", ARG),
@@ -186,3 +206,14 @@ def test_argument_checks(host_results, key, want):
 def test_status_strings(host_results):
     s = host_results["status_strings"]
     assert s[0] == "ok" and len(set(s)) == 10
+
+
+def test_binding_status_checks_are_well_formed():
+    """Every status check in the binding names its call (static scan, no GPU)."""
+    import ast
+    src = open(os.path.join(ROOT, "rmsnorm_linear_projection_gb300", "_native.py")).read()
+    calls = [n for n in ast.walk(ast.parse(src))
+             if isinstance(n, ast.Call) and getattr(n.func, "id", None) == "_check"]
+    assert len(calls) >= 15
+    bad = [n.lineno for n in calls if len(n.args) != 2 or isinstance(n.args[1], ast.Tuple)]
+    assert not bad, f"_check calls with the wrong arguments at lines {bad}"
