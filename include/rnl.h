@@ -253,8 +253,8 @@ rnl_status rmsnorm_linear_w8a8(const void *x, const void *gamma, const int8_t *W
  * saturated to +-448.  Codes and scales are exact functions of x, gamma and
  * eps (the FP32 sum of squares is the rounding of the exact sum).  The
  * product is accumulated in FP32 on the tensor cores from the exactly
- * dequantised operands.  K % block == 0; x, gamma, w_codes, out 16-byte
- * aligned.  Workspace: rnl_workspace_size(RNL_OP_MXFP8, T, K, N, 0) bytes.
+ * dequantised operands.  K % block == 0, T * K and N * K below 2^36
+ * (else RNL_ERR_SHAPE); x, gamma, w_codes, out 16-byte aligned.  Workspace: rnl_workspace_size(RNL_OP_MXFP8, T, K, N, 0) bytes.
  * Non-finite inputs and weights whose dequantised values exceed the bf16
  * range give unspecified (but memory-safe) results.
  */

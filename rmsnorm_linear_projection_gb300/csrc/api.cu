@@ -153,6 +153,11 @@ QmrsLayout qmrs_layout(void* ws, int64_t B, int64_t M, int64_t K, int64_t N) {
   return l;
 }
 
+// The MXFP8 kernels index 16-code vectors of either operand in 32 bits.
+inline bool mx_too_large(int64_t T, int64_t K, int64_t N) {
+  return T * K / 16 >= (int64_t{1} << 32) || N * K / 16 >= (int64_t{1} << 32);
+}
+
 struct MxLayout {
   void* A = nullptr;   // bf16 [T, K] dequantised activations
   void* Wb = nullptr;  // bf16 [N, K] dequantised weight
@@ -614,7 +619,7 @@ rnl_status rmsnorm_linear_mxfp8(const void* x, const void* gamma, const uint8_t*
   if (bad_mode(norm_mode) || bad_eps(eps) || !mx_block_ok(block) ||
       (out_dtype != RNL_OUT_BF16 && out_dtype != RNL_OUT_FP32))
     return RNL_ERR_ARG;
-  if (K % block != 0) return RNL_ERR_SHAPE;
+  if (K % block != 0 || mx_too_large(T, K, N)) return RNL_ERR_SHAPE;
   if (T == 0) return RNL_OK;
   if (!x || !w_codes || !w_scale || !out) return RNL_ERR_NULL;
   if (!aligned16(x) || !aligned16(w_codes) || !aligned16(out) || (gamma && !aligned16(gamma)) ||
@@ -640,7 +645,7 @@ rnl_status mxfp8_scaled_mm(const uint8_t* x_codes, const uint8_t* x_scale, const
   if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
   if (!mx_block_ok(block) || (out_dtype != RNL_OUT_BF16 && out_dtype != RNL_OUT_FP32))
     return RNL_ERR_ARG;
-  if (K % block != 0) return RNL_ERR_SHAPE;
+  if (K % block != 0 || mx_too_large(T, K, N)) return RNL_ERR_SHAPE;
   if (T == 0) return RNL_OK;
   if (!x_codes || !x_scale || !w_codes || !w_scale || !out) return RNL_ERR_NULL;
   if (!aligned16(x_codes) || !aligned16(w_codes) || !aligned16(out) ||

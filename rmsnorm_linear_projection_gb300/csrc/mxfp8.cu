@@ -136,7 +136,9 @@ __device__ __forceinline__ void load_y(const uint4& u, const uint4* gamma, int v
 }
 
 // One token row.  VPL > 0: the row's vectors stay in registers (K <= 256 *
-// VPL); VPL == 0: any K, x read twice (the sum of squares, then the blocks).
+// VPL); VPL == 0: any K, x read twice (the sum of squares, then the blocks;
+// the second read mostly hits L2), each pass with several 16-byte loads in
+// flight per lane.
 template <int MODE, int VPL, int BLK>
 __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
   const int lane = threadIdx.x & 31;
@@ -162,7 +164,19 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
       ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
     }
   } else {
-    for (int v = lane; v < p.nvec; v += 32) {
+    int v = lane;
+    for (; v + 96 < p.nvec; v += 128) {
+      uint4 w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = __ldg(xr + v + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float f[8];
+        unpack8(w[j], f);
+        ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
+      }
+    }
+    for (; v < p.nvec; v += 32) {
       float f[8];
       unpack8(__ldg(xr + v), f);
       ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
@@ -184,12 +198,22 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
       quant_vec<BLK>(f, live, ar + v, qr ? qr + v : nullptr, sr ? sr + v / (BLK / 8) : nullptr);
     }
   } else {
-    for (int i = 0; i < iters; ++i) {
-      const int v = lane + 32 * i;
-      const bool live = v < p.nvec;
-      float f[8];
-      load_y(live ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u), live ? p.gamma : nullptr, v, rstd, f);
-      quant_vec<BLK>(f, live, ar + v, qr ? qr + v : nullptr, sr ? sr + v / (BLK / 8) : nullptr);
+    for (int i = 0; i < iters; i += 2) {  // two vectors per lane in flight
+      uint4 w[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int v = lane + 32 * (i + j);
+        w[j] = (i + j < iters && v < p.nvec) ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (i + j >= iters) break;  // warp-uniform
+        const int v = lane + 32 * (i + j);
+        const bool live = v < p.nvec;
+        float f[8];
+        load_y(w[j], live ? p.gamma : nullptr, v, rstd, f);
+        quant_vec<BLK>(f, live, ar + v, qr ? qr + v : nullptr, sr ? sr + v / (BLK / 8) : nullptr);
+      }
     }
   }
 }
@@ -210,10 +234,13 @@ __device__ __forceinline__ void mx_dequant_block(unsigned block, const uint4* __
     sc[i] = 0.f;
     if (v < nvec16) {
       u[i] = __ldg(src + v);
-      const int64_t n = v / k_vec16;
-      const int64_t k = (v - n * k_vec16) * 16;
-      const int nb = k_vec16 * 16 / BLK;
-      const int s = __ldg(scales + n * nb + k / BLK);
+      // row and column of the vector (32-bit division: nvec16 < 2^32 is
+      // checked on the host)
+      const uint32_t vv = static_cast<uint32_t>(v);
+      const uint32_t n = vv / static_cast<uint32_t>(k_vec16);
+      const uint32_t kv = vv - n * static_cast<uint32_t>(k_vec16);
+      const int64_t nb = static_cast<int64_t>(k_vec16) * 16 / BLK;
+      const int s = __ldg(scales + n * nb + kv * 16 / BLK);
       sc[i] = s == 255 ? __uint_as_float(0x7FC00000u) : pow2f(s - 127);
     }
   }
@@ -239,7 +266,7 @@ __device__ __forceinline__ void mx_dequant_block(unsigned block, const uint4* __
 // dequantising the weight (HBM bound) share no data, so their blocks are
 // interleaved (even / odd while both last) and run side by side on every SM.
 template <int MODE, int VPL, int BLK>
-__global__ void __launch_bounds__(kWarps * 32, 2) mx_front_kernel(MxRows p) {
+__global__ void __launch_bounds__(kWarps * 32, 4) mx_front_kernel(MxRows p) {
   const unsigned b = blockIdx.x;
   const unsigned both = p.quant_blocks < p.dq_blocks ? p.quant_blocks : p.dq_blocks;
   bool quant;
@@ -273,12 +300,11 @@ __global__ void __launch_bounds__(256)
 template <int MODE, int BLK>
 void front_vpl(int vpl, unsigned grid, const MxRows& p, cudaStream_t s) {
   constexpr unsigned kT = kWarps * 32;
+  // at most 64 registers a thread (four blocks of 256 threads per SM): the
+  // weight's dequantisation is latency bound and wants the warps; rows
+  // longer than 1024 take the two-read form
   if (vpl <= 4)
     mx_front_kernel<MODE, 4, BLK><<<grid, kT, 0, s>>>(p);
-  else if (vpl <= 8)
-    mx_front_kernel<MODE, 8, BLK><<<grid, kT, 0, s>>>(p);
-  else if (vpl <= 16)
-    mx_front_kernel<MODE, 16, BLK><<<grid, kT, 0, s>>>(p);
   else
     mx_front_kernel<MODE, 0, BLK><<<grid, kT, 0, s>>>(p);
 }

@@ -117,6 +117,7 @@ CHILD = textwrap.dedent("""
     r["mx_small_ws"] = mx(A, None, A, A, 4, 128, 8, 1e-6, 0, 64, A, 0, None, None, ws, 64, None)
     r["mx_T0"] = mx(None, None, None, None, 0, 128, 8, 1e-6, 0, 64, None, 0, None, None, None, 0, None)
     r["mx_no_device"] = mx(A, A, A, A, 4, 128, 8, 1e-6, 0, 32, A, 1, A, A, ws, 1 << 30, None)
+    r["mx_too_large"] = mx(A, None, A, A, 4, 1 << 20, 1 << 17, 1e-6, 0, 64, A, 0, None, None, ws, 1 << 30, None)
     sm = lib.mxfp8_scaled_mm
     r["mxmm_null_x_scale"] = sm(A, None, A, A, 4, 128, 8, 64, A, 0, ws, 1 << 30, None)
     r["mxmm_bad_block"] = sm(A, A, A, A, 4, 128, 8, 16, A, 0, ws, 1 << 30, None)
@@ -192,7 +193,7 @@ def test_workspace_sizes(host_results):
     ("qmrs_N_not_mult16", ALIGN), ("qmrs_B0", SHAPE), ("qmrs_M0", OK), ("qmrs_null_scale", NULL),
     ("qmrs_small_ws", WORKSPACE), ("qmrs_no_device", DEVICE),
     ("mx_bad_block", ARG), ("mx_K_not_mult_block", SHAPE), ("mx_bad_dtype", ARG), ("mx_null_scale", NULL),
-    ("mx_misaligned_codes_out", ALIGN), ("mx_small_ws", WORKSPACE), ("mx_T0", OK), ("mx_no_device", DEVICE),
+    ("mx_misaligned_codes_out", ALIGN), ("mx_small_ws", WORKSPACE), ("mx_T0", OK), ("mx_too_large", SHAPE), ("mx_no_device", DEVICE),
     ("mxmm_null_x_scale", NULL), ("mxmm_bad_block", ARG), ("mxmm_no_device", DEVICE),
     ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
     ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
