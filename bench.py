@@ -56,12 +56,12 @@ TRAFFIC = {
     # gemm_pair_kernel<0,256>: 98.13 MB read + 39.87 MB written
     # (profiles/qkv_step_kernels_4096x6144x4096.md)
     "qkv": 138.00e6,
-    # both MLA GEMM stages: 59.92 MB + 155.11 MB
-    # (profiles/mla_gemm_stages_2048x7168x1536x24576.md)
-    "mla": 215.03e6,
     # gemm_kernel<2,256,0>: 125.17 MB read + 46.38 MB written
     # (profiles/w8a8_front_and_int_gemm_8192x4096x4096.md)
     "w8a8": 171.55e6,
+    # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.24 MB read + 39.96 MB written
+    # (profiles/mxfp8_front_and_gemm_4096x4096x6144.md)
+    "mxfp8": 137.20e6,
     # skinny_kernel<32,0>: 123.03 MB at T = 2048, scaled by rows to T = 16384
     # (profiles/skinny_stream_mhc_pre.md)
     "skinny": 984.2e6,
