@@ -65,6 +65,7 @@ def _declare(lib):
         "orc_rmsnorm_linear_ex": (C, [P, P, P, P, P, P, I64, I64, I64, D, C, P, P, P, P]),
         "orc_qkv_rope": (C, [P, I64, I64, I64, I64, P, P, D, P, P, I64, P, P, P]),
         "orc_quant_matmul_reduce_sum": (C, [P, P, P, P, I64, I64, I64, I64, P, P]),
+        "orc_head_rmsnorm": (C, [P, I64, I64, I64, P, D, C, P]),
         "orc_e4m3_value": (D, [ctypes.c_uint8]),
         "orc_e4m3_rne_sat": (ctypes.c_uint8, [D]),
         "orc_e8m0_value": (D, [ctypes.c_uint8]),
@@ -241,6 +242,16 @@ class Oracle:
         return ref, out
 
     # -- MLA q chain ----------------------------------------------------------
+    def head_rmsnorm(self, y, H, D, gamma, eps, variant):
+        """Per-head RMSNorm of y (bf16 bits [T, H*D]): bf16 bits [T, H*D]."""
+        y = _c(y, np.uint16)
+        T = y.shape[0]
+        assert y.shape[1] == H * D
+        out = np.empty((T, H * D), np.uint16)
+        _check(self.lib.orc_head_rmsnorm(_ptr(y), T, H, D, _ptr(_c(gamma, np.uint16)), float(eps),
+                                         int(variant), _ptr(out)), "head_rmsnorm")
+        return out
+
     def mla_q_chain(self, x, W_qa, gamma_cq, W_qb, eps, variant):
         """Returns (qa, ref, out)."""
         x, W_qa, W_qb = _c(x, np.uint16), _c(W_qa, np.uint16), _c(W_qb, np.uint16)

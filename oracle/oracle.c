@@ -701,6 +701,37 @@ int orc_mla_q_chain(const uint16_t *x, const uint16_t *W_qa, const uint16_t *gam
 }
 
 /* ------------------------------------------------------------------------ */
+/* Per-head RMSNorm after a projection.  [AT10] sec. 9 (the golden chain of */
+/* the MLA prolog test): q_b_proj is reshaped to [num_heads, head_dim] and  */
+/* normalised again, each head row on its own; the rms_norm_new helper of   */
+/* that test has no gamma (an optional gamma [D] is accepted here).  Each   */
+/* head row of D values of the bf16 input y [T, H*D] gets the row norm of   */
+/* the chosen variant in binary64, (y * rstd) * gamma, cast to bf16.        */
+/* ------------------------------------------------------------------------ */
+
+int orc_head_rmsnorm(const uint16_t *y, int64_t T, int64_t H, int64_t D, const uint16_t *gamma,
+                     double eps, int variant, uint16_t *out)
+{
+    if (!y || !out || T < 0 || H <= 0 || D <= 0 || (variant != 0 && variant != 1))
+        return ORC_EARG;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t h = 0; h < H; ++h) {
+            const uint16_t *yh = y + (t * H + h) * D;
+            uint16_t *oh = out + (t * H + h) * D;
+            const double r = row_rstd_f64(yh, D, eps, variant);
+            for (int64_t i = 0; i < D; ++i) {
+                double v = orc_bf16_value(yh[i]) * r;
+                if (gamma)
+                    v = v * orc_bf16_value(gamma[i]);
+                oh[i] = orc_bf16_rne(v);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* W8A8 front end: AT-03 RMSNorm then AT-05 per-token symmetric INT8 quant,  */
 /* in binary32, the pages' order.  [AT10] sec. 3 (norm steps), sec. 4       */
 /* (AT-05: amax = max|y|, multiplier 127/amax, rounding + saturating casts), */

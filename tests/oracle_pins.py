@@ -1109,7 +1109,78 @@ def pin_mxfp8_composition(orc):
     assert np.abs(ref - full).max() < 0.1 * np.abs(full).max()
 
 
+# ---------------------------------------------------------------------------
+# Per-head RMSNorm after a projection (the MLA chain's norm after q_b_proj)
+# ---------------------------------------------------------------------------
+
+def pin_head_norm_constant_heads(orc):
+    # every head constant (a different value per head), eps = 0: each head
+    # normalises to sign(c) * gamma exactly, whatever the other heads hold
+    rng = _rng(70)
+    T, H, D = 3, 5, 64
+    c = _bf16_bits_of_f32((rng.uniform(0.1, 50, (T, H)) * rng.choice([-1, 1], (T, H))).astype(np.float32))
+    y = np.repeat(c[:, :, None], D, axis=2).reshape(T, H * D)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    for variant in (0, 1):
+        out = orc.head_rmsnorm(y, H, D, g, 0.0, variant).reshape(T, H, D)
+        want = np.where(bf16_bits_to_f64(c)[:, :, None] < 0, g | np.uint16(0x8000), g)
+        assert np.array_equal(out, np.broadcast_to(want, (T, H, D)))
+        no_g = orc.head_rmsnorm(y, H, D, None, 0.0, variant).reshape(T, H, D)
+        assert np.array_equal(no_g, np.where(bf16_bits_to_f64(c)[:, :, None] < 0, 0xBF80, 0x3F80).astype(np.uint16)
+                              .repeat(D, axis=2))
+
+
+def pin_head_norm_torch(orc):
+    import torch
+    rng = _rng(71)
+    T, H, D = 6, 7, 96
+    y = _rand_bf16(rng, (T, H * D), 2.0)
+    y[2, 3 * D:4 * D] = _rand_bf16(rng, (D,), 1e-3)  # a quiet head beside loud ones
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    for eps in (1e-6, 0.5):
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(bf16_bits_to_f64(y).reshape(T, H, D)), (D,),
+                                           torch.from_numpy(bf16_bits_to_f64(g)), eps).numpy()
+        for variant in (0, 1):
+            out = orc.head_rmsnorm(y, H, D, g, eps, variant).reshape(T, H, D)
+            for idx in np.ndindex(T, H, D):
+                bits, near = exact.bf16_round_exact(Fraction(float(ref[idx])))
+                assert near or int(out[idx]) == bits, (eps, variant, idx)
+
+
+def pin_head_norm_scale_invariance(orc):
+    # eps = 0: scaling each head by its own power of two changes nothing
+    rng = _rng(72)
+    T, H, D = 4, 6, 32
+    y = _rand_bf16(rng, (T, H * D))
+    s = np.ldexp(1.0, rng.integers(-6, 7, (T, H))).repeat(D, axis=1)
+    ys = _bf16_bits_of_f32((bf16_bits_to_f64(y) * s).astype(np.float32))
+    for variant in (0, 1):
+        assert np.array_equal(orc.head_rmsnorm(y, H, D, None, 0.0, variant),
+                              orc.head_rmsnorm(ys, H, D, None, 0.0, variant))
+
+
+def pin_head_norm_exact_small(orc):
+    rng = _rng(73)
+    T, H, D = 2, 3, 4
+    y = _rand_bf16(rng, (T, H * D))
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    eps = 0.25
+    for variant in (0, 1):
+        out = orc.head_rmsnorm(y, H, D, g, eps, variant)
+        for t in range(T):
+            for h in range(H):
+                v = [Fraction(exact.bf16_value(int(b))) for b in y[t, h * D:(h + 1) * D]]
+                r = exact.dec_sqrt_recip(sum(a * a for a in v) / D + Fraction(eps))
+                for i in range(D):
+                    bits, near = exact.bf16_round_exact(v[i] * r * Fraction(exact.bf16_value(int(g[i]))))
+                    assert near or int(out[t, h * D + i]) == bits
+
+
 ALL_PINS = [
+    pin_head_norm_constant_heads,
+    pin_head_norm_torch,
+    pin_head_norm_scale_invariance,
+    pin_head_norm_exact_small,
     pin_e4m3_codec,
     pin_e8m0_scale,
     pin_mxfp8_constructed_ties,

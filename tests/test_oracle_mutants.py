@@ -86,6 +86,14 @@ MUTANTS = [
      "((uint16_t *)out)[t * N + n] = orc_bf16_rne(acc);"),
     ("mx_scale_byte_bias", "scales[t * (K / block) + b0 / block] = (uint8_t)(X + 127);",
      "scales[t * (K / block) + b0 / block] = (uint8_t)(X + 128);"),
+    # per-head RMSNorm
+    ("head_norm_over_whole_row", "const double r = row_rstd_f64(yh, D, eps, variant);",
+     "const double r = row_rstd_f64(y + t * H * D, H * D, eps, variant);"),
+    ("head_norm_drops_eps", "const double r = row_rstd_f64(yh, D, eps, variant);",
+     "const double r = row_rstd_f64(yh, D, 0.0, variant);"),
+    ("head_norm_drops_gamma", "                if (gamma)\n                    v = v * orc_bf16_value(gamma[i]);\n                oh[i]",
+     "                oh[i]"),
+    ("head_norm_head_stride", "const uint16_t *yh = y + (t * H + h) * D;", "const uint16_t *yh = y + (t * H + h % 2) * D;"),
     ("rope_split_off_by_one_head", "            if (h < Hq) {\n                dst = q + (t * Hq + h) * D;",
      "            if (h <= Hq && h < Hq + Hkv) {\n                dst = q + (t * Hq + (h < Hq ? h : 0)) * D;"),
 ]
