@@ -236,6 +236,36 @@ rnl_status rmsnorm_linear_w8a8(const void *x, const void *gamma, const int8_t *W
                                void *workspace, size_t workspace_bytes, rnl_stream_t stream);
 
 /*
+ * Per-head RMSNorm of a projection output (AT-10 pattern page, sec. 9: the
+ * MLA prolog's golden chain reshapes q_b_proj to [num_heads, head_dim] and
+ * normalises it again, each head row on its own).
+ *   y      bf16 [T, n_heads * head_dim]
+ *   gamma  bf16 [head_dim] or NULL (the page's helper for this norm has none)
+ *   out    bf16 [T, n_heads * head_dim]; may be y itself (in place), must not
+ *          overlap it otherwise (RNL_ERR_ARG)
+ *   per head: rstd as norm_mode (FP32), out = bf16((y * rstd) * gamma)
+ * head_dim a multiple of 64 in [64, 512] (else RNL_ERR_UNSUPPORTED); y, out,
+ * gamma 16-byte aligned.  No workspace.
+ */
+rnl_status rnl_head_rmsnorm(const void *y, int64_t T, int64_t n_heads, int64_t head_dim,
+                            const void *gamma, float eps, int norm_mode, void *out,
+                            rnl_stream_t stream);
+
+/*
+ * mla_q_chain followed by rnl_head_rmsnorm on its output, in place: the MLA
+ * q chain up to the per-head norm after q_b (the same page passage).  The
+ * head norm uses the chain's norm_mode (the page's chain uses the sqrt+div
+ * form for both norms), head_eps and head_gamma (bf16 [head_dim] or NULL);
+ * N2 % head_dim == 0.  Arguments and workspace otherwise as mla_q_chain
+ * (rnl_workspace_size(RNL_OP_MLA, ...)).
+ */
+rnl_status mla_q_chain_head_norm(const void *x, const void *W_qa, const void *gamma_cq,
+                                 const void *W_qb, int64_t T, int64_t K, int64_t N1, int64_t N2,
+                                 float eps, int norm_mode, int64_t head_dim, const void *head_gamma,
+                                 float head_eps, void *out, void *qa_out, void *workspace,
+                                 size_t workspace_bytes, rnl_stream_t stream);
+
+/*
  * AT-11 in MXFP8 mode: RMSNorm, MX quantisation of the normed rows, and
  * scaled_mm(x_fp8, w_fp8, FP32, x_scale, w_scale) against an MXFP8 weight
  * (AT-10 pattern page, sec. 4, AT-09 quant_mode mxfp8; SK-14 skeleton page,

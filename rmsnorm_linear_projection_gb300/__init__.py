@@ -9,6 +9,8 @@ arguments; the computation runs in the library's CUDA kernels.
                           projection bias
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
+    mla_q_chain_head_norm / rnl_head_rmsnorm
+                          the same chain with the per-head RMSNorm after q_b, and that norm alone
     rnl_gemm_s8s8s32      the exact INT8 matmul on its own
     quant_matmul_reduce_sum  QuantMatMulReduceSum: batched exact INT8 matmul, FP32
                           dequant and sum over the batch
@@ -36,6 +38,7 @@ from ._native import (  # noqa: F401
     RnlError,
     load,
     mla_q_chain,
+    mla_q_chain_head_norm,
     mxfp8_scaled_mm,
     quant_matmul_reduce_sum,
     rmsnorm_linear_bf16,
@@ -46,6 +49,7 @@ from ._native import (  # noqa: F401
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
     rnl_gemm_s8s8s32,
+    rnl_head_rmsnorm,
     rnl_pipeline_create,
     rnl_pipeline_destroy,
     rnl_pipeline_submit_bf16,

@@ -35,7 +35,7 @@ EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_li
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
            "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex", "rnl_qkv_rope",
            "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum", "rmsnorm_linear_mxfp8",
-           "mxfp8_scaled_mm")
+           "mxfp8_scaled_mm", "rnl_head_rmsnorm", "mla_q_chain_head_norm")
 
 
 class RnlError(RuntimeError):
@@ -74,6 +74,8 @@ def _declare(lib):
         "quant_matmul_reduce_sum": (I, [P, P, P, P, I64, I64, I64, I64, P, P, SZ, P]),
         "rmsnorm_linear_mxfp8": (I, [P, P, P, P, I64, I64, I64, F, I, I64, P, I, P, P, P, SZ, P]),
         "mxfp8_scaled_mm": (I, [P, P, P, P, I64, I64, I64, I64, P, I, P, SZ, P]),
+        "rnl_head_rmsnorm": (I, [P, I64, I64, I64, P, F, I, P, P]),
+        "mla_q_chain_head_norm": (I, [P, P, P, P, I64, I64, I64, I64, F, I, I64, P, F, P, P, P, SZ, P]),
         "rmsnorm_linear_qkv_rope": (I, [P, P, P, I64, I64, I64, I64, I64, F, I, P, P, F, P, P, I64,
                                         P, P, P, P, SZ, P]),
     }
@@ -350,6 +352,50 @@ def mxfp8_scaled_mm(x_codes, x_scale, w_codes, w_scale, block=64, out=None, out_
                                   int(block), _ptr(out), int(out_dtype), _ptr(ws),
                                   ws.numel() * ws.element_size(), _stream(dev, stream)),
            "mxfp8_scaled_mm")
+    return out
+
+
+def rnl_head_rmsnorm(y, n_heads, head_dim, gamma=None, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
+                     stream=None):
+    """Per-head RMSNorm of y [T, n_heads * head_dim] (bf16); out may be y (in place)."""
+    T = y.shape[0]
+    dev = y.device
+    _need(y, "y", torch.bfloat16, (T, n_heads * head_dim), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (head_dim,), dev)
+    if out is None:
+        out = torch.empty_like(y)
+    _need(out, "out", torch.bfloat16, (T, n_heads * head_dim), dev)
+    _check(load().rnl_head_rmsnorm(_ptr(y), T, n_heads, head_dim, _ptr(gamma), float(eps), int(norm_mode),
+                                   _ptr(out), _stream(dev, stream)),
+           "rnl_head_rmsnorm")
+    return out
+
+
+def mla_q_chain_head_norm(x, W_qa, gamma_cq, W_qb, head_dim, head_gamma=None, eps=1e-6,
+                          norm_mode=NORM_SQRT_DIV, head_eps=1e-6, out=None, qa_out=None,
+                          workspace=None, stream=None):
+    """MLA q chain, then the per-head RMSNorm of its output (in place)."""
+    T, K = x.shape
+    N1, N2 = W_qa.shape[0], W_qb.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(W_qa, "W_qa", torch.bfloat16, (N1, K), dev)
+    _need(gamma_cq, "gamma_cq", torch.bfloat16, (N1,), dev)
+    _need(W_qb, "W_qb", torch.bfloat16, (N2, N1), dev)
+    if head_gamma is not None:
+        _need(head_gamma, "head_gamma", torch.bfloat16, (head_dim,), dev)
+    if out is None:
+        out = torch.empty((T, N2), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, N2), dev)
+    if qa_out is not None:
+        _need(qa_out, "qa_out", torch.bfloat16, (T, N1), dev)
+    ws = _workspace(workspace_size(OP_MLA, T, K, N1, N2), dev, workspace)
+    _check(load().mla_q_chain_head_norm(_ptr(x), _ptr(W_qa), _ptr(gamma_cq), _ptr(W_qb), T, K, N1, N2,
+                                        float(eps), int(norm_mode), int(head_dim), _ptr(head_gamma),
+                                        float(head_eps), _ptr(out), _ptr(qa_out), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(dev, stream)),
+           "mla_q_chain_head_norm")
     return out
 
 

@@ -723,6 +723,42 @@ rnl_status mla_q_chain(const void* x, const void* W_qa, const void* gamma_cq, co
   return launch_gemm(g2, s);
 }
 
+rnl_status rnl_head_rmsnorm(const void* y, int64_t T, int64_t n_heads, int64_t head_dim,
+                            const void* gamma, float eps, int norm_mode, void* out,
+                            rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(n_heads) || bad_dim(head_dim) || n_heads == 0 ||
+      bad_dim(T * n_heads) || bad_dim(n_heads * head_dim))
+    return RNL_ERR_SHAPE;
+  if (!head_norm_dim_ok(head_dim)) return RNL_ERR_UNSUPPORTED;
+  if (bad_mode(norm_mode) || bad_eps(eps)) return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!y || !out) return RNL_ERR_NULL;
+  if (!aligned16(y) || !aligned16(out) || (gamma && !aligned16(gamma))) return RNL_ERR_ALIGN;
+  const uintptr_t bytes = static_cast<uintptr_t>(T) * n_heads * head_dim * 2;
+  const uintptr_t yb = reinterpret_cast<uintptr_t>(y), ob = reinterpret_cast<uintptr_t>(out);
+  if (yb != ob && yb < ob + bytes && ob < yb + bytes) return RNL_ERR_ARG;  // partial overlap
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  return launch_head_norm(y, T, n_heads, head_dim, gamma, eps, norm_mode, out, cs(stream));
+}
+
+rnl_status mla_q_chain_head_norm(const void* x, const void* W_qa, const void* gamma_cq,
+                                 const void* W_qb, int64_t T, int64_t K, int64_t N1, int64_t N2,
+                                 float eps, int norm_mode, int64_t head_dim, const void* head_gamma,
+                                 float head_eps, void* out, void* qa_out, void* workspace,
+                                 size_t workspace_bytes, rnl_stream_t stream) {
+  if (bad_dim(head_dim) || head_dim == 0 || N2 % head_dim != 0) return RNL_ERR_SHAPE;
+  if (!head_norm_dim_ok(head_dim)) return RNL_ERR_UNSUPPORTED;
+  if (bad_eps(head_eps)) return RNL_ERR_ARG;
+  if (head_gamma && !aligned16(head_gamma)) return RNL_ERR_ALIGN;
+  rnl_status st = mla_q_chain(x, W_qa, gamma_cq, W_qb, T, K, N1, N2, eps, norm_mode, out, qa_out,
+                              workspace, workspace_bytes, stream);
+  if (st != RNL_OK || T == 0) return st;
+  return rnl_head_rmsnorm(out, T, N2 / head_dim, head_dim, head_gamma, head_eps, norm_mode, out,
+                          stream);
+}
+
 rnl_status rnl_gemm_s8s8s32(const int8_t* A, const int8_t* B, int32_t* C, int64_t M, int64_t N,
                             int64_t K, void* workspace, size_t workspace_bytes,
                             rnl_stream_t stream) {

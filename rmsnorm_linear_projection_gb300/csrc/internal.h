@@ -92,6 +92,14 @@ rnl_status launch_mx_dequant2(const uint8_t* a_codes, const uint8_t* a_scale, in
                               const uint8_t* b_codes, const uint8_t* b_scale, int64_t N, int64_t K,
                               int64_t block, void* A, void* B, cudaStream_t s);
 
+// ---- per-head RMSNorm (headnorm.cu) ----
+// head_dim a multiple of 64 in [64, 512]
+bool head_norm_dim_ok(int64_t D);
+// out (may be y) = bf16((y * rstd) * gamma) per head row of D values of y
+// [T, H * D]; gamma [D] may be null.
+rnl_status launch_head_norm(const void* y, int64_t T, int64_t H, int64_t D, const void* gamma,
+                            float eps, int mode, void* out, cudaStream_t s);
+
 // ---- QKV split + per-head RMSNorm + RoPE (qkvrope.cu) ----
 bool qkv_rope_head_dim_ok(int64_t D);
 rnl_status launch_qkv_rope(const void* y, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,

@@ -118,6 +118,16 @@ CHILD = textwrap.dedent("""
     r["mx_T0"] = mx(None, None, None, None, 0, 128, 8, 1e-6, 0, 64, None, 0, None, None, None, 0, None)
     r["mx_no_device"] = mx(A, A, A, A, 4, 128, 8, 1e-6, 0, 32, A, 1, A, A, ws, 1 << 30, None)
     r["mx_too_large"] = mx(A, None, A, A, 4, 1 << 20, 1 << 17, 1e-6, 0, 64, A, 0, None, None, ws, 1 << 30, None)
+    hn = lib.rnl_head_rmsnorm
+    r["hn_bad_dim"] = hn(A, 4, 8, 96, None, 1e-6, 1, A, None)
+    r["hn_partial_overlap"] = hn(A, 4, 8, 128, None, 1e-6, 1, P(0x10010), None)
+    r["hn_null_y"] = hn(None, 4, 8, 128, None, 1e-6, 1, A, None)
+    r["hn_T0"] = hn(None, 0, 8, 128, None, 1e-6, 1, None, None)
+    r["hn_in_place_no_device"] = hn(A, 4, 8, 192, None, 1e-6, 1, A, None)
+    r["hn_bad_eps"] = hn(A, 4, 8, 128, None, -1.0, 1, A, None)
+    mh = lib.mla_q_chain_head_norm
+    r["mlahn_N2_not_mult"] = mh(A, A, A, A, 4, 64, 32, 1000, 1e-6, 1, 192, None, 1e-6, A, None, ws, 1 << 30, None)
+    r["mlahn_bad_dim"] = mh(A, A, A, A, 4, 64, 32, 960, 1e-6, 1, 96, None, 1e-6, A, None, ws, 1 << 30, None)
     sm = lib.mxfp8_scaled_mm
     r["mxmm_null_x_scale"] = sm(A, None, A, A, 4, 128, 8, 64, A, 0, ws, 1 << 30, None)
     r["mxmm_bad_block"] = sm(A, A, A, A, 4, 128, 8, 16, A, 0, ws, 1 << 30, None)
@@ -194,6 +204,8 @@ def test_workspace_sizes(host_results):
     ("qmrs_small_ws", WORKSPACE), ("qmrs_no_device", DEVICE),
     ("mx_bad_block", ARG), ("mx_K_not_mult_block", SHAPE), ("mx_bad_dtype", ARG), ("mx_null_scale", NULL),
     ("mx_misaligned_codes_out", ALIGN), ("mx_small_ws", WORKSPACE), ("mx_T0", OK), ("mx_too_large", SHAPE), ("mx_no_device", DEVICE),
+    ("hn_bad_dim", UNSUP), ("hn_partial_overlap", ARG), ("hn_null_y", NULL), ("hn_T0", OK),
+    ("hn_in_place_no_device", DEVICE), ("hn_bad_eps", ARG), ("mlahn_N2_not_mult", SHAPE), ("mlahn_bad_dim", UNSUP),
     ("mxmm_null_x_scale", NULL), ("mxmm_bad_block", ARG), ("mxmm_no_device", DEVICE),
     ("pipe_null_out", NULL), ("pipe_bad_op", ARG), ("pipe_zero_K", SHAPE),
     ("pipe_bad_dtype", ARG), ("pipe_no_device", DEVICE), ("pipe_handle_after_fail", None),
