@@ -140,6 +140,7 @@ struct QmrsLayout {
   void* x2 = nullptr;     // bf16 [B*N, K] transposed, widened x2
   float* ws = nullptr;    // fp32 [N] x2_scale
   float* acc = nullptr;   // fp32 [M, N] running sum over the batch
+  uint64_t* flags = nullptr;  // per (output tile, epilogue warp): batch b's sum is written
   size_t bytes = 0;
 };
 QmrsLayout qmrs_layout(void* ws, int64_t B, int64_t M, int64_t K, int64_t N) {
@@ -149,6 +150,7 @@ QmrsLayout qmrs_layout(void* ws, int64_t B, int64_t M, int64_t K, int64_t N) {
   l.x2 = c.take(static_cast<size_t>(B) * N * K * 2);
   l.ws = static_cast<float*>(c.take(static_cast<size_t>(N) * 4));
   l.acc = static_cast<float*>(c.take(B > 1 ? static_cast<size_t>(M) * N * 4 : 0));
+  l.flags = static_cast<uint64_t*>(c.take(B > 1 ? batch_flag_bytes(M, N) : 0));
   l.bytes = c.used;
   return l;
 }
@@ -532,8 +534,8 @@ rnl_status quant_matmul_reduce_sum(const int8_t* x1, const int8_t* x2, const flo
                                    const void* x2_scale, int64_t B, int64_t M, int64_t K,
                                    int64_t N, void* out, void* workspace, size_t workspace_bytes,
                                    rnl_stream_t stream) {
-  if (bad_dim(B) || bad_dim(M) || bad_dim(K) || bad_dim(N) || B == 0 || K == 0 || N == 0 ||
-      bad_dim(B * M) || bad_dim(B * N))
+  if (bad_dim(B) || bad_dim(M) || bad_dim(K) || bad_dim(N) || B == 0 || B > 65535 || K == 0 ||
+      N == 0 || bad_dim(B * M) || bad_dim(B * N))
     return RNL_ERR_SHAPE;
   if (M == 0) return RNL_OK;
   if (!x1 || !x2 || !x1_scale || !x2_scale || !out) return RNL_ERR_NULL;
@@ -548,29 +550,24 @@ rnl_status quant_matmul_reduce_sum(const int8_t* x1, const int8_t* x2, const flo
   if (st != RNL_OK) return st;
   const QmrsLayout l = qmrs_layout(workspace, B, M, K, N);
   cudaStream_t s = cs(stream);
-  st = launch_s8_to_bf16(x1, B * M * K, l.x1, s);
+  st = launch_qmrs_prep(x1, x2, x2_scale, B, M, K, N, l.x1, l.x2, l.ws, s);
   if (st != RNL_OK) return st;
-  st = launch_s8_transpose_widen(x2, B, K, N, l.x2, s);
-  if (st != RNL_OK) return st;
-  st = launch_bf16_to_f32(x2_scale, N, l.ws, s);
-  if (st != RNL_OK) return st;
-  for (int64_t b = 0; b < B; ++b) {
-    GemmArgs g;
-    g.A = static_cast<const char*>(l.x1) + static_cast<size_t>(b) * M * K * 2;
-    g.B = static_cast<const char*>(l.x2) + static_cast<size_t>(b) * N * K * 2;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.out = l.acc;
-    g.out_final = out;
-    g.row_scale = x1_scale + b * M;
-    g.col_scale = l.ws;
-    g.epi = Epi::kDequantAccF32;
-    g.acc_mode = (b > 0 ? 1 : 0) | (b == B - 1 ? 2 : 0);
-    st = launch_gemm(g, s);
-    if (st != RNL_OK) return st;
-  }
-  return RNL_OK;
+  // all batches in one launch: items (b, tile), each adding its FP32 values to
+  // the running sum of batches 0 .. b-1 of the same tile (gemm_tc.cu)
+  GemmArgs g;
+  g.A = l.x1;
+  g.B = l.x2;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.out = l.acc;
+  g.out_final = out;
+  g.row_scale = x1_scale;
+  g.col_scale = l.ws;
+  g.epi = Epi::kDequantBatchSum;
+  g.nbatch = static_cast<int>(B);
+  g.batch_flags = l.flags;
+  return launch_gemm(g, s);
 }
 
 rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* Wq,

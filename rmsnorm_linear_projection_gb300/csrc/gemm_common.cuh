@@ -220,13 +220,13 @@ __device__ __forceinline__ void store_dequant_acc_32(float* acc_buf, __nv_bfloat
   const bool full = n0 + 32 <= N;
   if (mode & 1) {
     if (full && rows_32b_aligned(acc_buf, N, 4)) {
+      uint32_t p[4][8];  // all four loads in flight before the first use
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t p[8];
-        ld_global_v8(arow + n0 + 8 * h, p);
+      for (int h = 0; h < 4; ++h) ld_global_v8(arow + n0 + 8 * h, p[h]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * h + i] = __fadd_rn(__uint_as_float(p[i]), v[8 * h + i]);
-      }
+      for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * h + i] = __fadd_rn(__uint_as_float(p[h][i]), v[8 * h + i]);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)

@@ -505,12 +505,6 @@ int grid_pairs(int64_t tiles, int num_kb, int max_pairs, bool have_partials) {
 // Epoch of each launch: a per-process start value from the clock, then one
 // step per launch, so a flag left in a reused workspace by an earlier launch
 // (or process) never matches.
-uint64_t next_epoch() {
-  static std::atomic<uint64_t> counter{
-      static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) * 2654435761ull};
-  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
-}
-
 template <int EPI, int BN>
 rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pairs, cudaStream_t s,
                           const char* name) {
@@ -563,7 +557,7 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
                                            static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                            pl.dp_tiles, pl.sk_tiles, g.out, g.row_scale,
-                                           g.col_scale, partial, flags, next_epoch(),
+                                           g.col_scale, partial, flags, next_flag_epoch(),
                                            static_cast<const __nv_bfloat16*>(g.bias));
   trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
@@ -664,6 +658,12 @@ rnl_status read_clear_error_pair(unsigned int* word) {
     return RNL_ERR_LAUNCH;
   *word = v;
   return RNL_OK;
+}
+
+uint64_t next_flag_epoch() {
+  static std::atomic<uint64_t> counter{
+      static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) * 2654435761ull};
+  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 }  // namespace rnl

@@ -25,6 +25,16 @@
 // K loop is cut into chunks of 16 k-blocks (1024 products); each chunk goes
 // to its own accumulator and the epilogue converts it exactly to int32 and
 // adds it in registers.
+//
+// Batched sum mode (QuantMatMulReduceSum, Epi::kDequantBatchSum): the work
+// items are (batch b, tile) in b-major order; the producer reads batch b's
+// rows of A and B, and the epilogue of item (b, tile) adds its dequantised
+// FP32 values to the running sum that item (b - 1, tile) left in global
+// memory, after waiting (bounded) for that item's flag: one 64-bit flag per
+// (tile, epilogue warp), set with a release store to tag | (b + 1) after the
+// warp's sums are written.  Item i waits only for item i - tiles, and every
+// CTA takes its items in increasing order with all CTAs resident, so every
+// wait ends.
 #include <cuda_bf16.h>
 
 #include <cstdlib>
@@ -85,10 +95,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int M, int N, int K, int group_m, void* __restrict__ out,
                 const float* __restrict__ row_scale, const float* __restrict__ col_scale,
                 const float* __restrict__ a_rstd, const uint4* __restrict__ a_gamma,
-                const __nv_bfloat16* __restrict__ bias, int acc_mode, void* out_final) {
+                const __nv_bfloat16* __restrict__ bias, int acc_mode, void* out_final, int nbatch,
+                uint64_t* batch_flags, uint64_t tag) {
+  constexpr bool kBatch = EPI == static_cast<int>(Epi::kDequantBatchSum);
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32) ||
-                         EPI == static_cast<int>(Epi::kDequantAccF32));
+                         EPI == static_cast<int>(Epi::kDequantAccF32) || kBatch);
   static_assert(!(NORM_A && kInt), "the fused norm feeds the bf16 GEMM only");
   constexpr int kStages = Tile<BN>::kStages;
   constexpr uint32_t kStageBytes = Tile<BN>::kStageBytes;
@@ -109,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
+  const int num_items = num_tiles * (kBatch ? nbatch : 1);
   const int num_kb = (K + BK - 1) / BK;
   const int kb_per_unit = kInt ? kChunkKBlocks : num_kb;
   const int units_per_tile = (num_kb + kb_per_unit - 1) / kb_per_unit;
@@ -146,7 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_a);
       tma_prefetch_map(&map_b);
       uint32_t stage = 0, phase = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+        const int b = kBatch ? item / num_tiles : 0;
+        const int tile = item - b * num_tiles;
         int mb, nb;
         tile_coords(tile, num_m, num_n, group_m, mb, nb);
         bool ok = true;
@@ -158,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + stage * kStageBytes;
           const uint32_t bar = smem_u32(&ctrl->full[stage]);
           mbar_arrive_expect_tx(bar, kStageBytes);
-          tma_load_2d(sa, &map_a, bar, kb * BK, mb * BM);
-          tma_load_2d(sa + kABytes, &map_b, bar, kb * BK, nb * BN);
+          tma_load_2d(sa, &map_a, bar, kb * BK, b * M + mb * BM);
+          tma_load_2d(sa + kABytes, &map_b, bar, kb * BK, b * N + nb * BN);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -175,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(BM, BN);
       uint32_t stage = 0, phase = 0, unit = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
         for (int u = 0; u < units_per_tile && ok; ++u, ++unit) {
           const uint32_t buf = unit & 1u;
           const uint32_t use = unit >> 1;
@@ -224,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t unit = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int item = blockIdx.x; item < num_items && ok; item += gridDim.x) {
+      const int b = kBatch ? item / num_tiles : 0;
+      const int tile = item - b * num_tiles;
       int mb, nb;
       tile_coords(tile, num_m, num_n, group_m, mb, nb);
       const int m = mb * BM + row_local;
@@ -232,14 +249,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = m < M;
       float rs = 0.f;
       if ((EPI == static_cast<int>(Epi::kRowScaleF32) || EPI == static_cast<int>(Epi::kDequantBf16) ||
-           EPI == static_cast<int>(Epi::kDequantAccF32)) && row_ok)
-        rs = row_scale != nullptr ? __ldg(row_scale + m) : 1.0f;
+           EPI == static_cast<int>(Epi::kDequantAccF32) || kBatch) && row_ok)
+        rs = row_scale != nullptr ? __ldg(row_scale + static_cast<int64_t>(b) * M + m) : 1.0f;
       int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
       if (kInt) {
 #pragma unroll
         for (int c = 0; c < (kInt ? kGroups : 1); ++c)
 #pragma unroll
           for (int j = 0; j < (kInt ? 32 : 1); ++j) iacc[c][j] = 0;
+      }
+      uint64_t* flag = nullptr;
+      if constexpr (kBatch) {
+        // wait for the running sum of batches 0 .. b-1 (item (b-1, tile),
+        // 1.7 waves back, normally long done) and pull this warp's part of it
+        // into L2 while the accumulators drain
+        flag = batch_flags + static_cast<int64_t>(tile) * kEpiWarps + ew;
+        if (b > 0) {
+          if (!__all_sync(0xFFFFFFFFu, flag_wait(flag, tag | static_cast<uint64_t>(b), abort, &g_err_gemm, 26))) {
+            ok = false;
+            break;
+          }
+          if (row_ok) {
+            const float* arow = static_cast<const float*>(out) + static_cast<int64_t>(m) * N;
+#pragma unroll
+            for (int c = 0; c < kGroups; ++c)
+              if (n_base + c * 32 < N) prefetch_l2(arow + n_base + c * 32);
+          }
+        }
       }
       for (int u = 0; u < units_per_tile; ++u, ++unit) {
         const uint32_t buf = unit & 1u;
@@ -274,7 +310,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
       }
       if (!ok) break;
-      if constexpr (kInt) {
+      if constexpr (kBatch) {
+        const int mode = (b > 0 ? 1 : 0) | (b == nbatch - 1 ? 2 : 0);
+        if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < kGroups; ++c)
+            store_dequant_acc_32(static_cast<float*>(out), static_cast<__nv_bfloat16*>(out_final), m,
+                                 n_base + c * 32, N, iacc[c], rs, col_scale, mode);
+        }
+        if (b < nbatch - 1) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) flag_release(flag, tag | static_cast<uint64_t>(b + 1));
+        }
+      } else if constexpr (kInt) {
         if (row_ok) {
 #pragma unroll
           for (int c = 0; c < kGroups; ++c) {
@@ -365,13 +414,17 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
       return RNL_ERR_LAUNCH;
     attr_set[dev.device] = true;
   }
+  constexpr bool kBatch = EPI == static_cast<int>(Epi::kDequantBatchSum);
+  const int64_t nbatch = kBatch ? g.nbatch : 1;
   CUtensorMap ma, mb;
-  rnl_status st = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, g.K * 2, BK, BM);
+  rnl_status st =
+      make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M * nbatch, g.K * 2, BK, BM);
   if (st != RNL_OK) return st;
-  st = make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.B, g.K, g.N, g.K * 2, BK, BN);
+  st = make_map_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.B, g.K, g.N * nbatch, g.K * 2, BK, BN);
   if (st != RNL_OK) return st;
-  const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * nbatch;
   const unsigned grid = static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count);
+  const uint64_t tag = kBatch ? next_flag_epoch() << 16 : 0;
   trace_before(s);
   const int num_m = static_cast<int>((g.M + BM - 1) / BM);
   const int group_m = (g.M * g.K * 2 <= (int64_t{48} << 20)) ? num_m : (num_m < 8 ? num_m : 8);
@@ -391,7 +444,7 @@ rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, 
                                            g.out, g.row_scale, g.col_scale, g.a_rstd,
                                            static_cast<const uint4*>(g.a_gamma),
                                            static_cast<const __nv_bfloat16*>(g.bias), g.acc_mode,
-                                           g.out_final);
+                                           g.out_final, static_cast<int>(nbatch), g.batch_flags, tag);
   trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -438,7 +491,9 @@ int tile_width(int64_t M, int64_t N, int64_t K, int sm_count) {
 
 template <int EPI>
 rnl_status launch_bn(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
-  switch (tile_width(g.M, g.N, g.K, dev.sm_count)) {
+  // the batched sum mode has nbatch times the tiles of one batch
+  const int64_t rows = EPI == static_cast<int>(Epi::kDequantBatchSum) ? g.M * g.nbatch : g.M;
+  switch (tile_width(rows, g.N, g.K, dev.sm_count)) {
     case 128: return launch_epi<EPI, 128, false>(g, dev, s, name);
     case 192: return launch_epi<EPI, 192, false>(g, dev, s, name);
     default: return launch_epi<EPI, 256, false>(g, dev, s, name);
@@ -463,14 +518,15 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
     if (e != nullptr && (e[0] == '0' || e[0] == '1')) {
       pair = e[0] == '1';
     } else {
-      const bool integer =
-          g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32 || g.epi == Epi::kDequantAccF32;
+      const bool integer = g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32 ||
+                           g.epi == Epi::kDequantAccF32 || g.epi == Epi::kDequantBatchSum;
       const int bn = pick_bn(g.M, g.N, g.K, dev.sm_count);
       pair = !integer && g.N >= 256 &&
              predict_pair_us(g.M, g.N, g.K, dev.sm_count, resident_pairs_for(dev)) <
                  predict_one_cta_us(g.M, g.N, g.K, dev.sm_count, bn);
     }
-    if (pair && g.epi != Epi::kDequantAccF32) return launch_gemm_pair(g, s);  // one CTA only
+    if (pair && g.epi != Epi::kDequantAccF32 && g.epi != Epi::kDequantBatchSum)
+      return launch_gemm_pair(g, s);  // one CTA only
   }
   if (g.a_rstd != nullptr) {  // fused norm: bf16 epilogue only
     if (g.epi != Epi::kBf16) return RNL_ERR_ARG;
@@ -486,6 +542,10 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
     case Epi::kDequantBf16: return launch_bn<2>(g, dev, s, "gemm_int_dequant");
     case Epi::kInt32: return launch_bn<3>(g, dev, s, "gemm_int_s32");
     case Epi::kDequantAccF32: return launch_bn<4>(g, dev, s, "gemm_int_dequant_acc");
+    case Epi::kDequantBatchSum:
+      if (g.nbatch < 1 || g.nbatch > 65535 || (g.nbatch > 1 && g.batch_flags == nullptr))
+        return RNL_ERR_ARG;
+      return launch_bn<5>(g, dev, s, "gemm_int_batch_sum");
   }
   return RNL_ERR_ARG;
 }

@@ -68,11 +68,13 @@ rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_
 rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                              int mode, void* A, int8_t* q_out, float* x_scale, const int8_t* Wq,
                              int64_t N, void* Wb, cudaStream_t s);
-// int8 [B, K, N] -> bf16 [B, N, K] (exact; the K-major operand of an ND int8
-// matrix), K % 16 == 0 and N % 16 == 0 (qmrs.cu); and bf16 -> fp32 of n values.
-rnl_status launch_s8_transpose_widen(const int8_t* src, int64_t B, int64_t K, int64_t N, void* dst,
-                                     cudaStream_t s);
-rnl_status launch_bf16_to_f32(const void* src, int64_t n, float* dst, cudaStream_t s);
+// QuantMatMulReduceSum operands in one launch (qmrs.cu): x1 int8 [B, M, K]
+// -> bf16 [B * M, K]; x2 int8 [B, K, N] -> bf16 [B * N, K] (exact; the K-major
+// operand of an ND int8 matrix); x2_scale bf16 [N] -> fp32.  K % 16 == 0 and
+// N % 16 == 0; x2_dst 32-byte aligned.
+rnl_status launch_qmrs_prep(const int8_t* x1, const int8_t* x2, const void* x2_scale, int64_t B,
+                            int64_t M, int64_t K, int64_t N, void* x1_dst, void* x2_dst,
+                            float* scale_dst, cudaStream_t s);
 // int8 -> bf16 (exact), n elements, n % 16 == 0.
 rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream_t s);
 
@@ -118,6 +120,12 @@ enum class Epi : int {
   // (earlier batches), bit 1 (last batch) writes bf16(v) to out_final instead
   // of v to `out`
   kDequantAccF32 = 4,
+  // QuantMatMulReduceSum, all batches in one launch: work items (b, tile) in
+  // b-major order; item (b, tile) adds v_b to the FP32 running sum that item
+  // (b - 1, tile) left in `out` (waiting for its flag), and the last batch
+  // writes bf16 to out_final.  A is [nbatch * M, K], B is [nbatch * N, K],
+  // row_scale is [nbatch * M]
+  kDequantBatchSum = 5,
 };
 
 struct GemmArgs {
@@ -143,8 +151,17 @@ struct GemmArgs {
   const char* trace_name = nullptr;
   // Epi::kDequantAccF32 only
   int acc_mode = 0;
-  void* out_final = nullptr;
+  void* out_final = nullptr;  // also Epi::kDequantBatchSum
+  // Epi::kDequantBatchSum only: the batch count and one 64-bit flag per
+  // (output tile, epilogue warp) of the 128 x 128 tiling (the finest), zeroed
+  // or not: each launch uses its own tag
+  int nbatch = 1;
+  uint64_t* batch_flags = nullptr;
 };
+// Bytes of the flags of Epi::kDequantBatchSum for M x N outputs.
+inline size_t batch_flag_bytes(int64_t M, int64_t N) {
+  return static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((N + 127) / 128) * 8 * 8;
+}
 
 // Partial-sum slots of the CTA-pair GEMM's stream-K tiles (2 x 128 x 256
 // 32-bit words each): one per pair, the last one holding the hand-off flags.
@@ -153,6 +170,9 @@ constexpr size_t kGemmPartialBytes = static_cast<size_t>(kMaxPartialSlots) * 2 *
 rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s);
 // The same GEMM on CTA pairs (tcgen05 cta_group::2, gemm_pair.cu); no fused norm.
 rnl_status launch_gemm_pair(const GemmArgs& g, cudaStream_t s);
+// A fresh tag for the cross-CTA flags of one launch (clock-seeded per-process
+// counter, gemm_pair.cu): flags left in a reused workspace never match.
+uint64_t next_flag_epoch();
 // Predicted pair-kernel time (microseconds) and resident CTA pairs (gemm_pair.cu).
 double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs);
 int resident_pairs_for(const DeviceInfo& dev);

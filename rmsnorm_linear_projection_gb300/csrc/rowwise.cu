@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "exactsum.cuh"
+#include "widen.cuh"
 #include "internal.h"
 
 namespace rnl {
@@ -352,42 +353,6 @@ void norm_quant_dispatch(const uint4* xp, const uint4* gp, int64_t T, int nvec, 
     norm_quant_regs_kernel<MODE, GAMMA, 16><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
   else
     norm_quant_kernel<MODE, GAMMA><<<blocks, kT, 0, s>>>(xp, gp, T, nvec, inv_d, eps, ap, qp, xs);
-}
-
-// int8 -> bf16 (exact): each thread widens 4 x 16 elements, issuing its four
-// 16-byte loads before converting.
-constexpr int kS8Vec = 4;
-
-__device__ __forceinline__ void widen16(const uint4& u, uint4* dst) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float a = static_cast<float>(static_cast<int8_t>(w[k] & 0xFF));
-    const float b = static_cast<float>(static_cast<int8_t>((w[k] >> 8) & 0xFF));
-    const float c = static_cast<float>(static_cast<int8_t>((w[k] >> 16) & 0xFF));
-    const float d = static_cast<float>(static_cast<int8_t>((w[k] >> 24) & 0xFF));
-    o[2 * k] = pack_bf16x2(a, b);
-    o[2 * k + 1] = pack_bf16x2(c, d);
-  }
-  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void widen_block(unsigned block, const uint4* __restrict__ src,
-                                            int64_t nvec16, uint4* __restrict__ dst) {
-  const int64_t base = (static_cast<int64_t>(block) * blockDim.x) * kS8Vec + threadIdx.x;
-  uint4 u[kS8Vec];
-#pragma unroll
-  for (int i = 0; i < kS8Vec; ++i) {
-    const int64_t v = base + static_cast<int64_t>(i) * blockDim.x;
-    u[i] = v < nvec16 ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int i = 0; i < kS8Vec; ++i) {
-    const int64_t v = base + static_cast<int64_t>(i) * blockDim.x;
-    if (v < nvec16) widen16(u[i], dst + 2 * v);
-  }
 }
 
 __global__ void __launch_bounds__(256)

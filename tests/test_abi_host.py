@@ -178,7 +178,9 @@ def test_workspace_sizes(host_results):
     # skinny partial records: (T/128 + 512) records of 128 rows x (32 + 1) floats
     assert r["ws_bf16_skinny"] == (16384 // 128 + 512) * 128 * 33 * 4
     # QuantMatMulReduceSum: widened x1 and x2, fp32 x2_scale, fp32 batch sum
-    assert r["ws_qmrs"] == 4 * 2048 * 4096 * 2 + 4 * 4096 * 4096 * 2 + 4096 * 4 + 2048 * 4096 * 4
+    # + the flags of the one-launch batch sum: (2048/128) x (4096/128) tiles x 8 warps x 8 bytes
+    assert r["ws_qmrs"] == (4 * 2048 * 4096 * 2 + 4 * 4096 * 4096 * 2 + 4096 * 4 + 2048 * 4096 * 4
+                            + 16 * 32 * 64)
     assert r["ws_qmrs_b1"] == 2048 * 4096 * 2 + 4096 * 4096 * 2 + 4096 * 4  # no running sum
     # MXFP8: dequantised bf16 activations and weight, GEMM partials
     assert r["ws_mxfp8"] == 4096 * 4096 * 2 + 6144 * 4096 * 2 + part
