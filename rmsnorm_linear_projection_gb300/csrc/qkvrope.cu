@@ -10,10 +10,8 @@
 //   with (c_i, s_i) read from the caller's angle table [P, D] (cos | sin) at
 //   the token's position; v heads are copied unchanged.
 //
-// One warp per (token, group of 8 heads): lane l holds D/32 consecutive
-// values of each head, the sum of squares is a warp reduction, and the
-// rotation partner of element i (i + D/2) sits in lane l ^ 16.  HBM / L2
-// bound: each head row is read once and written once.
+// One warp per (token, group of 8 heads); each head row is read once and
+// written once (HBM bound).
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -30,28 +28,21 @@ __device__ __forceinline__ float bf16_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-template <int E>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&f)[E]) {
-  if constexpr (E == 2) {
+// N consecutive bf16 (N = 1, 2, 4) <-> floats, and N consecutive floats.
+template <int N>
+__device__ __forceinline__ void load_bf16n(const __nv_bfloat16* p, float (&f)[N]) {
+  if constexpr (N == 1) {
+    f[0] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+  } else if constexpr (N == 2) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
     f[0] = __uint_as_float(w << 16);
     f[1] = __uint_as_float(w & 0xFFFF0000u);
-  } else if constexpr (E == 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
   } else {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xFFFF0000u);
   }
 }
 
@@ -60,15 +51,31 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int E>
-__device__ __forceinline__ void store_bf16(__nv_bfloat16* p, const float (&f)[E]) {
-  if constexpr (E == 2) {
+template <int N>
+__device__ __forceinline__ void store_bf16n(__nv_bfloat16* p, const float (&f)[N]) {
+  if constexpr (N == 1) {
+    *p = __float2bfloat16_rn(f[0]);
+  } else if constexpr (N == 2) {
     *reinterpret_cast<uint32_t*>(p) = pack2(f[0], f[1]);
-  } else if constexpr (E == 4) {
-    *reinterpret_cast<uint2*>(p) = make_uint2(pack2(f[0], f[1]), pack2(f[2], f[3]));
   } else {
-    *reinterpret_cast<uint4*>(p) =
-        make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack2(f[0], f[1]), pack2(f[2], f[3]));
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void load_f32n(const float* p, float (&f)[N]) {
+  if constexpr (N == 1) {
+    f[0] = *p;
+  } else if constexpr (N == 2) {
+    const float2 u = *reinterpret_cast<const float2*>(p);
+    f[0] = u.x;
+    f[1] = u.y;
+  } else {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = u.x;
+    f[1] = u.y;
+    f[2] = u.z;
+    f[3] = u.w;
   }
 }
 
@@ -77,26 +84,14 @@ __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, const float (&f)[E]
 // processed.
 constexpr int kHeadsPerWarp = 8;
 
-template <int E>
-__device__ __forceinline__ void load_f32v(const float* p, float (&f)[E]) {
-  if constexpr (E == 2) {
-    const float2 u = *reinterpret_cast<const float2*>(p);
-    f[0] = u.x;
-    f[1] = u.y;
-  } else if constexpr (E == 4) {
-    const float4 u = *reinterpret_cast<const float4*>(p);
-    f[0] = u.x;
-    f[1] = u.y;
-    f[2] = u.z;
-    f[3] = u.w;
-  } else {
-    const float4 u0 = *reinterpret_cast<const float4*>(p);
-    const float4 u1 = *reinterpret_cast<const float4*>(p + 4);
-    f[0] = u0.x; f[1] = u0.y; f[2] = u0.z; f[3] = u0.w;
-    f[4] = u1.x; f[5] = u1.y; f[6] = u1.z; f[7] = u1.w;
-  }
-}
-
+// Lane l holds R = D/64 elements of each half of a head row: i in
+// [l R, l R + R) and their rotation partners i + D/2, so the rotation needs
+// no shuffle, and every load or store instruction of the warp covers a
+// contiguous 32 R elements.  The 8 heads' sums of squares are reduced
+// together (a reduce-scatter: 4 + 2 + 1 shuffles leave each lane with one
+// head's partial over 4 lanes, 2 more finish it), one rsqrt a lane, and
+// 8 shuffles hand every head its factor: 17 shuffles and 1 rsqrt for 8
+// heads instead of 40 and 8.
 template <int D>
 __global__ void __launch_bounds__(kRopeWarps * 32)
     qkv_rope_kernel(const __nv_bfloat16* __restrict__ y, int64_t T, int Hq, int Hkv, int groups,
@@ -105,7 +100,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32)
                     const int* __restrict__ pos, const float* __restrict__ cs, int P,
                     __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
                     __nv_bfloat16* __restrict__ v) {
-  constexpr int E = D / 32;  // values per lane
+  constexpr int R = D / 64;  // values of each half per lane
+  constexpr int kHalf = D / 2;
   const int lane = threadIdx.x & 31;
   const int H = Hq + 2 * Hkv;
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * kRopeWarps + (threadIdx.x >> 5);
@@ -113,60 +109,95 @@ __global__ void __launch_bounds__(kRopeWarps * 32)
   const int64_t t = wid / groups;
   const int h0 = static_cast<int>(wid - t * groups) * kHeadsPerWarp;
   const int nh = H - h0 < kHeadsPerWarp ? H - h0 : kHeadsPerWarp;
-  const __nv_bfloat16* yt = y + t * H * D + lane * E;
+  const __nv_bfloat16* yt = y + t * H * D + lane * R;
   // every head row of the group first
-  float f[kHeadsPerWarp][E];
+  float lo[kHeadsPerWarp][R], hi[kHeadsPerWarp][R];
 #pragma unroll
   for (int j = 0; j < kHeadsPerWarp; ++j)
-    if (j < nh) load_bf16<E>(yt + (h0 + j) * D, f[j]);
-  const bool any_qk = h0 < Hq + Hkv;
-  int p = 0;
+    if (j < nh) {
+      load_bf16n<R>(yt + (h0 + j) * D, lo[j]);
+      load_bf16n<R>(yt + (h0 + j) * D + kHalf, hi[j]);
+    }
+  const int nqk = Hq + Hkv;  // heads below this index are normalised and rotated
+  const bool any_qk = h0 < nqk;
   bool p_ok = true;
-  float c[E], sn[E], gq[E], gk[E];
+  float c[R], sn[R], gql[R], gqh[R], gkl[R], gkh[R];
   if (any_qk) {
-    p = __ldg(pos + t);
+    const int p = __ldg(pos + t);
     p_ok = p >= 0 && p < P;
     if (!p_ok) {  // nothing is read from the table; the caller gets RNL_ERR_ARG
       if (lane == 0) atomicCAS(&g_err_rope, 0u, kErrArg | (40u << 8));
     } else {
-      const float* row = cs + static_cast<int64_t>(p) * D + (lane & 15) * E;
-      load_f32v<E>(row, c);
-      load_f32v<E>(row + D / 2, sn);
+      const float* row = cs + static_cast<int64_t>(p) * D + lane * R;
+      load_f32n<R>(row, c);
+      load_f32n<R>(row + kHalf, sn);
     }
-    if (Hq > 0) load_bf16<E>(q_gamma + lane * E, gq);
-    if (Hkv > 0) load_bf16<E>(k_gamma + lane * E, gk);
+    if (Hq > 0) {
+      load_bf16n<R>(q_gamma + lane * R, gql);
+      load_bf16n<R>(q_gamma + kHalf + lane * R, gqh);
+    }
+    if (Hkv > 0) {
+      load_bf16n<R>(k_gamma + lane * R, gkl);
+      load_bf16n<R>(k_gamma + kHalf + lane * R, gkh);
+    }
+  }
+  float r[kHeadsPerWarp];
+  if (any_qk) {
+    float ss[kHeadsPerWarp];
+#pragma unroll
+    for (int j = 0; j < kHeadsPerWarp; ++j) {
+      ss[j] = 0.f;
+      if (j < nh && h0 + j < nqk) {
+#pragma unroll
+        for (int e = 0; e < R; ++e) ss[j] = fmaf(lo[j][e], lo[j][e], ss[j]);
+#pragma unroll
+        for (int e = 0; e < R; ++e) ss[j] = fmaf(hi[j][e], hi[j][e], ss[j]);
+      }
+    }
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float s4[4], s2[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = b4 ? ss[i] : ss[i + 4];
+      s4[i] = (b4 ? ss[i + 4] : ss[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = b3 ? s4[i] : s4[i + 2];
+      s2[i] = (b3 ? s4[i + 2] : s4[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float s1 = (b2 ? s2[1] : s2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? s2[0] : s2[1], 4);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    // this lane now holds head ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)
+    const float rl = rsqrtf(s1 * (1.0f / D) + eps);
+#pragma unroll
+    for (int j = 0; j < kHeadsPerWarp; ++j)
+      r[j] = __shfl_sync(0xffffffffu, rl, ((j >> 2) & 1) << 4 | ((j >> 1) & 1) << 3 | (j & 1) << 2);
   }
 #pragma unroll
   for (int j = 0; j < kHeadsPerWarp; ++j) {
     if (j >= nh) break;
     const int h = h0 + j;
-    if (h >= Hq + Hkv) {  // v head: copied
-      store_bf16<E>(v + (t * Hkv + (h - Hq - Hkv)) * D + lane * E, f[j]);
+    if (h >= nqk) {  // v head: copied
+      __nv_bfloat16* dv = v + (t * Hkv + (h - nqk)) * D + lane * R;
+      store_bf16n<R>(dv, lo[j]);
+      store_bf16n<R>(dv + kHalf, hi[j]);
       continue;
     }
     if (!p_ok) continue;
     const bool is_q = h < Hq;
-    __nv_bfloat16* dst = is_q ? q + (t * Hq + h) * D : k + (t * Hkv + (h - Hq)) * D;
-    float ss = 0.f;
+    __nv_bfloat16* dst = (is_q ? q + (t * Hq + h) * D : k + (t * Hkv + (h - Hq)) * D) + lane * R;
+    float ol[R], oh[R];
 #pragma unroll
-    for (int e = 0; e < E; ++e) ss = fmaf(f[j][e], f[j][e], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss * (1.0f / D) + eps);
-    float z[E], zp[E], out[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      z[e] = bf16_round(__fmul_rn(__fmul_rn(f[j][e], r), is_q ? gq[e] : gk[e]));
-#pragma unroll
-    for (int e = 0; e < E; ++e) zp[e] = __shfl_xor_sync(0xffffffffu, z[e], 16);
-    if (lane < 16) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) out[e] = __fsub_rn(__fmul_rn(z[e], c[e]), __fmul_rn(zp[e], sn[e]));
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) out[e] = __fadd_rn(__fmul_rn(z[e], c[e]), __fmul_rn(zp[e], sn[e]));
+    for (int e = 0; e < R; ++e) {
+      const float zl = bf16_round(__fmul_rn(__fmul_rn(lo[j][e], r[j]), is_q ? gql[e] : gkl[e]));
+      const float zh = bf16_round(__fmul_rn(__fmul_rn(hi[j][e], r[j]), is_q ? gqh[e] : gkh[e]));
+      ol[e] = __fsub_rn(__fmul_rn(zl, c[e]), __fmul_rn(zh, sn[e]));
+      oh[e] = __fadd_rn(__fmul_rn(zh, c[e]), __fmul_rn(zl, sn[e]));
     }
-    store_bf16<E>(dst + lane * E, out);
+    store_bf16n<R>(dst, ol);
+    store_bf16n<R>(dst + kHalf, oh);
   }
 }
 
