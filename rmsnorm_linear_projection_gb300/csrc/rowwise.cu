@@ -159,7 +159,19 @@ __device__ __forceinline__ float row_rstd_exactsum(const uint4* xr, int nvec, fl
   float hs[8], ls[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) hs[j] = ls[j] = 0.f;
-  for (int v = lane; v < nvec; v += 32) {
+  int v = lane;
+  for (; v + 96 < nvec; v += 128) {  // four 16-byte loads in flight per lane
+    uint4 w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = ldg16(xr + v + 32 * j);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      unpack8(w[j], f);
+      ff_add_squares8<MODE>(f, inv_d, hs, ls);
+    }
+  }
+  for (; v < nvec; v += 32) {
     float f[8];
     unpack8(ldg16(xr + v), f);
     ff_add_squares8<MODE>(f, inv_d, hs, ls);
@@ -173,13 +185,17 @@ __device__ __forceinline__ float row_rstd_exactsum(const uint4* xr, int nvec, fl
 // rint is round-half-even; |y * qs| <= 127 up to rounding, and the clamp to
 // [-127, 127] only removes that overshoot.  amax == 0 gives q = 0 and
 // x_scale = 0.
+// Any K: x is read three times (sum of squares, amax, codes; the second and
+// third mostly from L1 / L2).
 template <int MODE, bool GAMMA>
-__global__ void __launch_bounds__(kWarps * 32)
-    norm_quant_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
-                      int nvec, float inv_d, float eps, uint4* __restrict__ A,
-                      uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+__device__ __forceinline__ void norm_quant_stream_rows(unsigned block, const uint4* __restrict__ x,
+                                                       const uint4* __restrict__ gamma, int64_t T,
+                                                       int nvec, float inv_d, float eps,
+                                                       uint4* __restrict__ A,
+                                                       uint2* __restrict__ q_out,
+                                                       float* __restrict__ x_scale) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t row = static_cast<int64_t>(block) * kWarps + (threadIdx.x >> 5);
   if (row >= T) return;
   const uint4* xr = x + row * nvec;
   const float rstd = row_rstd_exactsum<MODE>(xr, nvec, inv_d, eps);
@@ -233,6 +249,14 @@ __global__ void __launch_bounds__(kWarps * 32)
       qr[v] = make_uint2(lo, hi);
     }
   }
+}
+
+template <int MODE, bool GAMMA>
+__global__ void __launch_bounds__(kWarps * 32)
+    norm_quant_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
+                      int nvec, float inv_d, float eps, uint4* __restrict__ A,
+                      uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+  norm_quant_stream_rows<MODE, GAMMA>(blockIdx.x, x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale);
 }
 
 // The same W8A8 front end with the whole row in registers (used up to
@@ -365,7 +389,7 @@ __global__ void __launch_bounds__(256)
 // data, so their blocks are interleaved in one grid (even / odd while both
 // last) and run side by side on every SM instead of one after the other.
 template <int MODE, bool GAMMA, int VPL>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 4)
     w8a8_front_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, int64_t T,
                       int nvec, float inv_d, float eps, uint4* __restrict__ A,
                       uint2* __restrict__ q_out, float* __restrict__ x_scale,
@@ -382,10 +406,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     quant = quant_blocks > widen_blocks;
     idx = b - both;
   }
-  if (quant)
-    norm_quant_regs_rows<MODE, GAMMA, VPL>(idx, x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale);
-  else
+  if (quant) {
+    if constexpr (VPL == 0)
+      norm_quant_stream_rows<MODE, GAMMA>(idx, x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale);
+    else
+      norm_quant_regs_rows<MODE, GAMMA, VPL>(idx, x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale);
+  } else {
     widen_block(idx, w_src, w_nvec16, w_dst);
+  }
 }
 
 inline rnl_status launched(cudaStream_t s, const char* name) {
@@ -489,14 +517,16 @@ template <int MODE, bool GAMMA>
 void front_vpl(int vpl, unsigned grid, const uint4* xp, const uint4* gp, int64_t T, int nvec,
                float inv_d, float eps, uint4* ap, uint2* qp, float* xs, const uint4* wp,
                int64_t w_nvec16, uint4* wd, unsigned qb, unsigned wb, cudaStream_t s) {
-  if (vpl <= 2)
+  // rows longer than 1024 are read three times (from L1 / L2 after the
+  // first): measured faster than holding them in registers, because the
+  // 64-register budget keeps four blocks per SM (48.4 against 54.2 us at
+  // 8192 x 4096 rows with a 4096 x 4096 weight)
+  if (vpl > 4)
+    front_launch<MODE, GAMMA, 0>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+  else if (vpl <= 2)
     front_launch<MODE, GAMMA, 2>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
-  else if (vpl <= 4)
-    front_launch<MODE, GAMMA, 4>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
-  else if (vpl <= 8)
-    front_launch<MODE, GAMMA, 8>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
   else
-    front_launch<MODE, GAMMA, 16>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
+    front_launch<MODE, GAMMA, 4>(grid, xp, gp, T, nvec, inv_d, eps, ap, qp, xs, wp, w_nvec16, wd, qb, wb, s);
 }
 }  // namespace
 
@@ -505,11 +535,7 @@ rnl_status launch_w8a8_front(const void* x, const void* gamma, int64_t T, int64_
                              int64_t N, void* Wb, cudaStream_t s) {
   const int nvec = static_cast<int>(K / 8);
   const int vpl = (nvec + 31) / 32;
-  if (T == 0 || vpl > 16) {  // long rows: the two kernels one after the other
-    rnl_status st = launch_norm_quant(x, gamma, T, K, eps, mode, A, q_out, x_scale, s);
-    if (st != RNL_OK) return st;
-    return launch_s8_to_bf16(Wq, N * K, Wb, s);
-  }
+  if (T == 0) return launch_s8_to_bf16(Wq, N * K, Wb, s);
   const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
   const int64_t w_nvec16 = N * K / 16;
   const unsigned qb = row_blocks(T);

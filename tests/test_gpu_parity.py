@@ -248,7 +248,12 @@ def _w8a8_run(d, eps, mode):
     return host_bits(out), q.cpu().numpy(), xs.cpu().numpy()
 
 
-@pytest.mark.parametrize("T,K,N,mode", [(200, 2048, 300, 0), (130, 4096, 520, 1), (5, 16, 7, 0)])
+@pytest.mark.parametrize("T,K,N,mode", [
+    (200, 2048, 300, 0), (130, 4096, 520, 1), (5, 16, 7, 0),
+    (40, 1024, 64, 0),     # the row held in registers
+    (64, 6144, 136, 1),    # rows read three times
+    (33, 8704, 96, 0),     # a row length that is not a multiple of 1024 elements
+])
 def test_w8a8_small(orc, T, K, N, mode):
     c = dict(seed=3 + T + N, T=T, K=K, N=N)
     d = si.make_w8a8(c)
