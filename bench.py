@@ -406,7 +406,8 @@ def oracle_sample(work_name: str, target_s: float = 12.0):
             dt = time.perf_counter() - t
             # the rotation mixes two normalised values that may each sit one
             # bf16 ulp from the oracle's (after the projection's own ulp):
-            # |err| <= 2^-6 (|z_i c| + |z_p s| + |o|) + 2^-20
+            # |err| <= 2^-6 (|z_i c| + |z_p s| + |o|) + 2^-20, or the
+            # acceptance bound where the projection output is near zero
             ident = np.concatenate([np.ones((1, D // 2), np.float32), np.zeros((1, D // 2), np.float32)], axis=1)
             zq, _, _ = o.qkv_rope(y, Hq, Hkv, D, r["q_gamma"], r["k_gamma"], c["head_eps"],
                                   np.zeros(len(rows), np.int32), ident)
@@ -416,7 +417,8 @@ def oracle_sample(work_name: str, target_s: float = 12.0):
             za, zb = np.abs(z[..., :h]), np.abs(z[..., h:])
             mix = np.concatenate([za * np.abs(cs[..., :h]) + zb * np.abs(cs[..., h:]),
                                   zb * np.abs(cs[..., :h]) + za * np.abs(cs[..., h:])], axis=-1)
-            bound = 2.0**-6 * (mix + np.abs(oracle.bf16_bits_to_f64(q))) + 2.0**-20
+            qv = np.abs(oracle.bf16_bits_to_f64(q))
+            bound = np.maximum(2.0**-6 * (mix + qv) + 2.0**-20, 1e-2 * np.maximum(1.0, qv))
             return dt, q.reshape(len(rows), -1), bound.reshape(len(rows), -1)
         if work_name == "qmrs":
             d = si.make_qmrs(c, rows=rows)

@@ -11,9 +11,11 @@ The oracle's z comes from the same stage run at angle 0.  v heads: bit-exact.
 
 For the whole chain (projection, then this stage) the expected values are the
 oracle's chain from the same x, W: its projection output y may differ from the
-GPU's by one bf16 ulp in some elements (the usual bf16 output bound), which
-moves z by at most one more ulp, so the factor is 2^-6 there and v is held to
-the bf16 output bound instead of bit equality.
+GPU's by one bf16 ulp where |y| is not small, which moves z by at most one
+more ulp, so the factor is 2^-6 there; where y is near zero after
+cancellation the projection's error is absolute (its FP32 accumulation), and
+such elements are held to the acceptance bound 1e-2 * max(1, |oracle|)
+instead.  v is held to the bf16 output bound instead of bit equality.
 """
 import numpy as np
 import pytest
@@ -55,6 +57,8 @@ def assert_rope_close(orc, got, want, y_bits, Hq, Hkv, D, qg, kg, eps, pos, cs, 
         hi = zb * np.abs(c) + za * np.abs(s)
         factor = 2.0**-6 if chain else 2.0**-7
         bound = factor * (np.concatenate([lo, hi], axis=-1) + np.abs(w)) + 2.0**-20
+        if chain:
+            bound = np.maximum(bound, 1e-2 * np.maximum(1.0, np.abs(w)))
         err = np.abs(g - w)
         bad = err > bound
         assert not bad.any(), f"{what} {name}: {bad.sum()} outside the bound, max err {err.max()}"
