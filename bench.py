@@ -53,12 +53,21 @@ METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 # roofline stage per step, from the ncu captures summarised under profiles/;
 # only for kernels unchanged since the capture.
 TRAFFIC = {
-    # gemm_pair_kernel<0,256>: 98.13 MB read + 39.87 MB written
+    # gemm_pair_kernel<0,256>: 96.80 MB read + 40.96 MB written
     # (profiles/qkv_step_kernels_4096x6144x4096.md)
-    "qkv": 138.00e6,
-    # gemm_kernel<2,256,0>: 125.17 MB read + 46.38 MB written
+    "qkv": 137.75e6,
+    # the same kernel on the same shape and inputs ahead of the rope stage
+    "qkv_rope": 137.75e6,
+    # both MLA GEMM stages: 51.79 MB (one CTA, BN 192) + 155.09 MB (pairs)
+    # (profiles/mla_gemm_stages_2048x7168x1536x24576.md); the same stages in mla_hn
+    "mla": 206.88e6,
+    "mla_hn": 206.88e6,
+    # gemm_kernel<2,256,0>: 121.75 MB read + 45.24 MB written
     # (profiles/w8a8_front_and_int_gemm_8192x4096x4096.md)
-    "w8a8": 171.55e6,
+    "w8a8": 167.00e6,
+    # gemm_kernel<5,256,0>, all batches: 289.46 MB read + 85.07 MB written
+    # (profiles/qmrs_prep_and_batch_gemm_4x2048x4096x4096.md)
+    "qmrs": 374.53e6,
     # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.24 MB read + 39.96 MB written
     # (profiles/mxfp8_front_and_gemm_4096x4096x6144.md)
     "mxfp8": 137.20e6,
