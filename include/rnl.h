@@ -184,10 +184,15 @@ rnl_status rnl_qkv_rope(const void *y, int64_t T, int64_t n_q_heads, int64_t n_k
 
 /*
  * rmsnorm_linear_bf16 (AT-10, bf16 out, N = (n_q_heads + 2 * n_kv_heads) *
- * head_dim) followed by rnl_qkv_rope on its output, which lives in the
- * workspace: rnl_workspace_size(RNL_OP_QKV_ROPE, T, K, N, 0) bytes.
- * head_eps is the per-head norms' eps.  Arguments of both stages are checked
- * before anything is enqueued.
+ * head_dim) followed by rnl_qkv_rope on its output.  With head_dim 128 and a
+ * projection large enough for the CTA-pair GEMM, the stage runs in that
+ * GEMM's epilogue on the bf16-rounded projection values and the projection
+ * output is never written; otherwise it lives in the workspace and the
+ * separate stage reads it.  Workspace: rnl_workspace_size(RNL_OP_QKV_ROPE,
+ * T, K, N, 0) bytes either way.  head_eps is the per-head norms' eps.
+ * Arguments of both stages are checked before anything is enqueued; a
+ * position outside [0, max_pos) is reported by rnl_check_device_error as
+ * RNL_ERR_ARG on both routes.
  */
 rnl_status rmsnorm_linear_qkv_rope(const void *x, const void *gamma, const void *W, int64_t T,
                                    int64_t K, int64_t n_q_heads, int64_t n_kv_heads,

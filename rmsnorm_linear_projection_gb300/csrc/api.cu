@@ -226,6 +226,15 @@ bool fused_norm() {
   return e != nullptr && e[0] == '1';
 }
 
+// The QKV split + per-head norm + RoPE runs in the CTA-pair GEMM's epilogue
+// when head_dim is 128 and the projection runs on CTA pairs; otherwise (and
+// with RNL_QKV_ROPE_EPILOGUE=0) the projection writes y and the separate
+// stage (qkvrope.cu) reads it.  Both give results within the same bounds.
+bool qkv_rope_in_epilogue() {
+  const char* e = std::getenv("RNL_QKV_ROPE_EPILOGUE");
+  return e == nullptr || e[0] != '0';
+}
+
 }  // namespace
 
 // ------------------------------------------------------------ shared helpers
@@ -523,6 +532,41 @@ rnl_status rmsnorm_linear_qkv_rope(const void* x, const void* gamma, const void*
       (q_out && !aligned16(q_out)) || (k_out && !aligned16(k_out)) || (v_out && !aligned16(v_out)) ||
       (reinterpret_cast<uintptr_t>(positions) & 3u))
     return RNL_ERR_ALIGN;
+  if (head_dim == 128 && !fused_norm() && qkv_rope_in_epilogue() && gemm_uses_pair(T, N, K)) {
+    // the stage in the CTA-pair GEMM's epilogue: y is never written
+    if (!x || !W) return RNL_ERR_NULL;
+    if (K % 8 != 0 || !aligned16(x) || !aligned16(W) || (gamma && !aligned16(gamma)))
+      return RNL_ERR_ALIGN;
+    DeviceInfo dev;
+    rnl_status st = current_device(&dev);
+    if (st != RNL_OK) return st;
+    const BF16Layout l = bf16_layout(workspace, T, K, N, RNL_OUT_BF16);
+    cudaStream_t s = cs(stream);
+    st = norm_cast_stream_fits(K) ? launch_norm_cast_stream(x, gamma, T, K, eps, norm_mode, l.A, s)
+                                  : launch_norm_cast(x, gamma, T, K, eps, norm_mode, l.A, nullptr, s);
+    if (st != RNL_OK) return st;
+    GemmArgs g;
+    g.A = l.A;
+    g.B = W;
+    g.M = T;
+    g.N = N;
+    g.K = K;
+    g.epi = Epi::kBf16QkvRope;
+    g.partial_ws = l.part;
+    g.partial_ws_bytes = kGemmPartialBytes;
+    g.rope.Hq = static_cast<int>(n_q_heads);
+    g.rope.Hkv = static_cast<int>(n_kv_heads);
+    g.rope.q_gamma = q_gamma;
+    g.rope.k_gamma = k_gamma;
+    g.rope.eps = head_eps;
+    g.rope.pos = positions;
+    g.rope.cos_sin = cos_sin;
+    g.rope.P = static_cast<int>(max_pos);
+    g.rope.q = q_out;
+    g.rope.k = k_out;
+    g.rope.v = v_out;
+    return launch_gemm(g, s);
+  }
   rnl_status st = rmsnorm_linear_bf16(x, gamma, W, T, K, N, eps, norm_mode, y, RNL_OUT_BF16,
                                       workspace, proj, stream);
   if (st != RNL_OK) return st;

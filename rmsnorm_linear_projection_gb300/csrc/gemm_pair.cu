@@ -146,6 +146,84 @@ __device__ __forceinline__ int partners_end(const Sched& sc, int pair, int t) {
   return q;
 }
 
+// The QKV split + per-head RMSNorm + RoPE of one 128-wide head of row m, in
+// the epilogue (AT-10 pattern page, sec. 6, Qwen3PreAttn): y holds the
+// thread's 128 bf16-rounded projection values of the head (columns n_base ..
+// n_base + 127).  The same arithmetic as the separate stage (qkvrope.cu):
+// r = rsqrt(mean(y^2) + eps), z = bf16((y r) gamma), the rotate-half pairs
+// (i, i + 64) are both in this thread; v heads are copied.  A position
+// outside [0, P) skips the row's q / k heads and records RNL_ERR_ARG.
+__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ void rope_head_epilogue(const float (&y)[4][32], int64_t m, int n_base,
+                                                   int N, const RopeEpiArgs& a, unsigned int* err) {
+  constexpr int D = 128;
+  if (n_base >= N) return;
+  const int h = n_base / D;
+  const int nqk = a.Hq + a.Hkv;
+  if (h >= nqk) {  // v head: copied
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.v) + (m * a.Hkv + (h - nqk)) * D);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = bf16x2_bits(y[c][8 * q8 + 2 * i], y[c][8 * q8 + 2 * i + 1]);
+        dst[c * 4 + q8] = make_uint4(o[0], o[1], o[2], o[3]);  // 16-byte stores: q, k, v are 16-byte aligned
+      }
+    return;
+  }
+  const int p = __ldg(a.pos + m);
+  if (p < 0 || p >= a.P) {
+    atomicCAS(err, 0u, kErrArg | (40u << 8));
+    return;
+  }
+  const bool is_q = h < a.Hq;
+  const uint4* g4 = static_cast<const uint4*>(is_q ? a.q_gamma : a.k_gamma);
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ss = fmaf(y[c][j], y[c][j], ss);
+  const float r = rsqrtf(ss * (1.0f / D) + a.eps);
+  const float4* row = reinterpret_cast<const float4*>(a.cos_sin + static_cast<int64_t>(p) * D);
+  __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q) + (m * a.Hq + h) * D
+                            : static_cast<__nv_bfloat16*>(a.k) + (m * a.Hkv + (h - a.Hq)) * D;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int q8 = 0; q8 < 4; ++q8) {
+      const int i0 = c * 32 + q8 * 8;  // elements i0 .. i0 + 7 and their partners + 64
+      const uint4 gl = __ldg(g4 + i0 / 8), gh = __ldg(g4 + (i0 + 64) / 8);
+      const float4 c0 = __ldg(row + i0 / 4), c1 = __ldg(row + i0 / 4 + 1);
+      const float4 s0 = __ldg(row + (i0 + 64) / 4), s1 = __ldg(row + (i0 + 64) / 4 + 1);
+      const float co[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float si[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const uint32_t glw[4] = {gl.x, gl.y, gl.z, gl.w}, ghw[4] = {gh.x, gh.y, gh.z, gh.w};
+      uint32_t ol[4], oh[4];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        float lo[2], hi[2];
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+          const int e = 2 * e2 + t2;
+          const float g_lo = __uint_as_float(t2 ? (glw[e2] & 0xFFFF0000u) : (glw[e2] << 16));
+          const float g_hi = __uint_as_float(t2 ? (ghw[e2] & 0xFFFF0000u) : (ghw[e2] << 16));
+          const float zl = bf16r(__fmul_rn(__fmul_rn(y[c][q8 * 8 + e], r), g_lo));
+          const float zh = bf16r(__fmul_rn(__fmul_rn(y[c + 2][q8 * 8 + e], r), g_hi));
+          lo[t2] = __fsub_rn(__fmul_rn(zl, co[e]), __fmul_rn(zh, si[e]));
+          hi[t2] = __fadd_rn(__fmul_rn(zh, co[e]), __fmul_rn(zl, si[e]));
+        }
+        ol[e2] = bf16x2_bits(lo[0], lo[1]);
+        oh[e2] = bf16x2_bits(hi[0], hi[1]);
+      }
+      *reinterpret_cast<uint4*>(dst + i0) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+      *reinterpret_cast<uint4*>(dst + i0 + 64) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    }
+  }
+}
+
 template <int EPI, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -153,9 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      int dp_tiles, int sk_tiles, void* __restrict__ out,
                      const float* __restrict__ row_scale, const float* __restrict__ col_scale,
                      uint32_t* partial, uint64_t* flags, uint64_t epoch,
-                     const __nv_bfloat16* __restrict__ bias) {
+                     const __nv_bfloat16* __restrict__ bias, const RopeEpiArgs rope) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
                          EPI == static_cast<int>(Epi::kInt32));
+  constexpr bool kRope = EPI == static_cast<int>(Epi::kBf16QkvRope);
+  static_assert(!kRope || BN == 256, "the rope epilogue takes one 128-wide head per warp");
   constexpr int kStages = PairTile<BN>::kStages;
   constexpr uint32_t kStageBytes = PairTile<BN>::kStageBytes;
   constexpr int kBHalf = PairTile<BN>::kBHalf;
@@ -339,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < (kInt ? 32 : 1); ++j) iacc[c][j] = 0;
       }
+      float yv[kRope ? 4 : 1][kRope ? 32 : 1];  // the head's bf16-rounded projection values
       for (int u = 0; u < units; ++u, ++unit) {
         const uint32_t buf = unit & 1u;
         const uint32_t use = unit >> 1;
@@ -382,7 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
-            if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
+            if constexpr (kRope) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) yv[c][j] = bf16r(__uint_as_float(r[j]));
+            } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
               if (row_ok) {
                 if (bias != nullptr)
                   store_bf16_bias_32(out, m, n0, N, r, bias);
@@ -404,6 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      if constexpr (kRope) {
+        if (prow == nullptr && row_ok) rope_head_epilogue(yv, m, n_base, N, rope, &g_err_pair);
+      }
       if constexpr (kInt) {
         if (prow != nullptr) {
 #pragma unroll
@@ -558,7 +645,7 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
                                            static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                            pl.dp_tiles, pl.sk_tiles, g.out, g.row_scale,
                                            g.col_scale, partial, flags, next_flag_epoch(),
-                                           static_cast<const __nv_bfloat16*>(g.bias));
+                                           static_cast<const __nv_bfloat16*>(g.bias), g.rope);
   trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -598,15 +685,19 @@ template <int EPI>
 rnl_status launch_pair_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s,
                            const char* name) {
   const int pairs = resident_pairs(dev);
-  int bn = 256;  // 128- and 192-wide pair tiles measured slower per flop than one-CTA tiles
-  if (const char* e = std::getenv("RNL_GEMM_BN")) {
-    const int v = std::atoi(e);
-    if (v == 128 || v == 192 || v == 256) bn = v;
-  }
-  switch (bn) {
-    case 128: return launch_pair_bn<EPI, 128>(g, dev, pairs, s, name);
-    case 192: return launch_pair_bn<EPI, 192>(g, dev, pairs, s, name);
-    default: return launch_pair_bn<EPI, 256>(g, dev, pairs, s, name);
+  if constexpr (EPI == static_cast<int>(Epi::kBf16QkvRope)) {
+    return launch_pair_bn<EPI, 256>(g, dev, pairs, s, name);  // one 128-wide head per warp
+  } else {
+    int bn = 256;  // 128- and 192-wide pair tiles measured slower per flop than one-CTA tiles
+    if (const char* e = std::getenv("RNL_GEMM_BN")) {
+      const int v = std::atoi(e);
+      if (v == 128 || v == 192 || v == 256) bn = v;
+    }
+    switch (bn) {
+      case 128: return launch_pair_bn<EPI, 128>(g, dev, pairs, s, name);
+      case 192: return launch_pair_bn<EPI, 192>(g, dev, pairs, s, name);
+      default: return launch_pair_bn<EPI, 256>(g, dev, pairs, s, name);
+    }
   }
 }
 
@@ -646,7 +737,9 @@ rnl_status launch_gemm_pair(const GemmArgs& g, cudaStream_t s) {
     case Epi::kRowScaleF32: return launch_pair_epi<1>(g, dev, s, "gemm_pair_rowscale_f32");
     case Epi::kDequantBf16: return launch_pair_epi<2>(g, dev, s, "gemm_pair_int_dequant");
     case Epi::kInt32: return launch_pair_epi<3>(g, dev, s, "gemm_pair_int_s32");
-    case Epi::kDequantAccF32: return RNL_ERR_UNSUPPORTED;  // one-CTA kernel only
+    case Epi::kBf16QkvRope: return launch_pair_epi<6>(g, dev, s, "gemm_pair_qkv_rope");
+    case Epi::kDequantAccF32:
+    case Epi::kDequantBatchSum: return RNL_ERR_UNSUPPORTED;  // one-CTA kernel only
   }
   return RNL_ERR_ARG;
 }

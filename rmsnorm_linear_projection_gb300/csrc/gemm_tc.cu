@@ -502,8 +502,19 @@ rnl_status launch_bn(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, c
 
 }  // namespace
 
+bool gemm_uses_pair(int64_t M, int64_t N, int64_t K) {
+  DeviceInfo dev;
+  if (current_device(&dev) != RNL_OK) return false;
+  if (const char* e = std::getenv("RNL_GEMM_PAIR"))
+    if (e[0] == '0' || e[0] == '1') return e[0] == '1';
+  const int bn = pick_bn(M, N, K, dev.sm_count);
+  return N >= 256 && predict_pair_us(M, N, K, dev.sm_count, resident_pairs_for(dev)) <
+                         predict_one_cta_us(M, N, K, dev.sm_count, bn);
+}
+
 rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.M == 0) return RNL_OK;
+  if (g.epi == Epi::kBf16QkvRope) return launch_gemm_pair(g, s);  // the epilogue exists there only
   DeviceInfo dev;
   rnl_status st = current_device(&dev);
   if (st != RNL_OK) return st;
@@ -546,6 +557,7 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
       if (g.nbatch < 1 || g.nbatch > 65535 || (g.nbatch > 1 && g.batch_flags == nullptr))
         return RNL_ERR_ARG;
       return launch_bn<5>(g, dev, s, "gemm_int_batch_sum");
+    case Epi::kBf16QkvRope: return RNL_ERR_UNSUPPORTED;
   }
   return RNL_ERR_ARG;
 }

@@ -126,6 +126,25 @@ enum class Epi : int {
   // writes bf16 to out_final.  A is [nbatch * M, K], B is [nbatch * N, K],
   // row_scale is [nbatch * M]
   kDequantBatchSum = 5,
+  // bf16 projection y = bf16(acc) followed, in the CTA-pair kernel's
+  // epilogue, by the QKV split + per-head RMSNorm + RoPE of head_dim 128
+  // (each epilogue warp holds one 128-wide head of 32 rows); y itself is not
+  // written
+  kBf16QkvRope = 6,
+};
+
+// Arguments of the Epi::kBf16QkvRope epilogue (as rnl_qkv_rope's).
+struct RopeEpiArgs {
+  int Hq = 0, Hkv = 0;
+  const void* q_gamma = nullptr;  // bf16 [128]
+  const void* k_gamma = nullptr;  // bf16 [128]
+  float eps = 0.f;
+  const int32_t* pos = nullptr;   // [T]
+  const float* cos_sin = nullptr; // [P, 128]
+  int P = 0;
+  void* q = nullptr;  // bf16 [T, Hq, 128]
+  void* k = nullptr;  // bf16 [T, Hkv, 128]
+  void* v = nullptr;  // bf16 [T, Hkv, 128]
 };
 
 struct GemmArgs {
@@ -157,6 +176,8 @@ struct GemmArgs {
   // or not: each launch uses its own tag
   int nbatch = 1;
   uint64_t* batch_flags = nullptr;
+  // Epi::kBf16QkvRope only
+  RopeEpiArgs rope;
 };
 // Bytes of the flags of Epi::kDequantBatchSum for M x N outputs.
 inline size_t batch_flag_bytes(int64_t M, int64_t N) {
@@ -173,6 +194,8 @@ rnl_status launch_gemm_pair(const GemmArgs& g, cudaStream_t s);
 // A fresh tag for the cross-CTA flags of one launch (clock-seeded per-process
 // counter, gemm_pair.cu): flags left in a reused workspace never match.
 uint64_t next_flag_epoch();
+// Whether launch_gemm runs a plain GEMM of this shape on CTA pairs.
+bool gemm_uses_pair(int64_t M, int64_t N, int64_t K);
 // Predicted pair-kernel time (microseconds) and resident CTA pairs (gemm_pair.cu).
 double predict_pair_us(int64_t M, int64_t N, int64_t K, int sm_count, int pairs);
 int resident_pairs_for(const DeviceInfo& dev);

@@ -155,3 +155,59 @@ def test_qkv_rope_bad_position_is_reported_and_context_survives(orc):
                       qg, kg, 1e-6, pos[keep], cs, "good tokens")
     got2 = _run(y, Hq, Hkv, D, qg, kg, pos, cs)
     assert_rope_close(orc, got2, want, y, Hq, Hkv, D, qg, kg, 1e-6, pos, cs, "after the error")
+
+
+@pytest.fixture
+def rope_route(monkeypatch):
+    """Set the environment that picks the chain's route (CTA pairs forced, the
+    stage in the GEMM epilogue or separate)."""
+    def set_route(pair, epilogue):
+        monkeypatch.setenv("RNL_GEMM_PAIR", "1" if pair else "0")
+        monkeypatch.setenv("RNL_QKV_ROPE_EPILOGUE", "1" if epilogue else "0")
+    return set_route
+
+
+@pytest.mark.parametrize("T,K,Hq,Hkv", [(300, 520, 4, 2), (777, 1024, 6, 3), (64, 256, 2, 1)])
+def test_qkv_rope_chain_in_pair_epilogue(orc, rope_route, T, K, Hq, Hkv):
+    """The stage fused into the CTA-pair GEMM's epilogue (forced onto pairs at
+    sizes where stream-K finishers add partner partial sums before it), and
+    the separate route on the same inputs: both against the oracle chain."""
+    D, P = 128, 1000
+    N = (Hq + 2 * Hkv) * D
+    d = si.make_projection(dict(seed=T + K, T=T, K=K, N=N, has_gamma=True))
+    _, qg, kg, pos, cs = _case(T + 1, T, Hq, Hkv, D, P)
+    _, y_ref = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, 0, 0)
+    want = orc.qkv_rope(y_ref, Hq, Hkv, D, qg, kg, 1e-6, pos, cs)
+    for epilogue in (True, False):
+        rope_route(True, epilogue)
+        q, k, v = rnl.rmsnorm_linear_qkv_rope(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]),
+                                              Hq, Hkv, D, dev_bf16(qg), dev_bf16(kg),
+                                              torch.from_numpy(pos).cuda(), torch.from_numpy(cs).cuda())
+        got = (host_bits(q), host_bits(k), host_bits(v))
+        assert_rope_close(orc, got, want, y_ref, Hq, Hkv, D, qg, kg, 1e-6, pos, cs,
+                          f"epilogue={epilogue}", chain=True)
+
+
+def test_qkv_rope_epilogue_bad_position(orc, rope_route):
+    """A bad position on the fused route: RNL_ERR_ARG, the other tokens right."""
+    T, K, Hq, Hkv, D, P = 260, 256, 2, 1, 128, 64
+    N = (Hq + 2 * Hkv) * D
+    d = si.make_projection(dict(seed=9, T=T, K=K, N=N, has_gamma=True))
+    _, qg, kg, pos, cs = _case(10, T, Hq, Hkv, D, P)
+    pos_bad = pos.copy()
+    pos_bad[7] = -1
+    rope_route(True, True)
+    rnl.rnl_check_device_error()
+    q, k, v = rnl.rmsnorm_linear_qkv_rope(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]),
+                                          Hq, Hkv, D, dev_bf16(qg), dev_bf16(kg),
+                                          torch.from_numpy(pos_bad).cuda(), torch.from_numpy(cs).cuda())
+    with pytest.raises(rnl.RnlError) as e:
+        rnl.rnl_check_device_error()
+    assert e.value.status == 4  # RNL_ERR_ARG
+    rnl.rnl_check_device_error()  # cleared
+    _, y_ref = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, 0, 0)
+    want = orc.qkv_rope(y_ref, Hq, Hkv, D, qg, kg, 1e-6, pos, cs)
+    keep = np.array([t for t in range(T) if t != 7])
+    got = (host_bits(q)[keep], host_bits(k)[keep], host_bits(v)[keep])
+    assert_rope_close(orc, got, tuple(w[keep] for w in want), y_ref[keep], Hq, Hkv, D, qg, kg, 1e-6, pos[keep],
+                      cs, "good tokens", chain=True)
