@@ -56,8 +56,6 @@ TRAFFIC = {
     # gemm_pair_kernel<0,256>: 96.80 MB read + 40.96 MB written
     # (profiles/qkv_step_kernels_4096x6144x4096.md)
     "qkv": 137.75e6,
-    # the same kernel on the same shape and inputs ahead of the rope stage
-    "qkv_rope": 137.75e6,
     # both MLA GEMM stages: 51.79 MB (one CTA, BN 192) + 155.09 MB (pairs)
     # (profiles/mla_gemm_stages_2048x7168x1536x24576.md); the same stages in mla_hn
     "mla": 206.88e6,
