@@ -518,6 +518,24 @@ def run_reference(args):
     return 0
 
 
+# --------------------------------------------------------------- ranks
+def max_over_ranks(seconds: float, dist) -> float:
+    """The job's time: the slowest rank's (every rank gets it); the value itself
+    when the run is not distributed."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, amount: float, seconds: float) -> float:
+    """Whole-job throughput: every rank runs `steps` steps of `amount` units
+    (an independent replica), all in the job's time."""
+    return world * steps * amount / seconds
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -595,14 +613,10 @@ def run_ours(args):
     trace = rnl.rnl_trace_read()
     rnl.rnl_check_device_error()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_s = sum(step_ms) / 1e3
-    if dist is not None:
-        tt = torch.tensor([total_s], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
+    total_s = max_over_ranks(sum(step_ms) / 1e3, dist)
 
     unit, amount = w.unit()
-    value = world * args.steps * amount / total_s
+    value = job_throughput(world, args.steps, amount, total_s)
 
     # roofline of the dominant kernel, from the library's per-launch events
     peaks = _peaks()
@@ -665,13 +679,9 @@ def run_ours(args):
         for _ in range(n_e2e):
             tk = submit()
         rnl.rnl_pipeline_wait(pipe, tk)
-        te = time.perf_counter() - te0
-        if dist is not None:
-            tt = torch.tensor([te], dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
+        te = max_over_ranks(time.perf_counter() - te0, dist)
         rnl.rnl_pipeline_destroy(pipe)
-        e2e = {"value": world * n_e2e * amount / te, "unit": unit, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(world, n_e2e, amount, te), "unit": unit, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e, "ms_per_step": te * 1e3 / n_e2e,
                "api": "rnl_pipeline_submit_* / rnl_pipeline_wait (host pointers, C ABI)",
                "copies": "x host->device and the output device->host every step (pinned, copy engines, "
