@@ -56,6 +56,9 @@ TRAFFIC = {
     # gemm_pair_kernel<0,256>: 96.80 MB read + 40.96 MB written
     # (profiles/qkv_step_kernels_4096x6144x4096.md)
     "qkv": 137.75e6,
+    # gemm_pair_kernel<6,256>, the rope stage in its epilogue: 117.41 MB read + 44.95 MB written
+    # (profiles/qkv_rope_fused_gemm_4096x6144x4096.md)
+    "qkv_rope": 162.36e6,
     # both MLA GEMM stages: 51.79 MB (one CTA, BN 192) + 155.09 MB (pairs)
     # (profiles/mla_gemm_stages_2048x7168x1536x24576.md); the same stages in mla_hn
     "mla": 206.88e6,
