@@ -226,6 +226,14 @@ bool fused_norm() {
   return e != nullptr && e[0] == '1';
 }
 
+// Up to 4 tokens against a weight of at least 1024 rows (a decode step) run
+// as a matrix-vector product that spreads the weight's rows over every SM
+// (decode.cu); RNL_DECODE=0 sends them to the tensor-core path.
+bool decode_path() {
+  const char* e = std::getenv("RNL_DECODE");
+  return e == nullptr || e[0] != '0';
+}
+
 // The QKV split + per-head norm + RoPE runs in the CTA-pair GEMM's epilogue
 // when head_dim is 128 and the projection runs on CTA pairs; otherwise (and
 // with RNL_QKV_ROPE_EPILOGUE=0) the projection writes y and the separate
@@ -381,6 +389,8 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
   const BF16Layout l = bf16_layout(workspace, T, K, N, out_dtype);
   cudaStream_t s = cs(stream);
 
+  if (out_dtype == RNL_OUT_BF16 && decode_path() && !fused_norm() && decode_fits(T, K, N))
+    return launch_decode(x, gamma, W, T, K, N, eps, norm_mode, out, dev.sm_count, s);
   if (out_dtype == RNL_OUT_BF16) {
     GemmArgs g;
     g.B = W;

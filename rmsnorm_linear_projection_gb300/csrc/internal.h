@@ -94,6 +94,13 @@ rnl_status launch_mx_dequant2(const uint8_t* a_codes, const uint8_t* a_scale, in
                               const uint8_t* b_codes, const uint8_t* b_scale, int64_t N, int64_t K,
                               int64_t block, void* A, void* B, cudaStream_t s);
 
+// ---- a few tokens against a wide weight (decode.cu) ----
+// T <= 4 rows, K >= 2048, N >= 1024 outputs, the normalised rows within 96 KB.
+bool decode_fits(int64_t T, int64_t K, int64_t N);
+// AT-10 RMSNorm + Linear, bf16 out, the weight's rows spread over every SM.
+rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
+                         int64_t N, float eps, int mode, void* out, int sm_count, cudaStream_t s);
+
 // ---- per-head RMSNorm (headnorm.cu) ----
 // head_dim a multiple of 64 in [64, 512]
 bool head_norm_dim_ok(int64_t D);

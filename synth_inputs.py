@@ -26,6 +26,8 @@ Workload recipes (shapes and distributions of the five projection cases):
              on [-127,127], w_scale[4096] fp32 ~U(1e-3,1e-2), eps 1e-6.
 * ``skinny`` x[16384,28672] ~N(0,1), no gamma, W[24,28672] ~N(0,0.02),
              eps 1e-6, rsqrt form, fp32 out (mhc_pre-style).
+* ``decode`` x[4,4096] ~N(0,1), gamma ~U(0.5,1.5), W[6144,4096] ~N(0,0.02): a decode
+             step of 4 tokens through the qkv weight, eps 1e-6, rsqrt form, bf16 out.
 * ``mxfp8``  x[4096,4096] ~N(0,1), gamma ~U(0.5,1.5), an MXFP8 weight [6144,4096]
              drawn directly as bytes: E4M3 codes with uniform sign, exponent
              field uniform on [10, 15] and mantissa uniform (the NaN pattern
@@ -62,6 +64,9 @@ CONFIGS = {
     "qmrs": dict(B=4, M=2048, K=4096, N=4096, seed=1005),
     # the qkv projection followed by the QKV split + per-head RMSNorm + RoPE
     # stage (Qwen3 layout: 32 query heads and 8 key/value heads of 128)
+    # a decode step: 4 tokens through the qkv weight (bound by reading W once)
+    "decode": dict(T=4, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
+                   out_dtype="bf16", seed=1007),
     # the qkv projection shape in MXFP8 mode (one E8M0 scale per 64 elements)
     "mxfp8": dict(T=4096, K=4096, N=6144, eps=1e-6, norm_mode=0, has_gamma=True,
                   out_dtype="bf16", block=64, seed=1006),

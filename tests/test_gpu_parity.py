@@ -59,6 +59,27 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
     assert_bf16_close(host_bits(out), want, f"bf16 {T}x{K}x{N}")
 
 
+@pytest.mark.parametrize("T,K,N,mode,gamma", [
+    (1, 4096, 6144, 0, True),   # one decode token through the qkv weight
+    (4, 4096, 1024, 1, False),  # the token limit
+    (4, 12288, 2048, 0, True),  # 96 KB of normalised rows
+    (3, 2056, 2000, 0, True),   # rows of 257 vectors: a ragged last lane stride
+    (2, 2048, 1025, 1, True),   # a ragged weight
+    (5, 4096, 1024, 0, True),   # beyond the token limit: the tensor-core path either way
+])
+@pytest.mark.parametrize("decode", ["1", "0"])
+def test_bf16_decode_sized_both_paths(orc, monkeypatch, decode, T, K, N, mode, gamma):
+    """Up to 4 tokens against a wide weight run as a matrix-vector product
+    over every SM (RNL_DECODE=0 sends them to the tensor-core path): both
+    against the oracle."""
+    monkeypatch.setenv("RNL_DECODE", decode)
+    d = _rand_case(13 + T + K + N, T, K, N, gamma)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]) if gamma else None,
+                                  dev_bf16(d["W"]), eps=1e-6, norm_mode=mode)
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, mode, 0)
+    assert_bf16_close(host_bits(out), want, f"decode={decode} {T}x{K}x{N}")
+
+
 @pytest.mark.parametrize("bn", [128, 192, 256])
 @pytest.mark.parametrize("T,K,N", [(300, 520, 600), (129, 4096, 256)])
 def test_bf16_each_tile_width(orc, monkeypatch, bn, T, K, N):
