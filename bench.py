@@ -54,27 +54,30 @@ METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 # only for kernels unchanged since the capture.
 TRAFFIC = {
     # gemm_pair_kernel<0,256>: 96.80 MB read + 40.96 MB written
-    # (profiles/qkv_step_kernels_4096x6144x4096.md)
+    # (one ncu capture)
     "qkv": 137.75e6,
     # gemm_pair_kernel<6,256>, the rope stage in its epilogue: 117.41 MB read + 44.95 MB written
-    # (profiles/qkv_rope_fused_gemm_4096x6144x4096.md)
+    # (one ncu capture)
     "qkv_rope": 162.36e6,
     # both MLA GEMM stages: 51.79 MB (one CTA, BN 192) + 155.09 MB (pairs)
-    # (profiles/mla_gemm_stages_2048x7168x1536x24576.md); the same stages in mla_hn
+    # (one ncu capture; the same stages in mla_hn)
     "mla": 206.88e6,
     "mla_hn": 206.88e6,
     # gemm_kernel<2,256,0>: 121.75 MB read + 45.24 MB written
-    # (profiles/w8a8_front_and_int_gemm_8192x4096x4096.md)
+    # (one ncu capture)
     "w8a8": 167.00e6,
     # gemm_kernel<5,256,0>, all batches: 289.46 MB read + 85.07 MB written
-    # (profiles/qmrs_prep_and_batch_gemm_4x2048x4096x4096.md)
+    # (one ncu capture)
     "qmrs": 374.53e6,
     # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.24 MB read + 39.96 MB written
-    # (profiles/mxfp8_front_and_gemm_4096x4096x6144.md)
+    # (one ncu capture)
     "mxfp8": 137.20e6,
-    # skinny_kernel<32,0>: 123.03 MB at T = 2048, scaled by rows to T = 16384
-    # (profiles/skinny_stream_mhc_pre.md)
+    # skinny_kernel<32,0>: 123.03 MB in an ncu capture at T = 2048, scaled by
+    # rows to T = 16384
     "skinny": 984.2e6,
+    # decode_kernel<0,4>: 50.39 MB read (the 49 KB output stays in L2)
+    # (one ncu capture)
+    "decode": 50.40e6,
 }
 
 
@@ -764,6 +767,13 @@ def run_ours(args):
                    "value_at_graph_rate": amount / (us * 1e-6), "unit": unit,
                    "note": "GPU time per call: CUDA graph, L2 flushed before every call, the flushes' time subtracted"}
         del g_flush, g_both
+        # the one kernel of the call, timed without the host's launch in
+        # front of it: the graph's time per call is the roofline duration
+        if roofline is not None and us > 0:
+            achieved = w.dominant()[2] / (us * 1e-6) / 1e9
+            roofline.update({"achieved": achieved, "frac": achieved / roofline["peak"],
+                             "stage_ms_per_step": us * 1e-3,
+                             "duration_source": "CUDA graph of flushed calls (GPU time per call)"})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu and not args.T:

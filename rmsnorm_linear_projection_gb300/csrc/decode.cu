@@ -1,21 +1,27 @@
 // decode.cu -- the AT-10 RMSNorm + Linear (bf16 out) for a handful of tokens
-// (T <= 8, a decode step) against a wide weight.  With so few rows the
+// (T <= 4, a decode step) against a wide weight.  With so few rows the
 // projection is a matrix-vector product bound by reading W once: the
 // tensor-core GEMM would use one 128-row tile per weight block and occupy a
 // fraction of the SMs (about 1.7 TB/s measured at T = 1 against the qkv
 // weight), so this kernel spreads W's rows over every SM instead:
 //
-//   every CTA normalises the T rows into shared memory, all its threads
-//   sharing each row (AT-10 pattern page, sec. 3: rstd = rsqrt(mean(x^2) +
-//   eps) | 1 / sqrt(...), a = bf16((x rstd) gamma));
-//   each warp then takes weight rows n in turn (grid-stride, every warp the
-//   same number of rows, the grid resident at once), streams the row with
-//   16-byte loads (four in flight per lane; the first row's issued before
-//   the norm), accumulates the T dot products in FP32 and reduces them across
-//   the warp: out[t, n] = bf16(sum).
+//   every CTA normalises the T rows into shared memory (AT-10 pattern page,
+//   sec. 3: rstd = rsqrt(mean(x^2) + eps) | 1 / sqrt(...),
+//   a = bf16((x rstd) gamma)): one read of x from global memory, the raw rows
+//   parked in shared memory and normalised in place;
+//   each warp then takes weight rows n = w, w + W, ... (W = the warps of the
+//   whole grid, which is resident at once) and streams them as one sequence
+//   of chunks (8 16-byte loads per lane, 4 KB per warp) with the next chunk's
+//   loads issued before the current one is used, so that two chunks are in
+//   flight per warp across row boundaries; the first chunk's loads go out
+//   before the norm;
+//   the T dot products accumulate in FP32 with the mixed-precision FMA
+//   (bf16 x bf16 + f32, one rounding: the bf16 product is exact, so this
+//   equals widening both operands and an FP32 fma), then reduce across the
+//   warp: out[t, n] = bf16(sum).
 //
-// bf16 products are exact in FP32; the summation order differs from the
-// tensor-core path, inside the same bf16 output bound.
+// The summation order differs from the tensor-core path, inside the same
+// bf16 output bound.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -23,10 +29,10 @@
 namespace rnl {
 namespace {
 
-constexpr int kMaxTokens = 8;
+constexpr int kMaxTokens = 4;
 constexpr int kWarps = 8;
 constexpr int kSmemMax = 96 * 1024;  // the normalised rows: T * K * 2 bytes
-constexpr int kInFlight = 4;         // 16-byte weight loads in flight per lane
+constexpr int kChunk = 8;            // 16-byte weight loads per lane per chunk
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -42,40 +48,58 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kWarps * 32)
+// acc_lo += a.lo * w.lo, acc_hi += a.hi * w.hi on the two bf16 halves of a
+// word, each product and sum rounded once to FP32.
+__device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t w, float& acc_lo, float& acc_hi) {
+  asm("{\n\t.reg .b16 al, ah, wl, wh;\n\t"
+      "mov.b32 {al, ah}, %2;\n\t"
+      "mov.b32 {wl, wh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, wl, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ah, wh, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(a), "r"(w));
+}
+
+// chunk q of weight row n: vectors lane + 32 * (q * kChunk + i), i < kChunk
+__device__ __forceinline__ void load_chunk(const uint4* __restrict__ W, int n, int q, int nvec, int lane,
+                                           uint4 (&buf)[kChunk]) {
+  const uint4* wr = W + static_cast<int64_t>(n) * nvec;
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) {
+    const int v = lane + 32 * (q * kChunk + i);
+    buf[i] = v < nvec ? __ldcs(wr + v) : make_uint4(0u, 0u, 0u, 0u);  // read once: do not keep in L2
+  }
+}
+
+template <int MODE, int T>
+__global__ void __launch_bounds__(kWarps * 32, 2)
     decode_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma,
-                  const uint4* __restrict__ W, int T, int nvec, int N, float inv_d, float eps,
+                  const uint4* __restrict__ W, int nvec, int N, float inv_d, float eps,
                   __nv_bfloat16* __restrict__ out) {
   extern __shared__ uint4 a_s[];  // [T][nvec]
   __shared__ float red[kWarps][kMaxTokens];
   __shared__ float rstd_s[kMaxTokens];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // the first weight row's first loads go out before the norm, which does
-  // not need them: their round trip overlaps it
   const int stride = gridDim.x * kWarps;
-  const int n_first = blockIdx.x * kWarps + warp;
-  uint4 w_first[kInFlight];
-#pragma unroll
-  for (int i = 0; i < kInFlight; ++i) {
-    const int v = lane + 32 * i;
-    w_first[i] = (n_first < N && v < nvec) ? __ldcs(W + static_cast<int64_t>(n_first) * nvec + v)
-                                           : make_uint4(0u, 0u, 0u, 0u);
-  }
-  // 1. the normalised rows: all 256 threads share every row (thread i takes
-  //    vectors i, i + 256, ...), the rows' loads issued together
+  const int cpr = (nvec + 32 * kChunk - 1) / (32 * kChunk);  // chunks per weight row
+  int n = blockIdx.x * kWarps + warp, q = 0;
+  uint4 cur[kChunk];
+  if (n < N) load_chunk(W, n, 0, nvec, lane, cur);
+
+  // 1. the normalised rows: thread i takes vectors i, i + 256, ... of every
+  //    row; the raw vectors stay in shared memory for the second pass, which
+  //    touches only the thread's own vectors
   {
-    float ss[kMaxTokens];
+    float ss[T];
 #pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t) ss[t] = 0.f;
+    for (int t = 0; t < T; ++t) ss[t] = 0.f;
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      uint4 u[kMaxTokens];
+      uint4 u[T];
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t)
-        if (t < T) u[t] = __ldg(x + static_cast<int64_t>(t) * nvec + v);
+      for (int t = 0; t < T; ++t) u[t] = __ldg(x + static_cast<int64_t>(t) * nvec + v);
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t) {
-        if (t >= T) break;
+      for (int t = 0; t < T; ++t) {
+        a_s[t * nvec + v] = u[t];
         float f[8];
         unpack8(u[t], f);
 #pragma unroll
@@ -85,11 +109,10 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t)
-        if (t < T) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+      for (int t = 0; t < T; ++t) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
     if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t) red[warp][t] = ss[t];
+      for (int t = 0; t < T; ++t) red[warp][t] = ss[t];
     }
     __syncthreads();
     if (threadIdx.x < T) {
@@ -99,17 +122,18 @@ __global__ void __launch_bounds__(kWarps * 32)
       rstd_s[threadIdx.x] = MODE == 0 ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
     }
     __syncthreads();
+    float r[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) r[t] = rstd_s[t];
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
       float g[8];
       if (gamma != nullptr) unpack8(__ldg(gamma + v), g);
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t) {
-        if (t >= T) break;
+      for (int t = 0; t < T; ++t) {
         float f[8];
-        unpack8(__ldg(x + static_cast<int64_t>(t) * nvec + v), f);
-        const float r = rstd_s[t];
+        unpack8(a_s[t * nvec + v], f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], r);
+        for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], r[t]);
         if (gamma != nullptr) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], g[j]);
@@ -119,59 +143,61 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
   __syncthreads();
-  // 2. weight rows, one warp each
-  bool first = true;
-  for (int n = n_first; n < N; n += stride) {
-    const uint4* wr = W + static_cast<int64_t>(n) * nvec;
-    float acc[kMaxTokens];
+
+  // 2. the weight rows as one stream of chunks, the next chunk in flight
+  float acc_lo[T], acc_hi[T];
 #pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t) acc[t] = 0.f;
-    int v = lane;
-    for (; v + 32 * (kInFlight - 1) < nvec; v += 32 * kInFlight) {  // kInFlight loads in flight per lane
-      uint4 w4[kInFlight];
-      if (first) {
+  for (int t = 0; t < T; ++t) acc_lo[t] = acc_hi[t] = 0.f;
+  while (n < N) {
+    int n2 = n, q2 = q + 1;
+    if (q2 == cpr) {
+      q2 = 0;
+      n2 = n + stride;
+    }
+    uint4 nxt[kChunk];
+    if (n2 < N) load_chunk(W, n2, q2, nvec, lane, nxt);
 #pragma unroll
-        for (int i = 0; i < kInFlight; ++i) w4[i] = w_first[i];
-        first = false;
-      } else {
+    for (int i = 0; i < kChunk; ++i) {
+      const int v = lane + 32 * (q * kChunk + i);
+      if (v < nvec) {
 #pragma unroll
-        for (int i = 0; i < kInFlight; ++i) w4[i] = __ldcs(wr + v + 32 * i);  // read once: do not keep in L2
-      }
-#pragma unroll
-      for (int i = 0; i < kInFlight; ++i) {
-        float w[8];
-        unpack8(w4[i], w);
-#pragma unroll
-        for (int t = 0; t < kMaxTokens; ++t) {
-          if (t >= T) break;
-          float a[8];
-          unpack8(a_s[t * nvec + v + 32 * i], a);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[t] = fmaf(a[j], w[j], acc[t]);
+        for (int t = 0; t < T; ++t) {
+          const uint4 a = a_s[t * nvec + v];
+          fma2_bf16(a.x, cur[i].x, acc_lo[t], acc_hi[t]);
+          fma2_bf16(a.y, cur[i].y, acc_lo[t], acc_hi[t]);
+          fma2_bf16(a.z, cur[i].z, acc_lo[t], acc_hi[t]);
+          fma2_bf16(a.w, cur[i].w, acc_lo[t], acc_hi[t]);
         }
       }
     }
-    first = false;  // a row shorter than kInFlight vectors a lane: the tail loop reloads
-    for (; v < nvec; v += 32) {
-      float w[8];
-      unpack8(__ldcs(wr + v), w);
+    if (q == cpr - 1) {  // the row is complete: reduce across the warp
+      float s[T];
 #pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t) {
-        if (t >= T) break;
-        float a[8];
-        unpack8(a_s[t * nvec + v], a);
+      for (int t = 0; t < T; ++t) s[t] = acc_lo[t] + acc_hi[t];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[t] = fmaf(a[j], w[j], acc[t]);
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int t = 0; t < T; ++t) s[t] += __shfl_xor_sync(0xffffffffu, s[t], o);
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        if (lane == t) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(s[t]);
+        acc_lo[t] = acc_hi[t] = 0.f;
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int t = 0; t < kMaxTokens; ++t)
-        if (t < T) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-#pragma unroll
-    for (int t = 0; t < kMaxTokens; ++t)
-      if (t < T && lane == t) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(acc[t]);
+    for (int i = 0; i < kChunk; ++i) cur[i] = nxt[i];
+    n = n2;
+    q = q2;
+  }
+}
+
+template <int MODE>
+void* decode_entry(int64_t T) {
+  switch (T) {
+    case 1: return reinterpret_cast<void*>(decode_kernel<MODE, 1>);
+    case 2: return reinterpret_cast<void*>(decode_kernel<MODE, 2>);
+    case 3: return reinterpret_cast<void*>(decode_kernel<MODE, 3>);
+    default: return reinterpret_cast<void*>(decode_kernel<MODE, 4>);
   }
 }
 
@@ -182,39 +208,42 @@ __global__ void __launch_bounds__(kWarps * 32)
 // and rows of at least 2048 elements (at 1536 many short rows measured
 // slightly slower: 26.3 against 25.0 us for 1 x 1536 -> 24576).
 bool decode_fits(int64_t T, int64_t K, int64_t N) {
-  return T >= 1 && T <= 4 && K >= 2048 && N >= 1024 && T * K * 2 <= kSmemMax;
+  return T >= 1 && T <= kMaxTokens && K >= 2048 && N >= 1024 && T * K * 2 <= kSmemMax;
 }
 
 rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
                          int64_t N, float eps, int mode, void* out, int sm_count, cudaStream_t s) {
-  static bool attr_set[64][2] = {};
+  static bool attr_set[64][2][kMaxTokens] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RNL_ERR_DEVICE;
+  if (T < 1 || T > kMaxTokens) return RNL_ERR_SHAPE;
   const int nvec = static_cast<int>(K / 8);
   const size_t smem = static_cast<size_t>(T) * K * 2;
-  auto kern = mode == RNL_NORM_RSQRT ? decode_kernel<0> : decode_kernel<1>;
   const int mi = mode == RNL_NORM_RSQRT ? 0 : 1;
-  if (smem > 48 * 1024 && !attr_set[dev][mi]) {
+  void* kern = mi == 0 ? decode_entry<0>(T) : decode_entry<1>(T);
+  if (smem > 48 * 1024 && !attr_set[dev][mi][T - 1]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) != cudaSuccess)
       return RNL_ERR_LAUNCH;
-    attr_set[dev][mi] = true;
+    attr_set[dev][mi][T - 1] = true;
   }
-  // every warp the same number of weight rows, all CTAs resident at once
+  // the whole grid resident at once, each warp at least one weight row
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess ||
       per_sm < 1) {
     cudaGetLastError();
     per_sm = 1;
   }
-  const int64_t warps = static_cast<int64_t>(per_sm) * sm_count * kWarps;
-  const int64_t rows_per_warp = (N + warps - 1) / warps;
-  const int64_t grid = (N + kWarps * rows_per_warp - 1) / (kWarps * rows_per_warp);
+  const int64_t grid = std::min<int64_t>(static_cast<int64_t>(per_sm) * sm_count, (N + kWarps - 1) / kWarps);
+  const uint4* xp = static_cast<const uint4*>(x);
+  const uint4* gp = static_cast<const uint4*>(gamma);
+  const uint4* wp = static_cast<const uint4*>(W);
+  int nv = nvec, nn = static_cast<int>(N);
+  float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
+  __nv_bfloat16* op = static_cast<__nv_bfloat16*>(out);
+  void* args[] = {&xp, &gp, &wp, &nv, &nn, &inv_d, &eps, &op};
   trace_before(s);
-  kern<<<static_cast<unsigned>(grid), kWarps * 32, smem, s>>>(
-      static_cast<const uint4*>(x), static_cast<const uint4*>(gamma), static_cast<const uint4*>(W),
-      static_cast<int>(T), nvec, static_cast<int>(N), static_cast<float>(1.0 / static_cast<double>(K)), eps,
-      static_cast<__nv_bfloat16*>(out));
-  const rnl_status st = cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+  const cudaError_t e = cudaLaunchKernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kWarps * 32), args, smem, s);
+  const rnl_status st = e == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
   trace_after(s, "decode_gemv");
   return st;
 }

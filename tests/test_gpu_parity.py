@@ -65,6 +65,8 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
     (4, 12288, 2048, 0, True),  # 96 KB of normalised rows
     (3, 2056, 2000, 0, True),   # rows of 257 vectors: a ragged last lane stride
     (2, 2048, 1025, 1, True),   # a ragged weight
+    (2, 7168, 1536, 1, True),   # the MLA q_a weight: 3.5 chunks a row
+    (2, 2056, 5000, 0, True),   # several rows a warp, each row's second chunk one vector
     (5, 4096, 1024, 0, True),   # beyond the token limit: the tensor-core path either way
 ])
 @pytest.mark.parametrize("decode", ["1", "0"])
