@@ -53,25 +53,25 @@ METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 # roofline stage per step, from the ncu captures summarised under profiles/;
 # only for kernels unchanged since the capture.
 TRAFFIC = {
-    # gemm_pair_kernel<0,256>: 96.80 MB read + 40.96 MB written
+    # gemm_pair_kernel<0,256>: 97.96 MB read + 39.78 MB written
     # (one ncu capture)
     "qkv": 137.75e6,
     # gemm_pair_kernel<6,256>, the rope stage in its epilogue: 117.41 MB read + 44.95 MB written
     # (one ncu capture)
     "qkv_rope": 162.36e6,
-    # both MLA GEMM stages: 51.79 MB (one CTA, BN 192) + 155.09 MB (pairs)
+    # both MLA GEMM stages: 51.86 MB (one CTA, BN 192) + 154.96 MB (pairs)
     # (one ncu capture; the same stages in mla_hn)
-    "mla": 206.88e6,
-    "mla_hn": 206.88e6,
+    "mla": 206.82e6,
+    "mla_hn": 206.82e6,
     # gemm_kernel<2,256,0>: 121.75 MB read + 45.24 MB written
     # (one ncu capture)
     "w8a8": 167.00e6,
     # gemm_kernel<5,256,0>, all batches: 289.46 MB read + 85.07 MB written
     # (one ncu capture)
     "qmrs": 374.53e6,
-    # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.24 MB read + 39.96 MB written
+    # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.23 MB read + 39.94 MB written
     # (one ncu capture)
-    "mxfp8": 137.20e6,
+    "mxfp8": 137.17e6,
     # skinny_kernel<32,0>: 123.03 MB in an ncu capture at T = 2048, scaled by
     # rows to T = 16384
     "skinny": 984.2e6,
