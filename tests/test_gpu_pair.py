@@ -28,7 +28,8 @@ def _case(seed, T, K, N, gamma=True):
 
 
 @pytest.mark.parametrize("T,K,N", [(256, 64, 256), (300, 520, 600), (129, 4096, 256),
-                                   (1000, 1024, 700), (16, 256, 128)])
+                                   (1000, 1024, 700), (16, 256, 128),
+                                   (600, 3000, 1000)])  # 12 tiles in 5 k ranges: split-K pieces
 def test_pair_bf16(orc, T, K, N):
     d = _case(T + K + N, T, K, N)
     out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
