@@ -75,7 +75,7 @@ TRAFFIC = {
     # skinny_kernel<32,0>: 123.03 MB in an ncu capture at T = 2048, scaled by
     # rows to T = 16384
     "skinny": 984.2e6,
-    # decode_kernel<0,4>: 50.39 MB read (the 49 KB output stays in L2)
+    # decode_kernel<0,4,2>: 50.40 MB read (the 49 KB output stays in L2)
     # (one ncu capture)
     "decode": 50.40e6,
 }

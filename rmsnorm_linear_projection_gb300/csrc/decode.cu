@@ -9,20 +9,22 @@
 //   sec. 3: rstd = rsqrt(mean(x^2) + eps) | 1 / sqrt(...),
 //   a = bf16((x rstd) gamma)): one read of x from global memory, the raw rows
 //   parked in shared memory and normalised in place;
-//   each warp then takes weight rows n = w, w + W, ... (W = the warps of the
-//   whole grid, which is resident at once) and streams them as one sequence
-//   of chunks (8 16-byte loads per lane, 4 KB per warp) with the next chunk's
-//   loads issued before the current one is used, so that two chunks are in
-//   flight per warp across row boundaries; the first chunk's loads go out
-//   before the norm;
-//   the T dot products accumulate in FP32 with the mixed-precision FMA
-//   (bf16 x bf16 + f32, one rounding: the bf16 product is exact, so this
-//   equals widening both operands and an FP32 fma), then reduce across the
-//   warp: out[t, n] = bf16(sum).
+//   each warp then takes groups of R adjacent weight rows, g = w, w + W, ...
+//   (W = the warps of the whole grid, which is resident at once), and streams
+//   them as one sequence of chunks (8 16-byte loads per lane: 8 / R of each
+//   row, 4 KB per warp) with the next chunk's loads issued before the current
+//   one is used, so that two chunks are in flight per warp across group
+//   boundaries; the first chunk's loads go out before the norm;
+//   each normalised 16-byte vector read from shared memory serves the R rows;
+//   the T x R dot products accumulate in FP32 with the mixed-precision FMA
+//   (bf16 x bf16 + f32, one rounding; the bf16 product is exact) and reduce
+//   across the warp: out[t, n] = bf16(sum).
 //
 // The summation order differs from the tensor-core path, inside the same
 // bf16 output bound.
 #include <cuda_bf16.h>
+
+#include <cstdlib>
 
 #include "internal.h"
 
@@ -49,7 +51,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // acc_lo += a.lo * w.lo, acc_hi += a.hi * w.hi on the two bf16 halves of a
-// word, each product and sum rounded once to FP32.
+// word, each product and sum rounded once to FP32 (the mixed-precision FMA:
+// the bf16 product is exact, so this equals widening both operands and an
+// FP32 fma).
 __device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t w, float& acc_lo, float& acc_hi) {
   asm("{\n\t.reg .b16 al, ah, wl, wh;\n\t"
       "mov.b32 {al, ah}, %2;\n\t"
@@ -60,18 +64,25 @@ __device__ __forceinline__ void fma2_bf16(uint32_t a, uint32_t w, float& acc_lo,
       : "r"(a), "r"(w));
 }
 
-// chunk q of weight row n: vectors lane + 32 * (q * kChunk + i), i < kChunk
-__device__ __forceinline__ void load_chunk(const uint4* __restrict__ W, int n, int q, int nvec, int lane,
-                                           uint4 (&buf)[kChunk]) {
-  const uint4* wr = W + static_cast<int64_t>(n) * nvec;
+// chunk q of the R weight rows from n0: vectors lane + 32 * (q * C + i),
+// i < C = kChunk / R, of each row (rows at or past N read as zero)
+template <int R>
+__device__ __forceinline__ void load_chunk(const uint4* __restrict__ W, int n0, int N, int q, int nvec,
+                                           int lane, uint4 (&buf)[kChunk]) {
+  constexpr int C = kChunk / R;
 #pragma unroll
-  for (int i = 0; i < kChunk; ++i) {
-    const int v = lane + 32 * (q * kChunk + i);
-    buf[i] = v < nvec ? __ldcs(wr + v) : make_uint4(0u, 0u, 0u, 0u);  // read once: do not keep in L2
+  for (int r = 0; r < R; ++r) {
+    const uint4* wr = W + static_cast<int64_t>(n0 + r) * nvec;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int v = lane + 32 * (q * C + i);
+      buf[r * C + i] = (n0 + r < N && v < nvec) ? __ldcs(wr + v)  // read once: do not keep in L2
+                                                : make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
-template <int MODE, int T>
+template <int MODE, int T, int R>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma,
                   const uint4* __restrict__ W, int nvec, int N, float inv_d, float eps,
@@ -80,11 +91,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   __shared__ float red[kWarps][kMaxTokens];
   __shared__ float rstd_s[kMaxTokens];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int stride = gridDim.x * kWarps;
-  const int cpr = (nvec + 32 * kChunk - 1) / (32 * kChunk);  // chunks per weight row
-  int n = blockIdx.x * kWarps + warp, q = 0;
+  constexpr int C = kChunk / R;           // vectors per lane of each row in a chunk
+  const int stride = gridDim.x * kWarps;  // in row groups
+  const int groups = (N + R - 1) / R;
+  const int cpr = (nvec + 32 * C - 1) / (32 * C);  // chunks per row group
+  int g = blockIdx.x * kWarps + warp, q = 0;
   uint4 cur[kChunk];
-  if (n < N) load_chunk(W, n, 0, nvec, lane, cur);
+  if (g < groups) load_chunk<R>(W, g * R, N, 0, nvec, lane, cur);
 
   // 1. the normalised rows: thread i takes vectors i, i + 256, ... of every
   //    row; the raw vectors stay in shared memory for the second pass, which
@@ -126,8 +139,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
     for (int t = 0; t < T; ++t) r[t] = rstd_s[t];
     for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-      float g[8];
-      if (gamma != nullptr) unpack8(__ldg(gamma + v), g);
+      float gm[8];
+      if (gamma != nullptr) unpack8(__ldg(gamma + v), gm);
 #pragma unroll
       for (int t = 0; t < T; ++t) {
         float f[8];
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], r[t]);
         if (gamma != nullptr) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], g[j]);
+          for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(f[j], gm[j]);
         }
         a_s[t * nvec + v] = make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
       }
@@ -144,61 +157,90 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
   __syncthreads();
 
-  // 2. the weight rows as one stream of chunks, the next chunk in flight
-  float acc_lo[T], acc_hi[T];
+  // 2. the row groups as one stream of chunks, the next chunk in flight
+  float acc[R][T], acc2[R][T];  // even and odd elements
 #pragma unroll
-  for (int t = 0; t < T; ++t) acc_lo[t] = acc_hi[t] = 0.f;
-  while (n < N) {
-    int n2 = n, q2 = q + 1;
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int t = 0; t < T; ++t) acc[r][t] = acc2[r][t] = 0.f;
+  while (g < groups) {
+    int g2 = g, q2 = q + 1;
     if (q2 == cpr) {
       q2 = 0;
-      n2 = n + stride;
+      g2 = g + stride;
     }
     uint4 nxt[kChunk];
-    if (n2 < N) load_chunk(W, n2, q2, nvec, lane, nxt);
+    if (g2 < groups) load_chunk<R>(W, g2 * R, N, q2, nvec, lane, nxt);
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      const int v = lane + 32 * (q * kChunk + i);
+    for (int i = 0; i < C; ++i) {
+      const int v = lane + 32 * (q * C + i);
       if (v < nvec) {
 #pragma unroll
         for (int t = 0; t < T; ++t) {
           const uint4 a = a_s[t * nvec + v];
-          fma2_bf16(a.x, cur[i].x, acc_lo[t], acc_hi[t]);
-          fma2_bf16(a.y, cur[i].y, acc_lo[t], acc_hi[t]);
-          fma2_bf16(a.z, cur[i].z, acc_lo[t], acc_hi[t]);
-          fma2_bf16(a.w, cur[i].w, acc_lo[t], acc_hi[t]);
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const uint4 w = cur[r * C + i];
+            fma2_bf16(a.x, w.x, acc[r][t], acc2[r][t]);
+            fma2_bf16(a.y, w.y, acc[r][t], acc2[r][t]);
+            fma2_bf16(a.z, w.z, acc[r][t], acc2[r][t]);
+            fma2_bf16(a.w, w.w, acc[r][t], acc2[r][t]);
+          }
         }
       }
     }
-    if (q == cpr - 1) {  // the row is complete: reduce across the warp
-      float s[T];
+    if (q == cpr - 1) {  // the group is complete: reduce across the warp
 #pragma unroll
-      for (int t = 0; t < T; ++t) s[t] = acc_lo[t] + acc_hi[t];
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          acc[r][t] += acc2[r][t];
+          acc2[r][t] = 0.f;
+        }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int t = 0; t < T; ++t) s[t] += __shfl_xor_sync(0xffffffffu, s[t], o);
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int t = 0; t < T; ++t) {
-        if (lane == t) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(s[t]);
-        acc_lo[t] = acc_hi[t] = 0.f;
+          for (int t = 0; t < T; ++t) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int n = g * R + r;
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          if (lane == r * T + t && n < N) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(acc[r][t]);
+          acc[r][t] = 0.f;
+        }
       }
     }
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) cur[i] = nxt[i];
-    n = n2;
+    g = g2;
     q = q2;
   }
 }
 
-template <int MODE>
+template <int MODE, int R>
 void* decode_entry(int64_t T) {
   switch (T) {
-    case 1: return reinterpret_cast<void*>(decode_kernel<MODE, 1>);
-    case 2: return reinterpret_cast<void*>(decode_kernel<MODE, 2>);
-    case 3: return reinterpret_cast<void*>(decode_kernel<MODE, 3>);
-    default: return reinterpret_cast<void*>(decode_kernel<MODE, 4>);
+    case 1: return reinterpret_cast<void*>(decode_kernel<MODE, 1, R>);
+    case 2: return reinterpret_cast<void*>(decode_kernel<MODE, 2, R>);
+    case 3: return reinterpret_cast<void*>(decode_kernel<MODE, 3, R>);
+    default: return reinterpret_cast<void*>(decode_kernel<MODE, 4, R>);
   }
+}
+
+// Weight rows per warp group: 2 for 3 or 4 tokens when the pairs of rows
+// still give every resident warp (two CTAs of 8 warps per SM) at least one
+// group, else 1.  Measured (GPU time, flushed CUDA graph): 4 x 4096 -> 6144
+// 15.4 us with pairs against 16.1 us; 1 and 2 tokens 13.3 and 14.0 us with
+// single rows against 13.5 and 14.5 us; 4 x 12288 -> 2048 (1024 pairs for
+// 2432 warps) 20.6 us single against 21.1 us.  RNL_DECODE_ROWS=1 or 2
+// overrides.
+int decode_rows(int64_t T, int64_t N, int sm_count) {
+  if (const char* e = std::getenv("RNL_DECODE_ROWS"))
+    if (e[0] == '1' || e[0] == '2') return e[0] - '0';
+  return T >= 3 && N / 2 >= static_cast<int64_t>(sm_count) * 2 * kWarps ? 2 : 1;
 }
 
 }  // namespace
@@ -213,27 +255,30 @@ bool decode_fits(int64_t T, int64_t K, int64_t N) {
 
 rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
                          int64_t N, float eps, int mode, void* out, int sm_count, cudaStream_t s) {
-  static bool attr_set[64][2][kMaxTokens] = {};
+  static bool attr_set[64][2][2][kMaxTokens] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RNL_ERR_DEVICE;
   if (T < 1 || T > kMaxTokens) return RNL_ERR_SHAPE;
   const int nvec = static_cast<int>(K / 8);
   const size_t smem = static_cast<size_t>(T) * K * 2;
   const int mi = mode == RNL_NORM_RSQRT ? 0 : 1;
-  void* kern = mi == 0 ? decode_entry<0>(T) : decode_entry<1>(T);
-  if (smem > 48 * 1024 && !attr_set[dev][mi][T - 1]) {
+  const int R = decode_rows(T, N, sm_count);
+  void* kern = R == 1 ? (mi == 0 ? decode_entry<0, 1>(T) : decode_entry<1, 1>(T))
+                      : (mi == 0 ? decode_entry<0, 2>(T) : decode_entry<1, 2>(T));
+  if (smem > 48 * 1024 && !attr_set[dev][R - 1][mi][T - 1]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) != cudaSuccess)
       return RNL_ERR_LAUNCH;
-    attr_set[dev][mi][T - 1] = true;
+    attr_set[dev][R - 1][mi][T - 1] = true;
   }
-  // the whole grid resident at once, each warp at least one weight row
+  // the whole grid resident at once, each warp at least one row group
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess ||
       per_sm < 1) {
     cudaGetLastError();
     per_sm = 1;
   }
-  const int64_t grid = std::min<int64_t>(static_cast<int64_t>(per_sm) * sm_count, (N + kWarps - 1) / kWarps);
+  const int64_t groups = (N + R - 1) / R;
+  const int64_t grid = std::min<int64_t>(static_cast<int64_t>(per_sm) * sm_count, (groups + kWarps - 1) / kWarps);
   const uint4* xp = static_cast<const uint4*>(x);
   const uint4* gp = static_cast<const uint4*>(gamma);
   const uint4* wp = static_cast<const uint4*>(W);

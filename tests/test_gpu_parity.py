@@ -69,12 +69,15 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
     (2, 2056, 5000, 0, True),   # several rows a warp, each row's second chunk one vector
     (5, 4096, 1024, 0, True),   # beyond the token limit: the tensor-core path either way
 ])
-@pytest.mark.parametrize("decode", ["1", "0"])
+@pytest.mark.parametrize("decode", ["1", "0", "rows1", "rows2"])
 def test_bf16_decode_sized_both_paths(orc, monkeypatch, decode, T, K, N, mode, gamma):
     """Up to 4 tokens against a wide weight run as a matrix-vector product
-    over every SM (RNL_DECODE=0 sends them to the tensor-core path): both
-    against the oracle."""
-    monkeypatch.setenv("RNL_DECODE", decode)
+    over every SM (RNL_DECODE=0 sends them to the tensor-core path; rows1 /
+    rows2 force one or two weight rows per warp group): all against the
+    oracle."""
+    monkeypatch.setenv("RNL_DECODE", "0" if decode == "0" else "1")
+    if decode.startswith("rows"):
+        monkeypatch.setenv("RNL_DECODE_ROWS", decode[-1])
     d = _rand_case(13 + T + K + N, T, K, N, gamma)
     out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]) if gamma else None,
                                   dev_bf16(d["W"]), eps=1e-6, norm_mode=mode)
