@@ -20,7 +20,10 @@
 //     tile, and at the end of each row-tile segment write the segment's
 //     partial dot products and partial sum of squares to the workspace.
 // A second small kernel adds the segments of each row in CTA order
-// (deterministic) and applies rstd.
+// (deterministic) and applies rstd.  It is launched as the stream kernel's
+// programmatic dependent: its CTAs are scheduled while the stream runs and
+// wait (griddepcontrol.wait) for the stream grid's completion and memory
+// before they read the partial records, so its launch latency is hidden.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -83,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t s_begin = range_begin(blockIdx.x, total, G);
   const int64_t s_end = range_begin(blockIdx.x + 1, total, G);
 
+  grid_launch_dependents();  // the reduce kernel may be scheduled now; it waits for this grid
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctrl->full[s]), 1);
@@ -252,6 +256,7 @@ __global__ void __launch_bounds__(128)
     skinny_reduce_kernel(const float* __restrict__ part, int T, int K, int N, int G, float inv_d,
                          float eps, float* __restrict__ out) {
   constexpr int kRec = NP + 1;
+  grid_dependency_wait();  // the stream grid has completed and its records are visible
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const int kbpr = (K + SK - 1) / SK;
@@ -300,11 +305,26 @@ rnl_status launch_np(const void* x, const void* W, int64_t T, int64_t K, int64_t
   kern<<<G, kThreads, smem_bytes<NP>(), s>>>(mx, mw, static_cast<int>(T), static_cast<int>(K), inv_d, part);
   trace_after(s, "skinny_stream");
   if (cudaGetLastError() != cudaSuccess) return RNL_ERR_LAUNCH;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((T + 127) / 128), 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   trace_before(s);
-  skinny_reduce_kernel<NP, MODE><<<static_cast<unsigned>((T + 127) / 128), 128, 0, s>>>(
-      part, static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), G, inv_d, eps, out);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_reduce_kernel<NP, MODE>, static_cast<const float*>(part),
+                                           static_cast<int>(T), static_cast<int>(K), static_cast<int>(N), G,
+                                           inv_d, eps, out);
   trace_after(s, "skinny_reduce");
-  return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RNL_ERR_LAUNCH;
+  }
+  return RNL_OK;
 }
 
 int grid_for(int64_t T, int64_t K, int sm_count) {
