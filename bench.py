@@ -72,9 +72,9 @@ TRAFFIC = {
     # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.23 MB read + 39.94 MB written
     # (one ncu capture)
     "mxfp8": 137.17e6,
-    # skinny_kernel<32,0>: 123.03 MB in an ncu capture at T = 2048, scaled by
+    # skinny_kernel<32,0>: 122.89 MB in an ncu capture at T = 2048, scaled by
     # rows to T = 16384
-    "skinny": 984.2e6,
+    "skinny": 983.1e6,
     # decode_kernel<0,4,2>: 50.40 MB read (the 49 KB output stays in L2)
     # (one ncu capture)
     "decode": 50.40e6,
