@@ -122,7 +122,8 @@ size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
  * Kernels: bf16 out -> row-norm/cast pass then the tcgen05 GEMM;
  * bf16 out with T <= 4, K >= 2048, N >= 1024 and T * K * 2 <= 96 KB (a
  * decode step) -> one matrix-vector launch over every SM (the environment
- * variable RNL_DECODE=0 selects the GEMM path instead; same result bound);
+ * variable RNL_DECODE=0 selects the GEMM path instead, RNL_DECODE_ROWS=1|2
+ * fixes the weight rows per warp group; same result bound);
  * fp32 out with N <= 64 -> the split-K streaming kernel (one read of x);
  * fp32 out with N > 64 -> row rstd pass then the GEMM with a row-scale
  * epilogue.
