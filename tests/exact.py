@@ -76,3 +76,37 @@ def dec_sqrt_recip(x: Fraction, digits: int = 60) -> Fraction:
 def rel_close(a: float, b: Fraction | float, rel: float) -> bool:
     b = float(b)
     return abs(a - b) <= rel * max(abs(b), 1e-300)
+
+
+def f32_round_exact(v) -> Fraction:
+    """Round an exact value to IEEE binary32, ties to even, by integer
+    arithmetic on the Fraction (normal and subnormal range; no overflow
+    handling: the callers stay far below 2^128)."""
+    f = Fraction(v)
+    if f == 0:
+        return Fraction(0)
+    sign = -1 if f < 0 else 1
+    a = -f if f < 0 else f
+    # e = floor(log2 a)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, -126) - 23)
+    m = a / ulp
+    r = m.numerator // m.denominator
+    rem = m - r
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and r % 2 == 1):
+        r += 1
+    return sign * r * ulp
+
+
+def f32_sqrt_exact(v: Fraction, digits: int = 60) -> Fraction:
+    """The binary32 rounding of sqrt(v) (v >= 0), from a 60-digit decimal
+    square root (a square root is never exactly halfway between two binary32
+    values, so the decimal precision decides every case)."""
+    with decimal.localcontext() as ctx:
+        ctx.prec = digits
+        d = decimal.Decimal(v.numerator) / decimal.Decimal(v.denominator)
+        return f32_round_exact(Fraction(d.sqrt()))

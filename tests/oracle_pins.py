@@ -338,6 +338,80 @@ def pin_quant_properties(orc):
             assert np.array_equal(q[t], np.clip(np.rint(v[t]), -127, 127).astype(np.int8))
 
 
+def _sum_of_squares_rows(rng, T, K):
+    """bf16 rows whose binary32 sum of squares depends on the order of the
+    additions.  Row kinds (cycled): one entry 2^12 first and the rest in
+    (-1, 1) -- every small square is below half a unit in the last place of
+    2^24, so a left-to-right binary32 sum returns 2^24 exactly while the
+    exact sum is larger by about K/3; big entries 2^12 at the head of every
+    64-element block with small ones between (a blocked or tree-shaped
+    binary32 sum loses them too); one entry 1.5 * 2^12 and the rest ~N(0,1)
+    (the running sum's last place is 4, so each addition rounds)."""
+    rows = np.zeros((T, K), np.float32)
+    for t in range(T):
+        kind = t % 3
+        if kind == 0:
+            rows[t] = rng.uniform(-0.99, 0.99, K)
+            rows[t, 0] = 4096.0
+        elif kind == 1:
+            rows[t] = rng.uniform(-0.99, 0.99, K)
+            rows[t, ::64] = 4096.0
+        else:
+            rows[t] = rng.standard_normal(K)
+            rows[t, 0] = 6144.0
+    return _bf16_bits_of_f32(rows)
+
+
+def _rstd_exact_sum_reading(xrow_bits, eps, variant):
+    """rstd of the binary32 norm under the reading "the FP32 sum of squares is
+    the binary32 rounding of the exact sum of the binary32 terms", every later
+    step one correctly rounded binary32 operation, computed in exact rationals
+    (AT-10 pattern page, sec. 3: the two RMSNorm variants in FP32).  K must be
+    a power of two (1/K exact)."""
+    K = xrow_bits.size
+    assert K & (K - 1) == 0
+    f32 = exact.f32_round_exact
+    inv_d = Fraction(1, K)
+    # each term: an exact binary64 product rounded once to binary32
+    v = bf16_bits_to_f64(xrow_bits)
+    terms = (v * v).astype(np.float32)
+    if variant == 1:
+        terms = (terms.astype(np.float64) * (1.0 / K)).astype(np.float32)
+    # their exact sum: every binary32 value is an integer multiple of 2^-149
+    total = sum(int(a) for a in np.ldexp(terms.astype(np.float64), 149).astype(object))
+    s = f32(Fraction(total, 2**149))
+    e = Fraction(float(np.float32(eps)))
+    var = f32(f32(s * inv_d) + e) if variant == 0 else f32(s + e)
+    return f32(1 / exact.f32_sqrt_exact(var))
+
+
+def pin_quant_sum_of_squares_reading(orc):
+    # The FP32 norm of the W8A8 and MXFP8 front ends decides integer codes, so
+    # its sum of squares is fixed as one rounding of the exact sum.  Rows where
+    # the order of binary32 additions changes the sum pin rstd (bit for bit)
+    # against that reading in exact rationals, then the codes and scales that
+    # follow from it (independent float32 steps; torch's E4M3 conversion).
+    rng = _rng(13)
+    T, K = 3, 4096
+    x = _sum_of_squares_rows(rng, T, K)
+    g = _bf16_bits_of_f32(rng.uniform(0.5, 1.5, K).astype(np.float32))
+    eps = 1e-6
+    xf = bf16_bits_to_f64(x).astype(np.float32)
+    gf = bf16_bits_to_f64(g).astype(np.float32)
+    for variant in (0, 1):
+        q, xs, rstd, _ = orc.quant_rows_f32(x, g, eps, variant)
+        want = np.array([float(_rstd_exact_sum_reading(x[t], eps, variant)) for t in range(T)], np.float32)
+        assert np.array_equal(rstd, want), (variant, rstd, want)
+        y = (xf * want[:, None]) * gf[None, :]  # binary32 products, as the method's FP32 norm
+        amax = np.abs(y).max(axis=1)
+        assert np.array_equal(xs, amax / np.float32(127))
+        qs = np.float32(127) / amax
+        assert np.array_equal(q, np.clip(np.rint(y * qs[:, None]), -127, 127).astype(np.int8))
+        codes, scales = orc.mxfp8_quant_rows(x, g, eps, variant)
+        want_c, want_s = _mx_expected(y.astype(np.float64))
+        assert np.array_equal(scales, want_s) and np.array_equal(codes, want_c)
+
+
 def pin_gemm_s8_bruteforce(orc):
     rng = _rng(12)
     for (M, N, K) in ((1, 1, 1), (3, 4, 5), (5, 7, 33)):
@@ -1224,6 +1298,7 @@ ALL_PINS = [
     pin_mla_composition,
     pin_quant_constructed_ties,
     pin_quant_properties,
+    pin_quant_sum_of_squares_reading,
     pin_gemm_s8_bruteforce,
     pin_dequant_exact,
     pin_w8a8_composition,

@@ -33,6 +33,16 @@ MUTANTS = [
     ("quant_dequant_scale_inverted", "x_scale[t] = amax / 127.0f;", "x_scale[t] = 127.0f / amax;"),
     ("quant_drop_gamma", "            if (gamma)\n                y = y * bf16_as_float(gamma[k]);\n            float v = y * qs;",
      "            float v = y * qs;"),
+    # the FP32 sum of squares taken as a left-to-right binary32 sum instead of
+    # the rounding of the exact sum (both front ends, both norm variants)
+    ("quant_sum_sequential_f32", "\n                s64 += (double)sq;",
+     "\n                s64 = (double)((float)s64 + sq);"),
+    ("quant_sum_sequential_f32_sqrt_div", "\n                s64 += (double)sc;",
+     "\n                s64 = (double)((float)s64 + sc);"),
+    ("mx_sum_sequential_f32", "\n                    s64 += (double)sq;",
+     "\n                    s64 = (double)((float)s64 + sq);"),
+    ("mx_sum_sequential_f32_sqrt_div", "\n                    s64 += (double)sc;",
+     "\n                    s64 = (double)((float)s64 + sc);"),
     ("gemm_s8_off_by_one", "for (int64_t k = 0; k < K; ++k)\n                acc += (int64_t)A[m * K + k]",
      "for (int64_t k = 1; k < K; ++k)\n                acc += (int64_t)A[m * K + k]"),
     ("dequant_wrong_scale", "double scale = (double)x_scale[m] * (double)w_scale[n];",
