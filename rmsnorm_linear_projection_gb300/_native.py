@@ -107,6 +107,15 @@ def _ptr(t):
 
 
 def _stream(device, stream):
+    """The stream handle for a call on `device`.  The C entry points work on the
+    current CUDA device (its kernels, its cached set-up), so tensors on
+    another device are refused here rather than handed over."""
+    if device.type != "cuda":
+        raise ValueError(f"tensors must be on a CUDA device, got {device}")
+    cur = torch.cuda.current_device()
+    if device.index is not None and device.index != cur:
+        raise ValueError(f"tensors are on {device} but the current CUDA device is cuda:{cur}; "
+                         f"make the call under torch.cuda.device({device})")
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
 

@@ -1,19 +1,21 @@
-"""The allocation-free entry point (rmsnorm_linear_skinny_noalloc) against the
-regular one (rmsnorm_linear_bf16, fp32 form), through the C ABI.
+"""The allocation-free entry point (rmsnorm_linear_skinny_noalloc), through the
+C ABI, against the CPU oracle and against the regular entry point
+(rmsnorm_linear_bf16, fp32 form).
 
 That entry point serves callers that cannot allocate device memory (code
 inside a host program that owns all device allocations); its scratch is an
-array built into the library and shared by every call, so two calls in a row
-must both match.  This file is collected last, so a run that stops at the
-first failure has run everything else first; it also passes on its own in a
-fresh process.
+array built into the library and shared by every call.  So the calls here
+come in a row, with a call on different activations in between: the scratch
+then holds values that are wrong for the next call, and that call must still
+match.  This file is collected last, so a run that stops at the first failure
+has run everything else first; it also passes on its own in a fresh process.
 """
 import numpy as np
 import pytest
 import torch
 
 import synth_inputs as si
-from gpu_util import assert_fp32_close, dev_bf16
+from gpu_util import assert_fp32_close, dev_bf16, sample_rows
 from oracle import bf16_bits_to_f64
 
 pytestmark = pytest.mark.gpu
@@ -30,25 +32,44 @@ def cuda_ready():
     torch.cuda.set_device(0)
 
 
-def _abs_sum(d, mode):
+def _abs_sum(orc, x_bits, W_bits, mode):
     """sum_k |y_k| |w_k| per output, the scale of the fp32 accumulation bound."""
-    xv = bf16_bits_to_f64(d["x"])
-    rstd = 1.0 / np.sqrt(np.mean(xv * xv, axis=1) + 1e-6)
-    return (np.abs(xv) * rstd[:, None]) @ np.abs(bf16_bits_to_f64(d["W"])).T
+    y, _ = orc.rmsnorm_f64(x_bits, None, 1e-6, mode)
+    return np.abs(y) @ np.abs(bf16_bits_to_f64(W_bits)).T
+
+
+def _noalloc(x, W, mode):
+    out = torch.full((x.shape[0], W.shape[0]), float("nan"), dtype=torch.float32, device="cuda")
+    rnl.rmsnorm_linear_skinny_noalloc(x, W, eps=1e-6, norm_mode=mode, out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
 
 
 @pytest.mark.parametrize("T,K,N,mode", [(1000, 16384, 24, 0), (300, 4160, 64, 1)])
-def test_noalloc_matches_regular_twice(T, K, N, mode):
+def test_noalloc_matches_oracle_and_regular(orc, T, K, N, mode):
     d = si.make_projection(dict(seed=77 + N, T=T, K=K, N=N, has_gamma=False))
-    x, W = dev_bf16(d["x"]), dev_bf16(d["W"])
-    ref = rnl.rmsnorm_linear_bf16(x, None, W, eps=1e-6, norm_mode=mode,
+    d2 = si.make_projection(dict(seed=177 + N, T=T, K=K, N=N, has_gamma=False))
+    x, W, x2 = dev_bf16(d["x"]), dev_bf16(d["W"]), dev_bf16(d2["x"])
+    rows = sample_rows(T, 96, seed=N)
+    want, _ = orc.rmsnorm_linear(d["x"][rows], None, d["W"], 1e-6, mode, 1)
+    want_scale = _abs_sum(orc, d["x"][rows], d["W"], mode)
+    reg = rnl.rmsnorm_linear_bf16(x, None, W, eps=1e-6, norm_mode=mode,
                                   out_dtype=rnl.OUT_FP32).cpu().numpy().astype(np.float64)
-    bound_scale = _abs_sum(d, mode)
-    for _ in range(2):  # the second call reuses the scratch left by the first
-        out = torch.full((T, N), float("nan"), dtype=torch.float32, device="cuda")
-        rnl.rmsnorm_linear_skinny_noalloc(x, W, eps=1e-6, norm_mode=mode, out=out)
-        torch.cuda.synchronize()
-        assert_fp32_close(out.cpu().numpy(), ref, bound_scale, "noalloc vs regular")
+    reg2 = rnl.rmsnorm_linear_bf16(x2, None, W, eps=1e-6, norm_mode=mode,
+                                   out_dtype=rnl.OUT_FP32).cpu().numpy().astype(np.float64)
+    reg_scale = _abs_sum(orc, d["x"], d["W"], mode)
+    reg2_scale = _abs_sum(orc, d2["x"], d["W"], mode)
+    # first call: against the oracle on sampled rows and the regular path on all rows
+    got = _noalloc(x, W, mode)
+    assert_fp32_close(got[rows], want, want_scale, "noalloc call 1 vs oracle")
+    assert_fp32_close(got, reg, reg_scale, "noalloc call 1 vs regular")
+    # a call on other activations leaves scratch values that are wrong for x
+    got2 = _noalloc(x2, W, mode)
+    assert_fp32_close(got2, reg2, reg2_scale, "noalloc call 2 (other x) vs regular")
+    # the next call on x must not see them
+    got3 = _noalloc(x, W, mode)
+    assert_fp32_close(got3[rows], want, want_scale, "noalloc call 3 vs oracle")
+    assert_fp32_close(got3, reg, reg_scale, "noalloc call 3 vs regular")
     rnl.rnl_check_device_error()
 
 
