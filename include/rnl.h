@@ -46,8 +46,20 @@
  *     RNL_ERR_LAUNCH reports a CUDA launch error.  A kernel that gives up on
  *     a wait (a bug, never expected) records it in a device error word that
  *     rnl_check_device_error() reads.
+ *   - The library keeps per-device set-up (kernel attributes, device
+ *     properties, the address of the built-in scratch array) for the life of
+ *     the process; after cudaDeviceReset() on a device, reload the library
+ *     before using that device again.
  *   - Calls on the same stream are ordered; calls that share a workspace
  *     must not overlap on the GPU.
+ *   - A call may be captured in a CUDA graph and replayed with new contents
+ *     in the same buffers.  Make one uncaptured call of the same kind first
+ *     (a first call per device and kernel does host-side set-up).  The
+ *     cross-CTA flags some calls keep in the workspace (the CTA-pair GEMM's
+ *     stream-K hand-off, QuantMatMulReduceSum's batch sum) are set back to 0
+ *     by the launch that consumes them, so every replay waits for its own.
+ *     After rnl_check_device_error() has reported RNL_ERR_TIMEOUT, set the
+ *     failed call's workspace to zero before a graph that uses it replays.
  */
 #ifndef RNL_H
 #define RNL_H
@@ -72,7 +84,8 @@ typedef enum rnl_status {
   RNL_ERR_LAUNCH = 6,      /* CUDA returned an error when launching */
   RNL_ERR_TIMEOUT = 7,     /* a kernel gave up waiting (device error word set) */
   RNL_ERR_UNSUPPORTED = 8, /* argument combination the library does not provide */
-  RNL_ERR_DEVICE = 9       /* no sm_103 device current, or a driver entry point missing */
+  RNL_ERR_DEVICE = 9,      /* no sm_103 device current, or a driver entry point missing */
+  RNL_ERR_BOUNDS = 10      /* a device-side bounds check failed (debug builds only) */
 } rnl_status;
 
 /* AT-03 rsqrt_mode */
@@ -92,6 +105,16 @@ enum {
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int rnl_version(void);
+
+/*
+ * 1 for a debug build (compiled with RNL_DEBUG), 0 otherwise.  A debug build
+ * computes the same results and additionally checks, on the device, every
+ * shared-memory stage offset, TMEM column range, workspace record or flag
+ * index and output index of its GEMM, norm-pass and skinny kernels before
+ * use; a failed check skips that access, and rnl_check_device_error() then
+ * returns RNL_ERR_BOUNDS with the check's site.  No kernel traps.
+ */
+int rnl_debug_build(void);
 
 /* Human-readable name of a status code (static string). */
 const char *rnl_status_string(rnl_status s);
@@ -397,6 +420,17 @@ rnl_status rnl_check_device_error(rnl_stream_t stream, int *site);
  * stays usable.  Returns RNL_OK when the kernel was enqueued.
  */
 rnl_status rnl_selftest_wait_timeout(rnl_stream_t stream);
+
+/*
+ * Bounds-check self-test of a debug build (no counterpart on the pages).
+ * Enqueues one small kernel whose device-side check compares an index with
+ * a deliberately smaller limit (the index still lies inside the kernel's own
+ * array, so no access can leave it); the check fails, records site 98 and
+ * skips the store.  A following rnl_check_device_error() reports
+ * RNL_ERR_BOUNDS with *site == 98.  Release builds return
+ * RNL_ERR_UNSUPPORTED and enqueue nothing.
+ */
+rnl_status rnl_selftest_bounds_check(rnl_stream_t stream);
 
 /*
  * Host-buffer pipeline (no counterpart on the pages: how the projection is

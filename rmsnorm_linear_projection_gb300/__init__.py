@@ -20,6 +20,8 @@ arguments; the computation runs in the library's CUDA kernels.
                           QKV split + per-head RMSNorm + RoPE after the qkv projection
     rnl_pipeline_*        host-buffer pipeline: calls fed from and answering into
                           pinned host memory, copies overlapped with the kernels
+    debug_library()       route calls through librnl_debug.so, the build whose
+                          kernels check their indices on the device
 """
 from ._native import (  # noqa: F401
     EXPORTS,
@@ -36,6 +38,7 @@ from ._native import (  # noqa: F401
     OUT_FP32,
     PipelineHandle,
     RnlError,
+    debug_library,
     load,
     mla_q_chain,
     mla_q_chain_head_norm,
@@ -48,6 +51,7 @@ from ._native import (  # noqa: F401
     rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,
     rnl_check_device_error,
+    rnl_debug_build,
     rnl_gemm_s8s8s32,
     rnl_head_rmsnorm,
     rnl_pipeline_create,
@@ -57,6 +61,7 @@ from ._native import (  # noqa: F401
     rnl_pipeline_submit_w8a8,
     rnl_pipeline_wait,
     rnl_qkv_rope,
+    rnl_selftest_bounds_check,
     rnl_selftest_wait_timeout,
     rnl_trace_enable,
     rnl_trace_read,

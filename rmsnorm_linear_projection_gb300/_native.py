@@ -9,6 +9,7 @@ has not been built, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -17,6 +18,7 @@ import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "librnl.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "librnl_debug.so")
 
 NORM_RSQRT, NORM_SQRT_DIV = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
@@ -25,10 +27,10 @@ OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS, OP_MXFP8 = 0, 1, 2, 
 STATUS = {
     0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
     5: "RNL_ERR_WORKSPACE", 6: "RNL_ERR_LAUNCH", 7: "RNL_ERR_TIMEOUT", 8: "RNL_ERR_UNSUPPORTED",
-    9: "RNL_ERR_DEVICE",
+    9: "RNL_ERR_DEVICE", 10: "RNL_ERR_BOUNDS",
 }
 
-EXPORTS = ("rnl_version", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
+EXPORTS = ("rnl_version", "rnl_debug_build", "rnl_selftest_bounds_check", "rnl_status_string", "rnl_workspace_size", "rmsnorm_linear_bf16",
            "rmsnorm_linear_w8a8", "mla_q_chain", "rnl_gemm_s8s8s32", "rnl_check_device_error",
            "rnl_trace_enable", "rnl_trace_read", "rmsnorm_linear_skinny_noalloc",
            "rnl_selftest_wait_timeout", "rnl_pipeline_create", "rnl_pipeline_submit_bf16",
@@ -52,6 +54,8 @@ def _declare(lib):
     P, I64, F, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
     sig = {
         "rnl_version": (I, []),
+        "rnl_debug_build": (I, []),
+        "rnl_selftest_bounds_check": (I, [P]),
         "rnl_status_string": (ctypes.c_char_p, [I]),
         "rnl_workspace_size": (SZ, [I, I64, I64, I64, I64]),
         "rmsnorm_linear_bf16": (I, [P, P, P, I64, I64, I64, F, I, P, I, P, SZ, P]),
@@ -100,6 +104,27 @@ def load(path: str | None = None):
                 return lib
             _lib = lib
     return _lib
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Route every call of this module through librnl_debug.so (the build with
+    device-side bounds checks, ``python -m rmsnorm_linear_projection_gb300.build
+    --debug``) while the context is open; yields that library."""
+    global _lib
+    dbg = load(DEBUG_LIB_PATH)
+    with _lock:
+        prev, _lib = _lib, dbg
+    try:
+        yield dbg
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def rnl_debug_build() -> bool:
+    """Whether the library in use is the debug build (bounds-checked kernels)."""
+    return bool(load().rnl_debug_build())
 
 
 def _ptr(t):
@@ -470,6 +495,14 @@ def rnl_selftest_wait_timeout(stream=None, device=None):
     """Enqueue the failure-detection self-test (a 1 ms bounded wait that must give up)."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     _check(load().rnl_selftest_wait_timeout(_stream(dev, stream)), "rnl_selftest_wait_timeout")
+
+
+def rnl_selftest_bounds_check(stream=None, device=None):
+    """Enqueue the debug build's bounds-check self-test (a check that must fail
+    on an index that still lies inside the kernel's own array); raises
+    RnlError(RNL_ERR_UNSUPPORTED) on a release build."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(load().rnl_selftest_bounds_check(_stream(dev, stream)), "rnl_selftest_bounds_check")
 
 
 def rnl_check_device_error(stream=None, device=None):

@@ -1,11 +1,16 @@
 """Compile the CUDA library ``librnl.so`` in-tree with nvcc for sm_103a.
 
-    python -m rmsnorm_linear_projection_gb300.build [--force] [--verbose]
+    python -m rmsnorm_linear_projection_gb300.build [--force] [--verbose] [--debug]
 
 Each ``csrc/*.cu`` translation unit is compiled in parallel to an object in
 ``_build/``; the objects are linked into ``librnl.so`` next to this file with
 the CUDA runtime linked statically (the library then loads on machines
 without a GPU driver, and only talks to the driver once it is called).
+
+``--debug`` builds ``librnl_debug.so`` from objects in ``_build_debug/`` with
+``RNL_DEBUG`` defined: the same kernels with device-side bounds checks that
+report RNL_ERR_BOUNDS through rnl_check_device_error() instead of accessing
+out of range (include/rnl.h, rnl_debug_build).
 """
 from __future__ import annotations
 
@@ -21,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "librnl.so")
+DEBUG_OBJ_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "librnl_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -44,16 +51,21 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Build (incrementally) and return the path of librnl.so."""
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Build (incrementally) and return the path of librnl.so, or of
+    librnl_debug.so with ``debug=True``."""
+    obj_dir = DEBUG_OBJ_DIR if debug else OBJ_DIR
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if debug:
+        extra_flags = (*extra_flags, "-DRNL_DEBUG")
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     nvcc = _nvcc()
     jobs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *hdrs]):
             jobs.append([nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj])
@@ -69,13 +81,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if jobs:
         with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp%d" % os.getpid()
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp%d" % os.getpid()
         run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="--verbose" in sys.argv)
-    print(LIB_PATH)
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -9,6 +9,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -287,6 +289,24 @@ rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
   return r == CUDA_SUCCESS ? RNL_OK : RNL_ERR_ARG;
 }
 
+namespace {
+std::mutex g_attr_mu;
+std::set<std::pair<const void*, int>> g_attr_done;
+}  // namespace
+
+rnl_status ensure_smem_attr(const void* kernel, int device, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  const auto key = std::make_pair(kernel, device);
+  if (g_attr_done.count(key) != 0) return RNL_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes)) != cudaSuccess) {
+    cudaGetLastError();
+    return RNL_ERR_LAUNCH;
+  }
+  g_attr_done.insert(key);
+  return RNL_OK;
+}
+
 void trace_before(cudaStream_t s) {
   if (!g_trace_on || g_trace_n >= kTraceCap) return;
   TraceRec& t = g_trace[g_trace_n];
@@ -317,6 +337,9 @@ rnl_status read_device_errors(int* site) {
   for (unsigned int w : words) {
     if (w != 0) {
       if (site) *site = static_cast<int>((w >> 8) & 0xFFu);
+      // a failed bounds check (debug builds) comes first: a wait that then
+      // timed out is its consequence
+      if (w & kErrBounds) return RNL_ERR_BOUNDS;
       return (w & kErrTimeout) ? RNL_ERR_TIMEOUT : RNL_ERR_ARG;
     }
   }
@@ -332,6 +355,14 @@ extern "C" {
 
 int rnl_version(void) { return 100; }
 
+int rnl_debug_build(void) {
+#ifdef RNL_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 const char* rnl_status_string(rnl_status s) {
   switch (s) {
     case RNL_OK: return "ok";
@@ -344,6 +375,7 @@ const char* rnl_status_string(rnl_status s) {
     case RNL_ERR_TIMEOUT: return "device wait timed out";
     case RNL_ERR_UNSUPPORTED: return "unsupported argument combination";
     case RNL_ERR_DEVICE: return "no sm_103 device or driver entry point";
+    case RNL_ERR_BOUNDS: return "device bounds check failed (debug build)";
   }
   return "unknown status";
 }

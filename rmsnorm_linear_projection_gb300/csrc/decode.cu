@@ -255,7 +255,6 @@ bool decode_fits(int64_t T, int64_t K, int64_t N) {
 
 rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
                          int64_t N, float eps, int mode, void* out, int sm_count, cudaStream_t s) {
-  static bool attr_set[64][2][2][kMaxTokens] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RNL_ERR_DEVICE;
   if (T < 1 || T > kMaxTokens) return RNL_ERR_SHAPE;
@@ -265,11 +264,7 @@ rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_
   const int R = decode_rows(T, N, sm_count);
   void* kern = R == 1 ? (mi == 0 ? decode_entry<0, 1>(T) : decode_entry<1, 1>(T))
                       : (mi == 0 ? decode_entry<0, 2>(T) : decode_entry<1, 2>(T));
-  if (smem > 48 * 1024 && !attr_set[dev][R - 1][mi][T - 1]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) != cudaSuccess)
-      return RNL_ERR_LAUNCH;
-    attr_set[dev][R - 1][mi][T - 1] = true;
-  }
+  if (smem > 48 * 1024 && ensure_smem_attr(kern, dev, kSmemMax) != RNL_OK) return RNL_ERR_LAUNCH;
   // the whole grid resident at once, each warp at least one row group
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, smem) != cudaSuccess ||

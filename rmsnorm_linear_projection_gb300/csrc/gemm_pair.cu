@@ -301,12 +301,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Work w = work_item(sc, pair, it);
         int mb, nb;
         tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
+        if (!RNL_DCHECK(&g_err_pair, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n && w.kb0 >= 0 &&
+                                         w.kb0 < w.kb1 && w.kb1 <= num_kb, 70))
+          break;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_wait_cluster(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_pair, 21)) {
             ok = false;
             break;
           }
           const uint32_t sa = base + stage * kStageBytes;
+          if (!RNL_DCHECK(&g_err_pair, stage < static_cast<uint32_t>(kStages) &&
+                                           sa + kStageBytes <= base + kStages * kStageBytes, 71)) {
+            ok = false;
+            break;
+          }
           const uint32_t full_local = smem_u32(&ctrl->full[stage]);
           const uint32_t full_even = mapa_shared(full_local, 0);
           if (rank == 0) mbar_arrive_expect_tx(full_local, 2 * kStageBytes);
@@ -341,6 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kAccStride;
+          if (!RNL_DCHECK(&g_err_pair, buf * kAccStride + BN <= kTmemCols, 72)) {
+            ok = false;
+            break;
+          }
           const int kb0 = w.kb0 + u * kb_per_unit;
           const int kb1 = min(w.kb1, kb0 + kb_per_unit);
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -350,6 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = base + stage * kStageBytes;
+            if (!RNL_DCHECK(&g_err_pair, stage < static_cast<uint32_t>(kStages), 73)) {
+              ok = false;
+              break;
+            }
             const uint64_t adesc = desc_kmajor_sw128(sa);
             const uint64_t bdesc = desc_kmajor_sw128(sa + kABytes);
 #pragma unroll
@@ -392,6 +408,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* prow = w.kind == kPartial ? partial + pair * slot_words + warp_off : nullptr;
       // a finisher adds the partial sums of pairs [pair + 1, q_end)
       const int q_end = w.kind == kFinish ? partners_end(sc, pair, w.sk_tile) : pair + 1;
+      // the host gives kMaxPartialSlots slots of slot_words words: one per pair
+      // (grid <= kMaxPartialSlots - 1 pairs), the flags in the last one; the
+      // highest word a warp touches is warp_off + (kGroups * 4 - 1) * 256 + 7
+      if (!RNL_DCHECK(&g_err_pair,
+                      (w.kind == kWhole || (partial != nullptr && flags != nullptr)) &&
+                          q_end <= kMaxPartialSlots - 1 && pair < kMaxPartialSlots - 1 &&
+                          warp_off + (kGroups * 4 - 1) * 256 + 8 <= slot_words &&
+                          (static_cast<int64_t>(q_end) * 2 + 1) * kEpiWarps <= slot_words / 2,
+                      74)) {
+        ok = false;
+        break;
+      }
       if (w.kind == kFinish) {
         // this warp reads only the words the same warp of each partner wrote
         bool got = true;
@@ -405,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int mb, nb;
       tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
+      if (!RNL_DCHECK(&g_err_pair, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n, 75)) {
+        ok = false;
+        break;
+      }
       const int64_t m = static_cast<int64_t>(mb) * 2 * BM + rank * BM + row_local;
       const int n_base = nb * BN + half * kColsPerEpiWarp;
       const bool row_ok = m < M;
@@ -430,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if (!RNL_DCHECK(&g_err_pair, buf * kAccStride + (half + 1) * kColsPerEpiWarp <= kTmemCols, 76)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < kGroups; ++c) {
           uint32_t r[32];
@@ -527,6 +563,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (w.kind == kFinish) {
+        // every flag published in a launch is consumed by exactly one
+        // finisher warp, which sets it back to 0 once the partial sums are
+        // read: a later launch with the same epoch (a replayed CUDA graph)
+        // then waits for flags published in that launch
+        __syncwarp();
+        if (lane == 0)
+          for (int q = pair + 1; q < q_end; ++q)
+            flags[(static_cast<int64_t>(q) * 2 + rank) * kEpiWarps + ew] = 0;
+      }
       if (w.kind == kPartial) {
         // every lane orders its partial stores, then one lane publishes this
         // warp's flag (release)
@@ -591,19 +637,16 @@ int grid_pairs(int64_t tiles, int num_kb, int max_pairs, bool have_partials) {
 
 // Epoch of each launch: a per-process start value from the clock, then one
 // step per launch, so a flag left in a reused workspace by an earlier launch
-// (or process) never matches.
+// (or process) never matches.  A launch captured in a CUDA graph keeps its
+// epoch on every replay; there the finishers' reset of every consumed flag
+// to 0 is what keeps a replay from reading the previous replay's flags.
 template <int EPI, int BN>
 rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pairs, cudaStream_t s,
                           const char* name) {
-  static bool attr_set[64] = {};
   auto kern = gemm_pair_kernel<EPI, BN>;
   const size_t smem = pair_smem_bytes<BN>();
-  if (!attr_set[dev.device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return RNL_ERR_LAUNCH;
-    attr_set[dev.device] = true;
-  }
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device, smem) != RNL_OK)
+    return RNL_ERR_LAUNCH;
   CUtensorMap ma, mb;
   rnl_status st = make_map_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, g.K * 2, BK, BM);
   if (st != RNL_OK) return st;
@@ -656,12 +699,13 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
 
 // Largest number of CTA pairs that can be resident at once.
 int resident_pairs(const DeviceInfo& dev) {
-  static int cached[64] = {};
-  if (cached[dev.device] > 0) return cached[dev.device];
+  static std::atomic<int> cached[64];  // 0 until measured; racing first calls store the same value
+  const int c = cached[dev.device].load(std::memory_order_relaxed);
+  if (c > 0) return c;
   auto kern = gemm_pair_kernel<0, 256>;
   int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(pair_smem_bytes<256>())) == cudaSuccess) {
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device, pair_smem_bytes<256>()) ==
+      RNL_OK) {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -677,7 +721,7 @@ int resident_pairs(const DeviceInfo& dev) {
   }
   cudaGetLastError();
   if (n <= 0) n = dev.sm_count / 2;
-  cached[dev.device] = n;
+  cached[dev.device].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -756,7 +800,8 @@ rnl_status read_clear_error_pair(unsigned int* word) {
 uint64_t next_flag_epoch() {
   static std::atomic<uint64_t> counter{
       static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) * 2654435761ull};
-  return counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  const uint64_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e != 0 ? e : 1;  // 0 is the value of a consumed flag
 }
 
 }  // namespace rnl

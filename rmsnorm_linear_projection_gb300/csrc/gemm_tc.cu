@@ -32,7 +32,8 @@
 // FP32 values to the running sum that item (b - 1, tile) left in global
 // memory, after waiting (bounded) for that item's flag: one 64-bit flag per
 // (tile, epilogue warp), set with a release store to tag | (b + 1) after the
-// warp's sums are written.  Item i waits only for item i - tiles, and every
+// warp's sums are written, and set back to 0 by the last batch's item, so a
+// replay of the launch with the same tag (a CUDA graph) starts from 0.  Item i waits only for item i - tiles, and every
 // CTA takes its items in increasing order with all CTAs resident, so every
 // wait ends.
 #include <cuda_bf16.h>
@@ -164,13 +165,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = item - b * num_tiles;
         int mb, nb;
         tile_coords(tile, num_m, num_n, group_m, mb, nb);
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        bool ok = RNL_DCHECK(&g_err_gemm, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n && b < nbatch, 60);
+        for (int kb = 0; kb < num_kb && ok; ++kb) {
           if (!mbar_wait(smem_u32(&ctrl->empty[stage]), phase ^ 1u, abort, &g_err_gemm, 1)) {
             ok = false;
             break;
           }
           const uint32_t sa = base + stage * kStageBytes;
+          if (!RNL_DCHECK(&g_err_gemm, stage < static_cast<uint32_t>(kStages) &&
+                                           sa + kStageBytes <= base + kStages * kStageBytes, 61)) {
+            ok = false;
+            break;
+          }
           const uint32_t bar = smem_u32(&ctrl->full[stage]);
           mbar_arrive_expect_tx(bar, kStageBytes);
           tma_load_2d(sa, &map_a, bar, kb * BK, b * M + mb * BM);
@@ -200,6 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * kAccStride;
+          if (!RNL_DCHECK(&g_err_gemm, buf * kAccStride + BN <= kTmemCols, 62)) {
+            ok = false;
+            break;
+          }
           const int kb0 = u * kb_per_unit;
           const int kb1 = min(num_kb, kb0 + kb_per_unit);
           for (int kb = kb0; kb < kb1; ++kb) {
@@ -210,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t sa = base + stage * kStageBytes;
+            if (!RNL_DCHECK(&g_err_gemm, stage < static_cast<uint32_t>(kStages), 63)) {
+              ok = false;
+              break;
+            }
             const uint64_t adesc = desc_kmajor_sw128(sa);
             const uint64_t bdesc = desc_kmajor_sw128(sa + kABytes);
 #pragma unroll
@@ -244,6 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = item - b * num_tiles;
       int mb, nb;
       tile_coords(tile, num_m, num_n, group_m, mb, nb);
+      if (!RNL_DCHECK(&g_err_gemm, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n && b < nbatch, 64)) {
+        ok = false;
+        break;
+      }
       const int m = mb * BM + row_local;
       const int n_base = nb * BN + half * kColsPerEpiWarp;
       const bool row_ok = m < M;
@@ -264,6 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 1.7 waves back, normally long done) and pull this warp's part of it
         // into L2 while the accumulators drain
         flag = batch_flags + static_cast<int64_t>(tile) * kEpiWarps + ew;
+        // the host sizes the flags for the 128 x 128 tiling (batch_flag_bytes)
+        if (!RNL_DCHECK(&g_err_gemm, static_cast<int64_t>(tile) * kEpiWarps + ew <
+                                         static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128) * 8, 65)) {
+          ok = false;
+          break;
+        }
         if (b > 0) {
           if (!__all_sync(0xFFFFFFFFu, flag_wait(flag, tag | static_cast<uint64_t>(b), abort, &g_err_gemm, 26))) {
             ok = false;
@@ -285,6 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        if (!RNL_DCHECK(&g_err_gemm, buf * kAccStride + (half + 1) * kColsPerEpiWarp <= kTmemCols &&
+                                         kColsPerEpiWarp * (kEpiWarps / 4) <= BN, 66)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < kGroups; ++c) {
           uint32_t r[32];
@@ -322,6 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __threadfence();
           __syncwarp();
           if (lane == 0) flag_release(flag, tag | static_cast<uint64_t>(b + 1));
+        } else if (b > 0) {
+          // the last batch consumed the flag: back to 0, so that a replay of
+          // this launch (same tag, in a CUDA graph) waits for its own flags
+          __syncwarp();
+          if (lane == 0) *flag = 0;
         }
       } else if constexpr (kInt) {
         if (row_ok) {
@@ -405,15 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int EPI, int BN, bool NORM_A>
 rnl_status launch_epi(const GemmArgs& g, const DeviceInfo& dev, cudaStream_t s, const char* name) {
-  static bool attr_set[64] = {};
   auto kern = gemm_kernel<EPI, BN, NORM_A>;
-  if (dev.device < 0 || dev.device >= 64) return RNL_ERR_DEVICE;
-  if (!attr_set[dev.device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN>())) != cudaSuccess)
-      return RNL_ERR_LAUNCH;
-    attr_set[dev.device] = true;
-  }
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device, smem_bytes<BN>()) != RNL_OK)
+    return RNL_ERR_LAUNCH;
   constexpr bool kBatch = EPI == static_cast<int>(Epi::kDequantBatchSum);
   const int64_t nbatch = kBatch ? g.nbatch : 1;
   CUtensorMap ma, mb;

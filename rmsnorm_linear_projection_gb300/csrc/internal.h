@@ -30,6 +30,12 @@ rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                        uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                        uint32_t box_outer);
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on `device` (the
+// current one) once per (kernel, device); thread-safe.  The cache outlives a
+// cudaDeviceReset, which drops the attribute, so a reset device needs the
+// library reloaded.
+rnl_status ensure_smem_attr(const void* kernel, int device, size_t bytes);
+
 // ---- kernel trace (api.cu) ----
 void trace_before(cudaStream_t s);
 void trace_after(cudaStream_t s, const char* name);

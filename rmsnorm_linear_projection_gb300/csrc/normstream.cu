@@ -137,6 +137,10 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         const int64_t row0 = r_begin + g * kGroupRows;
         const int rows = static_cast<int>(r_end - row0 < kGroupRows ? r_end - row0 : kGroupRows);
         const uint32_t dst = base + stage * stage_bytes;
+        if (!RNL_DCHECK(&g_err_norm, stages <= kMaxNsStages && stage < static_cast<uint32_t>(stages) &&
+                                         static_cast<size_t>(stages) * stage_bytes <= kRingBytes &&
+                                         row0 >= 0 && row0 + rows <= T, 50))
+          break;
         for (int r = 0; r < rows; ++r) {
           const uint32_t bar = smem_u32(&ctrl->full[stage][r]);
           mbar_arrive_expect_tx(bar, row_bytes);
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
         if (ext.rstd_out != nullptr && lane == 0) ext.rstd_out[row] = rstd;
         uint4* ar = A + row * nvec;
+        if (!RNL_DCHECK(&g_err_norm, row < T && nvec <= 32 * VPL, 51)) break;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int v = lane + 32 * i;  // the elements this lane wrote above
@@ -259,6 +264,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         s = warp_sum(s);
         const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
         uint4* ar = A + row * nvec;
+        if (!RNL_DCHECK(&g_err_norm, row < T && nvec <= 32 * VPL, 52)) break;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int v = lane + 32 * i;
@@ -296,15 +302,10 @@ template <int MODE, bool GAMMA, int VPL, bool EXT>
 rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int stages, float inv_d,
                      float eps, void* A, const NsExt& ext, size_t smem, const DeviceInfo& dev,
                      cudaStream_t s) {
-  static bool attr_set[64] = {};
   auto kern = norm_cast_stream_kernel<MODE, GAMMA, VPL, EXT>;
-  if (!attr_set[dev.device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kRingBytes + 128 + 2 * 8192 + sizeof(NsCtrl))) !=
-        cudaSuccess)
-      return RNL_ERR_LAUNCH;
-    attr_set[dev.device] = true;
-  }
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device,
+                       kRingBytes + 128 + 2 * 8192 + sizeof(NsCtrl)) != RNL_OK)
+    return RNL_ERR_LAUNCH;
   const int64_t groups = (T + kGroupRows - 1) / kGroupRows;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

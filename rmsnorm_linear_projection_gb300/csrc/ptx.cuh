@@ -19,7 +19,26 @@ namespace rnl {
 constexpr uint32_t kErrTimeout = 1u;
 // bit 1: an argument found bad on the device (e.g. a position outside its table)
 constexpr uint32_t kErrArg = 2u;
+// bit 2: a bounds check of a debug build failed (RNL_DCHECK below)
+constexpr uint32_t kErrBounds = 4u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Debug builds (compiled with -DRNL_DEBUG) check shared-memory stage
+// offsets, TMEM columns and global indices before they are used:
+// RNL_DCHECK(err, cond, site) is true when cond holds; otherwise it records
+// kErrBounds and the site in the module's error word *err and is false, and
+// the caller skips the access and carries on (no trap).  Release builds
+// compile every check to true.
+__device__ __forceinline__ bool dcheck_fail(unsigned int* err, uint32_t site) {
+  atomicCAS(err, 0u, kErrBounds | (site << 8));
+  atomicOr(err, kErrBounds);
+  return false;
+}
+#ifdef RNL_DEBUG
+#define RNL_DCHECK(err, cond, site) ((cond) ? true : ::rnl::dcheck_fail((err), (site)))
+#else
+#define RNL_DCHECK(err, cond, site) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

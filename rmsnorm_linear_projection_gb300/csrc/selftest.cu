@@ -1,4 +1,4 @@
-// selftest.cu -- failure-detection self-test: a kernel waits on an mbarrier
+// selftest.cu -- failure-detection self-tests.  The wait test: a kernel waits on an mbarrier
 // that nothing ever arrives on, through the same bounded wait every kernel of
 // the library uses, with a 1 ms limit.  The wait gives up, records its site
 // in this module's device error word and the kernel returns normally; the
@@ -13,6 +13,15 @@ namespace {
 __device__ unsigned int g_err_selftest;
 
 constexpr uint32_t kSelftestSite = 99;
+constexpr uint32_t kBoundsSite = 98;
+
+// Two words; the check below treats only the first as in range, so the
+// index it refuses still lies inside this array.
+__device__ int g_bounds_selftest[2];
+
+__global__ void bounds_check_kernel(int n_valid, int index) {
+  if (RNL_DCHECK(&g_err_selftest, index < n_valid, kBoundsSite)) g_bounds_selftest[index] = 1;
+}
 
 __global__ void wait_timeout_kernel(unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -50,4 +59,18 @@ extern "C" rnl_status rnl_selftest_wait_timeout(rnl_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rnl::wait_timeout_kernel<<<1, 32, 0, s>>>(1000000ull);  // 1 ms
   return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+}
+
+extern "C" rnl_status rnl_selftest_bounds_check(rnl_stream_t stream) {
+#ifdef RNL_DEBUG
+  rnl::DeviceInfo dev;
+  rnl_status st = rnl::current_device(&dev);
+  if (st != RNL_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rnl::bounds_check_kernel<<<1, 1, 0, s>>>(1, 1);  // index 1 of a 1-word range, inside the array
+  return cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+#else
+  (void)stream;
+  return RNL_ERR_UNSUPPORTED;
+#endif
 }

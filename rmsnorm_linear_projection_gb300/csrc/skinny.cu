@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = static_cast<int>(st / kbpr);
         const int kb = static_cast<int>(st - static_cast<int64_t>(r) * kbpr);
         const uint32_t sx = base + stage * kStage;
+        if (!RNL_DCHECK(&g_err_skinny, stage < static_cast<uint32_t>(kStages) && st < total &&
+                                           r * SM_ROWS < T && kb * SK < K, 80))
+          break;
         const uint32_t bar = smem_u32(&ctrl->full[stage]);
         mbar_arrive_expect_tx(bar, kStage);
         tma_load_2d_hint(sx, &map_x, bar, kb * SK, r * SM_ROWS, pol_x);
@@ -225,6 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, got)) break;
       tc_fence_after();
       float* rec = part + ((static_cast<int64_t>(r) + blockIdx.x) * SM_ROWS + row_local) * kRec;
+      // records hold ceil(T / 128) + gridDim.x row tiles (the host's sizing)
+      if (!RNL_DCHECK(&g_err_skinny, static_cast<int64_t>(r) + blockIdx.x <
+                                         static_cast<int64_t>((T + SM_ROWS - 1) / SM_ROWS) + gridDim.x &&
+                                         buf * NP + NP <= 2 * NP, 81))
+        break;
 #pragma unroll
       for (int c = 0; c < NP / 32; ++c) {
         uint32_t v[32];
@@ -275,6 +283,9 @@ __global__ void __launch_bounds__(128)
     const int64_t b = range_begin(c, total, G), e = range_begin(c + 1, total, G);
     if (e <= f0 || b >= f1) continue;
     const float* rec = part + ((static_cast<int64_t>(r) + c) * SM_ROWS + (t - r * SM_ROWS)) * kRec;
+    if (!RNL_DCHECK(&g_err_skinny, static_cast<int64_t>(r) + c < static_cast<int64_t>((T + SM_ROWS - 1) / SM_ROWS) + G,
+                    82))
+      break;
 #pragma unroll
     for (int j = 0; j < NP; ++j) acc[j] += rec[j];
     ss += rec[NP];
@@ -287,14 +298,9 @@ __global__ void __launch_bounds__(128)
 template <int NP, int MODE>
 rnl_status launch_np(const void* x, const void* W, int64_t T, int64_t K, int64_t N, float eps,
                      float* out, float* part, int G, const DeviceInfo& dev, cudaStream_t s) {
-  static bool attr_set[64] = {};
   auto kern = skinny_kernel<NP, MODE>;
-  if (!attr_set[dev.device]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<NP>())) != cudaSuccess)
-      return RNL_ERR_LAUNCH;
-    attr_set[dev.device] = true;
-  }
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device, smem_bytes<NP>()) != RNL_OK)
+    return RNL_ERR_LAUNCH;
   CUtensorMap mx, mw;
   rnl_status st = make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, T, K * 2, SK, SM_ROWS);
   if (st != RNL_OK) return st;

@@ -54,6 +54,8 @@ CHILD = textwrap.dedent("""
     ws = P(0x20000)
     r = {{}}
     r["version"] = lib.rnl_version()
+    r["debug_build"] = lib.rnl_debug_build()
+    r["bounds_selftest_release"] = lib.rnl_selftest_bounds_check(None)
     r["ws_bf16_qkv"] = lib.rnl_workspace_size(0, 4096, 4096, 6144, 0)
     r["ws_bf16_skinny"] = lib.rnl_workspace_size(0, 16384, 28672, 24, 1)
     r["ws_w8a8"] = lib.rnl_workspace_size(1, 8192, 4096, 4096, 0)
@@ -147,7 +149,7 @@ CHILD = textwrap.dedent("""
     r["pipe_submit_mla_bad_mode"] = lib.rnl_pipeline_submit_mla(None, A, A, A, A, 1e-6, 5, A, ctypes.byref(tk))
     r["pipe_wait_null"] = lib.rnl_pipeline_wait(None, 0, None)
     r["pipe_destroy_null"] = lib.rnl_pipeline_destroy(None)
-    r["status_strings"] = [lib.rnl_status_string(i).decode() for i in range(10)]
+    r["status_strings"] = [lib.rnl_status_string(i).decode() for i in range(11)]
     r["trace_enable"] = lib.rnl_trace_enable(1)
     r["trace_read_empty"] = lib.rnl_trace_read(None, (ctypes.c_float * 4)(), 4)
     lib.rnl_trace_enable(0)
@@ -199,6 +201,7 @@ def test_workspace_sizes(host_results):
     ("mla_null_gamma", NULL), ("mla_N1_not_mult8", ALIGN),
     ("s8_K_not_mult16", ALIGN), ("s8_M0", OK),
     ("trace_enable", OK), ("trace_read_empty", 0),
+    ("debug_build", 0), ("bounds_selftest_release", UNSUP),
     ("ex_sum_without_residual", ARG), ("ex_sum_partial_overlap", ARG), ("ex_misaligned_bias", ALIGN),
     ("ex_misaligned_rstd", ALIGN), ("ex_null_W", NULL), ("ex_bad_mode", ARG), ("ex_small_ws", WORKSPACE),
     ("ex_in_place_no_device", DEVICE),
@@ -220,7 +223,7 @@ def test_argument_checks(host_results, key, want):
 
 def test_status_strings(host_results):
     s = host_results["status_strings"]
-    assert s[0] == "ok" and len(set(s)) == 10
+    assert s[0] == "ok" and len(set(s)) == 11
 
 
 def test_binding_status_checks_are_well_formed():
