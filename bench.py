@@ -49,36 +49,47 @@ DEFAULT_STEPS = {"qkv": 2000, "tiny": 4000, "mla": 2000, "w8a8": 1500, "skinny":
 METRIC = "fused RMSNorm→Linear TFLOP/s (or GB/s) and % of roofline on 1 GB300"
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes) of the
-# roofline stage per step, from the ncu captures summarised under profiles/;
-# only for kernels unchanged since the capture.
-TRAFFIC = {
-    # gemm_pair_kernel<0,256>: 97.96 MB read + 39.78 MB written
-    # (one ncu capture)
-    "qkv": 137.75e6,
-    # gemm_pair_kernel<6,256>, the rope stage in its epilogue: 117.41 MB read + 44.95 MB written
-    # (one ncu capture)
-    "qkv_rope": 162.36e6,
-    # both MLA GEMM stages: 51.86 MB (one CTA, BN 192) + 154.96 MB (pairs)
-    # (one ncu capture; the same stages in mla_hn)
-    "mla": 206.82e6,
-    "mla_hn": 206.82e6,
-    # gemm_kernel<2,256,0>: 121.75 MB read + 45.24 MB written
-    # (one ncu capture)
-    "w8a8": 167.00e6,
-    # gemm_kernel<5,256,0>, all batches: 289.46 MB read + 85.07 MB written
-    # (one ncu capture)
-    "qmrs": 374.53e6,
-    # gemm_pair_kernel<0,256> on the MXFP8 operands: 97.23 MB read + 39.94 MB written
-    # (one ncu capture)
-    "mxfp8": 137.17e6,
-    # skinny_kernel<32,0>: 122.89 MB in an ncu capture at T = 2048, scaled by
-    # rows to T = 16384
-    "skinny": 983.1e6,
-    # decode_kernel<0,4,2>: 50.40 MB read (the 49 KB output stays in L2)
-    # (one ncu capture)
-    "decode": 50.40e6,
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum, bytes per step)
+# of the roofline stage, from the ncu captures summarised under profiles/.
+# Each entry names its profile and the hash of the kernel sources it was
+# captured with (source_hash(), `python bench.py --source-hashes`); when the
+# sources differ now, the line reports traffic null and says why.
+CSRC = "rmsnorm_linear_projection_gb300/csrc/"
+KERNEL_SOURCES = {
+    "pair": [CSRC + "gemm_pair.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
+    "one_cta": [CSRC + "gemm_tc.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
+    "mla": [CSRC + "gemm_pair.cu", CSRC + "gemm_tc.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
+    "mx": [CSRC + "mxgemm.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
+    "skinny": [CSRC + "skinny.cu", CSRC + "ptx.cuh"],
+    "decode": [CSRC + "decode.cu"],
 }
+WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": "mla", "mla_hn": "mla",
+                    "w8a8": "one_cta", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
+                    "decode": "decode", "tiny": "one_cta"}
+TRAFFIC = {}
+
+
+def source_hash(workload):
+    """First 16 hex digits of the SHA-256 of the dominant kernel's sources."""
+    import hashlib
+    key = WORKLOAD_SOURCES.get(workload)
+    if key is None:
+        return None
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[key]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(workload):
+    """(bytes or None, note) of the dominant stage's measured DRAM traffic."""
+    t = TRAFFIC.get(workload)
+    if t is None:
+        return None, "no ncu capture of this stage recorded"
+    if t["sources"] != source_hash(workload):
+        return None, "kernel sources changed since the capture in " + t["profile"]
+    return t["bytes"], t["profile"]
 
 
 def _peaks():
@@ -635,17 +646,36 @@ def run_ours(args):
     dom_name, prefix, dom_amount, bound = w.dominant()
     roofline = None
     dom_ms = [ms for name, ms in trace if name.startswith(prefix)]
+    all_ms = [ms for _, ms in trace]
     if dom_ms:
-        per_step_s = sum(dom_ms) / 1e3 / trace_steps
+        # The traced pass puts events around every launch, which removes the
+        # programmatic-dependent-launch overlap of the timed steps, so the
+        # traced times add up to more than a timed step.  The stage's time is
+        # its share of the traced kernel time applied to the timed step time.
+        traced_s = sum(dom_ms) / 1e3 / trace_steps
+        share = sum(dom_ms) / sum(all_ms)
+        step_s = total_s / args.steps
+        per_step_s = share * step_s
+        fp8 = any(name.startswith("gemm_mxfp8_block_scaled") for name, _ in trace)
         if bound == "hbm":
             achieved, peak, punit = dom_amount / per_step_s / 1e9, peaks["hbm"], "GB/s"
+            psrc = peaks["source"]
+        elif fp8:
+            # E4M3 inputs on the block-scaled tensor cores: the measured bf16
+            # peak times the nominal dense FP8 : BF16 ratio (4.5 : 2.25 PFLOP/s)
+            achieved, peak, punit = dom_amount / per_step_s / 1e12, 2.0 * peaks["bf16"], "TFLOP/s"
+            psrc = peaks["source"] + " bf16 burst x 2 (nominal dense FP8 : BF16 ratio)"
         else:
             achieved, peak, punit = dom_amount / per_step_s / 1e12, peaks["bf16"], "TFLOP/s"
+            psrc = peaks["source"] + " burst"
+        traffic, traffic_note = traffic_of(w.name) if not args.T else (None, "scaled workload (--T)")
         roofline = {"bound": bound, "kernel": dom_name, "achieved": achieved, "peak": peak,
-                    "peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
-                    "unit": punit, "frac": achieved / peak,
-                    "traffic": TRAFFIC.get(w.name) if not args.T else None,
-                    "stage_ms_per_step": per_step_s * 1e3}
+                    "peak_source": psrc, "unit": punit, "frac": achieved / peak,
+                    "traffic": traffic, "traffic_source": traffic_note,
+                    "stage_ms_per_step": per_step_s * 1e3,
+                    "stage_method": "share of the traced per-launch times (events around each launch, "
+                                    "separate pass) applied to the timed step time",
+                    "stage_share": share, "stage_traced_ms_per_step": traced_s * 1e3}
     kernels = {k: {"launches": len(v), "total_ms": sum(v), "avg_ms": statistics.mean(v)}
                for k, v in per_kernel.items()}
     gpu_launches = int(round(len(trace) / trace_steps * args.steps))
@@ -773,7 +803,8 @@ def run_ours(args):
             achieved = w.dominant()[2] / (us * 1e-6) / 1e9
             roofline.update({"achieved": achieved, "frac": achieved / roofline["peak"],
                              "stage_ms_per_step": us * 1e-3,
-                             "duration_source": "CUDA graph of flushed calls (GPU time per call)"})
+                             "stage_method": "CUDA graph of flushed calls (GPU time per call; the "
+                                             "call is this one kernel)"})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu and not args.T:
@@ -818,6 +849,8 @@ def run_ours(args):
 
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--source-hashes", action="store_true",
+                    help="print the hash of each workload's dominant kernel sources and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
@@ -832,6 +865,9 @@ def main():
     ap.add_argument("--T", type=int, default=None,
                     help="override the number of token rows (profiling captures of a smaller case)")
     args = ap.parse_args()
+    if args.source_hashes:
+        print(json.dumps({w: source_hash(w) for w in WORKLOADS}))
+        return 0
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.workload] if args.impl == "ours" else 5
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup

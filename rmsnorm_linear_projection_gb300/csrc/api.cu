@@ -163,14 +163,20 @@ inline bool mx_too_large(int64_t T, int64_t K, int64_t N) {
 }
 
 struct MxLayout {
-  void* A = nullptr;   // bf16 [T, K] dequantised activations
-  void* Wb = nullptr;  // bf16 [N, K] dequantised weight
+  uint8_t* codes = nullptr;  // E4M3 [T, K] activation codes when the caller takes none
+  uint8_t* sfa = nullptr;    // scale atoms of the activations (block-scaled GEMM)
+  uint8_t* sfb = nullptr;    // scale atoms of the weight
+  void* A = nullptr;         // bf16 [T, K] dequantised activations (emulation path)
+  void* Wb = nullptr;        // bf16 [N, K] dequantised weight (emulation path)
   void* part = nullptr;
   size_t bytes = 0;
 };
 MxLayout mx_layout(void* ws, int64_t T, int64_t K, int64_t N) {
   MxLayout l;
   Carve c(ws);
+  l.codes = static_cast<uint8_t*>(c.take(static_cast<size_t>(T) * K));
+  l.sfa = static_cast<uint8_t*>(c.take(mx_sf_atoms_bytes(T, K, 128)));
+  l.sfb = static_cast<uint8_t*>(c.take(mx_sf_atoms_bytes(N, K, mx_native_bn())));
   l.A = c.take(static_cast<size_t>(T) * K * 2);
   l.Wb = c.take(static_cast<size_t>(N) * K * 2);
   l.part = c.take(kGemmPartialBytes);
@@ -228,6 +234,16 @@ bool fused_norm() {
   return e != nullptr && e[0] == '1';
 }
 
+// The MXFP8 mode multiplies on the block-scaled tensor cores
+// (tcgen05.mma kind::mxf8f6f4.block_scale, mxgemm.cu) straight from the E4M3
+// codes; RNL_MXFP8_NATIVE=0 selects the exact emulation instead (operands
+// dequantised to bf16, the bf16 GEMM).  Both give results within the same
+// FP32-accumulation bound.
+bool mx_native() {
+  const char* e = std::getenv("RNL_MXFP8_NATIVE");
+  return e == nullptr || e[0] != '0';
+}
+
 // Up to 4 tokens against a weight of at least 1024 rows (a decode step) run
 // as a matrix-vector product that spreads the weight's rows over every SM
 // (decode.cu); RNL_DECODE=0 sends them to the tensor-core path.
@@ -274,9 +290,10 @@ rnl_status current_device(DeviceInfo* info) {
   return RNL_OK;
 }
 
-rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
-                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                       uint32_t box_outer) {
+namespace {
+rnl_status encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return RNL_ERR_DEVICE;
   const cuuint64_t dims[2] = {inner, outer};
@@ -284,9 +301,24 @@ rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? RNL_OK : RNL_ERR_ARG;
+}
+}  // namespace
+
+rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                       uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                       uint32_t box_outer) {
+  return encode_2d(map, dtype, base, inner, outer, row_bytes, box_inner, box_outer,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+rnl_status make_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                             uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_outer) {
+  return encode_2d(map, dtype, base, inner, outer, row_bytes, box_inner, box_outer,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 namespace {
@@ -328,11 +360,11 @@ void trace_after(cudaStream_t s, const char* name) {
 }
 
 rnl_status read_device_errors(int* site) {
-  unsigned int words[7] = {0, 0, 0, 0, 0, 0, 0};
+  unsigned int words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
       read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
       read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK ||
-      read_clear_error_rope(&words[6]) != RNL_OK)
+      read_clear_error_rope(&words[6]) != RNL_OK || read_clear_error_mx(&words[7]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {
@@ -715,8 +747,15 @@ rnl_status rmsnorm_linear_mxfp8(const void* x, const void* gamma, const uint8_t*
   if (st != RNL_OK) return st;
   const MxLayout l = mx_layout(workspace, T, K, N);
   cudaStream_t s = cs(stream);
+  if (mx_native()) {
+    uint8_t* codes = x_codes_out != nullptr ? x_codes_out : l.codes;
+    st = launch_mx_front(x, gamma, T, K, eps, norm_mode, block, nullptr, codes, x_scale_out, w_codes,
+                         w_scale, N, nullptr, l.sfa, l.sfb, mx_native_bn(), s);
+    if (st != RNL_OK) return st;
+    return launch_mx_gemm_native(codes, w_codes, l.sfa, l.sfb, T, N, K, out, out_dtype, s);
+  }
   st = launch_mx_front(x, gamma, T, K, eps, norm_mode, block, l.A, x_codes_out, x_scale_out,
-                       w_codes, w_scale, N, l.Wb, s);
+                       w_codes, w_scale, N, l.Wb, nullptr, nullptr, 0, s);
   if (st != RNL_OK) return st;
   return mx_gemm(l, T, K, N, out, out_dtype, s);
 }
@@ -741,6 +780,11 @@ rnl_status mxfp8_scaled_mm(const uint8_t* x_codes, const uint8_t* x_scale, const
   if (st != RNL_OK) return st;
   const MxLayout l = mx_layout(workspace, T, K, N);
   cudaStream_t s = cs(stream);
+  if (mx_native()) {
+    st = launch_mx_sf_prep(x_scale, T, w_scale, N, K, block, l.sfa, l.sfb, mx_native_bn(), s);
+    if (st != RNL_OK) return st;
+    return launch_mx_gemm_native(x_codes, w_codes, l.sfa, l.sfb, T, N, K, out, out_dtype, s);
+  }
   st = launch_mx_dequant2(x_codes, x_scale, T, w_codes, w_scale, N, K, block, l.A, l.Wb, s);
   if (st != RNL_OK) return st;
   return mx_gemm(l, T, K, N, out, out_dtype, s);

@@ -29,6 +29,10 @@ rnl_status current_device(DeviceInfo* info);
 rnl_status make_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
                        uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
                        uint32_t box_outer);
+// The same without swizzle (boxes land in shared memory row after row).
+rnl_status make_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                             uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                             uint32_t box_inner, uint32_t box_outer);
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` on `device` (the
 // current one) once per (kernel, device); thread-safe.  The cache outlives a
@@ -87,18 +91,37 @@ rnl_status launch_s8_to_bf16(const int8_t* src, int64_t n, void* dst, cudaStream
 // ---- MXFP8 (mxfp8.cu) ----
 // block must be 32 or 64 (elements per E8M0 scale along K).
 bool mx_block_ok(int64_t block);
-// norm + MX quantisation of x's rows (A = bf16 of the dequantised codes;
-// codes [T, K] and scale bytes [T, K / block] optional) and dequantisation
-// of the E4M3 weight [N, K] with its scales [N, K / block] into Wb, in one
-// launch.  K % block == 0.
+// norm + MX quantisation of x's rows, in one launch with the weight's part.
+// Emulation path (sfa null): A = bf16 of the dequantised codes, codes
+// [T, K] and scale bytes [T, K / block] optional, and the E4M3 weight
+// [N, K] with its scales [N, K / block] dequantised into Wb.  Block-scaled
+// path (sfa, sfb given): codes into q_out (required), scale bytes into s_out
+// (optional), the scale atoms of the rows into sfa (128-row tiles) and of
+// the weight into sfb (bn-row tiles), as mx_gemm_native reads them; A and Wb
+// unused.  K % block == 0.
 rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                            int mode, int64_t block, void* A, uint8_t* q_out, uint8_t* s_out,
                            const uint8_t* w_codes, const uint8_t* w_scale, int64_t N, void* Wb,
-                           cudaStream_t s);
+                           uint8_t* sfa, uint8_t* sfb, int bn, cudaStream_t s);
+// Scale atoms of both operands from scale bytes [M, K / block] and [N, K / block].
+rnl_status launch_mx_sf_prep(const uint8_t* a_scale, int64_t M, const uint8_t* b_scale, int64_t N,
+                             int64_t K, int64_t block, uint8_t* sfa, uint8_t* sfb, int bn,
+                             cudaStream_t s);
 // Dequantisation of two MXFP8 operands [M, K] and [N, K] into bf16 A and B.
 rnl_status launch_mx_dequant2(const uint8_t* a_codes, const uint8_t* a_scale, int64_t M,
                               const uint8_t* b_codes, const uint8_t* b_scale, int64_t N, int64_t K,
                               int64_t block, void* A, void* B, cudaStream_t s);
+
+// ---- block-scaled MXFP8 GEMM (mxgemm.cu) ----
+// Rows of B per output tile (the tiling of the weight's scale atoms).
+int mx_native_bn();
+// Bytes of the scale atoms of a [rows, K] operand cut into tiles of rows_per_tile rows.
+size_t mx_sf_atoms_bytes(int64_t rows, int64_t K, int rows_per_tile);
+// out [M, N] (bf16 or fp32) = scaled_mm of E4M3 codes a [M, K], b [N, K]
+// (16-byte aligned, K % 32 == 0) with their scale atoms.
+rnl_status launch_mx_gemm_native(const uint8_t* a_codes, const uint8_t* b_codes, const uint8_t* sfa,
+                                 const uint8_t* sfb, int64_t M, int64_t N, int64_t K, void* out,
+                                 int out_dtype, cudaStream_t s);
 
 // ---- a few tokens against a wide weight (decode.cu) ----
 // T <= 4 rows, K >= 2048, N >= 1024 outputs, the normalised rows within 96 KB.
@@ -227,6 +250,7 @@ rnl_status read_clear_error_pair(unsigned int* word);
 rnl_status read_clear_error_norm(unsigned int* word);
 rnl_status read_clear_error_selftest(unsigned int* word);
 rnl_status read_clear_error_rope(unsigned int* word);
+rnl_status read_clear_error_mx(unsigned int* word);
 // Reads and clears all of them without synchronising (api.cu): RNL_OK, or
 // RNL_ERR_TIMEOUT / RNL_ERR_ARG with the first recorded site in *site
 // (optional).

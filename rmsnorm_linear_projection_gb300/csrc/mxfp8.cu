@@ -12,18 +12,20 @@
 //   scale  = X + 127                                 (the E8M0 byte)
 //   code   = E4M3(y * 2^-X)                          round to nearest even,
 //                                                     saturating to +-448
-//   A      = bf16(value(code) * 2^X)                 the GEMM's operand
-// The weight [N, K] arrives as E4M3 codes with E8M0 scales [N, K/BLK] and is
-// dequantised the same way.  value(code) * 2^X has four significant bits, so
-// it is exact in bf16 whenever it lies in bf16's normal range (it can only
-// fall below it for blocks with amax < 2^-116); the tcgen05 GEMM on these
-// operands then computes scaled_mm's sum with FP32 accumulation.
+// The weight [N, K] arrives as E4M3 codes with E8M0 scales [N, K/BLK].
 //
-// Why not the block-scaled MMA (tcgen05.mma kind::mxf8f6f4.block_scale): its
-// scale factors sit in tensor memory in a layout fixed per scale vector size,
-// and its hardware block is 32 elements; the exact emulation above keeps the
-// page's 64-element block, reuses the measured bf16 GEMM, and gives codes and
-// scales that match the oracle bit for bit.
+// Block-scaled path (the default): the codes go to the block-scaled tensor
+// cores as they are (mxgemm.cu); this front end writes the rows' codes and
+// their scale atoms (the 512-byte blocks the GEMM copies into tensor memory,
+// each 64-element scale given to both 32-element hardware blocks), and its
+// weight blocks arrange the weight's scales into atoms of the GEMM's tiles.
+//
+// Emulation path (RNL_MXFP8_NATIVE=0): A = bf16(value(code) * 2^X), and the
+// weight is dequantised the same way.  value(code) * 2^X has four
+// significant bits, so it is exact in bf16 whenever it lies in bf16's normal
+// range (it can only fall below it for blocks with amax < 2^-116); the bf16
+// tcgen05 GEMM on these operands then computes scaled_mm's sum with FP32
+// accumulation.
 //
 // The codes of y * 2^-X come from cuda_fp8.h's saturating E4M3 conversion; y
 // * 2^-X is exact (a power-of-two scaling that stays inside binary32's range:
@@ -72,13 +74,14 @@ __device__ __forceinline__ uint32_t e4m3x2_code(float a, float b) {
 }
 
 // Quantises the 8 values f of one 16-byte vector of a row (lanes in groups
-// of BLK/8 hold one block): writes the dequantised bf16 operand, and the
-// codes and the block's scale byte when asked.  Every lane of the warp calls
-// it (the block maximum is a shuffle); `live` says whether this lane's vector
-// is inside the row.
+// of BLK/8 hold one block): writes the dequantised bf16 operand (a_dst, the
+// emulation path) and the codes and the block's scale byte when asked, and
+// returns the block's scale byte (127 for a lane outside the row).  Every
+// lane of the warp calls it (the block maximum is a shuffle); `live` says
+// whether this lane's vector is inside the row.
 template <int BLK>
-__device__ __forceinline__ void quant_vec(const float (&f)[8], bool live, uint4* a_dst,
-                                          uint2* q_dst, uint8_t* s_dst) {
+__device__ __forceinline__ int quant_vec(const float (&f)[8], bool live, uint4* a_dst,
+                                         uint2* q_dst, uint8_t* s_dst) {
   constexpr int kGroup = BLK / 8;  // lanes per block
   float am = 0.f;
 #pragma unroll
@@ -88,21 +91,55 @@ __device__ __forceinline__ void quant_vec(const float (&f)[8], bool live, uint4*
   const int eb = static_cast<int>((__float_as_uint(am) >> 23) & 0xFFu);
   int X = eb == 0 ? -127 : eb - 127 - 8;  // floor(log2 amax) - 8 for normal amax
   if (X < -127) X = -127;
-  if (!live) return;
+  if (!live) return 127;
   const float inv = pow2f(-X);
-  const float p = pow2f(X);
   uint32_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) c[i] = e4m3x2_code(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
-  uint32_t o[4];
+  if (a_dst != nullptr) {
+    const float p = pow2f(X);
+    uint32_t o[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = e4m3x2_value(c[i]);
-    o[i] = pack_bf16x2(__fmul_rn(v.x, p), __fmul_rn(v.y, p));
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = e4m3x2_value(c[i]);
+      o[i] = pack_bf16x2(__fmul_rn(v.x, p), __fmul_rn(v.y, p));
+    }
+    *a_dst = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  *a_dst = make_uint4(o[0], o[1], o[2], o[3]);
   if (q_dst != nullptr) *q_dst = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   if (s_dst != nullptr && (threadIdx.x & (kGroup - 1)) == 0) *s_dst = static_cast<uint8_t>(X + 127);
+  return X + 127;
+}
+
+// Scale-factor atoms of the block-scaled GEMM (mxgemm.cu): for a matrix of
+// `rows` rows cut into tiles of `rpt` rows, atom (tile, kg, t) holds the
+// scale bytes of the tile's rows t * 128 .. t * 128 + 127 for the four
+// 32-element blocks of k-block kg (128 elements); row r of the atom at word
+// 4 (r % 32) + r / 32, byte j for block j.  A page block of 64 gives the same
+// byte to its two 32-element halves; rows past the matrix and blocks past K
+// get 127 (scale 1; their codes are zero).
+template <int BLK>
+__device__ __forceinline__ uint32_t sf_atom_word(const uint8_t* __restrict__ scales, int64_t rows, int K,
+                                                 int rpt, int atoms, int num_kg, int64_t w) {
+  const int64_t atom = w >> 7;
+  const int within = static_cast<int>(w & 127);
+  const int r = (within >> 2) + 32 * (within & 3);
+  const int t = static_cast<int>(atom % atoms);
+  const int64_t rest = atom / atoms;
+  const int kg = static_cast<int>(rest % num_kg);
+  const int64_t tile = rest / num_kg;
+  const int rt = t * 128 + r;
+  const int64_t row = tile * rpt + rt;
+  if (rt >= rpt || row >= rows) return 0x7F7F7F7Fu;
+  const int nb = K / BLK;
+  uint32_t word = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int k0 = (4 * kg + j) * 32;
+    const uint32_t s = k0 < K ? __ldg(scales + row * nb + k0 / BLK) : 127u;
+    word |= s << (8 * j);
+  }
+  return word;
 }
 
 struct MxRows {
@@ -111,15 +148,25 @@ struct MxRows {
   int64_t T;
   int nvec;  // K / 8
   float inv_d, eps;
-  uint4* A;           // bf16 [T, K]
+  uint4* A;           // bf16 [T, K] (emulation path) or null
   uint2* q_out;       // E4M3 [T, K] or null
   uint8_t* s_out;     // E8M0 [T, K / BLK] or null
   const uint4* w;     // E4M3 [N, K]
   const uint8_t* ws;  // E8M0 [N, K / BLK]
   int64_t w_nvec16;   // N * K / 16
   int k_vec16;        // K / 16
-  uint4* Wb;          // bf16 [N, K]
+  uint4* Wb;          // bf16 [N, K] (emulation path)
   unsigned quant_blocks, dq_blocks;
+  // block-scaled path: the weight blocks write the weight's scale atoms
+  // instead of dequantising it, the rows write their own atoms
+  bool native;
+  uint32_t* sfa;      // A atoms (128-row tiles), words
+  uint32_t* sfb;      // B atoms (bn-row tiles), words
+  int64_t T_pad;      // T rounded up to 128: rows T .. T_pad - 1 get padding atoms
+  int num_kg;         // k-blocks of 128
+  int64_t N;
+  int bn, b_atoms;
+  int64_t sfb_words;
 };
 
 __device__ __forceinline__ void load_y(const uint4& u, const uint4* gamma, int v, float rstd,
@@ -135,6 +182,20 @@ __device__ __forceinline__ void load_y(const uint4& u, const uint4* gamma, int v
   }
 }
 
+// The 16 lanes holding the 16 vectors (128 elements) of k-block kg = v / 16
+// hand their blocks' scale bytes to the first of them, which writes the row's
+// atom word: bytes of the 32-element blocks at lanes +0, +4, +8, +12.  Every
+// lane calls it (shuffles).
+__device__ __forceinline__ void put_atom_word(uint32_t* sfa_row, int sb, int v, int lane, int num_kg) {
+  const int s1 = __shfl_down_sync(0xffffffffu, sb, 4);
+  const int s2 = __shfl_down_sync(0xffffffffu, sb, 8);
+  const int s3 = __shfl_down_sync(0xffffffffu, sb, 12);
+  const int kg = v >> 4;
+  if ((lane & 15) == 0 && kg < num_kg)
+    sfa_row[static_cast<int64_t>(kg) * 128] = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(s1) << 8) |
+                                              (static_cast<uint32_t>(s2) << 16) | (static_cast<uint32_t>(s3) << 24);
+}
+
 // One token row.  VPL > 0: the row's vectors stay in registers (K <= 256 *
 // VPL); VPL == 0: any K, x read twice (the sum of squares, then the blocks;
 // the second read mostly hits L2), each pass with several 16-byte loads in
@@ -143,7 +204,16 @@ template <int MODE, int VPL, int BLK>
 __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(block) * kWarps + (threadIdx.x >> 5);
-  if (row >= p.T) return;
+  // the block-scaled path's atom words of this row: word 4 (row % 32) + (row / 32) % 4
+  // of atom (row / 128, kg)
+  uint32_t* const sfa_row = p.sfa != nullptr
+                                ? p.sfa + (row / 128) * p.num_kg * 128 + 4 * (row % 32) + (row / 32) % 4
+                                : nullptr;
+  if (row >= p.T) {
+    if (sfa_row != nullptr && row < p.T_pad)
+      for (int kg = lane; kg < p.num_kg; kg += 32) sfa_row[static_cast<int64_t>(kg) * 128] = 0x7F7F7F7Fu;
+    return;
+  }
   const uint4* xr = p.x + row * p.nvec;
   const int iters = (p.nvec + 31) / 32;  // the same on every lane
   constexpr int kR = VPL > 0 ? VPL : 1;
@@ -184,7 +254,7 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
   }
   const float rstd = rstd_of_sum<MODE>(ff_warp_total(hs, ls), p.inv_d, p.eps);
   const int nb = p.nvec / (BLK / 8);  // blocks per row
-  uint4* ar = p.A + row * p.nvec;
+  uint4* ar = p.A != nullptr ? p.A + row * p.nvec : nullptr;
   uint2* qr = p.q_out != nullptr ? p.q_out + row * p.nvec : nullptr;
   uint8_t* sr = p.s_out != nullptr ? p.s_out + row * nb : nullptr;
   if (VPL > 0) {
@@ -195,7 +265,9 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
       const bool live = v < p.nvec;
       float f[8];
       load_y(u[i], live ? p.gamma : nullptr, v, rstd, f);
-      quant_vec<BLK>(f, live, ar + v, qr ? qr + v : nullptr, sr ? sr + v / (BLK / 8) : nullptr);
+      const int sb = quant_vec<BLK>(f, live, ar ? ar + v : nullptr, qr ? qr + v : nullptr,
+                                    sr ? sr + v / (BLK / 8) : nullptr);
+      if (sfa_row != nullptr) put_atom_word(sfa_row, sb, v, lane, p.num_kg);
     }
   } else {
     for (int i = 0; i < iters; i += 2) {  // two vectors per lane in flight
@@ -212,7 +284,9 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
         const bool live = v < p.nvec;
         float f[8];
         load_y(w[j], live ? p.gamma : nullptr, v, rstd, f);
-        quant_vec<BLK>(f, live, ar + v, qr ? qr + v : nullptr, sr ? sr + v / (BLK / 8) : nullptr);
+        const int sb = quant_vec<BLK>(f, live, ar ? ar + v : nullptr, qr ? qr + v : nullptr,
+                                      sr ? sr + v / (BLK / 8) : nullptr);
+        if (sfa_row != nullptr) put_atom_word(sfa_row, sb, v, lane, p.num_kg);
       }
     }
   }
@@ -278,10 +352,32 @@ __global__ void __launch_bounds__(kWarps * 32, 4) mx_front_kernel(MxRows p) {
     quant = p.quant_blocks > p.dq_blocks;
     idx = b - both;
   }
-  if (quant)
+  if (quant) {
     mx_quant_row<MODE, VPL, BLK>(idx, p);
-  else
+  } else if (p.native) {
+    // the weight's scale atoms: one word a thread
+    const int64_t w = static_cast<int64_t>(idx) * blockDim.x + threadIdx.x;
+    if (w < p.sfb_words)
+      p.sfb[w] = sf_atom_word<BLK>(p.ws, p.N, p.k_vec16 * 16, p.bn, p.b_atoms, p.num_kg, w);
+  } else {
     mx_dequant_block<BLK>(idx, p.w, p.ws, p.w_nvec16, p.k_vec16, p.Wb);
+  }
+}
+
+// Both operands' scale atoms from scale bytes in the page's layout [rows,
+// K / BLK] (scaled_mm on codes that were quantised elsewhere): one word a
+// thread, A's atoms (128-row tiles) first.
+template <int BLK>
+__global__ void __launch_bounds__(256)
+    mx_sf_prep_kernel(const uint8_t* __restrict__ a_scale, int64_t M, uint32_t* __restrict__ sfa,
+                      int64_t a_words, const uint8_t* __restrict__ b_scale, int64_t N,
+                      uint32_t* __restrict__ sfb, int64_t b_words, int K, int num_kg, int bn,
+                      int b_atoms) {
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (w < a_words)
+    sfa[w] = sf_atom_word<BLK>(a_scale, M, K, 128, 1, num_kg, w);
+  else if (w - a_words < b_words)
+    sfb[w - a_words] = sf_atom_word<BLK>(b_scale, N, K, bn, b_atoms, num_kg, w - a_words);
 }
 
 // Dequantisation of two operands (activation codes, then weight codes).
@@ -321,7 +417,7 @@ bool mx_block_ok(int64_t block) { return block == 32 || block == 64; }
 rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                            int mode, int64_t block, void* A, uint8_t* q_out, uint8_t* s_out,
                            const uint8_t* w_codes, const uint8_t* w_scale, int64_t N, void* Wb,
-                           cudaStream_t s) {
+                           uint8_t* sfa, uint8_t* sfb, int bn, cudaStream_t s) {
   MxRows p;
   p.x = static_cast<const uint4*>(x);
   p.gamma = static_cast<const uint4*>(gamma);
@@ -337,8 +433,17 @@ rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t 
   p.w_nvec16 = N * K / 16;
   p.k_vec16 = static_cast<int>(K / 16);
   p.Wb = static_cast<uint4*>(Wb);
-  p.quant_blocks = static_cast<unsigned>((T + kWarps - 1) / kWarps);
-  p.dq_blocks = dq_blocks_for(p.w_nvec16);
+  p.native = sfa != nullptr;
+  p.sfa = reinterpret_cast<uint32_t*>(sfa);
+  p.sfb = reinterpret_cast<uint32_t*>(sfb);
+  p.T_pad = (T + 127) / 128 * 128;
+  p.num_kg = static_cast<int>((K + 127) / 128);
+  p.N = N;
+  p.bn = bn;
+  p.b_atoms = (bn + 127) / 128;
+  p.sfb_words = p.native ? ((N + bn - 1) / bn) * p.num_kg * p.b_atoms * 128 : 0;
+  p.quant_blocks = static_cast<unsigned>(((p.native ? p.T_pad : T) + kWarps - 1) / kWarps);
+  p.dq_blocks = p.native ? static_cast<unsigned>((p.sfb_words + 255) / 256) : dq_blocks_for(p.w_nvec16);
   const unsigned grid = p.quant_blocks + p.dq_blocks;
   if (grid == 0) return RNL_OK;
   const int vpl = (p.nvec + 31) / 32;
@@ -377,6 +482,29 @@ rnl_status launch_mx_dequant2(const uint8_t* a_codes, const uint8_t* a_scale, in
                                                    b_scale, b16, static_cast<uint4*>(B), kv);
   const rnl_status st = cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
   trace_after(s, "mxfp8_dequant");
+  return st;
+}
+
+rnl_status launch_mx_sf_prep(const uint8_t* a_scale, int64_t M, const uint8_t* b_scale, int64_t N,
+                             int64_t K, int64_t block, uint8_t* sfa, uint8_t* sfb, int bn,
+                             cudaStream_t s) {
+  const int num_kg = static_cast<int>((K + 127) / 128);
+  const int b_atoms = (bn + 127) / 128;
+  const int64_t a_words = ((M + 127) / 128) * num_kg * 128;
+  const int64_t b_words = ((N + bn - 1) / bn) * num_kg * b_atoms * 128;
+  const int64_t blocks = (a_words + b_words + 255) / 256;
+  if (blocks == 0) return RNL_OK;
+  auto* wa = reinterpret_cast<uint32_t*>(sfa);
+  auto* wb = reinterpret_cast<uint32_t*>(sfb);
+  trace_before(s);
+  if (block == 64)
+    mx_sf_prep_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        a_scale, M, wa, a_words, b_scale, N, wb, b_words, static_cast<int>(K), num_kg, bn, b_atoms);
+  else
+    mx_sf_prep_kernel<32><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        a_scale, M, wa, a_words, b_scale, N, wb, b_words, static_cast<int>(K), num_kg, bn, b_atoms);
+  const rnl_status st = cudaGetLastError() == cudaSuccess ? RNL_OK : RNL_ERR_LAUNCH;
+  trace_after(s, "mxfp8_scale_atoms");
   return st;
 }
 

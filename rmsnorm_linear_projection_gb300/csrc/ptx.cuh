@@ -193,6 +193,18 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completion counted on `bar` as
+// transaction bytes.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -397,6 +409,77 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
   return d;
+}
+
+// Shared-memory descriptor of a block without swizzle: 16-byte rows, 8-row
+// core matrices `sbo` bytes apart (`lbo` between core matrices along the
+// row, unused for blocks one core matrix wide).
+__device__ __forceinline__ uint64_t desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copy 32 rows of 16 bytes (one 512-byte block, row r at byte 16 r) from
+// shared memory into TMEM: row r lands in lane r of each of the four 32-lane
+// quarters (the same data four times), as 4 consecutive 32-bit columns.
+// Issued by one thread; ordered before that thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// The same on a CTA pair, issued by one thread of the even CTA: each CTA's
+// block (at the same shared-memory offset in both) goes to its own TMEM.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with E4M3 A and B in shared memory
+// and E8M0 scale factors in TMEM (kind::mxf8f6f4, one scale per 32 elements
+// of K, K = 32 per instruction).  The scale of A row m is byte `id` of the
+// 32-bit word at lane m % 32, column sfa + m / 32 (any lane quarter); B row n
+// at lane n % 32, column sfb + 4 (n / 128) + (n % 128) / 32; the byte id sits
+// in the instruction descriptor (idesc_mxf8_id).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Pair form (M = 256 over the two CTAs), issued by one thread of the even
+// CTA; each CTA's tensor core uses the scale factors in its own TMEM (its own
+// 128 rows of A, all of B's rows).
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 for E4M3 A and B (K-major), E8M0
+// scale factors and an fp32 accumulator of M x N; the scale-factor byte ids
+// (bits 29-30 for A, 4-5 for B) are added by idesc_mxf8_id.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
+  return (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                             // scale factors: E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_mxf8_id(uint32_t idesc, uint32_t id) {
+  return idesc | (id << 29) | (id << 4);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B (both K-major) and

@@ -185,7 +185,10 @@ def test_workspace_sizes(host_results):
                             + 16 * 32 * 64)
     assert r["ws_qmrs_b1"] == 2048 * 4096 * 2 + 4096 * 4096 * 2 + 4096 * 4  # no running sum
     # MXFP8: dequantised bf16 activations and weight, GEMM partials
-    assert r["ws_mxfp8"] == 4096 * 4096 * 2 + 6144 * 4096 * 2 + part
+    # codes + scale atoms of x (32 row blocks x 32 k-blocks) and W (32 tiles of 192 rows x 32 x 2)
+    # for the block-scaled GEMM, then the dequantised operands of the emulation path
+    assert r["ws_mxfp8"] == (4096 * 4096 + 32 * 32 * 512 + 32 * 32 * 2 * 512 + 4096 * 4096 * 2 +
+                             6144 * 4096 * 2 + part)
     max_size = (1 << 64) - 1
     assert r["ws_bad_op"] == max_size and r["ws_neg"] == max_size
 

@@ -6,8 +6,10 @@ every later step one correctly rounded operation), the block exponent is read
 from the FP32 block maximum, and y * 2^-X is exact, so the E4M3 rounding sees
 the same value on both sides.
 
-Products: the GPU multiplies the exactly dequantised operands on the tensor
-cores with FP32 accumulation; fp32 out is held to the FP32 accumulation bound
+Products, on both routes (the block-scaled tensor cores fed the E4M3 codes
+and their scales, and the exact emulation with RNL_MXFP8_NATIVE=0 that
+multiplies the dequantised operands with the bf16 GEMM), both with FP32
+accumulation: fp32 out is held to the FP32 accumulation bound
 |gpu - ref| <= 2^-16 sum_k |a_k w_k| + 2^-20 |ref| (ref the oracle's binary64
 sum), bf16 out to the acceptance bound 1e-2 * max(1, |oracle|).
 """
@@ -31,6 +33,19 @@ def cuda_ready():
     build.build()
     torch.cuda.set_device(0)
     yield
+    rnl.rnl_check_device_error()
+
+
+@pytest.fixture(autouse=True, params=["native", "native_one_cta", "emulated"])
+def route(request, monkeypatch):
+    """Every test on the block-scaled route (CTA pairs for more than 128 rows,
+    and the one-CTA kernel forced) and on the emulation route."""
+    monkeypatch.setenv("RNL_MXFP8_NATIVE", "0" if request.param == "emulated" else "1")
+    if request.param == "native_one_cta":
+        monkeypatch.setenv("RNL_MXFP8_PAIR", "0")
+    else:
+        monkeypatch.delenv("RNL_MXFP8_PAIR", raising=False)
+    yield request.param
     rnl.rnl_check_device_error()
 
 
