@@ -175,7 +175,8 @@ MxLayout mx_layout(void* ws, int64_t T, int64_t K, int64_t N) {
   MxLayout l;
   Carve c(ws);
   l.codes = static_cast<uint8_t*>(c.take(static_cast<size_t>(T) * K));
-  l.sfa = static_cast<uint8_t*>(c.take(mx_sf_atoms_bytes(T, K, 128)));
+  // A's atoms cover whole 256-row tiles (the CTA-pair GEMM reads both halves)
+  l.sfa = static_cast<uint8_t*>(c.take(mx_sf_atoms_bytes((T + 255) / 256 * 256, K, 128)));
   l.sfb = static_cast<uint8_t*>(c.take(mx_sf_atoms_bytes(N, K, mx_native_bn())));
   l.A = c.take(static_cast<size_t>(T) * K * 2);
   l.Wb = c.take(static_cast<size_t>(N) * K * 2);

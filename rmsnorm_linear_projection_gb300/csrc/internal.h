@@ -96,9 +96,9 @@ bool mx_block_ok(int64_t block);
 // [T, K] and scale bytes [T, K / block] optional, and the E4M3 weight
 // [N, K] with its scales [N, K / block] dequantised into Wb.  Block-scaled
 // path (sfa, sfb given): codes into q_out (required), scale bytes into s_out
-// (optional), the scale atoms of the rows into sfa (128-row tiles) and of
-// the weight into sfb (bn-row tiles), as mx_gemm_native reads them; A and Wb
-// unused.  K % block == 0.
+// (optional), the scale atoms of the rows into sfa (128-row tiles, padded
+// to a multiple of 256 rows) and of the weight into sfb (bn-row tiles), as
+// mx_gemm_native reads them; A and Wb unused.  K % block == 0.
 rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                            int mode, int64_t block, void* A, uint8_t* q_out, uint8_t* s_out,
                            const uint8_t* w_codes, const uint8_t* w_scale, int64_t N, void* Wb,

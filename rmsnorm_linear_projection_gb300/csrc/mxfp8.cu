@@ -162,7 +162,7 @@ struct MxRows {
   bool native;
   uint32_t* sfa;      // A atoms (128-row tiles), words
   uint32_t* sfb;      // B atoms (bn-row tiles), words
-  int64_t T_pad;      // T rounded up to 128: rows T .. T_pad - 1 get padding atoms
+  int64_t T_pad;      // T rounded up to 256: rows T .. T_pad - 1 get padding atoms
   int num_kg;         // k-blocks of 128
   int64_t N;
   int bn, b_atoms;
@@ -436,7 +436,7 @@ rnl_status launch_mx_front(const void* x, const void* gamma, int64_t T, int64_t 
   p.native = sfa != nullptr;
   p.sfa = reinterpret_cast<uint32_t*>(sfa);
   p.sfb = reinterpret_cast<uint32_t*>(sfb);
-  p.T_pad = (T + 127) / 128 * 128;
+  p.T_pad = (T + 255) / 256 * 256;  // whole 256-row tiles of the CTA-pair GEMM
   p.num_kg = static_cast<int>((K + 127) / 128);
   p.N = N;
   p.bn = bn;
@@ -490,7 +490,7 @@ rnl_status launch_mx_sf_prep(const uint8_t* a_scale, int64_t M, const uint8_t* b
                              cudaStream_t s) {
   const int num_kg = static_cast<int>((K + 127) / 128);
   const int b_atoms = (bn + 127) / 128;
-  const int64_t a_words = ((M + 127) / 128) * num_kg * 128;
+  const int64_t a_words = ((M + 255) / 256) * 2 * num_kg * 128;  // whole 256-row tiles
   const int64_t b_words = ((N + bn - 1) / bn) * num_kg * b_atoms * 128;
   const int64_t blocks = (a_words + b_words + 255) / 256;
   if (blocks == 0) return RNL_OK;

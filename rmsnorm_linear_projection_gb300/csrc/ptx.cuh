@@ -396,6 +396,19 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Each thread of the warp writes 4 consecutive 32-bit columns of its own TMEM
+// lane (lane = the warp's lane quarter * 32 + lane id); tmem_st_wait waits
+// until this thread's stores are done.
+__device__ __forceinline__ void tmem_st_4cols(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile stored the way
 // a TMA load with 128-byte swizzle leaves it: rows of 128 bytes (64 bf16),
 // 8-row groups 1024 bytes apart, 16-byte chunks XOR-permuted by row % 8.

@@ -36,13 +36,13 @@ def cuda_ready():
     rnl.rnl_check_device_error()
 
 
-@pytest.fixture(autouse=True, params=["native", "native_one_cta", "emulated"])
+@pytest.fixture(autouse=True, params=["native", "native_pair", "emulated"])
 def route(request, monkeypatch):
-    """Every test on the block-scaled route (CTA pairs for more than 128 rows,
-    and the one-CTA kernel forced) and on the emulation route."""
+    """Every test on the block-scaled route (the default one-CTA kernel, and
+    the CTA-pair form forced) and on the emulation route."""
     monkeypatch.setenv("RNL_MXFP8_NATIVE", "0" if request.param == "emulated" else "1")
-    if request.param == "native_one_cta":
-        monkeypatch.setenv("RNL_MXFP8_PAIR", "0")
+    if request.param == "native_pair":
+        monkeypatch.setenv("RNL_MXFP8_PAIR", "1")
     else:
         monkeypatch.delenv("RNL_MXFP8_PAIR", raising=False)
     yield request.param
