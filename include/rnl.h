@@ -100,7 +100,8 @@ enum {
   RNL_OP_GEMM_S8 = 3,
   RNL_OP_QKV_ROPE = 4,
   RNL_OP_QMRS = 5,
-  RNL_OP_MXFP8 = 6
+  RNL_OP_MXFP8 = 6,
+  RNL_OP_W8A8_PREPARED = 7
 };
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -128,6 +129,7 @@ const char *rnl_status_string(rnl_status s);
  *   RNL_OP_QKV_ROPE: T, K, N = (n_q_heads + 2 * n_kv_heads) * head_dim; N2 ignored
  *   RNL_OP_QMRS:    T = M, K, N, N2 = B (the batch)
  *   RNL_OP_MXFP8:   T, K, N; N2 ignored (rmsnorm_linear_mxfp8 and mxfp8_scaled_mm)
+ *   RNL_OP_W8A8_PREPARED: T, K, N; N2 ignored (rmsnorm_linear_w8a8_prepared)
  * Returns (size_t)-1 for invalid sizes.  Host-only; needs no GPU.
  */
 size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2);
@@ -260,12 +262,39 @@ rnl_status quant_matmul_reduce_sum(const int8_t *x1, const int8_t *x2, const flo
  * The integer accumulation is exact for every input (chunks of at most 1024
  * products are summed exactly on the tensor pipe, then added in int32);
  * a sum outside the int32 range wraps as two's complement (impossible for
- * K <= 133144).
+ * K <= 133144).  Each call widens Wq to the tensor cores' bf16 operand in
+ * the workspace; a weight used for many calls is better prepared once
+ * (rnl_w8a8_prepare_weight, rmsnorm_linear_w8a8_prepared).
  */
 rnl_status rmsnorm_linear_w8a8(const void *x, const void *gamma, const int8_t *Wq,
                                const float *w_scale, int64_t T, int64_t K, int64_t N, float eps,
                                int norm_mode, void *out, int8_t *q_out, float *x_scale_out,
                                void *workspace, size_t workspace_bytes, rnl_stream_t stream);
+
+/*
+ * The W8A8 weight prepared once, outside the per-call path, as the pages do
+ * with weights (the SK-03 skeleton page, "shape variant: huge reduction x
+ * tiny output width": the weight is transposed once on the host, not per
+ * call).  Wq int8 [N, K] with values in [-127, 127] is widened exactly to
+ * Wb bf16 [N, K], the operand the integer matmul reads (caller-owned,
+ * 2 N K bytes).  K % 16 == 0; Wq and Wb 16-byte aligned.  Enqueued on
+ * `stream`.
+ */
+rnl_status rnl_w8a8_prepare_weight(const int8_t *Wq, int64_t N, int64_t K, void *Wb,
+                                   rnl_stream_t stream);
+
+/*
+ * rmsnorm_linear_w8a8 with a weight prepared by rnl_w8a8_prepare_weight:
+ * Wb bf16 [N, K] (the exact integers of Wq; any other contents void the
+ * exactness of the integer sums).  Other arguments, results and alignment
+ * as rmsnorm_linear_w8a8; workspace rnl_workspace_size(RNL_OP_W8A8_PREPARED,
+ * T, K, N, 0) bytes (no room for a widened weight).
+ */
+rnl_status rmsnorm_linear_w8a8_prepared(const void *x, const void *gamma, const void *Wb,
+                                        const float *w_scale, int64_t T, int64_t K, int64_t N,
+                                        float eps, int norm_mode, void *out, int8_t *q_out,
+                                        float *x_scale_out, void *workspace, size_t workspace_bytes,
+                                        rnl_stream_t stream);
 
 /*
  * Per-head RMSNorm of a projection output (AT-10 pattern page, sec. 9: the

@@ -8,6 +8,8 @@ arguments; the computation runs in the library's CUDA kernels.
     rmsnorm_linear_bf16_ex  the same with residual add, norm bias, output_rstd and
                           projection bias
     rmsnorm_linear_w8a8   AT-11 RMSNorm + INT8 quant + exact INT8 matmul + dequant
+    rnl_w8a8_prepare_weight / rmsnorm_linear_w8a8_prepared
+                          the same with the weight widened once
     mla_q_chain           MLA q_a projection -> RMSNorm * gamma_cq -> q_b projection
     mla_q_chain_head_norm / rnl_head_rmsnorm
                           the same chain with the per-head RMSNorm after q_b, and that norm alone
@@ -34,6 +36,7 @@ from ._native import (  # noqa: F401
     OP_QKV_ROPE,
     OP_QMRS,
     OP_W8A8,
+    OP_W8A8_PREPARED,
     OUT_BF16,
     OUT_FP32,
     PipelineHandle,
@@ -50,6 +53,7 @@ from ._native import (  # noqa: F401
     rmsnorm_linear_qkv_rope,
     rmsnorm_linear_skinny_noalloc,
     rmsnorm_linear_w8a8,
+    rmsnorm_linear_w8a8_prepared,
     rnl_check_device_error,
     rnl_debug_build,
     rnl_gemm_s8s8s32,
@@ -65,5 +69,6 @@ from ._native import (  # noqa: F401
     rnl_selftest_wait_timeout,
     rnl_trace_enable,
     rnl_trace_read,
+    rnl_w8a8_prepare_weight,
     workspace_size,
 )

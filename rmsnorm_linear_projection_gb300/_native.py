@@ -22,7 +22,7 @@ DEBUG_LIB_PATH = os.path.join(PKG, "librnl_debug.so")
 
 NORM_RSQRT, NORM_SQRT_DIV = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
-OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS, OP_MXFP8 = 0, 1, 2, 3, 4, 5, 6
+OP_BF16, OP_W8A8, OP_MLA, OP_GEMM_S8, OP_QKV_ROPE, OP_QMRS, OP_MXFP8, OP_W8A8_PREPARED = range(8)
 
 STATUS = {
     0: "RNL_OK", 1: "RNL_ERR_NULL", 2: "RNL_ERR_SHAPE", 3: "RNL_ERR_ALIGN", 4: "RNL_ERR_ARG",
@@ -37,7 +37,8 @@ EXPORTS = ("rnl_version", "rnl_debug_build", "rnl_selftest_bounds_check", "rnl_s
            "rnl_pipeline_submit_w8a8", "rnl_pipeline_submit_mla", "rnl_pipeline_wait",
            "rnl_pipeline_destroy", "rmsnorm_linear_bf16_ex", "rnl_qkv_rope",
            "rmsnorm_linear_qkv_rope", "quant_matmul_reduce_sum", "rmsnorm_linear_mxfp8",
-           "mxfp8_scaled_mm", "rnl_head_rmsnorm", "mla_q_chain_head_norm")
+           "mxfp8_scaled_mm", "rnl_head_rmsnorm", "mla_q_chain_head_norm", "rnl_w8a8_prepare_weight",
+           "rmsnorm_linear_w8a8_prepared")
 
 
 class RnlError(RuntimeError):
@@ -60,6 +61,8 @@ def _declare(lib):
         "rnl_workspace_size": (SZ, [I, I64, I64, I64, I64]),
         "rmsnorm_linear_bf16": (I, [P, P, P, I64, I64, I64, F, I, P, I, P, SZ, P]),
         "rmsnorm_linear_w8a8": (I, [P, P, P, P, I64, I64, I64, F, I, P, P, P, P, SZ, P]),
+        "rmsnorm_linear_w8a8_prepared": (I, [P, P, P, P, I64, I64, I64, F, I, P, P, P, P, SZ, P]),
+        "rnl_w8a8_prepare_weight": (I, [P, I64, I64, P, P]),
         "mla_q_chain": (I, [P, P, P, P, I64, I64, I64, I64, F, I, P, P, P, SZ, P]),
         "rnl_gemm_s8s8s32": (I, [P, P, P, I64, I64, I64, P, SZ, P]),
         "rnl_check_device_error": (I, [P, ctypes.POINTER(I)]),
@@ -332,6 +335,47 @@ def rmsnorm_linear_w8a8(x, gamma, Wq, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, o
                                       _ptr(x_scale_out), _ptr(ws), ws.numel() * ws.element_size(),
                                       _stream(dev, stream)),
            "rmsnorm_linear_w8a8")
+    return out
+
+
+def rnl_w8a8_prepare_weight(Wq, out=None, stream=None):
+    """The W8A8 weight prepared once: int8 Wq [N, K] widened exactly to the
+    bf16 operand [N, K] that rmsnorm_linear_w8a8_prepared reads."""
+    N, K = Wq.shape
+    dev = Wq.device
+    _need(Wq, "Wq", torch.int8, (N, K), dev)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    _need(out, "Wb", torch.bfloat16, (N, K), dev)
+    _check(load().rnl_w8a8_prepare_weight(_ptr(Wq), N, K, _ptr(out), _stream(dev, stream)),
+           "rnl_w8a8_prepare_weight")
+    return out
+
+
+def rmsnorm_linear_w8a8_prepared(x, gamma, Wb, w_scale, eps=1e-6, norm_mode=NORM_RSQRT, out=None,
+                                 q_out=None, x_scale_out=None, workspace=None, stream=None):
+    """rmsnorm_linear_w8a8 with the weight from rnl_w8a8_prepare_weight (bf16 [N, K])."""
+    T, K = x.shape
+    N = Wb.shape[0]
+    dev = x.device
+    _need(x, "x", torch.bfloat16, (T, K), dev)
+    _need(Wb, "Wb", torch.bfloat16, (N, K), dev)
+    _need(w_scale, "w_scale", torch.float32, (N,), dev)
+    if gamma is not None:
+        _need(gamma, "gamma", torch.bfloat16, (K,), dev)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, N), dev)
+    if q_out is not None:
+        _need(q_out, "q_out", torch.int8, (T, K), dev)
+    if x_scale_out is not None:
+        _need(x_scale_out, "x_scale_out", torch.float32, (T,), dev)
+    ws = _workspace(workspace_size(OP_W8A8_PREPARED, T, K, N), dev, workspace)
+    _check(load().rmsnorm_linear_w8a8_prepared(_ptr(x), _ptr(gamma), _ptr(Wb), _ptr(w_scale), T, K, N,
+                                               float(eps), int(norm_mode), _ptr(out), _ptr(q_out),
+                                               _ptr(x_scale_out), _ptr(ws), ws.numel() * ws.element_size(),
+                                               _stream(dev, stream)),
+           "rmsnorm_linear_w8a8_prepared")
     return out
 
 

@@ -119,6 +119,23 @@ W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
   return l;
 }
 
+// rmsnorm_linear_w8a8_prepared: the weight arrives widened, so no Wb
+struct W8A8PLayout {
+  void* A = nullptr;        // bf16 [T, K] integer codes
+  float* xs = nullptr;      // [T] x_scale when the caller passes none
+  void* part = nullptr;     // gemm K-split partial sums
+  size_t bytes = 0;
+};
+W8A8PLayout w8a8p_layout(void* ws, int64_t T, int64_t K) {
+  W8A8PLayout l;
+  Carve c(ws);
+  l.A = c.take(static_cast<size_t>(T) * K * 2);
+  l.xs = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.part = c.take(kGemmPartialBytes);
+  l.bytes = c.used;
+  return l;
+}
+
 struct MLALayout {
   void* qa = nullptr;     // bf16 [T, N1] stage-1 output when the caller passes none
   void* z = nullptr;      // bf16 [T, N1] normed * gamma_cq (two-kernel form)
@@ -220,6 +237,36 @@ S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
 }
 
 inline cudaStream_t cs(rnl_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// The W8A8 front end's quantising part: the streamed form (each row read
+// once into registers, quantstream.cu) for rows of up to 4096 elements, else
+// the three-read row kernels (rowwise.cu).  RNL_W8A8_STREAM=0 forces the
+// latter; both give the same codes and scales.
+rnl_status w8a8_quantise(const void* x, const void* gamma, int64_t T, int64_t K, float eps, int mode,
+                         void* A, int8_t* q_out, float* xs, cudaStream_t s) {
+  const char* e = std::getenv("RNL_W8A8_STREAM");
+  if (quant_stream_fits(K) && (e == nullptr || e[0] != '0'))
+    return launch_quant_stream(x, gamma, T, K, eps, mode, A, q_out, xs, s);
+  return launch_norm_quant(x, gamma, T, K, eps, mode, A, q_out, xs, s);
+}
+
+// The exact integer GEMM with the dequant epilogue: out = bf16(float(A Wb^T) * (xs * w_scale)).
+rnl_status w8a8_gemm(const void* A, const void* Wb, int64_t T, int64_t K, int64_t N, const float* xs,
+                     const float* w_scale, void* out, void* part, cudaStream_t s) {
+  GemmArgs g;
+  g.A = A;
+  g.B = Wb;
+  g.M = T;
+  g.N = N;
+  g.K = K;
+  g.out = out;
+  g.row_scale = xs;
+  g.col_scale = w_scale;
+  g.epi = Epi::kDequantBf16;
+  g.partial_ws = part;
+  g.partial_ws_bytes = kGemmPartialBytes;
+  return launch_gemm(g, s);
+}
 
 // Two forms of the normalise-and-cast step compute the same values:
 //   two-kernel (default): a row pass writes the bf16 A operand [T, K], the
@@ -361,11 +408,12 @@ void trace_after(cudaStream_t s, const char* name) {
 }
 
 rnl_status read_device_errors(int* site) {
-  unsigned int words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  unsigned int words[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
       read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
       read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK ||
-      read_clear_error_rope(&words[6]) != RNL_OK || read_clear_error_mx(&words[7]) != RNL_OK)
+      read_clear_error_rope(&words[6]) != RNL_OK || read_clear_error_mx(&words[7]) != RNL_OK ||
+      read_clear_error_quant(&words[8]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {
@@ -420,6 +468,7 @@ size_t rnl_workspace_size(int op, int64_t T, int64_t K, int64_t N, int64_t N2) {
       if (N2 != RNL_OUT_BF16 && N2 != RNL_OUT_FP32) return static_cast<size_t>(-1);
       return bf16_layout(nullptr, T, K, N, static_cast<int>(N2)).bytes;
     case RNL_OP_W8A8: return w8a8_layout(nullptr, T, K, N).bytes;
+    case RNL_OP_W8A8_PREPARED: return w8a8p_layout(nullptr, T, K).bytes;
     case RNL_OP_MLA: return mla_layout(nullptr, T, N).bytes;
     case RNL_OP_GEMM_S8: return s8_layout(nullptr, T, K, N).bytes;
     case RNL_OP_QMRS:
@@ -709,21 +758,52 @@ rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* W
   const W8A8Layout l = w8a8_layout(workspace, T, K, N);
   cudaStream_t s = cs(stream);
   float* xs = x_scale_out ? x_scale_out : l.xs;
-  st = launch_w8a8_front(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, Wq, N, l.Wb, s);
+  if (quant_stream_fits(K)) {
+    // the weight widened by its own launch, then the streamed quantiser
+    st = launch_s8_to_bf16(Wq, N * K, l.Wb, s);
+    if (st == RNL_OK) st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
+  } else {
+    st = launch_w8a8_front(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, Wq, N, l.Wb, s);
+  }
   if (st != RNL_OK) return st;
-  GemmArgs g;
-  g.A = l.A;
-  g.B = l.Wb;
-  g.M = T;
-  g.N = N;
-  g.K = K;
-  g.out = out;
-  g.row_scale = xs;
-  g.col_scale = w_scale;
-  g.epi = Epi::kDequantBf16;
-  g.partial_ws = l.part;
-  g.partial_ws_bytes = kGemmPartialBytes;
-  return launch_gemm(g, s);
+  return w8a8_gemm(l.A, l.Wb, T, K, N, xs, w_scale, out, l.part, s);
+}
+
+rnl_status rnl_w8a8_prepare_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wb,
+                                   rnl_stream_t stream) {
+  if (bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (!Wq || !Wb) return RNL_ERR_NULL;
+  if (K % 16 != 0 || !aligned16(Wq) || !aligned16(Wb)) return RNL_ERR_ALIGN;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  return launch_s8_to_bf16(Wq, N * K, Wb, cs(stream));
+}
+
+rnl_status rmsnorm_linear_w8a8_prepared(const void* x, const void* gamma, const void* Wb,
+                                        const float* w_scale, int64_t T, int64_t K, int64_t N,
+                                        float eps, int norm_mode, void* out, int8_t* q_out,
+                                        float* x_scale_out, void* workspace, size_t workspace_bytes,
+                                        rnl_stream_t stream) {
+  if (bad_dim(T) || bad_dim(K) || bad_dim(N) || K == 0 || N == 0) return RNL_ERR_SHAPE;
+  if (bad_mode(norm_mode) || bad_eps(eps)) return RNL_ERR_ARG;
+  if (T == 0) return RNL_OK;
+  if (!x || !Wb || !w_scale || !out) return RNL_ERR_NULL;
+  if (K % 16 != 0 || !aligned16(x) || !aligned16(Wb) || !aligned16(out) ||
+      (gamma && !aligned16(gamma)) || (q_out && !aligned16(q_out)) ||
+      (workspace && !aligned16(workspace)))
+    return RNL_ERR_ALIGN;
+  const W8A8PLayout need = w8a8p_layout(nullptr, T, K);
+  if (!workspace || workspace_bytes < need.bytes) return RNL_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rnl_status st = current_device(&dev);
+  if (st != RNL_OK) return st;
+  const W8A8PLayout l = w8a8p_layout(workspace, T, K);
+  cudaStream_t s = cs(stream);
+  float* xs = x_scale_out ? x_scale_out : l.xs;
+  st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
+  if (st != RNL_OK) return st;
+  return w8a8_gemm(l.A, Wb, T, K, N, xs, w_scale, out, l.part, s);
 }
 
 rnl_status rmsnorm_linear_mxfp8(const void* x, const void* gamma, const uint8_t* w_codes,

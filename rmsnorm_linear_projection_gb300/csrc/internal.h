@@ -72,6 +72,11 @@ rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int m
 // q_out (optional) as int8, x_scale = amax / 127.
 rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                              int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
+// The same as a persistent stream (quantstream.cu) for K <= 4096: each row
+// read once into registers; codes, int8 copy and x_scale as above.
+bool quant_stream_fits(int64_t K);
+rnl_status launch_quant_stream(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
+                               int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
 // Both of the above in one launch (norm-quantise rows of x and widening of
 // the N x K weight run side by side); rows longer than 4096 fall back to the
 // two launches.
@@ -251,6 +256,7 @@ rnl_status read_clear_error_norm(unsigned int* word);
 rnl_status read_clear_error_selftest(unsigned int* word);
 rnl_status read_clear_error_rope(unsigned int* word);
 rnl_status read_clear_error_mx(unsigned int* word);
+rnl_status read_clear_error_quant(unsigned int* word);
 // Reads and clears all of them without synchronising (api.cu): RNL_OK, or
 // RNL_ERR_TIMEOUT / RNL_ERR_ARG with the first recorded site in *site
 // (optional).

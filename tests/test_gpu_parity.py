@@ -264,60 +264,6 @@ def test_gemm_s8_bit_exact_worst_case(orc):
     assert np.array_equal(C, want)
 
 
-def _w8a8_run(d, eps, mode):
-    T, K = d["x"].shape
-    q = torch.empty((T, K), dtype=torch.int8, device="cuda")
-    xs = torch.empty((T,), dtype=torch.float32, device="cuda")
-    out = rnl.rmsnorm_linear_w8a8(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev(d["Wq"]),
-                                  dev(d["w_scale"]), eps=eps, norm_mode=mode, q_out=q,
-                                  x_scale_out=xs)
-    return host_bits(out), q.cpu().numpy(), xs.cpu().numpy()
-
-
-@pytest.mark.parametrize("T,K,N,mode", [
-    (200, 2048, 300, 0), (130, 4096, 520, 1), (5, 16, 7, 0),
-    (40, 1024, 64, 0),     # the row held in registers
-    (64, 6144, 136, 1),    # rows read three times
-    (33, 8704, 96, 0),     # a row length that is not a multiple of 1024 elements
-])
-def test_w8a8_small(orc, T, K, N, mode):
-    c = dict(seed=3 + T + N, T=T, K=K, N=N)
-    d = si.make_w8a8(c)
-    out, q, xs = _w8a8_run(d, 1e-6, mode)
-    r = orc.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], 1e-6, mode)
-    assert np.array_equal(q, r["q"]), "INT8 codes differ"
-    assert np.array_equal(xs, r["x_scale"]), "x_scale differs"
-    assert_bf16_close(out, r["out"], "w8a8 out")
-
-
-def test_w8a8_zero_row(orc):
-    c = dict(seed=5, T=4, K=64, N=16)
-    d = si.make_w8a8(c)
-    d["x"][2] = 0
-    out, q, xs = _w8a8_run(d, 1e-6, 0)
-    assert not q[2].any() and xs[2] == 0.0
-    assert not bf16_bits_to_f64(out[2]).any()
-    r = orc.rmsnorm_linear_w8a8(d["x"], d["gamma"], d["Wq"], d["w_scale"], 1e-6, 0)
-    assert np.array_equal(q, r["q"])
-    assert_bf16_close(out, r["out"], "w8a8 zero row")
-
-
-def test_w8a8_full_sampled(orc):
-    c = si.CONFIGS["w8a8"]
-    d = si.make_w8a8(c)
-    out, q, xs = _w8a8_run(d, c["eps"], c["norm_mode"])
-    rows = sample_rows(c["T"], 48)
-    r = orc.rmsnorm_linear_w8a8(d["x"][rows], d["gamma"], d["Wq"], d["w_scale"], c["eps"],
-                                c["norm_mode"])
-    assert np.array_equal(q[rows], r["q"])
-    assert np.array_equal(xs[rows], r["x_scale"])
-    assert_bf16_close(out[rows], r["out"], "w8a8 sampled rows")
-    # the int32 accumulation of the full-size run is exact: recompute the
-    # sampled rows' products from the oracle's own codes through the INT8 hook
-    C = rnl.rnl_gemm_s8s8s32(dev(r["q"]), dev(d["Wq"])).cpu().numpy()
-    assert np.array_equal(C, r["acc"])
-
-
 # ------------------------------------------------------------- edge cases
 def test_empty_T_is_noop():
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
