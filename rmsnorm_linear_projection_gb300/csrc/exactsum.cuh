@@ -34,17 +34,9 @@ __device__ __forceinline__ void ff_add_squares8(const float (&f)[8], float inv_d
   }
 }
 
-// Merges the eight chains of every lane of the warp; returns the binary32
-// rounding of the total (the same value on every lane).
-__device__ __forceinline__ float ff_warp_total(const float (&hs)[8], const float (&ls)[8]) {
-  float hi = hs[0], lo = ls[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) {
-    float sum, e;
-    two_sum(hi, hs[j], sum, e);
-    lo = __fadd_rn(__fadd_rn(lo, ls[j]), e);
-    hi = sum;
-  }
+// Adds the float-float pairs (hi, lo) of the warp's 32 lanes (butterfly):
+// the same pair on every lane.
+__device__ __forceinline__ void ff_warp_merge(float& hi, float& lo) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
@@ -54,6 +46,30 @@ __device__ __forceinline__ float ff_warp_total(const float (&hs)[8], const float
     lo = __fadd_rn(__fadd_rn(lo, l2), e);
     hi = sum;
   }
+}
+
+// Merges the eight chains of every lane of the warp into one float-float
+// pair (hi, lo), the same on every lane, left unrounded so that several
+// warps' pairs can be merged further.
+__device__ __forceinline__ void ff_warp_hilo(const float (&hs)[8], const float (&ls)[8], float& hi_out,
+                                             float& lo_out) {
+  float hi = hs[0], lo = ls[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) {
+    float sum, e;
+    two_sum(hi, hs[j], sum, e);
+    lo = __fadd_rn(__fadd_rn(lo, ls[j]), e);
+    hi = sum;
+  }
+  ff_warp_merge(hi, lo);
+  hi_out = hi;
+  lo_out = lo;
+}
+
+// The binary32 rounding of the warp's total (the same value on every lane).
+__device__ __forceinline__ float ff_warp_total(const float (&hs)[8], const float (&ls)[8]) {
+  float hi, lo;
+  ff_warp_hilo(hs, ls, hi, lo);
   return __fadd_rn(hi, lo);
 }
 

@@ -466,16 +466,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        if constexpr (kInt) {
+          // 16 columns at a time: with the int32 sums of all the warp's
+          // columns live across the chunks, a 32-column load would spill
 #pragma unroll
-        for (int c = 0; c < kGroups; ++c) {
+          for (int c = 0; c < kGroups; ++c) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t r[16];
+              tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32 + h * 16,
+                             r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) iacc[c][16 * h + j] += __float2int_rn(__uint_as_float(r[j]));
+            }
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < (kInt ? 0 : kGroups); ++c) {
           uint32_t r[32];
           tmem_ld_32cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32, r);
           tmem_ld_wait();
           const int n0 = n_base + c * 32;
-          if constexpr (kInt) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) iacc[c][j] += __float2int_rn(__uint_as_float(r[j]));
-          } else if (prow != nullptr) {
+          if (prow != nullptr) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               uint32_t v[8];
