@@ -109,6 +109,29 @@ def test_gemm_s8_each_tile_width(orc, monkeypatch, bn):
     assert np.array_equal(C, want)
 
 
+# 40 x 4 = 160 tiles of 128 x 256: more tiles than one wave of CTAs, N
+# ragged (the last tile column straddles N), K two exact-integer chunks, the
+# second partial.
+def test_gemm_s8_past_one_wave(orc, monkeypatch):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
+    monkeypatch.setenv("RNL_GEMM_BN", "256")
+    rng = np.random.default_rng(160)
+    A = rng.integers(-127, 128, (5120, 1040)).astype(np.int8)  # two chunks, the second partial
+    B = rng.integers(-127, 128, (1000, 1040)).astype(np.int8)
+    C = rnl.rnl_gemm_s8s8s32(dev(A), dev(B)).cpu().numpy()
+    want, _ = orc.gemm_s8(A, B)
+    assert np.array_equal(C, want)
+
+
+def test_bf16_past_one_wave(orc, monkeypatch):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
+    monkeypatch.setenv("RNL_GEMM_BN", "256")
+    d = _rand_case(161, 5120, 520, 1000, True)
+    out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
+    _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, 0, 0)
+    assert_bf16_close(host_bits(out), want, "bf16 one-CTA 5120x520x1000")
+
+
 @pytest.mark.parametrize("T,K,N,mode,gamma", [(130, 72, 300, 0, True), (640, 4096, 512, 1, False)])
 def test_bf16_fused_norm_form(orc, monkeypatch, T, K, N, mode, gamma):
     """RNL_FUSED_NORM=1: transform warps normalise the A stages inside the GEMM."""
