@@ -61,7 +61,7 @@ KERNEL_SOURCES = {
     "mla": [CSRC + "gemm_pair.cu", CSRC + "gemm_tc.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
     "mx": [CSRC + "mxgemm.cu", CSRC + "gemm_common.cuh", CSRC + "ptx.cuh"],
     "skinny": [CSRC + "skinny.cu", CSRC + "ptx.cuh"],
-    "decode": [CSRC + "decode.cu"],
+    "decode": [CSRC + "decode.cu", CSRC + "decode_mma.cu", CSRC + "ptx.cuh"],
 }
 WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": "mla", "mla_hn": "mla",
                     "w8a8": "one_cta", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
@@ -779,12 +779,15 @@ def run_ours(args):
         stream.wait_stream(side)
         torch.cuda.synchronize()
         g_flush, g_both = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        # the same flush as the timed steps (written, then read back): a flush
+        # that only writes leaves the L2 full of dirty lines, whose write-back
+        # the next kernel's reads would pay for
         with torch.cuda.graph(g_flush, capture_error_mode="thread_local"):
             for _ in range(calls):
-                flush.zero_()
+                flush_l2()
         with torch.cuda.graph(g_both, capture_error_mode="thread_local"):
             for _ in range(calls):
-                flush.zero_()
+                flush_l2()
                 w.call()
 
         def replay_us(gr):

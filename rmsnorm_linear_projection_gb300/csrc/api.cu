@@ -9,7 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
-#include <set>
+#include <map>
 #include <utility>
 
 #include "internal.h"
@@ -293,11 +293,18 @@ bool mx_native() {
 }
 
 // Up to 4 tokens against a weight of at least 1024 rows (a decode step) run
-// as a matrix-vector product that spreads the weight's rows over every SM
-// (decode.cu); RNL_DECODE=0 sends them to the tensor-core path.
+// as a matrix-vector product that spreads the weight over every SM, on the
+// CUDA cores (decode.cu), or with RNL_DECODE_MMA=1 on the tensor cores with
+// the weight streamed by TMA and the K ranges split over several CTAs
+// (decode_mma.cu: as fast at a 50 MB weight, slower at 12.6 and 101 MB);
+// RNL_DECODE=0 sends them to the GEMM path.
 bool decode_path() {
   const char* e = std::getenv("RNL_DECODE");
   return e == nullptr || e[0] != '0';
+}
+bool decode_mma() {
+  const char* e = std::getenv("RNL_DECODE_MMA");
+  return e != nullptr && e[0] == '1';
 }
 
 // The QKV split + per-head norm + RoPE runs in the CTA-pair GEMM's epilogue
@@ -371,19 +378,20 @@ rnl_status make_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const 
 
 namespace {
 std::mutex g_attr_mu;
-std::set<std::pair<const void*, int>> g_attr_done;
+std::map<std::pair<const void*, int>, size_t> g_attr_done;  // the dynamic shared memory each kernel may use
 }  // namespace
 
 rnl_status ensure_smem_attr(const void* kernel, int device, size_t bytes) {
   std::lock_guard<std::mutex> lk(g_attr_mu);
   const auto key = std::make_pair(kernel, device);
-  if (g_attr_done.count(key) != 0) return RNL_OK;
+  const auto it = g_attr_done.find(key);
+  if (it != g_attr_done.end() && it->second >= bytes) return RNL_OK;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(bytes)) != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
   }
-  g_attr_done.insert(key);
+  g_attr_done[key] = bytes;
   return RNL_OK;
 }
 
@@ -408,12 +416,12 @@ void trace_after(cudaStream_t s, const char* name) {
 }
 
 rnl_status read_device_errors(int* site) {
-  unsigned int words[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  unsigned int words[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (read_clear_error_rowwise(&words[0]) != RNL_OK || read_clear_error_gemm(&words[1]) != RNL_OK ||
       read_clear_error_skinny(&words[2]) != RNL_OK || read_clear_error_pair(&words[3]) != RNL_OK ||
       read_clear_error_norm(&words[4]) != RNL_OK || read_clear_error_selftest(&words[5]) != RNL_OK ||
       read_clear_error_rope(&words[6]) != RNL_OK || read_clear_error_mx(&words[7]) != RNL_OK ||
-      read_clear_error_quant(&words[8]) != RNL_OK)
+      read_clear_error_quant(&words[8]) != RNL_OK || read_clear_error_decmma(&words[9]) != RNL_OK)
     return RNL_ERR_LAUNCH;
   for (unsigned int w : words) {
     if (w != 0) {
@@ -503,8 +511,12 @@ rnl_status rmsnorm_linear_bf16(const void* x, const void* gamma, const void* W, 
   const BF16Layout l = bf16_layout(workspace, T, K, N, out_dtype);
   cudaStream_t s = cs(stream);
 
-  if (out_dtype == RNL_OUT_BF16 && decode_path() && !fused_norm() && decode_fits(T, K, N))
+  if (out_dtype == RNL_OUT_BF16 && decode_path() && !fused_norm() && decode_fits(T, K, N)) {
+    if (decode_mma() && decode_mma_fits(T, K, N, dev.sm_count) &&
+        decode_mma_workspace_bytes(N) <= kGemmPartialBytes)
+      return launch_decode_mma(x, gamma, W, T, K, N, eps, norm_mode, out, l.part, kGemmPartialBytes, s);
     return launch_decode(x, gamma, W, T, K, N, eps, norm_mode, out, dev.sm_count, s);
+  }
   if (out_dtype == RNL_OUT_BF16) {
     GemmArgs g;
     g.B = W;

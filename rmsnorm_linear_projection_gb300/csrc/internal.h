@@ -34,8 +34,9 @@ rnl_status make_map_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const 
                              uint64_t inner, uint64_t outer, uint64_t row_bytes,
                              uint32_t box_inner, uint32_t box_outer);
 
-// Raises a kernel's dynamic shared-memory limit to `bytes` on `device` (the
-// current one) once per (kernel, device); thread-safe.  The cache outlives a
+// Raises a kernel's dynamic shared-memory limit on `device` (the current one)
+// to at least `bytes`: set on a (kernel, device)'s first call and again only
+// when a call needs more than was set; thread-safe.  The cache outlives a
 // cudaDeviceReset, which drops the attribute, so a reset device needs the
 // library reloaded.
 rnl_status ensure_smem_attr(const void* kernel, int device, size_t bytes);
@@ -134,6 +135,14 @@ bool decode_fits(int64_t T, int64_t K, int64_t N);
 // AT-10 RMSNorm + Linear, bf16 out, the weight's rows spread over every SM.
 rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
                          int64_t N, float eps, int mode, void* out, int sm_count, cudaStream_t s);
+// The same on the tensor cores (decode_mma.cu): T <= 4, K % 8 == 0 and a K
+// split whose ring and normalised rows fit in shared memory; the K split's
+// partial sums and flags take decode_mma_workspace_bytes(N) of `ws`.
+bool decode_mma_fits(int64_t T, int64_t K, int64_t N, int sm_count);
+size_t decode_mma_workspace_bytes(int64_t N);
+rnl_status launch_decode_mma(const void* x, const void* gamma, const void* W, int64_t T, int64_t K,
+                             int64_t N, float eps, int mode, void* out, void* ws, size_t ws_bytes,
+                             cudaStream_t s);
 
 // ---- per-head RMSNorm (headnorm.cu) ----
 // head_dim a multiple of 64 in [64, 512]
@@ -257,6 +266,7 @@ rnl_status read_clear_error_selftest(unsigned int* word);
 rnl_status read_clear_error_rope(unsigned int* word);
 rnl_status read_clear_error_mx(unsigned int* word);
 rnl_status read_clear_error_quant(unsigned int* word);
+rnl_status read_clear_error_decmma(unsigned int* word);
 // Reads and clears all of them without synchronising (api.cu): RNL_OK, or
 // RNL_ERR_TIMEOUT / RNL_ERR_ARG with the first recorded site in *site
 // (optional).

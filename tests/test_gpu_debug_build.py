@@ -71,10 +71,13 @@ def test_selftest_check_fires():
     (300, 520, 600, "0"),     # one CTA, ragged M, N, K tail
     (1000, 1024, 700, "1"),   # CTA pairs, data-parallel + stream-K
     (600, 3000, 1000, "1"),   # CTA pairs, every tile split
-    (4, 4096, 2048, None),    # the decode-step kernel
+    (4, 4096, 2048, None),    # the decode-step kernel (CUDA cores)
+    (3, 2056, 2000, "mma"),   # the decode-step kernel on the tensor cores, K split over 8 CTAs
 ])
 def test_bf16(monkeypatch, T, K, N, pair):
-    if pair is not None:
+    if pair == "mma":
+        monkeypatch.setenv("RNL_DECODE_MMA", "1")
+    elif pair is not None:
         monkeypatch.setenv("RNL_GEMM_PAIR", pair)
     d = si.make_projection(dict(seed=T + N, T=T, K=K, N=N))
     x, g, W = dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"])

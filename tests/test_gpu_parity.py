@@ -69,13 +69,15 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
     (2, 2056, 5000, 0, True),   # several rows a warp, each row's second chunk one vector
     (5, 4096, 1024, 0, True),   # beyond the token limit: the tensor-core path either way
 ])
-@pytest.mark.parametrize("decode", ["1", "0", "rows1", "rows2"])
+@pytest.mark.parametrize("decode", ["mma", "0", "rows1", "rows2"])
 def test_bf16_decode_sized_both_paths(orc, monkeypatch, decode, T, K, N, mode, gamma):
     """Up to 4 tokens against a wide weight run as a matrix-vector product
-    over every SM (RNL_DECODE=0 sends them to the tensor-core path; rows1 /
-    rows2 force one or two weight rows per warp group): all against the
-    oracle."""
+    over every SM: on the tensor cores with the K ranges split over CTA
+    clusters (mma), or on the CUDA cores with one or two weight rows per warp
+    group (rows1 / rows2); RNL_DECODE=0 sends them to the GEMM path.  All
+    against the oracle."""
     monkeypatch.setenv("RNL_DECODE", "0" if decode == "0" else "1")
+    monkeypatch.setenv("RNL_DECODE_MMA", "1" if decode == "mma" else "0")
     if decode.startswith("rows"):
         monkeypatch.setenv("RNL_DECODE_ROWS", decode[-1])
     d = _rand_case(13 + T + K + N, T, K, N, gamma)
