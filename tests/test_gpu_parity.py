@@ -72,8 +72,8 @@ def test_bf16_small(orc, T, K, N, mode, gamma):
 @pytest.mark.parametrize("decode", ["mma", "0", "rows1", "rows2"])
 def test_bf16_decode_sized_both_paths(orc, monkeypatch, decode, T, K, N, mode, gamma):
     """Up to 4 tokens against a wide weight run as a matrix-vector product
-    over every SM: on the tensor cores with the K ranges split over CTA
-    clusters (mma), or on the CUDA cores with one or two weight rows per warp
+    over every SM: on the tensor cores with the K ranges split over several
+    CTAs (mma), or on the CUDA cores with one or two weight rows per warp
     group (rows1 / rows2); RNL_DECODE=0 sends them to the GEMM path.  All
     against the oracle."""
     monkeypatch.setenv("RNL_DECODE", "0" if decode == "0" else "1")
@@ -132,6 +132,33 @@ def test_bf16_past_one_wave(orc, monkeypatch):
     out = rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"]))
     _, want = orc.rmsnorm_linear(d["x"], d["gamma"], d["W"], 1e-6, 0, 0)
     assert_bf16_close(host_bits(out), want, "bf16 one-CTA 5120x520x1000")
+
+
+# The one-CTA kernel with one partial wave of tiles (3200 x 1024 at BN = 256:
+# 100 tiles) and with a whole wave and then a partial one (8064 x 1024: 252);
+# K ragged, 2096 spanning three exact-int32 chunks.
+@pytest.mark.parametrize("M", [3200, 8064])
+def test_gemm_s8_partial_wave(orc, monkeypatch, M):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
+    monkeypatch.setenv("RNL_GEMM_BN", "256")
+    rng = np.random.default_rng(M)
+    A = rng.integers(-127, 128, (M, 2096)).astype(np.int8)
+    B = rng.integers(-127, 128, (1024, 2096)).astype(np.int8)
+    C = rnl.rnl_gemm_s8s8s32(dev(A), dev(B)).cpu().numpy()
+    rows = sample_rows(M, 64, seed=M)
+    want, _ = orc.gemm_s8(A[rows], B)
+    assert np.array_equal(C[rows], want)
+
+
+@pytest.mark.parametrize("T", [3200, 8064])
+def test_bf16_partial_wave(orc, monkeypatch, T):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "0")
+    monkeypatch.setenv("RNL_GEMM_BN", "256")
+    d = _rand_case(T + 7, T, 1000, 1024, True)
+    out = host_bits(rnl.rmsnorm_linear_bf16(dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"])))
+    rows = sample_rows(T, 64, seed=T)
+    _, want = orc.rmsnorm_linear(d["x"][rows], d["gamma"], d["W"], 1e-6, 0, 0)
+    assert_bf16_close(out[rows], want, f"bf16 one-CTA {T}x1000x1024")
 
 
 @pytest.mark.parametrize("T,K,N,mode,gamma", [(130, 72, 300, 0, True), (640, 4096, 512, 1, False)])

@@ -55,10 +55,13 @@ def _capture(fn):
 @pytest.mark.parametrize("shape,force_pair", [
     ((4096, 4096, 6144), None),  # the qkv size: 4 data-parallel waves + stream-K tail
     ((600, 3000, 1000), "1"),    # 12 tiles on CTA pairs: every tile split
+    ((3200, 1000, 1024), "0"),   # 100 one-CTA tiles of 128 x 256 (no hand-off: the baseline)
 ])
 def test_graph_replay_bf16_stream_k(orc, monkeypatch, shape, force_pair):
     if force_pair is not None:
         monkeypatch.setenv("RNL_GEMM_PAIR", force_pair)
+    if force_pair == "0":
+        monkeypatch.setenv("RNL_GEMM_BN", "256")
     T, K, N = shape
     d = si.make_projection(dict(seed=31 + T, T=T, K=K, N=N))
     xs = [d["x"], si.make_projection(dict(seed=32 + T, T=T, K=K, N=N))["x"]]
@@ -127,6 +130,15 @@ def test_deterministic_stream_k_split_small(monkeypatch):
     d = si.make_projection(dict(seed=7, T=600, K=3000, N=1000))
     x, gamma, W = dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev_bf16(d["W"])
     _repeat_identical(lambda: host_bits(rnl.rmsnorm_linear_bf16(x, gamma, W)), 8)
+
+
+def test_deterministic_w8a8_full():
+    """W8A8 at full size: the streamed quantiser and the exact-integer GEMM."""
+    c = si.CONFIGS["w8a8"]
+    d = si.make_w8a8(c)
+    x, g, Wq, ws_ = dev_bf16(d["x"]), dev_bf16(d["gamma"]), dev(d["Wq"]), dev(d["w_scale"])
+    Wb = rnl.rnl_w8a8_prepare_weight(Wq)
+    _repeat_identical(lambda: host_bits(rnl.rmsnorm_linear_w8a8_prepared(x, g, Wb, ws_)), 3)
 
 
 def test_deterministic_qmrs_full():
