@@ -66,7 +66,19 @@ KERNEL_SOURCES = {
 WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": "mla", "mla_hn": "mla",
                     "w8a8": "one_cta", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
                     "decode": "decode", "tiny": "one_cta"}
-TRAFFIC = {}
+TRAFFIC = {
+    "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
+    "tiny": {"bytes": 110000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
+    "mla": {"bytes": 203390000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5a4c5a7beb7756ad"},
+    "w8a8": {"bytes": 172540000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
+    "skinny": {"bytes": 946180000, "profile": "profiles/traffic_roofline_stages.md", "sources": "cab190e5a3867f6b"},
+    "qkv_ex": {"bytes": 135680000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
+    "qkv_rope": {"bytes": 158900000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
+    "qmrs": {"bytes": 385010000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
+    "mxfp8": {"bytes": 55920000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5d9aed71d1d08303"},
+    "mla_hn": {"bytes": 203300000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5a4c5a7beb7756ad"},
+    "decode": {"bytes": 50400000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0cbb868f949b8b56"},
+}
 
 
 def source_hash(workload):
