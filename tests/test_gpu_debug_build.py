@@ -1,7 +1,9 @@
 """The debug build (librnl_debug.so, compiled with RNL_DEBUG) on small ragged
 shapes of every kernel family that carries device-side bounds checks (the
 one-CTA and CTA-pair GEMMs incl. stream-K hand-offs and the integer and
-batch-sum modes, the streamed norm pass, the skinny stream and its reduce).
+batch-sum modes, the streamed norm pass and W8A8 quantiser, the W8A8 weight
+preparation, the MXFP8 front end and block-scaled GEMM, the skinny stream and
+its reduce, and both decode-step kernels).
 
 Each case runs through the release library and then through the debug
 library: no check may fire (rnl_check_device_error is clean), and the
@@ -121,6 +123,11 @@ def test_w8a8_and_s8(monkeypatch, pair):
         xs = torch.empty(300, dtype=torch.float32, device="cuda")
         return rnl.rmsnorm_linear_w8a8(x, g, Wq, ws, q_out=q, x_scale_out=xs), q, xs
     _both(call)
+
+    def call_prepared():
+        Wb = rnl.rnl_w8a8_prepare_weight(Wq)
+        return Wb, rnl.rmsnorm_linear_w8a8_prepared(x, g, Wb, ws)
+    _both(call_prepared)
     rng = np.random.default_rng(1)
     A = dev(rng.integers(-127, 128, (260, 2048)).astype(np.int8))
     B = dev(rng.integers(-127, 128, (300, 2048)).astype(np.int8))
