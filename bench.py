@@ -64,7 +64,7 @@ KERNEL_SOURCES = {
     "decode": [CSRC + "decode.cu", CSRC + "decode_mma.cu", CSRC + "ptx.cuh"],
 }
 WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": "mla", "mla_hn": "mla",
-                    "w8a8": "one_cta", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
+                    "w8a8": "pair", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
                     "decode": "decode", "tiny": "one_cta"}
 TRAFFIC = {
     "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},

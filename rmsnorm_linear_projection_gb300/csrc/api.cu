@@ -105,7 +105,9 @@ struct W8A8Layout {
   void* A = nullptr;        // bf16 [T, K] integer codes
   void* Wb = nullptr;       // bf16 [N, K] widened weight
   float* xs = nullptr;      // [T] x_scale when the caller passes none
+  float* gmax = nullptr;    // max |gamma| (the integer GEMM's exactness bound)
   void* part = nullptr;     // gemm K-split partial sums
+  void* chunk = nullptr;    // the pair GEMM's running int32 sums of chunked tiles
   size_t bytes = 0;
 };
 W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
@@ -114,7 +116,9 @@ W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
   l.A = c.take(static_cast<size_t>(T) * K * 2);
   l.Wb = c.take(static_cast<size_t>(N) * K * 2);
   l.xs = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.gmax = static_cast<float*>(c.take(4));
   l.part = c.take(kGemmPartialBytes);
+  l.chunk = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -123,7 +127,9 @@ W8A8Layout w8a8_layout(void* ws, int64_t T, int64_t K, int64_t N) {
 struct W8A8PLayout {
   void* A = nullptr;        // bf16 [T, K] integer codes
   float* xs = nullptr;      // [T] x_scale when the caller passes none
+  float* gmax = nullptr;    // max |gamma| (the integer GEMM's exactness bound)
   void* part = nullptr;     // gemm K-split partial sums
+  void* chunk = nullptr;    // the pair GEMM's running int32 sums of chunked tiles
   size_t bytes = 0;
 };
 W8A8PLayout w8a8p_layout(void* ws, int64_t T, int64_t K) {
@@ -131,7 +137,9 @@ W8A8PLayout w8a8p_layout(void* ws, int64_t T, int64_t K) {
   Carve c(ws);
   l.A = c.take(static_cast<size_t>(T) * K * 2);
   l.xs = static_cast<float*>(c.take(static_cast<size_t>(T) * 4));
+  l.gmax = static_cast<float*>(c.take(4));
   l.part = c.take(kGemmPartialBytes);
+  l.chunk = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -224,6 +232,7 @@ struct S8Layout {
   void* A = nullptr;
   void* B = nullptr;
   void* part = nullptr;
+  void* chunk = nullptr;  // the pair GEMM's running int32 sums of chunked tiles
   size_t bytes = 0;
 };
 S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
@@ -232,6 +241,7 @@ S8Layout s8_layout(void* ws, int64_t M, int64_t K, int64_t N) {
   l.A = c.take(static_cast<size_t>(M) * K * 2);
   l.B = c.take(static_cast<size_t>(N) * K * 2);
   l.part = c.take(kGemmPartialBytes);
+  l.chunk = c.take(kGemmPartialBytes);
   l.bytes = c.used;
   return l;
 }
@@ -241,18 +251,28 @@ inline cudaStream_t cs(rnl_stream_t s) { return reinterpret_cast<cudaStream_t>(s
 // The W8A8 front end's quantising part: the streamed form (each row read
 // once into registers, quantstream.cu) for rows of up to 4096 elements, else
 // the three-read row kernels (rowwise.cu).  RNL_W8A8_STREAM=0 forces the
-// latter; both give the same codes and scales.
+// latter; both give the same codes and scales.  The streamed form also
+// writes max |gamma| (into *gmax when gamma is given) for the integer GEMM's
+// exactness bound (*exact = true); after the row kernels the GEMM takes
+// every tile in chunks (*exact = false).
 rnl_status w8a8_quantise(const void* x, const void* gamma, int64_t T, int64_t K, float eps, int mode,
-                         void* A, int8_t* q_out, float* xs, cudaStream_t s) {
+                         void* A, int8_t* q_out, float* xs, float* gmax, bool* exact, cudaStream_t s) {
   const char* e = std::getenv("RNL_W8A8_STREAM");
-  if (quant_stream_fits(K) && (e == nullptr || e[0] != '0'))
-    return launch_quant_stream(x, gamma, T, K, eps, mode, A, q_out, xs, s);
+  *exact = false;
+  if (quant_stream_fits(K) && (e == nullptr || e[0] != '0')) {
+    *exact = true;
+    return launch_quant_stream(x, gamma, T, K, eps, mode, A, q_out, xs, gamma ? gmax : nullptr, s);
+  }
   return launch_norm_quant(x, gamma, T, K, eps, mode, A, q_out, xs, s);
 }
 
 // The exact integer GEMM with the dequant epilogue: out = bf16(float(A Wb^T) * (xs * w_scale)).
+// With the streamed quantiser's exactness bound (exact: rows of RMSNorm
+// codes, gmax = max |gamma| or null) the CTA-pair kernel takes it where it is
+// predicted faster (gemm_tc.cu launch_gemm).
 rnl_status w8a8_gemm(const void* A, const void* Wb, int64_t T, int64_t K, int64_t N, const float* xs,
-                     const float* w_scale, void* out, void* part, cudaStream_t s) {
+                     const float* w_scale, bool exact, const float* gmax, void* out, void* part,
+                     void* chunk, cudaStream_t s) {
   GemmArgs g;
   g.A = A;
   g.B = Wb;
@@ -262,6 +282,10 @@ rnl_status w8a8_gemm(const void* A, const void* Wb, int64_t T, int64_t K, int64_
   g.out = out;
   g.row_scale = xs;
   g.col_scale = w_scale;
+  g.exact_rows = exact;
+  g.gamma_max = gmax;
+  g.chunk_ws = chunk;
+  g.chunk_ws_bytes = kGemmPartialBytes;
   g.epi = Epi::kDequantBf16;
   g.partial_ws = part;
   g.partial_ws_bytes = kGemmPartialBytes;
@@ -770,15 +794,16 @@ rnl_status rmsnorm_linear_w8a8(const void* x, const void* gamma, const int8_t* W
   const W8A8Layout l = w8a8_layout(workspace, T, K, N);
   cudaStream_t s = cs(stream);
   float* xs = x_scale_out ? x_scale_out : l.xs;
+  bool exact = false;
   if (quant_stream_fits(K)) {
     // the weight widened by its own launch, then the streamed quantiser
     st = launch_s8_to_bf16(Wq, N * K, l.Wb, s);
-    if (st == RNL_OK) st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
+    if (st == RNL_OK) st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, l.gmax, &exact, s);
   } else {
     st = launch_w8a8_front(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, Wq, N, l.Wb, s);
   }
   if (st != RNL_OK) return st;
-  return w8a8_gemm(l.A, l.Wb, T, K, N, xs, w_scale, out, l.part, s);
+  return w8a8_gemm(l.A, l.Wb, T, K, N, xs, w_scale, exact, gamma ? l.gmax : nullptr, out, l.part, l.chunk, s);
 }
 
 rnl_status rnl_w8a8_prepare_weight(const int8_t* Wq, int64_t N, int64_t K, void* Wb,
@@ -813,9 +838,10 @@ rnl_status rmsnorm_linear_w8a8_prepared(const void* x, const void* gamma, const 
   const W8A8PLayout l = w8a8p_layout(workspace, T, K);
   cudaStream_t s = cs(stream);
   float* xs = x_scale_out ? x_scale_out : l.xs;
-  st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, s);
+  bool exact = false;
+  st = w8a8_quantise(x, gamma, T, K, eps, norm_mode, l.A, q_out, xs, l.gmax, &exact, s);
   if (st != RNL_OK) return st;
-  return w8a8_gemm(l.A, Wb, T, K, N, xs, w_scale, out, l.part, s);
+  return w8a8_gemm(l.A, Wb, T, K, N, xs, w_scale, exact, gamma ? l.gmax : nullptr, out, l.part, l.chunk, s);
 }
 
 rnl_status rmsnorm_linear_mxfp8(const void* x, const void* gamma, const uint8_t* w_codes,
@@ -1009,6 +1035,8 @@ rnl_status rnl_gemm_s8s8s32(const int8_t* A, const int8_t* B, int32_t* C, int64_
   g.epi = Epi::kInt32;
   g.partial_ws = l.part;
   g.partial_ws_bytes = kGemmPartialBytes;
+  g.chunk_ws = l.chunk;
+  g.chunk_ws_bytes = kGemmPartialBytes;
   return launch_gemm(g, s);
 }
 

@@ -199,6 +199,26 @@ __device__ __forceinline__ void store_dequant_32(void* out, int64_t m, int n0, i
     store_bf16_32(out, m, n0, N, v);
 }
 
+// The same dequant of an accumulator that holds the exact integer sum as a
+// binary32 value (|sum| < 2^24): float(acc) is then acc itself, so the
+// output is the one store_dequant_32 writes for that integer.
+__device__ __forceinline__ void store_dequant_f32_32(void* out, int64_t m, int n0, int N,
+                                                     const uint32_t (&r)[32], float xs,
+                                                     const float* __restrict__ w_scale,
+                                                     const __nv_bfloat16* __restrict__ bias) {
+  uint32_t v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int n = n0 + j;
+    const float ws = n < N ? __ldg(w_scale + n) : 0.f;
+    v[j] = __float_as_uint(__uint_as_float(r[j]) * (xs * ws));
+  }
+  if (bias != nullptr)
+    store_bf16_bias_32(out, m, n0, N, v, bias);
+  else
+    store_bf16_32(out, m, n0, N, v);
+}
+
 // QuantMatMulReduceSum epilogue of one batch (SK-14 skeleton page, variant A)
 // for outputs [m, n0 .. n0+31]: v = fp32(acc) * (x1_scale * x2_scale), each a
 // correctly rounded FP32 operation; mode bit 0: v = acc_buf[m, n] + v (the

@@ -64,13 +64,23 @@ struct PairTile {
           : kMaxStages;
 };
 
+// The integer mode's exactness marks (kWideRowL1, internal.h), one byte per
+// 256-row block, for up to this many blocks (M <= 262144); larger problems
+// run every tile in chunks.  The MMA thread reads them per work item, for the
+// first kMaxMarkItems items of its pair from a byte each.
+constexpr int kMaxMarkBlocks = 1024;
+constexpr int kMaxMarkItems = 256;
+
 struct __align__(8) PairCtrl {
   uint64_t full[kMaxStages];   // even CTA: both CTAs' loads of a stage
   uint64_t empty[kMaxStages];  // each CTA: its stage consumed by the pair MMA
   uint64_t tmem_full[2];       // each CTA: accumulator ready
   uint64_t tmem_empty[2];      // even CTA: both CTAs' epilogues drained it
+  uint64_t marks_ready;        // each CTA: block_marks written (one arrival per epilogue warp)
   uint32_t tmem_base;
   int abort;
+  uint8_t item_chunked[kMaxMarkItems];  // nonzero: item it of this pair in chunks
+  uint8_t block_marks[kMaxMarkBlocks];  // nonzero: a marked row in the 256-row block
 };
 
 template <int BN>
@@ -78,6 +88,9 @@ constexpr size_t pair_smem_bytes() {
   return 1024 + static_cast<size_t>(PairTile<BN>::kStages) * PairTile<BN>::kStageBytes +
          sizeof(PairCtrl);
 }
+static_assert(pair_smem_bytes<128>() <= kSmemLimit && pair_smem_bytes<192>() <= kSmemLimit &&
+                  pair_smem_bytes<256>() <= kSmemLimit,
+              "pipeline stages and control block fit the opt-in shared memory");
 
 // The work list shape (identical in every role and CTA).
 struct Sched {
@@ -230,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap map_b, int M, int N, int K, int group_m,
                      int dp_tiles, int sk_tiles, void* __restrict__ out,
                      const float* __restrict__ row_scale, const float* __restrict__ col_scale,
+                     const float* __restrict__ gamma_max, int exact_rows, uint32_t* chunk_ws,
                      uint32_t* partial, uint64_t* flags, uint64_t epoch,
                      const __nv_bfloat16* __restrict__ bias, const RopeEpiArgs rope) {
   constexpr bool kInt = (EPI == static_cast<int>(Epi::kDequantBf16) ||
@@ -272,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);
       mbar_init(smem_u32(&ctrl->tmem_empty[b]), 2 * kEpiWarps);
     }
+    mbar_init(smem_u32(&ctrl->marks_ready), kEpiWarps);
     ctrl->abort = 0;
     fence_mbar_init();
   }
@@ -335,9 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(2 * BM, BN);
       uint32_t stage = 0, phase = 0, unit = 0;
       bool ok = true;
+      // the per-item marks, written by this CTA's epilogue warps at the start
+      if (kInt && exact_rows)
+        ok = mbar_wait(smem_u32(&ctrl->marks_ready), 0u, abort, &g_err_pair, 27);
       for (int it = 0; it < n_items && ok; ++it) {
         const Work w = work_item(sc, pair, it);
-        const int kb_per_unit = kInt ? kChunkKBlocks : (w.kb1 - w.kb0);
+        bool chunked = kInt;
+        if (kInt && exact_rows) {
+          if (it < kMaxMarkItems) {
+            chunked = ctrl->item_chunked[it] != 0;
+          } else {
+            int mb, nb;
+            tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
+            chunked = ctrl->block_marks[mb] != 0;
+          }
+        }
+        const int kb_per_unit = chunked ? kChunkKBlocks : (w.kb1 - w.kb0);
         const int units = (w.kb1 - w.kb0 + kb_per_unit - 1) / kb_per_unit;
         for (int u = 0; u < units && ok; ++u, ++unit) {
           const uint32_t buf = unit & 1u;
@@ -395,9 +423,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t empty_even_1 = mapa_shared(smem_u32(&ctrl->tmem_empty[1]), 0);
     uint32_t unit = 0;
     bool ok = true;
+    if (kInt && exact_rows) {
+      // one byte per 256-row block: does the block hold a row whose x_scale
+      // is not above exact_row_floor (a row that may need the chunks)?  The
+      // epilogue waits for its first accumulator anyway; four blocks per
+      // warp at a time, all loads issued before any vote.
+      const float gmx = gamma_max != nullptr ? __ldg(gamma_max) : 1.0f;  // loaded beside the x_scale values
+      for (int b0 = ew; b0 < num_m; b0 += 4 * kEpiWarps) {
+        float xs[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int64_t r = static_cast<int64_t>(b0 + i * kEpiWarps) * 2 * BM + 8 * lane;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            xs[i][j] = (b0 + i * kEpiWarps < num_m && r + j < M) ? __ldg(row_scale + r + j) : INFINITY;
+        }
+        const float floor_xs = exact_row_floor(static_cast<float>(K), gmx);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          bool wide = false;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) wide |= !(xs[i][j] > floor_xs);  // NaN: wide
+          const int b = b0 + i * kEpiWarps;
+          wide = __any_sync(0xFFFFFFFFu, wide);
+          if (b < num_m && lane == 0 && RNL_DCHECK(&g_err_pair, b < kMaxMarkBlocks, 77))
+            ctrl->block_marks[b] = wide ? 1 : 0;
+        }
+      }
+      // then one byte per work item of this pair, for the MMA thread (the
+      // epilogue warps, 256 threads, meet at named barrier 1 first)
+      asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+      for (int i = ew * 32 + lane; i < n_items && i < kMaxMarkItems; i += kEpiWarps * 32) {
+        const Work wi = work_item(sc, pair, i);
+        int mb, nb;
+        tile_coords(wi.tile, num_m, num_n, group_m, mb, nb);
+        ctrl->item_chunked[i] = ctrl->block_marks[mb];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctrl->marks_ready));
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&ctrl->marks_ready), 0u, abort, &g_err_pair, 27));
+    }
     for (int it = 0; it < n_items && ok; ++it) {
       const Work w = work_item(sc, pair, it);
-      const int kb_per_unit = kInt ? kChunkKBlocks : (w.kb1 - w.kb0);
+      int mb, nb;
+      tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
+      if (!RNL_DCHECK(&g_err_pair, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n, 75)) {
+        ok = false;
+        break;
+      }
+      // the integer mode accumulates in 1024-product chunks only where a row
+      // of the tile may need it (the MMA thread takes the same decision)
+      const bool chunked = kInt && (!exact_rows || ctrl->block_marks[mb] != 0);
+      const int kb_per_unit = chunked ? kChunkKBlocks : (w.kb1 - w.kb0);
       const int units = (w.kb1 - w.kb0 + kb_per_unit - 1) / kb_per_unit;
       // partial slots: [pair][rank][epilogue warp][32-byte chunk][lane] words,
       // lane-major so that one warp instruction moves 1 KB of contiguous
@@ -413,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // highest word a warp touches is warp_off + (kGroups * 4 - 1) * 256 + 7
       if (!RNL_DCHECK(&g_err_pair,
                       (w.kind == kWhole || (partial != nullptr && flags != nullptr)) &&
+                          (!chunked || chunk_ws != nullptr) &&
                           q_end <= kMaxPartialSlots - 1 && pair < kMaxPartialSlots - 1 &&
                           warp_off + (kGroups * 4 - 1) * 256 + 8 <= slot_words &&
                           (static_cast<int64_t>(q_end) * 2 + 1) * kEpiWarps <= slot_words / 2,
@@ -431,12 +509,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      int mb, nb;
-      tile_coords(w.tile, num_m, num_n, group_m, mb, nb);
-      if (!RNL_DCHECK(&g_err_pair, mb >= 0 && mb < num_m && nb >= 0 && nb < num_n, 75)) {
-        ok = false;
-        break;
-      }
       const int64_t m = static_cast<int64_t>(mb) * 2 * BM + rank * BM + row_local;
       const int n_base = nb * BN + half * kColsPerEpiWarp;
       const bool row_ok = m < M;
@@ -444,89 +516,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((EPI == static_cast<int>(Epi::kRowScaleF32) ||
            EPI == static_cast<int>(Epi::kDequantBf16)) && row_ok)
         rs = row_scale != nullptr ? __ldg(row_scale + m) : 1.0f;
-      int iacc[kInt ? kGroups : 1][kInt ? 32 : 1];
-      if (kInt) {
-#pragma unroll
-        for (int c = 0; c < (kInt ? kGroups : 1); ++c)
-#pragma unroll
-          for (int j = 0; j < (kInt ? 32 : 1); ++j) iacc[c][j] = 0;
-      }
-      float yv[kRope ? 4 : 1][kRope ? 32 : 1];  // the head's bf16-rounded projection values
-      for (int u = 0; u < units; ++u, ++unit) {
-        const uint32_t buf = unit & 1u;
-        const uint32_t use = unit >> 1;
+      // the accumulator of unit u: wait until the pair's MMAs have filled it
+      auto acc_wait = [&](uint32_t buf, uint32_t use) -> bool {
         const bool got = mbar_wait_cluster(smem_u32(&ctrl->tmem_full[buf]), use & 1u, abort,
                                            &g_err_pair, 24);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
-          ok = false;
-          break;
-        }
+        if (!__all_sync(0xFFFFFFFFu, got)) return false;
         tc_fence_after();
-        if (!RNL_DCHECK(&g_err_pair, buf * kAccStride + (half + 1) * kColsPerEpiWarp <= kTmemCols, 76)) {
-          ok = false;
-          break;
-        }
-        if constexpr (kInt) {
-          // 16 columns at a time: with the int32 sums of all the warp's
-          // columns live across the chunks, a 32-column load would spill
-#pragma unroll
-          for (int c = 0; c < kGroups; ++c) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t r[16];
-              tmem_ld_16cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32 + h * 16,
-                             r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) iacc[c][16 * h + j] += __float2int_rn(__uint_as_float(r[j]));
-            }
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < (kInt ? 0 : kGroups); ++c) {
-          uint32_t r[32];
-          tmem_ld_32cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32, r);
-          tmem_ld_wait();
-          const int n0 = n_base + c * 32;
-          if (prow != nullptr) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = r[8 * j + i];
-              st_global_v8(prow + (c * 4 + j) * 256, v);
-            }
-          } else {
-            if (row_ok) {
-              // the partners' fp32 partial sums, added in pair order (plain
-              // loads: they were written during this grid)
-              for (int q = pair + 1; q < q_end; ++q) {
-                const uint32_t* src = partial + q * slot_words + warp_off;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  uint32_t v[8];
-                  ld_global_v8(src + (c * 4 + j) * 256, v);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    r[8 * j + i] = __float_as_uint(__uint_as_float(r[8 * j + i]) + __uint_as_float(v[i]));
-                }
-              }
-            }
-            if constexpr (kRope) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) yv[c][j] = bf16r(__uint_as_float(r[j]));
-            } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
-              if (row_ok) {
-                if (bias != nullptr)
-                  store_bf16_bias_32(out, m, n0, N, r, bias);
-                else
-                  store_bf16_32(out, m, n0, N, r);
-              }
-            } else {
-              if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
-            }
-          }
-        }
+        return RNL_DCHECK(&g_err_pair, buf * kAccStride + (half + 1) * kColsPerEpiWarp <= kTmemCols, 76);
+      };
+      // ... and hand it back to the MMA thread once drained
+      auto acc_release = [&](uint32_t buf) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -535,46 +534,130 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             mbar_arrive_cluster(buf ? empty_even_1 : empty_even_0);
         }
+      };
+      // chunked tiles: the int32 sums of the chunks so far, per thread, in
+      // this pair's scratch slot (same lane-major layout as the partials)
+      uint32_t* cws = chunked ? chunk_ws + pair * slot_words + warp_off : nullptr;
+      float yv[kRope ? 4 : 1][kRope ? 32 : 1];  // the head's bf16-rounded projection values
+      for (int u = 0; u < units; ++u, ++unit) {
+        const uint32_t buf = unit & 1u;
+        if (!acc_wait(buf, unit >> 1)) {
+          ok = false;
+          break;
+        }
+        if (kInt && chunked) {
+          // -------- exact int32 sums of the 1024-product chunks: the running
+          // sums in the scratch slot, the last chunk's to the partial slot or
+          // (with the partners' partial sums) to the output
+          const bool last = u + 1 == units;
+          uint32_t* dst = last ? prow : cws;
+#pragma unroll
+          for (int c = 0; c < kGroups; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32, r);
+            tmem_ld_wait();
+            // the int32 sums in the same registers (two's complement bits)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j])));
+            if (u > 0) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t v[8];
+                ld_global_v8(cws + (c * 4 + j) * 256, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[8 * j + i] += v[i];
+              }
+            }
+            if (dst != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = r[8 * j + i];
+                st_global_v8(dst + (c * 4 + j) * 256, v);
+              }
+            } else if (row_ok) {
+              // the partners' exact int32 partial sums, in pair order
+              for (int q = pair + 1; q < q_end; ++q) {
+                const uint32_t* src = partial + q * slot_words + warp_off;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  uint32_t v[8];
+                  ld_global_v8(src + (c * 4 + j) * 256, v);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) r[8 * j + i] += v[i];
+                }
+              }
+              const int(&a)[32] = reinterpret_cast<const int(&)[32]>(r);
+              if constexpr (EPI == static_cast<int>(Epi::kInt32))
+                store_i32_32(out, m, n_base + c * 32, N, a);
+              else
+                store_dequant_32(out, m, n_base + c * 32, N, a, rs, col_scale, bias);
+            }
+          }
+        } else {
+          // -------- one FP32 accumulator (in the integer mode: the exact sum)
+#pragma unroll
+          for (int c = 0; c < kGroups; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp + c * 32, r);
+            tmem_ld_wait();
+            const int n0 = n_base + c * 32;
+            if (prow != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                uint32_t v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = r[8 * j + i];
+                st_global_v8(prow + (c * 4 + j) * 256, v);
+              }
+            } else {
+              if (row_ok) {
+                // the partners' fp32 partial sums, added in pair order (plain
+                // loads: they were written during this grid); in the integer
+                // mode they are exact integers, and so is every sum of them
+                for (int q = pair + 1; q < q_end; ++q) {
+                  const uint32_t* src = partial + q * slot_words + warp_off;
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    uint32_t v[8];
+                    ld_global_v8(src + (c * 4 + j) * 256, v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                      r[8 * j + i] = __float_as_uint(__uint_as_float(r[8 * j + i]) + __uint_as_float(v[i]));
+                  }
+                }
+              }
+              if constexpr (kRope) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) yv[c][j] = bf16r(__uint_as_float(r[j]));
+              } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
+                if (row_ok) {
+                  if (bias != nullptr)
+                    store_bf16_bias_32(out, m, n0, N, r, bias);
+                  else
+                    store_bf16_32(out, m, n0, N, r);
+                }
+              } else if constexpr (EPI == static_cast<int>(Epi::kDequantBf16)) {
+                if (row_ok) store_dequant_f32_32(out, m, n0, N, r, rs, col_scale, bias);
+              } else if constexpr (EPI == static_cast<int>(Epi::kInt32)) {
+                if (row_ok) {
+                  int a[32];
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) a[j] = __float2int_rn(__uint_as_float(r[j]));
+                  store_i32_32(out, m, n0, N, a);
+                }
+              } else {
+                if (row_ok) store_f32_scaled_32(out, m, n0, N, r, rs);
+              }
+            }
+          }
+        }
+        acc_release(buf);
       }
       if (!ok) break;
       if constexpr (kRope) {
         if (prow == nullptr && row_ok) rope_head_epilogue(yv, m, n_base, N, rope, &g_err_pair);
-      }
-      if constexpr (kInt) {
-        if (prow != nullptr) {
-#pragma unroll
-          for (int c = 0; c < kGroups; ++c) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = static_cast<uint32_t>(iacc[c][8 * j + i]);
-              st_global_v8(prow + (c * 4 + j) * 256, v);
-            }
-          }
-        } else if (row_ok) {
-          // the partners' exact int32 partial sums
-          for (int q = pair + 1; q < q_end; ++q) {
-            const uint32_t* src = partial + q * slot_words + warp_off;
-#pragma unroll
-            for (int c = 0; c < kGroups; ++c) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                uint32_t v[8];
-                ld_global_v8(src + (c * 4 + j) * 256, v);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) iacc[c][8 * j + i] += static_cast<int>(v[i]);
-              }
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < kGroups; ++c) {
-            if constexpr (EPI == static_cast<int>(Epi::kInt32))
-              store_i32_32(out, m, n_base + c * 32, N, iacc[c]);
-            else
-              store_dequant_32(out, m, n_base + c * 32, N, iacc[c], rs, col_scale, bias);
-          }
-        }
       }
       if (w.kind == kFinish) {
         // every flag published in a launch is consumed by exactly one
@@ -675,6 +758,14 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   const bool have_partials = g.partial_ws != nullptr &&
                              g.partial_ws_bytes >= kMaxPartialSlots * slot_bytes;
   const int pairs = grid_pairs(tiles, num_kb, max_pairs, have_partials);
+  // the exactness marks serve up to kMaxMarkBlocks 256-row blocks
+  const int exact_rows = (g.exact_rows && g.row_scale != nullptr && num_m <= kMaxMarkBlocks &&
+                          exact_rows_possible(g.K)) ? 1 : 0;
+  // the integer mode's chunked tiles keep their running int32 sums in one
+  // scratch slot per pair
+  constexpr bool kInt = EPI == static_cast<int>(Epi::kDequantBf16) || EPI == static_cast<int>(Epi::kInt32);
+  if (kInt && (g.chunk_ws == nullptr || g.chunk_ws_bytes < static_cast<size_t>(pairs) * slot_bytes))
+    return RNL_ERR_WORKSPACE;
   const Plan pl = make_plan(tiles, pairs, have_partials);
   uint32_t* partial = static_cast<uint32_t*>(g.partial_ws);
   uint64_t* flags = have_partials ? reinterpret_cast<uint64_t*>(static_cast<char*>(g.partial_ws) +
@@ -700,7 +791,8 @@ rnl_status launch_pair_bn(const GemmArgs& g, const DeviceInfo& dev, int max_pair
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<int>(g.M),
                                            static_cast<int>(g.N), static_cast<int>(g.K), group_m,
                                            pl.dp_tiles, pl.sk_tiles, g.out, g.row_scale,
-                                           g.col_scale, partial, flags, next_flag_epoch(),
+                                           g.col_scale, g.gamma_max, exact_rows, static_cast<uint32_t*>(g.chunk_ws),
+                                           partial, flags, next_flag_epoch(),
                                            static_cast<const __nv_bfloat16*>(g.bias), g.rope);
   trace_after(s, g.trace_name ? g.trace_name : name);
   if (e != cudaSuccess) {

@@ -548,23 +548,28 @@ rnl_status launch_gemm(const GemmArgs& g, cudaStream_t s) {
   if (st != RNL_OK) return st;
   // Kernel choice for plain GEMMs: the CTA-pair kernel (gemm_pair.cu) when its
   // predicted time beats the best one-CTA tile width.  The exact-integer mode
-  // stays on one CTA (measured faster there: its per-chunk accumulator
-  // hand-off waits on both CTAs of a pair).  RNL_GEMM_PAIR=0/1 forces the
-  // choice; the fused-norm form always runs here.
+  // in 1024-product chunks stays on one CTA (measured faster there: the
+  // per-chunk accumulator hand-off waits on both CTAs of a pair); with the
+  // rows of an RMSNorm quantiser (exact_rows) the pair kernel accumulates
+  // every tile whose rows pass the exactness bound in one FP32 accumulator,
+  // and the prediction is the plain one.  RNL_GEMM_PAIR=0/1 forces the choice; the fused-norm form
+  // always runs here.
   if (g.a_rstd == nullptr) {
     const char* e = std::getenv("RNL_GEMM_PAIR");
     bool pair;
     if (e != nullptr && (e[0] == '0' || e[0] == '1')) {
       pair = e[0] == '1';
     } else {
-      const bool integer = g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32 ||
-                           g.epi == Epi::kDequantAccF32 || g.epi == Epi::kDequantBatchSum;
+      const bool integer = (g.epi == Epi::kDequantBf16 && (!g.exact_rows || g.chunk_ws == nullptr)) ||
+                           g.epi == Epi::kInt32 || g.epi == Epi::kDequantAccF32 ||
+                           g.epi == Epi::kDequantBatchSum;
       const int bn = pick_bn(g.M, g.N, g.K, dev.sm_count);
       pair = !integer && g.N >= 256 &&
              predict_pair_us(g.M, g.N, g.K, dev.sm_count, resident_pairs_for(dev)) <
                  predict_one_cta_us(g.M, g.N, g.K, dev.sm_count, bn);
     }
-    if (pair && g.epi != Epi::kDequantAccF32 && g.epi != Epi::kDequantBatchSum)
+    const bool int_no_scratch = (g.epi == Epi::kDequantBf16 || g.epi == Epi::kInt32) && g.chunk_ws == nullptr;
+    if (pair && g.epi != Epi::kDequantAccF32 && g.epi != Epi::kDequantBatchSum && !int_no_scratch)
       return launch_gemm_pair(g, s);  // one CTA only
   }
   if (g.a_rstd != nullptr) {  // fused norm: bf16 epilogue only

@@ -74,10 +74,31 @@ rnl_status launch_row_rstd(const void* x, int64_t T, int64_t K, float eps, int m
 rnl_status launch_norm_quant(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
                              int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
 // The same as a persistent stream (quantstream.cu) for K <= 4096: each row
-// read once into registers; codes, int8 copy and x_scale as above.
+// read once into registers; codes, int8 copy and x_scale as above.  With
+// gamma and gmax_out (a device float, may be null): *gmax_out = max |gamma|.
 bool quant_stream_fits(int64_t K);
 rnl_status launch_quant_stream(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
-                               int mode, void* A, int8_t* q_out, float* x_scale, cudaStream_t s);
+                               int mode, void* A, int8_t* q_out, float* x_scale, float* gmax_out,
+                               cudaStream_t s);
+
+// Exact integer products without chunks: a row of codes a (|a| <= 127) times
+// an int8 weight row w (|w| <= 128) has every partial sum, in any order,
+// bounded by 128 * sum_k |a_k|.  Below 2^24 every partial sum is an integer
+// that binary32 holds exactly, so one FP32 accumulator over all of K gives
+// the exact sum: sum_k |a_k| < 2^24 / 128.  For RMSNorm-quantised rows
+// (q = rint(y * 127 / amax), y = (x * rstd) * gamma):
+//   |q_k| <= |y_k| * 127 / amax + 1/2,  |y_k| <= |x_k| rstd max|gamma|,
+//   sum |x_k| <= sqrt(K sum x_k^2)  (Cauchy-Schwarz),
+//   rstd^2 sum x_k^2 = K ms / (ms + eps) <= K  (ms the mean square),
+// each up to a few roundings, so sum |q| <= K max|gamma| / x_scale + K/2
+// (x_scale = amax / 127): below the limit for every x_scale above
+// exact_row_floor (the 1.005 covers the roundings many times over).
+constexpr float kWideRowL1 = 131072.0f;
+__host__ __device__ inline float exact_row_floor(float K, float gamma_max) {
+  return K * gamma_max * 1.005f / (kWideRowL1 - 0.5f * K - 1.0f);
+}
+// the bound needs K/2 + 1 well below the limit
+inline bool exact_rows_possible(int64_t K) { return K > 0 && K <= 65536; }
 // Both of the above in one launch (norm-quantise rows of x and widening of
 // the N x K weight run side by side); rows longer than 4096 fall back to the
 // two launches.
@@ -204,6 +225,13 @@ struct GemmArgs {
   void* out = nullptr;
   const float* row_scale = nullptr;
   const float* col_scale = nullptr;
+  // Epi::kDequantBf16 on CTA pairs with A the codes of RMSNorm-quantised rows
+  // (row_scale = x_scale = amax / 127, quantstream.cu): a tile whose rows all
+  // pass the exactness bound on sum |q| (kWideRowL1) is accumulated in one
+  // FP32 accumulator, the rest in 1024-product chunks; gamma_max (device
+  // scalar, null: no gamma) is max |gamma|.  False: every tile in chunks.
+  bool exact_rows = false;
+  const float* gamma_max = nullptr;
   Epi epi = Epi::kBf16;
   // fused norm (bf16 epilogue only): A is raw x; the kernel feeds the MMA
   // bf16((x * a_rstd[m]) * a_gamma[k]) (a_gamma may be null)
@@ -216,6 +244,11 @@ struct GemmArgs {
   // gemm_pair.cu); without it every tile runs whole
   void* partial_ws = nullptr;
   size_t partial_ws_bytes = 0;
+  // the CTA-pair GEMM's integer mode: one scratch slot per pair for the
+  // running int32 sums of chunked tiles (kGemmPartialBytes suffice); the
+  // integer mode runs on pairs only with it
+  void* chunk_ws = nullptr;
+  size_t chunk_ws_bytes = 0;
   // name of the launch in the kernel trace (default: the kernel's kind)
   const char* trace_name = nullptr;
   // Epi::kDequantAccF32 only

@@ -58,6 +58,7 @@ struct __align__(8) QsCtrl {
   float hi[kPairs][2], lo[kPairs][2];  // each half's float-float sum of squares
   uint32_t amax[kPairs][2];            // each half's max |y|
   int ok[kPairs][2];                   // each warp's row arrived
+  uint32_t gmax[kConsumerWarps + 1];   // each warp's max |gamma| over its staged part
   int abort;
 };
 
@@ -246,7 +247,8 @@ template <int MODE, bool GAMMA, int VPL>
 __global__ void __launch_bounds__(kThreadsQS, 1)
     quant_stream_kernel(const uint8_t* x, const uint4* __restrict__ gamma, int64_t T, int nvec,
                         int slots, float inv_d, float eps, uint4* __restrict__ A,
-                        uint2* __restrict__ q_out, float* __restrict__ x_scale) {
+                        uint2* __restrict__ q_out, float* __restrict__ x_scale,
+                        float* __restrict__ gmax_out) {
   constexpr uint32_t kSlotBytes = 64u * VPL * 16u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -282,13 +284,18 @@ __global__ void __launch_bounds__(kThreadsQS, 1)
   }
   grid_dependency_wait();  // everything below may touch the previous kernel's data
   if (GAMMA) {  // gamma staged once in shared memory for all rows, widened to binary32, zero past the row
+    uint32_t gm = 0;  // max |gamma| of this thread's part (non-negative binary32 values order like their bits)
     for (int v = threadIdx.x; v < 64 * VPL; v += blockDim.x) {
       const uint4 g = v < nvec ? __ldg(gamma + v) : make_uint4(0u, 0u, 0u, 0u);
       ga_s[v] = make_float4(__uint_as_float(g.x << 16), __uint_as_float(g.x & 0xFFFF0000u),
                             __uint_as_float(g.y << 16), __uint_as_float(g.y & 0xFFFF0000u));
       gb_s[v] = make_float4(__uint_as_float(g.z << 16), __uint_as_float(g.z & 0xFFFF0000u),
                             __uint_as_float(g.w << 16), __uint_as_float(g.w & 0xFFFF0000u));
+      gm = max(gm, max(max((g.x << 16) & 0x7FFFFFFFu, g.x & 0x7FFF0000u), max((g.y << 16) & 0x7FFFFFFFu, g.y & 0x7FFF0000u)));
+      gm = max(gm, max(max((g.z << 16) & 0x7FFFFFFFu, g.z & 0x7FFF0000u), max((g.w << 16) & 0x7FFFFFFFu, g.w & 0x7FFF0000u)));
     }
+    gm = __reduce_max_sync(0xFFFFFFFFu, gm);
+    if (lane == 0) ctrl->gmax[warp] = gm;
   }
   __syncthreads();
   volatile int* abort = &ctrl->abort;
@@ -318,6 +325,13 @@ __global__ void __launch_bounds__(kThreadsQS, 1)
   // 32 sub + lane + 64 i); named barrier 1 + p joins the pair
   const int pair = warp >> 1, sub = warp & 1;
   const uint32_t pbar = 1u + static_cast<uint32_t>(pair);
+  // max |gamma| for the integer GEMM's exactness bound (gemm_pair.cu), from
+  // one thread of the grid (every CTA stages all of gamma)
+  if (GAMMA && gmax_out != nullptr && blockIdx.x == 0 && warp == 0 && lane == 0) {
+    uint32_t gm = ctrl->gmax[0];
+    for (int i = 1; i <= kConsumerWarps; ++i) gm = max(gm, ctrl->gmax[i]);
+    *gmax_out = __uint_as_float(gm);
+  }
   for (int64_t j = pair; j < rows; j += kPairs) {
     const uint32_t s = static_cast<uint32_t>(j % slots);
     const uint32_t use = static_cast<uint32_t>(j / slots);
@@ -354,7 +368,10 @@ __global__ void __launch_bounds__(kThreadsQS, 1)
     pass_codes<GAMMA, VPL>(xv, ga_s + 32 * sub, gb_s + 32 * sub, nvec - 32 * sub, lane, rstd, qs,
                            A + row * nvec + 32 * sub,
                            q_out != nullptr ? q_out + row * nvec + 32 * sub : nullptr);
-    if (lane == 0 && sub == 0) x_scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    if (lane == 0 && sub == 0) {
+      x_scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+    }
+
   }
 }
 
@@ -365,7 +382,7 @@ size_t qs_smem(int vpl, int slots) {
 
 template <int MODE, bool GAMMA, int VPL>
 rnl_status launch_qs(const void* x, const void* gamma, int64_t T, int nvec, float inv_d, float eps, void* A,
-                     int8_t* q_out, float* x_scale, const DeviceInfo& dev, cudaStream_t s) {
+                     int8_t* q_out, float* x_scale, float* gmax_out, const DeviceInfo& dev, cudaStream_t s) {
   int slots = static_cast<int>(kRingBytes / (1024u * VPL));
   if (slots > kMaxSlots) slots = kMaxSlots;
   const size_t smem = qs_smem(VPL, slots);
@@ -383,7 +400,8 @@ rnl_status launch_qs(const void* x, const void* gamma, int64_t T, int nvec, floa
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(x),
                                            static_cast<const uint4*>(gamma), T, nvec, slots, inv_d, eps,
-                                           static_cast<uint4*>(A), reinterpret_cast<uint2*>(q_out), x_scale);
+                                           static_cast<uint4*>(A), reinterpret_cast<uint2*>(q_out), x_scale,
+                                           gmax_out);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RNL_ERR_LAUNCH;
@@ -393,12 +411,12 @@ rnl_status launch_qs(const void* x, const void* gamma, int64_t T, int nvec, floa
 
 template <int VPL>
 rnl_status dispatch_mode(const void* x, const void* gamma, int64_t T, int nvec, float inv_d, float eps, void* A,
-                         int8_t* q, float* xs, const DeviceInfo& dev, cudaStream_t s, int mode) {
+                         int8_t* q, float* xs, float* gm, const DeviceInfo& dev, cudaStream_t s, int mode) {
   if (mode == RNL_NORM_RSQRT)
-    return gamma ? launch_qs<0, true, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, dev, s)
-                 : launch_qs<0, false, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, dev, s);
-  return gamma ? launch_qs<1, true, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, dev, s)
-               : launch_qs<1, false, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, dev, s);
+    return gamma ? launch_qs<0, true, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, gm, dev, s)
+                 : launch_qs<0, false, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, gm, dev, s);
+  return gamma ? launch_qs<1, true, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, gm, dev, s)
+               : launch_qs<1, false, VPL>(x, gamma, T, nvec, inv_d, eps, A, q, xs, gm, dev, s);
 }
 
 }  // namespace
@@ -406,7 +424,7 @@ rnl_status dispatch_mode(const void* x, const void* gamma, int64_t T, int nvec, 
 bool quant_stream_fits(int64_t K) { return K > 0 && K <= 8 * 64 * kMaxVpl && K % 8 == 0; }
 
 rnl_status launch_quant_stream(const void* x, const void* gamma, int64_t T, int64_t K, float eps, int mode,
-                               void* A, int8_t* q_out, float* x_scale, cudaStream_t s) {
+                               void* A, int8_t* q_out, float* x_scale, float* gmax_out, cudaStream_t s) {
   if (T == 0) return RNL_OK;
   if (!quant_stream_fits(K)) return RNL_ERR_UNSUPPORTED;
   DeviceInfo dev;
@@ -417,13 +435,13 @@ rnl_status launch_quant_stream(const void* x, const void* gamma, int64_t T, int6
   const int vpl = (nvec + 63) / 64;  // vectors a lane holds (two warps per row)
   trace_before(s);
   if (vpl <= 1)
-    st = dispatch_mode<1>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, dev, s, mode);
+    st = dispatch_mode<1>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, gmax_out, dev, s, mode);
   else if (vpl <= 2)
-    st = dispatch_mode<2>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, dev, s, mode);
+    st = dispatch_mode<2>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, gmax_out, dev, s, mode);
   else if (vpl <= 4)
-    st = dispatch_mode<4>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, dev, s, mode);
+    st = dispatch_mode<4>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, gmax_out, dev, s, mode);
   else
-    st = dispatch_mode<8>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, dev, s, mode);
+    st = dispatch_mode<8>(x, gamma, T, nvec, inv_d, eps, A, q_out, x_scale, gmax_out, dev, s, mode);
   trace_after(s, "w8a8_quant");
   return st;
 }

@@ -175,7 +175,9 @@ def test_workspace_sizes(host_results):
     assert r["version"] >= 100
     part = 128 * 2 * 128 * 256 * 4  # GEMM K-split partial sums
     assert r["ws_bf16_qkv"] == 4096 * 4 + 4096 * 4096 * 2 + part  # rstd + A + partials
-    assert r["ws_w8a8"] == 8192 * 4096 * 2 + 4096 * 4096 * 2 + 8192 * 4 + part
+    # codes + widened weight + x_scale + max |gamma| (one 256-byte unit) + partials
+    # + the pair GEMM's running int32 sums of chunked tiles (as large as the partials)
+    assert r["ws_w8a8"] == 8192 * 4096 * 2 + 4096 * 4096 * 2 + 8192 * 4 + 256 + 2 * part
     assert r["ws_mla"] == 2 * 2048 * 1536 * 2 + 2048 * 4 + part
     # skinny partial records: (T/128 + 512) records of 128 rows x (32 + 1) floats
     assert r["ws_bf16_skinny"] == (16384 // 128 + 512) * 128 * 33 * 4

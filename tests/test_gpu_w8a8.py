@@ -146,3 +146,120 @@ def test_prepared_weight_is_the_exact_integers():
     Wq = rng.integers(-127, 128, (300, 272)).astype(np.int8)
     Wb = rnl.rnl_w8a8_prepare_weight(dev(Wq)).float().cpu().numpy()
     assert np.array_equal(Wb, Wq.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# The integer GEMM on CTA pairs without chunks.  For RMSNorm-quantised rows
+# sum |q| <= K max|gamma| / x_scale + K/2; a tile whose rows all keep that
+# bound below 2^24 / 128 is accumulated in one FP32 accumulator (every
+# partial sum an integer below 2^24: exact), any other tile in 1024-product
+# chunks.  Both must give the exact integer sums, so the output is the
+# dequant of the exact sums: the same bits as the one-CTA kernel (always
+# chunked) and as an FP32 emulation of the dequant on the exact products.
+
+def _bf16_rne_bits(f32: np.ndarray) -> np.ndarray:
+    b = f32.astype(np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _dequant_emulated(q, Wq, xs, ws):
+    """bf16(float(acc) * (x_scale * w_scale)) in binary32, acc exact."""
+    acc = q.astype(np.int64) @ Wq.astype(np.int64).T
+    scale = (xs.astype(np.float32)[:, None] * ws.astype(np.float32)[None, :]).astype(np.float32)
+    return _bf16_rne_bits((acc.astype(np.float32) * scale).astype(np.float32))
+
+
+def _run_route(x, Wb, ws, pair, monkeypatch, T, K, gamma=None):
+    monkeypatch.setenv("RNL_GEMM_PAIR", "1" if pair else "0")
+    q = torch.empty((T, K), dtype=torch.int8, device="cuda")
+    xs = torch.empty((T,), dtype=torch.float32, device="cuda")
+    out = rnl.rmsnorm_linear_w8a8_prepared(x, gamma, Wb, ws, eps=1e-6, norm_mode=0, q_out=q, x_scale_out=xs)
+    torch.cuda.synchronize()
+    rnl.rnl_check_device_error()
+    return host_bits(out), q.cpu().numpy(), xs.cpu().numpy()
+
+
+def _const_rows(n_nonzero, K, rows, value=1.0):
+    """rows x K bf16 bits: `value` in the first n_nonzero columns, 0 after."""
+    x = np.zeros((rows, K), np.float32)
+    x[:, :n_nonzero] = value
+    return (x.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _both_routes_exact(orc, monkeypatch, x, W, ws, T, K):
+    xd, Wb, wsd = dev_bf16(x), rnl.rnl_w8a8_prepare_weight(dev(W)), dev(ws)
+    got_pair = _run_route(xd, Wb, wsd, True, monkeypatch, T, K)
+    got_one = _run_route(xd, Wb, wsd, False, monkeypatch, T, K)
+    r = orc.rmsnorm_linear_w8a8(x, None, W, ws, 1e-6, 0)
+    for got in (got_pair, got_one):  # the same front end on both routes, as the oracle's
+        assert np.array_equal(got[1], r["q"]) and np.array_equal(got[2], r["x_scale"])
+    want = _dequant_emulated(r["q"], W, r["x_scale"], ws)
+    assert np.array_equal(got_one[0], want), "one-CTA chunked route"
+    assert np.array_equal(got_pair[0], want), "pair route"
+    assert_bf16_close(got_pair[0], r["out"], "pair route vs oracle")
+    return got_pair[0], r
+
+
+def test_unchunked_pair_tiles_exact_near_the_bound(orc, monkeypatch):
+    """K = 1008: rows of equal values give x_scale = 1/127, just above the
+    bound's floor, so their tiles take one FP32 accumulator although
+    sum |q| = 127 * 1008 = 128016: products summing to 16.26 M, to -16.39 M
+    (int8 -128 weights) and to exactly 0 after partial sums of 8.1 M."""
+    monkeypatch.setenv("RNL_W8A8_STREAM", "1")
+    T, K, N = 512, 1008, 264
+    d = si.make_w8a8(dict(seed=45, T=T, K=K, N=N))
+    x = d["x"].copy()
+    x[:256] = _const_rows(K, K, 256)
+    W = d["Wq"].copy()
+    W[0] = 127
+    W[1, :504], W[1, 504:] = 127, -127
+    W[2] = -128
+    out, r = _both_routes_exact(orc, monkeypatch, x, W, d["w_scale"], T, K)
+    assert np.abs(r["q"][:256].astype(np.int64)).sum(1).min() == 127 * K
+    assert (r["acc"][:256, 0] == 127 * 127 * K).all() and (r["acc"][:256, 2] == -128 * 127 * K).all()
+    assert not bf16_bits_to_f64(out[:256, 1]).any()
+
+
+def test_chunked_pair_tiles_exact_past_the_bound(orc, monkeypatch):
+    """K = 4096: random rows (their tiles unchunked) beside rows of 1000,
+    1100 and 4096 codes of 127 (their tiles in chunks: sum |q| up to 520192),
+    with weight rows whose products cancel to exactly 0 after partial sums of
+    8 M and 33 M."""
+    monkeypatch.setenv("RNL_W8A8_STREAM", "1")
+    T, K, N = 768, 4096, 512
+    d = si.make_w8a8(dict(seed=41, T=T, K=K, N=N))
+    x = d["x"].copy()
+    x[256:512:2] = _const_rows(1100, K, 128)
+    x[257:512:2] = _const_rows(K, K, 128)
+    x[512:768] = _const_rows(1000, K, 256)
+    W = d["Wq"].copy()
+    W[0] = 0
+    W[0, :500], W[0, 500:1000] = 127, -127          # 0 after +8 M
+    W[1] = 0
+    W[1, :2048], W[1, 2048:] = 127, -127             # 4096-code rows: 0 after +33 M
+    W[2] = 127
+    W[3] = -128
+    out, r = _both_routes_exact(orc, monkeypatch, x, W, d["w_scale"], T, K)
+    assert np.abs(r["q"][257:512:2].astype(np.int64)).sum(1).min() == 127 * K
+    assert not bf16_bits_to_f64(out[512:, 0]).any()
+    assert not bf16_bits_to_f64(out[257:512:2, 1]).any()
+
+
+@pytest.mark.parametrize("T,N", [(1000, 1000), (8192, 4096)])
+def test_pair_and_one_cta_integer_routes_identical(orc, monkeypatch, T, N):
+    """Random rows (every tile within the bound): the pair route's single
+    FP32 accumulator and stream-K FP32 partials give the one-CTA route's
+    bits, and the FP32 emulation of the dequant on sampled rows."""
+    monkeypatch.setenv("RNL_W8A8_STREAM", "1")
+    K = 4096
+    c = dict(seed=43 + T, T=T, K=K, N=N)
+    d = si.make_w8a8(c)
+    xd, Wb, wsd = dev_bf16(d["x"]), rnl.rnl_w8a8_prepare_weight(dev(d["Wq"])), dev(d["w_scale"])
+    got_pair = _run_route(xd, Wb, wsd, True, monkeypatch, T, K)
+    got_one = _run_route(xd, Wb, wsd, False, monkeypatch, T, K)
+    assert np.array_equal(got_pair[1], got_one[1]) and np.array_equal(got_pair[2], got_one[2])
+    assert np.array_equal(got_pair[0], got_one[0]), \
+        f"{(got_pair[0] != got_one[0]).sum()} outputs differ between the routes"
+    rows = sample_rows(T, 32, seed=T)
+    want = _dequant_emulated(got_one[1][rows], d["Wq"], got_one[2][rows], d["w_scale"])
+    assert np.array_equal(got_pair[0][rows], want)
