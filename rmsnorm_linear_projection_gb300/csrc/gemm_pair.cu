@@ -168,43 +168,70 @@ __device__ __forceinline__ int partners_end(const Sched& sc, int pair, int t) {
 // outside [0, P) skips the row's q / k heads and records RNL_ERR_ARG.
 __device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-__device__ __forceinline__ void rope_head_epilogue(const float (&y)[4][32], int64_t m, int n_base,
-                                                   int N, const RopeEpiArgs& a, unsigned int* err) {
+// One 128-wide head of one row, read from the accumulator in tensor memory
+// (taddr: the warp's lane quarter and column half) with the partners'
+// partial sums added (stream-K finishers); ss: the sum of squares of its
+// bf16-rounded values (pass 1, during the drain); p: the row's position.  v
+// heads are copied; q and k heads are normalised and rotated, two 32-column
+// groups (c, c + 2) at a time, so that only 64 values are live.  Called by
+// the whole warp: the tensor-memory loads are warp-collective, so every lane
+// takes them and only the lanes of valid rows (row_ok, a position inside the
+// table) compute and store.
+__device__ __forceinline__ void rope_head_tmem(uint32_t taddr, const uint32_t* partial_w, int64_t slot_words,
+                                               int q0, int q1, float ss, int p, bool row_ok, int64_t m,
+                                               int n_base, int N, const RopeEpiArgs& a, unsigned int* err) {
   constexpr int D = 128;
-  if (n_base >= N) return;
+  if (n_base >= N) return;  // the same on every lane
   const int h = n_base / D;
   const int nqk = a.Hq + a.Hkv;
+  auto group = [&](int c, uint32_t (&r)[32]) {
+    tmem_ld_32cols(taddr + c * 32, r);  // every lane
+    tmem_ld_wait();
+    for (int q = q0; q < q1 && row_ok; ++q) {
+      const uint32_t* src = partial_w + q * slot_words;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[8];
+        ld_global_v8(src + (c * 4 + j) * 256, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          r[8 * j + i] = __float_as_uint(__uint_as_float(r[8 * j + i]) + __uint_as_float(v[i]));
+      }
+    }
+  };
   if (h >= nqk) {  // v head: copied
     uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.v) + (m * a.Hkv + (h - nqk)) * D);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      group(c, r);
+      if (!row_ok) continue;
 #pragma unroll
       for (int q8 = 0; q8 < 4; ++q8) {
         uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[i] = bf16x2_bits(y[c][8 * q8 + 2 * i], y[c][8 * q8 + 2 * i + 1]);
+        for (int i = 0; i < 4; ++i)
+          o[i] = bf16x2_bits(__uint_as_float(r[8 * q8 + 2 * i]), __uint_as_float(r[8 * q8 + 2 * i + 1]));
         dst[c * 4 + q8] = make_uint4(o[0], o[1], o[2], o[3]);  // 16-byte stores: q, k, v are 16-byte aligned
       }
+    }
     return;
   }
-  const int p = __ldg(a.pos + m);
-  if (p < 0 || p >= a.P) {
-    atomicCAS(err, 0u, kErrArg | (40u << 8));
-    return;
-  }
+  const bool pos_ok = p >= 0 && p < a.P;
+  if (row_ok && !pos_ok) atomicCAS(err, 0u, kErrArg | (40u << 8));
+  const bool work = row_ok && pos_ok;  // this lane's row is normalised, rotated and stored
   const bool is_q = h < a.Hq;
   const uint4* g4 = static_cast<const uint4*>(is_q ? a.q_gamma : a.k_gamma);
-  float ss = 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) ss = fmaf(y[c][j], y[c][j], ss);
   const float r = rsqrtf(ss * (1.0f / D) + a.eps);
-  const float4* row = reinterpret_cast<const float4*>(a.cos_sin + static_cast<int64_t>(p) * D);
+  const float4* row = reinterpret_cast<const float4*>(a.cos_sin + static_cast<int64_t>(work ? p : 0) * D);
   __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q) + (m * a.Hq + h) * D
                             : static_cast<__nv_bfloat16*>(a.k) + (m * a.Hkv + (h - a.Hq)) * D;
-#pragma unroll
+#pragma unroll 1
   for (int c = 0; c < 2; ++c) {
+    uint32_t ylo[32], yhi[32];  // columns 32 c .. and their rotation partners 64 + 32 c ..
+    group(c, ylo);
+    group(c + 2, yhi);
+    if (!work) continue;
 #pragma unroll
     for (int q8 = 0; q8 < 4; ++q8) {
       const int i0 = c * 32 + q8 * 8;  // elements i0 .. i0 + 7 and their partners + 64
@@ -223,8 +250,10 @@ __device__ __forceinline__ void rope_head_epilogue(const float (&y)[4][32], int6
           const int e = 2 * e2 + t2;
           const float g_lo = __uint_as_float(t2 ? (glw[e2] & 0xFFFF0000u) : (glw[e2] << 16));
           const float g_hi = __uint_as_float(t2 ? (ghw[e2] & 0xFFFF0000u) : (ghw[e2] << 16));
-          const float zl = bf16r(__fmul_rn(__fmul_rn(y[c][q8 * 8 + e], r), g_lo));
-          const float zh = bf16r(__fmul_rn(__fmul_rn(y[c + 2][q8 * 8 + e], r), g_hi));
+          const float yl = bf16r(__uint_as_float(ylo[q8 * 8 + e]));
+          const float yh = bf16r(__uint_as_float(yhi[q8 * 8 + e]));
+          const float zl = bf16r(__fmul_rn(__fmul_rn(yl, r), g_lo));
+          const float zh = bf16r(__fmul_rn(__fmul_rn(yh, r), g_hi));
           lo[t2] = __fsub_rn(__fmul_rn(zl, co[e]), __fmul_rn(zh, si[e]));
           hi[t2] = __fadd_rn(__fmul_rn(zh, co[e]), __fmul_rn(zl, si[e]));
         }
@@ -516,6 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((EPI == static_cast<int>(Epi::kRowScaleF32) ||
            EPI == static_cast<int>(Epi::kDequantBf16)) && row_ok)
         rs = row_scale != nullptr ? __ldg(row_scale + m) : 1.0f;
+      int rope_p = 0;  // the row's position, loaded before the drain
+      if (kRope && row_ok && prow == nullptr) rope_p = __ldg(rope.pos + m);
       // the accumulator of unit u: wait until the pair's MMAs have filled it
       auto acc_wait = [&](uint32_t buf, uint32_t use) -> bool {
         const bool got = mbar_wait_cluster(smem_u32(&ctrl->tmem_full[buf]), use & 1u, abort,
@@ -538,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // chunked tiles: the int32 sums of the chunks so far, per thread, in
       // this pair's scratch slot (same lane-major layout as the partials)
       uint32_t* cws = chunked ? chunk_ws + pair * slot_words + warp_off : nullptr;
-      float yv[kRope ? 4 : 1][kRope ? 32 : 1];  // the head's bf16-rounded projection values
+      float ss = 0.f;  // the rope epilogue's sum of squares of the head's bf16-rounded values
       for (int u = 0; u < units; ++u, ++unit) {
         const uint32_t buf = unit & 1u;
         if (!acc_wait(buf, unit >> 1)) {
@@ -630,7 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if constexpr (kRope) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) yv[c][j] = bf16r(__uint_as_float(r[j]));
+                for (int j = 0; j < 32; ++j) {
+                  const float v = bf16r(__uint_as_float(r[j]));
+                  ss = fmaf(v, v, ss);
+                }
               } else if constexpr (EPI == static_cast<int>(Epi::kBf16)) {
                 if (row_ok) {
                   if (bias != nullptr)
@@ -653,12 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if constexpr (kRope) {  // pass 2, from the accumulator still held (the whole warp)
+          if (prow == nullptr)
+            rope_head_tmem(tmem_base + lane_addr + buf * kAccStride + half * kColsPerEpiWarp, partial + warp_off,
+                           slot_words, pair + 1, q_end, ss, rope_p, row_ok, m, n_base, N, rope, &g_err_pair);
+        }
         acc_release(buf);
       }
       if (!ok) break;
-      if constexpr (kRope) {
-        if (prow == nullptr && row_ok) rope_head_epilogue(yv, m, n_base, N, rope, &g_err_pair);
-      }
       if (w.kind == kFinish) {
         // every flag published in a launch is consumed by exactly one
         // finisher warp, which sets it back to 0 once the partial sums are
