@@ -67,16 +67,16 @@ WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": 
                     "w8a8": "pair", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
                     "decode": "decode", "tiny": "one_cta"}
 TRAFFIC = {
-    "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
-    "tiny": {"bytes": 110000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
-    "mla": {"bytes": 203390000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5a4c5a7beb7756ad"},
-    "w8a8": {"bytes": 172540000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
+    "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "tiny": {"bytes": 110000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
+    "mla": {"bytes": 203560000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8e792bd2d24af733"},
+    "w8a8": {"bytes": 225770000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
     "skinny": {"bytes": 946180000, "profile": "profiles/traffic_roofline_stages.md", "sources": "cab190e5a3867f6b"},
-    "qkv_ex": {"bytes": 135680000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
-    "qkv_rope": {"bytes": 158900000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0efeecf86668ae55"},
-    "qmrs": {"bytes": 385010000, "profile": "profiles/traffic_roofline_stages.md", "sources": "50c35ec834224a5f"},
-    "mxfp8": {"bytes": 55920000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5d9aed71d1d08303"},
-    "mla_hn": {"bytes": 203300000, "profile": "profiles/traffic_roofline_stages.md", "sources": "5a4c5a7beb7756ad"},
+    "qkv_ex": {"bytes": 136610000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "qkv_rope": {"bytes": 144240000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "qmrs": {"bytes": 373960000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
+    "mxfp8": {"bytes": 55750000, "profile": "profiles/traffic_roofline_stages.md", "sources": "44d1e228dcf671fc"},
+    "mla_hn": {"bytes": 203520000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8e792bd2d24af733"},
     "decode": {"bytes": 50400000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0cbb868f949b8b56"},
 }
 
