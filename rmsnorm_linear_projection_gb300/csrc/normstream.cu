@@ -44,9 +44,10 @@ struct __align__(8) NsCtrl {
 // Options of the extended form (EXT = true; every pointer may be null): the
 // residual row is added first (x_add = bf16(x + residual)), x_add is written
 // to x_sum, beta is added after gamma, rstd is written per row.  Each
-// consumer warp loads its residual row from global memory before it waits
-// for the x row, so the load overlaps the bulk copy (the ring holds x rows
-// only and keeps its depth).  x_add then replaces the x row in the warp's ring
+// consumer warp loads the residual row of its next row from global memory as
+// soon as the current row's first pass has used its own, so the load
+// overlaps the output pass and the wait for the next x row (the ring holds x
+// rows only and keeps its depth).  x_add then replaces the x row in the warp's ring
 // slot and the output pass reads it from there, so no row is held in
 // registers across the two passes.
 struct NsExt {
@@ -154,18 +155,22 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
     uint32_t stage = 0, phase = 0;
+    // the residual row of this warp's next row, loaded while the current one
+    // is finished (plain loads: x_sum may be the residual itself; the next
+    // row is never the one being written)
+    uint4 rv[EXT ? VPL : 1];
+    auto load_residual = [&](int64_t r) {
+      const uint4* qr = ext.residual + r * nvec;
+#pragma unroll
+      for (int i = 0; i < (EXT ? VPL : 1); ++i) {
+        const int v = lane + 32 * i;
+        rv[i] = v < nvec ? qr[v] : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    if (EXT && has_res && r_begin + warp < r_end) load_residual(r_begin + warp);
     for (int64_t g = 0; g < groups; ++g) {
       const int64_t row = r_begin + g * kGroupRows + warp;
       if (row < r_end && EXT) {
-        uint4 rv[EXT ? VPL : 1];
-        if (has_res) {  // plain loads: x_sum may be the residual itself
-          const uint4* qr = ext.residual + row * nvec;
-#pragma unroll
-          for (int i = 0; i < VPL; ++i) {
-            const int v = lane + 32 * i;
-            rv[i] = v < nvec ? qr[v] : make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
         const bool got = mbar_wait(smem_u32(&ctrl->full[stage][warp]), phase, abort, &g_err_norm, 32);
         if (!__all_sync(0xFFFFFFFFu, got)) break;
         uint4* rp = reinterpret_cast<uint4*>(smem + stage * stage_bytes + warp * row_bytes);
@@ -198,6 +203,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
             }
           }
         }
+        if (has_res && row + kGroupRows < r_end) load_residual(row + kGroupRows);
         s = warp_sum(s);
         const float rstd = (MODE == 0) ? rsqrtf(s * inv_d + eps) : 1.0f / sqrtf(s + eps);
         if (ext.rstd_out != nullptr && lane == 0) ext.rstd_out[row] = rstd;
