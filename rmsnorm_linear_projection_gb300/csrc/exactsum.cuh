@@ -73,6 +73,78 @@ __device__ __forceinline__ float ff_warp_total(const float (&hs)[8], const float
   return __fadd_rn(hi, lo);
 }
 
+// ---- The same float-float sum on packed f32x2 arithmetic: two chains per
+// instruction.  Four packed chains per lane (eight scalar chains, one per
+// element position of a 16-byte bf16 vector), merged into one pair.  A
+// packed product feeding a packed sum could be contracted by ptxas into one
+// fused multiply-add, so the terms' products (which must be rounded, in the
+// sqrt+div form) are scalar __fmul_rn; the squares of bf16 values are exact.
+__device__ __forceinline__ uint64_t ffx2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void ffx2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffx2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffx2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffx2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// TwoSum of (hi, t) per half, the error added to lo
+__device__ __forceinline__ void ffx2_two_sum(uint64_t& hi, uint64_t& lo, uint64_t t) {
+  const uint64_t s = ffx2_add(hi, t);
+  const uint64_t bb = ffx2_sub(s, hi);
+  const uint64_t e = ffx2_add(ffx2_sub(hi, ffx2_sub(s, bb)), ffx2_sub(t, bb));
+  hi = s;
+  lo = ffx2_add(lo, e);
+}
+// the eight terms of one 16-byte bf16 vector into the lane's four packed chains
+template <int MODE>
+__device__ __forceinline__ void ffx2_add_squares8(const uint4& u, float inv_d, uint64_t (&hs)[4],
+                                                  uint64_t (&ls)[4]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint64_t xx = ffx2_pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+    uint64_t t = ffx2_mul(xx, xx);  // exact: bf16 squares
+    if (MODE == 1) {
+      float t0, t1;
+      ffx2_unpack(t, t0, t1);
+      t = ffx2_pack(__fmul_rn(t0, inv_d), __fmul_rn(t1, inv_d));
+    }
+    ffx2_two_sum(hs[k], ls[k], t);
+  }
+}
+// the binary32 rounding of the warp's total of all lanes' chains
+__device__ __forceinline__ float ffx2_warp_total(uint64_t (&hs)[4], uint64_t (&ls)[4]) {
+  ffx2_two_sum(hs[0], ls[0], hs[1]);
+  ls[0] = ffx2_add(ls[0], ls[1]);
+  ffx2_two_sum(hs[2], ls[2], hs[3]);
+  ls[2] = ffx2_add(ls[2], ls[3]);
+  ffx2_two_sum(hs[0], ls[0], hs[2]);
+  ls[0] = ffx2_add(ls[0], ls[2]);
+  float h0, h1, l0, l1;
+  ffx2_unpack(hs[0], h0, h1);
+  ffx2_unpack(ls[0], l0, l1);
+  float hi, e;
+  two_sum(h0, h1, hi, e);
+  float lo = __fadd_rn(__fadd_rn(l0, l1), e);
+  ff_warp_merge(hi, lo);
+  return __fadd_rn(hi, lo);
+}
+
 // rstd from the binary32 sum, one correctly rounded operation per step:
 // 1 / sqrt(ss * (1/K) + eps) (rsqrt form, MODE 0) or 1 / sqrt(ss + eps)
 // (sqrt+div form, whose terms already carry 1/K).

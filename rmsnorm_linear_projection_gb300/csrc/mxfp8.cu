@@ -218,9 +218,7 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
   const int iters = (p.nvec + 31) / 32;  // the same on every lane
   constexpr int kR = VPL > 0 ? VPL : 1;
   uint4 u[kR];
-  float hs[8], ls[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) hs[j] = ls[j] = 0.f;
+  uint64_t hs[4] = {0, 0, 0, 0}, ls[4] = {0, 0, 0, 0};  // packed float-float chains, (+0, +0)
   if (VPL > 0) {
 #pragma unroll
     for (int i = 0; i < kR; ++i) {
@@ -228,11 +226,7 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
       u[i] = v < p.nvec ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int i = 0; i < kR; ++i) {
-      float f[8];
-      unpack8(u[i], f);
-      ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
-    }
+    for (int i = 0; i < kR; ++i) ffx2_add_squares8<MODE>(u[i], p.inv_d, hs, ls);
   } else {
     int v = lane;
     for (; v + 96 < p.nvec; v += 128) {
@@ -240,19 +234,11 @@ __device__ __forceinline__ void mx_quant_row(unsigned block, const MxRows& p) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) w[j] = __ldg(xr + v + 32 * j);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float f[8];
-        unpack8(w[j], f);
-        ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
-      }
+      for (int j = 0; j < 4; ++j) ffx2_add_squares8<MODE>(w[j], p.inv_d, hs, ls);
     }
-    for (; v < p.nvec; v += 32) {
-      float f[8];
-      unpack8(__ldg(xr + v), f);
-      ff_add_squares8<MODE>(f, p.inv_d, hs, ls);
-    }
+    for (; v < p.nvec; v += 32) ffx2_add_squares8<MODE>(__ldg(xr + v), p.inv_d, hs, ls);
   }
-  const float rstd = rstd_of_sum<MODE>(ff_warp_total(hs, ls), p.inv_d, p.eps);
+  const float rstd = rstd_of_sum<MODE>(ffx2_warp_total(hs, ls), p.inv_d, p.eps);
   const int nb = p.nvec / (BLK / 8);  // blocks per row
   uint4* ar = p.A != nullptr ? p.A + row * p.nvec : nullptr;
   uint2* qr = p.q_out != nullptr ? p.q_out + row * p.nvec : nullptr;
