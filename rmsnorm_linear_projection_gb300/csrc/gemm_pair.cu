@@ -34,6 +34,18 @@
 // order.  All pairs of the grid are resident at once (the grid is sized from
 // the occupancy of the cluster launch), and a pair only waits for pairs of
 // higher index, which never wait on it.
+//
+// Exact integer mode (W8A8: codes and int8 weights as exact bf16 integers).
+// Binary32 holds every integer below 2^24 exactly, so a tile whose rows keep
+// 128 sum |q| below 2^24 (the bound on RMSNorm-quantised codes in internal.h,
+// kWideRowL1, read from x_scale and max |gamma|) is accumulated over all of K
+// in one FP32 accumulator and drained through the FP32 epilogue; any other
+// tile is accumulated in chunks of 1024 products, each chunk converted to
+// int32 and added into a per-pair scratch slot in global memory.  At the
+// start the epilogue warps (idle until their first accumulator) reduce the
+// test to one byte per 256-row block and one per work item in shared memory,
+// so that the MMA thread reads one byte per item.  Both kinds of tile give
+// the exact int32 sums, and the dequant is the same arithmetic on them.
 #include <cuda_bf16.h>
 
 #include <atomic>
