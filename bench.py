@@ -67,16 +67,16 @@ WORKLOAD_SOURCES = {"qkv": "pair", "qkv_ex": "pair", "qkv_rope": "pair", "mla": 
                     "w8a8": "pair", "qmrs": "one_cta", "mxfp8": "mx", "skinny": "skinny",
                     "decode": "decode", "tiny": "one_cta"}
 TRAFFIC = {
-    "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "qkv": {"bytes": 137360000, "profile": "profiles/traffic_roofline_stages.md", "sources": "4e525195315ad8ec"},
     "tiny": {"bytes": 110000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
-    "mla": {"bytes": 203560000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8e792bd2d24af733"},
-    "w8a8": {"bytes": 225770000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "mla": {"bytes": 203560000, "profile": "profiles/traffic_roofline_stages.md", "sources": "14f7e1c2fe6abad4"},
+    "w8a8": {"bytes": 225770000, "profile": "profiles/traffic_roofline_stages.md", "sources": "4e525195315ad8ec"},
     "skinny": {"bytes": 946180000, "profile": "profiles/traffic_roofline_stages.md", "sources": "cab190e5a3867f6b"},
-    "qkv_ex": {"bytes": 136610000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
-    "qkv_rope": {"bytes": 144240000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8f3d957c921b8711"},
+    "qkv_ex": {"bytes": 136610000, "profile": "profiles/traffic_roofline_stages.md", "sources": "4e525195315ad8ec"},
+    "qkv_rope": {"bytes": 144240000, "profile": "profiles/traffic_roofline_stages.md", "sources": "4e525195315ad8ec"},
     "qmrs": {"bytes": 373960000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
     "mxfp8": {"bytes": 55750000, "profile": "profiles/traffic_roofline_stages.md", "sources": "44d1e228dcf671fc"},
-    "mla_hn": {"bytes": 203520000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8e792bd2d24af733"},
+    "mla_hn": {"bytes": 203520000, "profile": "profiles/traffic_roofline_stages.md", "sources": "14f7e1c2fe6abad4"},
     "decode": {"bytes": 50400000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0cbb868f949b8b56"},
 }
 
