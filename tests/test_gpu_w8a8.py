@@ -263,3 +263,19 @@ def test_pair_and_one_cta_integer_routes_identical(orc, monkeypatch, T, N):
     rows = sample_rows(T, 32, seed=T)
     want = _dequant_emulated(got_one[1][rows], d["Wq"], got_one[2][rows], d["w_scale"])
     assert np.array_equal(got_pair[0][rows], want)
+
+
+def test_pair_route_past_the_mark_table_chunks_every_tile(orc, monkeypatch):
+    """More 256-row blocks than the pair kernel's mark table holds (1024):
+    every tile in 1024-product chunks on CTA pairs, the same bits as the
+    one-CTA route, and the oracle's on sampled rows."""
+    monkeypatch.setenv("RNL_W8A8_STREAM", "1")
+    T, K, N = 1025 * 256 + 37, 64, 48
+    d = si.make_w8a8(dict(seed=47, T=T, K=K, N=N))
+    d["gamma"] = None  # the routes run without gamma
+    xd, Wb, wsd = dev_bf16(d["x"]), rnl.rnl_w8a8_prepare_weight(dev(d["Wq"])), dev(d["w_scale"])
+    got_pair = _run_route(xd, Wb, wsd, True, monkeypatch, T, K)
+    got_one = _run_route(xd, Wb, wsd, False, monkeypatch, T, K)
+    assert np.array_equal(got_pair[0], got_one[0])
+    rows = sample_rows(T, 64, seed=3)
+    _check(orc, d, 1e-6, 0, got_pair, rows)
