@@ -77,7 +77,7 @@ TRAFFIC = {
     "qmrs": {"bytes": 373960000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
     "mxfp8": {"bytes": 55750000, "profile": "profiles/traffic_roofline_stages.md", "sources": "44d1e228dcf671fc"},
     "mla_hn": {"bytes": 203520000, "profile": "profiles/traffic_roofline_stages.md", "sources": "14f7e1c2fe6abad4"},
-    "decode": {"bytes": 50400000, "profile": "profiles/traffic_roofline_stages.md", "sources": "0cbb868f949b8b56"},
+    "decode": {"bytes": 50400000, "profile": "profiles/traffic_roofline_stages.md", "sources": "ec698d44ff8625e6"},
 }
 
 
@@ -802,7 +802,7 @@ def run_ours(args):
                 flush_l2()
                 w.call()
 
-        def replay_us(gr):
+        def replay_us(gr, n=calls):
             gr.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -811,7 +811,7 @@ def run_ours(args):
                 gr.replay()
             e1.record(stream)
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+            return e0.elapsed_time(e1) * 1e3 / (reps * n)
 
         us = replay_us(g_both) - replay_us(g_flush)
         rnl.rnl_check_device_error()
@@ -819,6 +819,31 @@ def run_ours(args):
                    "value_at_graph_rate": amount / (us * 1e-6), "unit": unit,
                    "note": "GPU time per call: CUDA graph, L2 flushed before every call, the flushes' time subtracted"}
         del g_flush, g_both
+
+        # a decode step of a deep model: one call per layer, each through its
+        # own weight (copies of W at distinct addresses, together far larger
+        # than L2, so every call reads its weight from HBM), back to back in a
+        # CUDA graph.  Every call waits for the kernel before it before it
+        # reads x, as a layer whose tokens the previous layer wrote must.
+        layers = 24
+        chain_w = [w.d["W"].clone() for _ in range(layers)]
+        g_chain = torch.cuda.CUDAGraph()
+        odt = rnl.OUT_BF16
+        with torch.cuda.graph(g_chain, capture_error_mode="thread_local"):
+            for Wl in chain_w:
+                rnl.rmsnorm_linear_bf16(w.d["x"], w.d["gamma"], Wl, eps=w.cfg["eps"],
+                                        norm_mode=w.cfg["norm_mode"], out=w.out, out_dtype=odt,
+                                        workspace=w.ws)
+        us_chain = replay_us(g_chain, layers)
+        rnl.rnl_check_device_error()
+        chain_gbs = w.dominant()[2] / (us_chain * 1e-6) / 1e9
+        latency["layer_chain"] = {
+            "layers": layers, "weights_bytes": layers * w.d["W"].numel() * 2, "us_per_call": us_chain,
+            "value": amount / (us_chain * 1e-6), "unit": unit, "weight_stream_gbs": chain_gbs,
+            **({"frac_of_hbm": chain_gbs / roofline["peak"]} if roofline is not None else {}),
+            "note": "GPU time per call in a CUDA graph of calls through distinct weights (no flush: "
+                    "the weights exceed L2), each call ordered after the previous kernel"}
+        del g_chain, chain_w
         # the one kernel of the call, timed without the host's launch in
         # front of it: the graph's time per call is the roofline duration
         if roofline is not None and us > 0:

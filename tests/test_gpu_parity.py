@@ -87,6 +87,38 @@ def test_bf16_decode_sized_both_paths(orc, monkeypatch, decode, T, K, N, mode, g
     assert_bf16_close(host_bits(out), want, f"decode={decode} {T}x{K}x{N}")
 
 
+@pytest.mark.parametrize("rewrite_weight", [False, True])
+def test_decode_chain_reads_what_the_kernel_before_wrote(orc, monkeypatch, rewrite_weight):
+    """Decode calls back to back, each taking the previous call's output as
+    its tokens (square weights).  The decode kernel is launched as a
+    programmatic dependent of the kernel before it, so it may start before
+    that kernel's writes are visible: the tokens (written by the previous
+    decode call) and, with rewrite_weight, the weight (written by a copy
+    kernel just before the call) must still be read as written.  Each call
+    against the oracle on the inputs it was given."""
+    monkeypatch.setenv("RNL_DECODE", "1")
+    monkeypatch.setenv("RNL_DECODE_MMA", "0")
+    T, K, layers = 4, 4096, 4
+    ds = [_rand_case(211 + i, T, K, K, True) for i in range(layers)]
+    gamma = dev_bf16(ds[0]["gamma"])
+    staged = [dev_bf16(d["W"]) for d in ds]
+    W_one = torch.empty_like(staged[0])
+    x, outs = dev_bf16(ds[0]["x"]), []
+    for i in range(layers):
+        if rewrite_weight:
+            W_one.copy_(staged[i])
+        out = rnl.rmsnorm_linear_bf16(x, gamma, W_one if rewrite_weight else staged[i], eps=1e-6, norm_mode=0)
+        outs.append(out)
+        x = out
+    torch.cuda.synchronize()
+    x_bits = ds[0]["x"]
+    for i in range(layers):
+        _, want = orc.rmsnorm_linear(x_bits, ds[0]["gamma"], ds[i]["W"], 1e-6, 0, 0)
+        got = host_bits(outs[i])
+        assert_bf16_close(got, want, f"decode chain call {i} rewrite_weight={rewrite_weight}")
+        x_bits = got
+
+
 @pytest.mark.parametrize("bn", [128, 192, 256])
 @pytest.mark.parametrize("T,K,N", [(300, 520, 600), (129, 4096, 256)])
 def test_bf16_each_tile_width(orc, monkeypatch, bn, T, K, N):
