@@ -10,15 +10,21 @@
 //   a = bf16((x rstd) gamma)): one read of x from global memory, the raw rows
 //   parked in shared memory and normalised in place, gamma read in the same
 //   pass and parked beside them when it fits;
-//   each warp then takes groups of R adjacent weight rows, g = w, w + W, ...
-//   (W = the warps of the whole grid, which is resident at once; warp w is
-//   warp w / grid of CTA w % grid), and streams
-//   them as one sequence of chunks (8 16-byte loads per lane: 8 / R of each
-//   row, 4 KB per warp) with the next chunk's loads issued before the current
-//   one is used, so that two chunks are in flight per warp across group
-//   boundaries; the first chunk's loads go out before the norm;
-//   each normalised 16-byte vector read from shared memory serves the R rows;
-//   the T x R dot products accumulate in FP32 with the mixed-precision FMA
+//   each warp then takes units of weight rows, u = w, w + W, ... (W = the
+//   warps of the whole grid, which is resident at once; warp w is warp
+//   w / grid of CTA w % grid): with R = 2 the first P units are pairs of
+//   adjacent rows and the rest single rows, where the host sets P to whole
+//   rounds of pairs when single rows for the remainder shorten the longest
+//   warp's sequence (at 6144 rows over 2432 warps: one round of pairs and
+//   1280 single rows, 6 chunks at most a warp instead of 8), else to all
+//   pairs; with R = 1 every unit is a row.  Each warp streams its units as
+//   one sequence of chunks (8 16-byte loads per lane: 4 of each row of a
+//   pair, 8 of a single row; 4 KB per warp) with the next chunk's loads
+//   issued before the current one is used, so that two chunks are in flight
+//   per warp across unit boundaries; the first chunk's loads go out before
+//   the norm;
+//   each normalised 16-byte vector read from shared memory serves the rows
+//   of the unit; the dot products accumulate in FP32 with the mixed-precision FMA
 //   (bf16 x bf16 + f32, one rounding; the bf16 product is exact) and reduce
 //   across the warp: out[t, n] = bf16(sum).
 //
@@ -92,26 +98,89 @@ __device__ __forceinline__ void load_chunk(const uint4* __restrict__ W, int n0, 
   }
 }
 
+// the T x R dot products of one chunk (C = kChunk / R vectors per lane of each row)
+template <int T, int R>
+__device__ __forceinline__ void dot_chunk(const uint4* __restrict__ a_s, const uint4 (&cur)[kChunk], int q,
+                                          int nvec, int lane, float (&acc)[2][T], float (&acc2)[2][T]) {
+  constexpr int C = kChunk / R;
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int v = lane + 32 * (q * C + i);
+    if (v < nvec) {
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        const uint4 a = a_s[t * nvec + v];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint4 w = cur[r * C + i];
+          fma2_bf16(a.x, w.x, acc[r][t], acc2[r][t]);
+          fma2_bf16(a.y, w.y, acc[r][t], acc2[r][t]);
+          fma2_bf16(a.z, w.z, acc[r][t], acc2[r][t]);
+          fma2_bf16(a.w, w.w, acc[r][t], acc2[r][t]);
+        }
+      }
+    }
+  }
+}
+
+// a unit of R rows from n0 is complete: reduce across the warp and store
+template <int T, int R>
+__device__ __forceinline__ void reduce_store(float (&acc)[2][T], float (&acc2)[2][T], int n0, int N, int lane,
+                                             __nv_bfloat16* __restrict__ out) {
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      acc[r][t] += acc2[r][t];
+      acc2[r][t] = 0.f;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < T; ++t) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int n = n0 + r;
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      if (lane == r * T + t && n < N) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(acc[r][t]);
+      acc[r][t] = 0.f;
+    }
+  }
+}
+
 template <int MODE, int T, int R>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma,
                   const uint4* __restrict__ W, int nvec, int N, float inv_d, float eps,
-                  int gamma_smem, __nv_bfloat16* __restrict__ out) {
+                  int gamma_smem, int P, __nv_bfloat16* __restrict__ out) {
   extern __shared__ uint4 a_s[];  // [T][nvec] rows, then [nvec] gamma when gamma_smem
   uint4* g_s = a_s + T * nvec;
   __shared__ float red[kWarps][kMaxTokens];
   __shared__ float rstd_s[kMaxTokens];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int C = kChunk / R;           // vectors per lane of each row in a chunk
-  const int stride = gridDim.x * kWarps;  // in row groups
-  const int groups = (N + R - 1) / R;
-  const int cpr = (nvec + 32 * C - 1) / (32 * C);  // chunks per row group
-  // warps numbered CTA-minor, so that the groups of a last, partial round
-  // fall to warps of every CTA (every SM) rather than to the first CTAs
-  int g = warp * gridDim.x + blockIdx.x, q = 0;
+  const int stride = gridDim.x * kWarps;  // in units
+  // units: with R = 2 the first P are pairs of rows (2p, 2p + 1), the rest
+  // single rows 2P + s; with R = 1 every unit is a single row
+  const int Pp = R == 2 ? P : 0;
+  const int S = N - 2 * Pp;
+  const int cpr2 = (nvec + 127) / 128, cpr1 = (nvec + 255) / 256;  // chunks per pair / single row
+  const int w0 = warp * gridDim.x + blockIdx.x;
+  const int kp = w0 < Pp ? (Pp - 1 - w0) / stride + 1 : 0;
+  const int ks = w0 < S ? (S - 1 - w0) / stride + 1 : 0;
+  const int units = kp + ks;
+  auto load = [&](int u, int qq, uint4 (&buf)[kChunk]) {
+    if (R == 2 && u < kp)
+      load_chunk<2>(W, 2 * (w0 + u * stride), N, qq, nvec, lane, buf);
+    else
+      load_chunk<1>(W, 2 * Pp + w0 + (u - kp) * stride, N, qq, nvec, lane, buf);
+  };
+  int u = 0, q = 0;
   grid_dependency_wait();  // x, gamma and W may come from the previous kernel
   uint4 cur[kChunk];
-  if (g < groups) load_chunk<R>(W, g * R, N, 0, nvec, lane, cur);
+  if (units > 0) load(0, 0, cur);
 
   // 1. the normalised rows: thread i takes vectors i, i + 256, ... of every
   //    row; the raw vectors stay in shared memory for the second pass, which
@@ -173,64 +242,31 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   __syncthreads();
 
   // 2. the row groups as one stream of chunks, the next chunk in flight
-  float acc[R][T], acc2[R][T];  // even and odd elements
+  float acc[2][T], acc2[2][T];  // even and odd elements
 #pragma unroll
-  for (int r = 0; r < R; ++r)
+  for (int r = 0; r < 2; ++r)
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[r][t] = acc2[r][t] = 0.f;
-  while (g < groups) {
-    int g2 = g, q2 = q + 1;
+  while (u < units) {
+    const bool pair = R == 2 && u < kp;
+    const int cpr = pair ? cpr2 : cpr1;
+    int u2 = u, q2 = q + 1;
     if (q2 == cpr) {
       q2 = 0;
-      g2 = g + stride;
+      u2 = u + 1;
     }
     uint4 nxt[kChunk];
-    if (g2 < groups) load_chunk<R>(W, g2 * R, N, q2, nvec, lane, nxt);
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-      const int v = lane + 32 * (q * C + i);
-      if (v < nvec) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          const uint4 a = a_s[t * nvec + v];
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const uint4 w = cur[r * C + i];
-            fma2_bf16(a.x, w.x, acc[r][t], acc2[r][t]);
-            fma2_bf16(a.y, w.y, acc[r][t], acc2[r][t]);
-            fma2_bf16(a.z, w.z, acc[r][t], acc2[r][t]);
-            fma2_bf16(a.w, w.w, acc[r][t], acc2[r][t]);
-          }
-        }
-      }
-    }
-    if (q == cpr - 1) {  // the group is complete: reduce across the warp
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          acc[r][t] += acc2[r][t];
-          acc2[r][t] = 0.f;
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-          for (int t = 0; t < T; ++t) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int n = g * R + r;
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          if (lane == r * T + t && n < N) out[static_cast<int64_t>(t) * N + n] = __float2bfloat16_rn(acc[r][t]);
-          acc[r][t] = 0.f;
-        }
-      }
+    if (u2 < units) load(u2, q2, nxt);
+    if (pair) {
+      dot_chunk<T, 2>(a_s, cur, q, nvec, lane, acc, acc2);
+      if (q == cpr - 1) reduce_store<T, 2>(acc, acc2, 2 * (w0 + u * stride), N, lane, out);
+    } else {
+      dot_chunk<T, 1>(a_s, cur, q, nvec, lane, acc, acc2);
+      if (q == cpr - 1) reduce_store<T, 1>(acc, acc2, 2 * Pp + w0 + (u - kp) * stride, N, lane, out);
     }
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) cur[i] = nxt[i];
-    g = g2;
+    u = u2;
     q = q2;
   }
 }
@@ -245,9 +281,9 @@ void* decode_entry(int64_t T) {
   }
 }
 
-// Weight rows per warp group: 2 for 3 or 4 tokens when the pairs of rows
-// still give every resident warp (two CTAs of 8 warps per SM) at least one
-// group, else 1.  Measured (GPU time, flushed CUDA graph): 4 x 4096 -> 6144
+// Units of two rows (pairs, with single rows for a remainder) for 3 or 4
+// tokens when the pairs of rows still give every resident warp (two CTAs of
+// 8 warps per SM) at least one pair, else single rows throughout.  Measured (GPU time, flushed CUDA graph): 4 x 4096 -> 6144
 // 15.4 us with pairs against 16.1 us; 1 and 2 tokens 13.3 and 14.0 us with
 // single rows against 13.5 and 14.5 us; 4 x 12288 -> 2048 (1024 pairs for
 // 2432 warps) 20.6 us single against 21.1 us.  RNL_DECODE_ROWS=1 or 2
@@ -291,13 +327,25 @@ rnl_status launch_decode(const void* x, const void* gamma, const void* W, int64_
   }
   const int64_t groups = (N + R - 1) / R;
   const int64_t grid = std::min<int64_t>(static_cast<int64_t>(per_sm) * sm_count, (groups + kWarps - 1) / kWarps);
+  // with pairs of rows: whole rounds of pairs for every warp and the rest as
+  // single rows (half the chunks of a pair) when that shortens the longest
+  // warp's sequence, else pairs throughout
+  const int64_t wt = grid * kWarps;
+  int P = 0;
+  if (R == 2) {
+    const int64_t k = N / (2 * wt), rest = N - 2 * k * wt;
+    const int64_t cpr2 = (nvec + 127) / 128, cpr1 = (nvec + 255) / 256;
+    const int64_t pairs_max = (groups + wt - 1) / wt * cpr2;
+    const int64_t mixed_max = k * cpr2 + (rest + wt - 1) / wt * cpr1;
+    P = static_cast<int>(mixed_max < pairs_max ? k * wt : groups);
+  }
   const uint4* xp = static_cast<const uint4*>(x);
   const uint4* gp = static_cast<const uint4*>(gamma);
   const uint4* wp = static_cast<const uint4*>(W);
   int nv = nvec, nn = static_cast<int>(N), gs = gamma_smem;
   float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
   __nv_bfloat16* op = static_cast<__nv_bfloat16*>(out);
-  void* args[] = {&xp, &gp, &wp, &nv, &nn, &inv_d, &eps, &gs, &op};
+  void* args[] = {&xp, &gp, &wp, &nv, &nn, &inv_d, &eps, &gs, &P, &op};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
