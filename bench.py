@@ -77,7 +77,7 @@ TRAFFIC = {
     "qmrs": {"bytes": 373960000, "profile": "profiles/traffic_roofline_stages.md", "sources": "8cdfcbb841cc0a10"},
     "mxfp8": {"bytes": 55750000, "profile": "profiles/traffic_roofline_stages.md", "sources": "44d1e228dcf671fc"},
     "mla_hn": {"bytes": 203520000, "profile": "profiles/traffic_roofline_stages.md", "sources": "14f7e1c2fe6abad4"},
-    "decode": {"bytes": 50410000, "profile": "profiles/traffic_roofline_stages.md", "sources": "af8b0d95586cd1c1"},
+    "decode": {"bytes": 50410000, "profile": "profiles/traffic_roofline_stages.md", "sources": "210bbf6298a6e578"},
 }
 
 
