@@ -10,8 +10,10 @@
 // counted on the stage's mbarrier), and 8 consumer warps each normalise one
 // row of the group from shared memory and store it with coalesced 16-byte
 // stores.  The ring holds up to 200 KB, so each SM keeps several row groups
-// in flight whatever the occupancy.  The per-row arithmetic is the same as
-// norm_cast_kernel (rowwise.cu), element for element and in the same order.
+// in flight whatever the occupancy; where a CTA's whole share of rows fits in
+// shared memory, the ring holds all of it and every row is requested at
+// once.  The per-row arithmetic is the same as norm_cast_kernel
+// (rowwise.cu), element for element and in the same order.
 //
 // Consumers keep the current row in registers (rows of up to 4096 elements)
 // and read gamma from shared memory, so the inner loops carry no global load.
@@ -20,6 +22,8 @@
 // previous kernel in the stream, every thread then waits for it
 // (griddepcontrol.wait), and the kernel lets the next one be scheduled early.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -34,6 +38,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreadsNS = (kConsumerWarps + 1) * 32;
 constexpr int kMaxNsStages = 16;
 constexpr size_t kRingBytes = 200 * 1024;
+constexpr size_t kNsSmemLimit = 232448;  // 227 KB opt-in shared memory per block
 
 struct __align__(8) NsCtrl {
   uint64_t full[kMaxNsStages][kGroupRows];  // one barrier per row slot: a warp starts on its row
@@ -83,7 +88,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int MODE, bool GAMMA, int VPL, bool EXT>
 __global__ void __launch_bounds__(kThreadsNS, 1)
     norm_cast_stream_kernel(const uint8_t* x, const uint4* __restrict__ gamma, int64_t T,
-                            int nvec, int stages, float inv_d, float eps, uint4* __restrict__ A,
+                            int nvec, int stages, int ring_rows, float inv_d, float eps,
+                            uint4* __restrict__ A,
                             const NsExt ext) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -93,9 +99,10 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
   const uint32_t stage_bytes = kGroupRows * row_bytes;
   const bool has_res = EXT && ext.residual != nullptr;
   const bool has_beta = EXT && ext.beta != nullptr;
-  uint4* gamma_s = reinterpret_cast<uint4*>(smem + static_cast<size_t>(stages) * stage_bytes);
+  // the ring holds ring_rows rows (stage s, row r at row s * kGroupRows + r)
+  uint4* gamma_s = reinterpret_cast<uint4*>(smem + static_cast<size_t>(ring_rows) * row_bytes);
   uint4* beta_s = gamma_s + nvec;  // EXT only
-  NsCtrl* ctrl = reinterpret_cast<NsCtrl*>(smem + static_cast<size_t>(stages) * stage_bytes +
+  NsCtrl* ctrl = reinterpret_cast<NsCtrl*>(smem + static_cast<size_t>(ring_rows) * row_bytes +
                                            (EXT ? 2 : 1) * row_bytes);
 
   const int warp = threadIdx.x >> 5;
@@ -130,7 +137,7 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
         const int rows = static_cast<int>(r_end - row0 < kGroupRows ? r_end - row0 : kGroupRows);
         const uint32_t dst = base + stage * stage_bytes;
         if (!RNL_DCHECK(&g_err_norm, stages <= kMaxNsStages && stage < static_cast<uint32_t>(stages) &&
-                                         static_cast<size_t>(stages) * stage_bytes <= kRingBytes &&
+                                         static_cast<int>(stage) * kGroupRows + rows <= ring_rows &&
                                          row0 >= 0 && row0 + rows <= T, 50))
           break;
         for (int r = 0; r < rows; ++r) {
@@ -296,12 +303,11 @@ __global__ void __launch_bounds__(kThreadsNS, 1)
 }
 
 template <int MODE, bool GAMMA, int VPL, bool EXT>
-rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int stages, float inv_d,
+rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int stages, int ring_rows, float inv_d,
                      float eps, void* A, const NsExt& ext, size_t smem, const DeviceInfo& dev,
                      cudaStream_t s) {
   auto kern = norm_cast_stream_kernel<MODE, GAMMA, VPL, EXT>;
-  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device,
-                       kRingBytes + 128 + 2 * 8192 + sizeof(NsCtrl)) != RNL_OK)
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kern), dev.device, smem) != RNL_OK)
     return RNL_ERR_LAUNCH;
   const int64_t groups = (T + kGroupRows - 1) / kGroupRows;
   cudaLaunchAttribute attr[1];
@@ -315,7 +321,7 @@ rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t*>(x),
-                                           static_cast<const uint4*>(gamma), T, nvec, stages,
+                                           static_cast<const uint4*>(gamma), T, nvec, stages, ring_rows,
                                            inv_d, eps, static_cast<uint4*>(A), ext);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -325,25 +331,25 @@ rnl_status launch_ns(const void* x, const void* gamma, int64_t T, int nvec, int 
 }
 
 template <int VPL, bool EXT>
-rnl_status dispatch_mode(const void* x, const void* gamma, int64_t T, int nvec, int stages,
+rnl_status dispatch_mode(const void* x, const void* gamma, int64_t T, int nvec, int stages, int ring_rows,
                          float inv_d, float eps, void* A, const NsExt& ext, size_t smem,
                          const DeviceInfo& dev, cudaStream_t s, int mode) {
   if (mode == RNL_NORM_RSQRT)
-    return gamma ? launch_ns<0, true, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s)
-                 : launch_ns<0, false, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s);
-  return gamma ? launch_ns<1, true, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s)
-               : launch_ns<1, false, VPL, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s);
+    return gamma ? launch_ns<0, true, VPL, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s)
+                 : launch_ns<0, false, VPL, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s);
+  return gamma ? launch_ns<1, true, VPL, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s)
+               : launch_ns<1, false, VPL, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s);
 }
 
 template <bool EXT>
-rnl_status dispatch_vpl(const void* x, const void* gamma, int64_t T, int nvec, int stages,
+rnl_status dispatch_vpl(const void* x, const void* gamma, int64_t T, int nvec, int stages, int ring_rows,
                         float inv_d, float eps, void* A, const NsExt& ext, size_t smem,
                         const DeviceInfo& dev, cudaStream_t s, int mode) {
   const int vpl = (nvec + 31) / 32;
-  if (vpl <= 2) return dispatch_mode<2, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
-  if (vpl <= 4) return dispatch_mode<4, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
-  if (vpl <= 8) return dispatch_mode<8, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
-  return dispatch_mode<16, EXT>(x, gamma, T, nvec, stages, inv_d, eps, A, ext, smem, dev, s, mode);
+  if (vpl <= 2) return dispatch_mode<2, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s, mode);
+  if (vpl <= 4) return dispatch_mode<4, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s, mode);
+  if (vpl <= 8) return dispatch_mode<8, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s, mode);
+  return dispatch_mode<16, EXT>(x, gamma, T, nvec, stages, ring_rows, inv_d, eps, A, ext, smem, dev, s, mode);
 }
 
 rnl_status launch_stream(const void* x, const void* gamma, int64_t T, int64_t K, float eps,
@@ -354,18 +360,32 @@ rnl_status launch_stream(const void* x, const void* gamma, int64_t T, int64_t K,
   rnl_status st = current_device(&dev);
   if (st != RNL_OK) return st;
   const int nvec = static_cast<int>(K / 8);
-  const size_t stage = static_cast<size_t>(kGroupRows) * static_cast<size_t>(K) * 2;
+  const size_t row_b = static_cast<size_t>(K) * 2;
+  const size_t stage = static_cast<size_t>(kGroupRows) * row_b;
   int stages = static_cast<int>(kRingBytes / stage);
   if (stages > kMaxNsStages) stages = kMaxNsStages;
+  int64_t ring_rows = static_cast<int64_t>(stages) * kGroupRows;
   // ring, then gamma [, beta] rows, then the barriers
-  const size_t smem = 128 + static_cast<size_t>(stages) * stage +
-                      static_cast<size_t>(ext ? 2 : 1) * static_cast<size_t>(K) * 2 + sizeof(NsCtrl);
+  const size_t fixed = 128 + static_cast<size_t>(ext ? 2 : 1) * row_b + sizeof(NsCtrl);
+  // When the fullest CTA's whole share of rows fits in shared memory, the
+  // ring holds all of it, one stage a group: every row is requested at once
+  // and no slot waits to be refilled.  (At 4096 rows of 4096 a CTA's 27 rows
+  // then stream without the last 3 waiting for the first group to be done.)
+  const int64_t grid = std::min<int64_t>((T + kGroupRows - 1) / kGroupRows, dev.sm_count);
+  const int64_t rows_max = (T + grid - 1) / grid;
+  const int64_t groups_max = (rows_max + kGroupRows - 1) / kGroupRows;
+  if (groups_max > stages && groups_max <= kMaxNsStages &&
+      fixed + static_cast<size_t>(rows_max) * row_b <= kNsSmemLimit) {
+    stages = static_cast<int>(groups_max);
+    ring_rows = rows_max;
+  }
+  const size_t smem = fixed + static_cast<size_t>(ring_rows) * row_b;
   const float inv_d = static_cast<float>(1.0 / static_cast<double>(K));
   trace_before(s);
   if (ext)
-    st = dispatch_vpl<true>(x, gamma, T, nvec, stages, inv_d, eps, A, *ext, smem, dev, s, mode);
+    st = dispatch_vpl<true>(x, gamma, T, nvec, stages, static_cast<int>(ring_rows), inv_d, eps, A, *ext, smem, dev, s, mode);
   else
-    st = dispatch_vpl<false>(x, gamma, T, nvec, stages, inv_d, eps, A, NsExt{}, smem, dev, s, mode);
+    st = dispatch_vpl<false>(x, gamma, T, nvec, stages, static_cast<int>(ring_rows), inv_d, eps, A, NsExt{}, smem, dev, s, mode);
   trace_after(s, ext ? "add_norm_cast" : "norm_cast");
   return st;
 }
